@@ -1,0 +1,351 @@
+"""Oracle for the tensor-parallel sharded linear pipeline (TEST INFRASTRUCTURE).
+
+This is a plain, slow, CPU-only statement of what the pipeline computes. Only
+the tests, the smoke check and the bench's CPU-baseline leg may import it; the
+product path (the CUDA library and its Python binding) never does, and the
+oracle imports nothing from the product.
+
+Arithmetic: whatever numpy dtype the caller passes. The tests pass float64
+(inputs are the bf16 / fp32 values the GPU sees, treated as exact reals; no
+intermediate is re-rounded) or int64 for integer-valued inputs, where every
+result is exact. A library matmul (``@``) is the only primitive used for a
+product; there is no blocking, fusion or reordering beyond what each
+definition states.
+
+Pages cited (by title and section):
+  [CTP]  "CUDA tensor parallel computations" learning notes (jokeuncle.github.io):
+         sections "minimal math foundation" (the X=[10,20], 2x4 W example),
+         "Column Parallel: split by output columns", "Row Parallel: split by
+         input rows", "cross-GPU communication" (all-gather, all-reduce,
+         reduce-scatter, broadcast), "local elementwise computation",
+         "putting it into a Transformer" (QKV, heads, O projection, MLP),
+         and the summary table.
+  [TUT]  "Tensor parallelism: splitting Transformer layers" tutorial
+         (freeguideonline.com): "column-wise sharding", "row-wise sharding",
+         "MLP block sharding", "self-attention block sharding",
+         "input and output layers", and the two-GPU PyTorch MLP sample.
+  [WIT]  "What is tensor parallelism" (aiug.cn): basic principle (column and
+         row parallel linear).
+  [TRT]  "Parallel strategies in TensorRT LLM" (developer.aliyun.com):
+         attention module, tensor parallel, GQA/MQA exception (KV replicated).
+
+Readings where the pages are silent or ambiguous (each is listed with its
+reason in the design notes of the repository):
+  * W is [in, out] and Y = X @ W  ([TUT] sample, [CTP] example).
+  * shard s is the s-th contiguous block; a dimension not divisible by tp is
+    an error ([CTP] column/row sections; [TUT] sample uses integer division).
+  * row-parallel bias is added once, after the sum.
+  * GELU is the exact erf form; SiLU(x) = x / (1 + exp(-x)); SwiGLU applies
+    SiLU to the gate and multiplies by the up projection.
+  * reduce-scatter splits the summed result along tokens into tp equal slices.
+  * KV heads are replicated when num_kv_heads < tp; q head h uses kv head
+    floor(h / (hq / hkv)).
+  * Between QKV and O, the attention core is the single-key case: each query
+    attends only to its own token, so the softmax weight is 1 and the context
+    of q head h is V of its kv head.
+  * RMSNorm: x * g / sqrt(mean(x^2) + eps), eps = 1e-5, statistics over the
+    full (replicated) hidden.
+  * Block wiring: x += O(ctx(QKV(norm(x)))); x += MLP(norm(x)); after the
+    last block a final norm and the column-split LM head, gathered.
+
+Parity pins: every function here is checked, without the GPU, against the
+worked example's printed values, brute force on tiny integer inputs, closed
+forms and library routines (see tests/test_oracle_pins.py). GELU and SiLU are
+pinned to scipy's normal CDF and logistic function; beyond that the float
+activations are "parity unpinned" against the pages, which print no values
+for them.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "linear", "column_shards", "row_shards", "split_columns",
+    "column_parallel", "all_gather", "row_parallel_partials", "all_reduce",
+    "reduce_scatter", "relu", "gelu", "silu", "swiglu", "ACTIVATIONS",
+    "mlp_block", "qkv_head_layout", "qkv_shards", "context_standin",
+    "attn_proj", "rmsnorm", "transformer_block", "stack_forward",
+]
+
+
+# ---------------------------------------------------------------------------
+# The linear layer and its two splits
+# ---------------------------------------------------------------------------
+
+def linear(X: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """Y = X @ W; y[t, n] = sum_k x[t, k] * w[k, n].  [CTP] minimal math
+    foundation: each output is a sum of products over the input dimension."""
+    return X @ W
+
+
+def _block(n: int, tp: int, what: str) -> int:
+    if tp < 1 or n % tp != 0:
+        raise ValueError(f"{what}={n} is not divisible by tp={tp}")
+    return n // tp
+
+
+def column_shards(W: np.ndarray, tp: int) -> list[np.ndarray]:
+    """W[:, s*N/tp:(s+1)*N/tp] for s = 0..tp-1.  [CTP] Column Parallel: GPU 0
+    holds the first block of output columns, GPU 1 the next; [TUT]
+    column-wise sharding."""
+    n = _block(W.shape[1], tp, "N")
+    return [W[:, s * n:(s + 1) * n] for s in range(tp)]
+
+
+def row_shards(W: np.ndarray, tp: int) -> list[np.ndarray]:
+    """W[s*K/tp:(s+1)*K/tp, :] for s = 0..tp-1.  [CTP] Row Parallel: the rows
+    of W (input dimension) are split; [TUT] row-wise sharding."""
+    k = _block(W.shape[0], tp, "K")
+    return [W[s * k:(s + 1) * k, :] for s in range(tp)]
+
+
+def split_columns(X: np.ndarray, tp: int) -> list[np.ndarray]:
+    """The input blocks matching row shards: X[:, s*K/tp:(s+1)*K/tp].
+    [CTP] Row Parallel: X is split along with the rows of W."""
+    k = _block(X.shape[1], tp, "K")
+    return [X[:, s * k:(s + 1) * k] for s in range(tp)]
+
+
+def column_parallel(X, W, tp, bias=None, act=None):
+    """Per-shard outputs Y_s = act(X @ W_s + b_s), X replicated on every shard.
+    [CTP] Column Parallel (each GPU computes X @ W_s) and local elementwise
+    computation (activation and bias are applied shard-locally); the bias is
+    split with its columns."""
+    Ws = column_shards(W, tp)
+    bs = column_shards(bias.reshape(1, -1), tp) if bias is not None else [None] * tp
+    out = []
+    for s in range(tp):
+        y = linear(X, Ws[s])
+        if bs[s] is not None:
+            y = y + bs[s]
+        if act is not None:
+            y = act(y)
+        out.append(y)
+    return out
+
+
+def all_gather(parts: list[np.ndarray]) -> np.ndarray:
+    """Concatenate shard outputs along the last (column) dimension.
+    [CTP] all-gather ("every GPU ends with [110, 140, 170, 200]") and the
+    Column Parallel merge: concatenation, not addition; [TUT] sample
+    torch.cat(dim=-1)."""
+    return np.concatenate(parts, axis=-1)
+
+
+def row_parallel_partials(Xs: list[np.ndarray], W: np.ndarray, tp: int) -> list[np.ndarray]:
+    """P_s = X_s @ W_s: each shard's contribution to the full output.
+    [CTP] Row Parallel ("GPU 0 computes a local contribution")."""
+    Ws = row_shards(W, tp)
+    if len(Xs) != tp:
+        raise ValueError("need one input block per shard")
+    return [linear(Xs[s], Ws[s]) for s in range(tp)]
+
+
+def all_reduce(partials: list[np.ndarray]) -> np.ndarray:
+    """Elementwise sum of the partials, taken in shard order s = 0..tp-1.
+    [CTP] all-reduce ("add the subtotals into the total") and the Row
+    Parallel merge: addition, not concatenation."""
+    total = np.zeros_like(partials[0])
+    for p in partials:
+        total = total + p
+    return total
+
+
+def reduce_scatter(partials: list[np.ndarray], tp: int) -> list[np.ndarray]:
+    """Sum the partials, then cut the total into tp slices; shard s keeps
+    token rows [s*T/tp, (s+1)*T/tp).  [CTP] reduce-scatter ("sum first,
+    then split the result, each GPU keeps the slice it needs"). The split
+    axis (tokens) is a reading: the page does not name it."""
+    total = all_reduce(partials)
+    rows = _block(total.shape[0], tp, "T")
+    return [total[s * rows:(s + 1) * rows] for s in range(tp)]
+
+
+# ---------------------------------------------------------------------------
+# Local elementwise operations ([CTP] local elementwise computation)
+# ---------------------------------------------------------------------------
+
+def relu(x):
+    """max(0, x)."""
+    return np.maximum(x, 0)
+
+
+def gelu(x):
+    """0.5 * x * (1 + erf(x / sqrt(2))): the exact GELU ([TUT] sample uses
+    nn.GELU(), whose default is this erf form)."""
+    erf = np.vectorize(math.erf, otypes=[np.float64])
+    return 0.5 * x * (1.0 + erf(np.asarray(x, np.float64) / math.sqrt(2.0)))
+
+
+def silu(x):
+    """x / (1 + exp(-x))."""
+    x = np.asarray(x, np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def swiglu(g, u):
+    """SwiGLU gate: silu(gate) * up.  [TUT] MLP block sharding: gate and up
+    projections multiplied elementwise, then the down projection; [CTP]
+    "multiply by a gate" is listed as a local elementwise op."""
+    return silu(g) * u
+
+
+ACTIVATIONS = {"none": None, "relu": relu, "gelu": gelu, "silu": silu}
+
+
+# ---------------------------------------------------------------------------
+# The MLP block: column -> local activation -> row -> sum
+# ---------------------------------------------------------------------------
+
+def mlp_block(X, W1, W2, tp, act="relu", W_up=None, b1=None, b1_up=None,
+              b2=None, residual=None):
+    """[CTP] "MLP: expand then contract, exactly Column + Row": the first
+    layer is column-split, the activation is applied locally to each
+    intermediate shard, the second layer is row-split on that same shard,
+    and the partial results are summed (all-reduce). [TUT] MLP block
+    sharding, steps 1-4. With act == "swiglu", W1 is the gate projection
+    and W_up the up projection; both are column-split the same way.
+
+    Returns (Hs, Y): the per-shard intermediate activations and the
+    combined output Y = sum_s Hs[s] @ W2_s (+ b2, once) (+ residual).
+    """
+    if act == "swiglu":
+        G = column_parallel(X, W1, tp, b1)
+        U = column_parallel(X, W_up, tp, b1_up)
+        Hs = [swiglu(G[s], U[s]) for s in range(tp)]
+    else:
+        Hs = column_parallel(X, W1, tp, b1, ACTIVATIONS[act])
+    partials = row_parallel_partials(Hs, W2, tp)
+    Y = all_reduce(partials)
+    if b2 is not None:
+        Y = Y + b2.reshape(1, -1)
+    if residual is not None:
+        Y = Y + residual
+    return Hs, Y
+
+
+# ---------------------------------------------------------------------------
+# Attention projections: QKV column-split by heads, O row-split
+# ---------------------------------------------------------------------------
+
+def qkv_head_layout(hq: int, hkv: int, tp: int):
+    """Heads held by each shard.  [CTP] QKV projection: each GPU takes a
+    subset of the attention heads; [TUT] split by number of heads, whole
+    heads per device; [TRT] GQA/MQA: when the KV heads cannot be split
+    (fewer KV heads than tp) they are replicated.
+
+    Returns a list over shards of (q_heads, kv_heads). q heads are split
+    evenly. If hkv >= tp the kv heads are split evenly too; otherwise shard
+    s holds the single kv head floor(s * hkv / tp), shared (replicated)
+    with the other shards of its group.
+    """
+    if hq % tp != 0:
+        raise ValueError("hq must be divisible by tp")
+    if hq % hkv != 0:
+        raise ValueError("hq must be a multiple of hkv")
+    if hkv >= tp:
+        if hkv % tp != 0:
+            raise ValueError("hkv must be divisible by tp when hkv >= tp")
+    elif tp % hkv != 0:
+        raise ValueError("tp must be a multiple of hkv when hkv < tp")
+    nq = hq // tp
+    out = []
+    for s in range(tp):
+        q = list(range(s * nq, (s + 1) * nq))
+        if hkv >= tp:
+            nk = hkv // tp
+            kv = list(range(s * nk, (s + 1) * nk))
+        else:
+            kv = [s * hkv // tp]
+        out.append((q, kv))
+    return out
+
+
+def _head_cols(W, heads, hd):
+    return np.concatenate([W[:, h * hd:(h + 1) * hd] for h in heads], axis=1)
+
+
+def qkv_shards(Wq, Wk, Wv, hq, hkv, hd, tp):
+    """Per-shard column weights [H, (nq + 2*nkv) * hd]: the shard's q head
+    columns, then its k head columns, then its v head columns."""
+    layout = qkv_head_layout(hq, hkv, tp)
+    return [np.concatenate([_head_cols(Wq, q, hd), _head_cols(Wk, kv, hd),
+                            _head_cols(Wv, kv, hd)], axis=1)
+            for q, kv in layout]
+
+
+def context_standin(qkv_s, q_heads, kv_heads, hq, hkv, hd):
+    """Attention context of one shard under the single-key reading: each
+    query attends only to its own token, the softmax over one score is 1,
+    and the context of q head h is V of kv head floor(h / (hq / hkv)).
+    [CTP] attention heads are local once Q/K/V of a head sit on one GPU.
+    Returns [T, len(q_heads) * hd]."""
+    nq, nkv = len(q_heads), len(kv_heads)
+    v0 = (nq + nkv) * hd
+    group = hq // hkv
+    cols = []
+    for h in q_heads:
+        j = kv_heads.index(h // group)
+        cols.append(qkv_s[:, v0 + j * hd:v0 + (j + 1) * hd])
+    return np.concatenate(cols, axis=1)
+
+
+def attn_proj(X, Wq, Wk, Wv, Wo, hq, hkv, hd, tp, ctx=None, residual=None):
+    """[CTP] QKV projection (column parallel by heads), local attention
+    heads, output projection (row parallel, then all-reduce); [TUT]
+    self-attention block sharding.
+
+    ctx, if given, is the per-shard attention output [tp][T, hq/tp*hd];
+    otherwise the single-key stand-in supplies it. Returns
+    (qkv per shard, ctx per shard, Y)."""
+    layout = qkv_head_layout(hq, hkv, tp)
+    Wqkv = qkv_shards(Wq, Wk, Wv, hq, hkv, hd, tp)
+    qkv = [linear(X, Wqkv[s]) for s in range(tp)]
+    if ctx is None:
+        ctx = [context_standin(qkv[s], layout[s][0], layout[s][1], hq, hkv, hd)
+               for s in range(tp)]
+    partials = row_parallel_partials(ctx, Wo, tp)
+    Y = all_reduce(partials)
+    if residual is not None:
+        Y = Y + residual
+    return qkv, ctx, Y
+
+
+# ---------------------------------------------------------------------------
+# Norm and the block stack
+# ---------------------------------------------------------------------------
+
+def rmsnorm(x, gamma=None, eps=1e-5):
+    """y = x * g / sqrt(mean over hidden of x^2 + eps). [CTP] local
+    elementwise computation: a norm needs statistics over the hidden
+    dimension and is local when run on the replicated hidden."""
+    x = np.asarray(x, np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    y = x / np.sqrt(ms + eps)
+    if gamma is not None:
+        y = y * gamma
+    return y
+
+
+def transformer_block(x, L, tp, hq, hkv, hd, eps=1e-5):
+    """Pre-norm block: x + O(ctx(QKV(norm(x)))), then + MLP(norm(x)).
+    Weights L: Wq, Wk, Wv, Wo, Wg, Wu, Wd."""
+    h = rmsnorm(x, None, eps)
+    _, _, x = attn_proj(h, L["Wq"], L["Wk"], L["Wv"], L["Wo"], hq, hkv, hd, tp,
+                        residual=x)
+    h = rmsnorm(x, None, eps)
+    _, x = mlp_block(h, L["Wg"], L["Wd"], tp, "swiglu", W_up=L["Wu"], residual=x)
+    return x
+
+
+def stack_forward(X, layers, W_lm, tp, hq, hkv, hd, eps=1e-5):
+    """Blocks in order, a final norm, then the LM head column-split over
+    the vocabulary and gathered ([TUT] input and output layers: the output
+    projection is split by columns and the logits gathered)."""
+    x = np.asarray(X, np.float64)
+    for L in layers:
+        x = transformer_block(x, L, tp, hq, hkv, hd, eps)
+    h = rmsnorm(x, None, eps)
+    return all_gather(column_parallel(h, W_lm, tp))

@@ -1,0 +1,497 @@
+"""Pins for the oracle, on the CPU.
+
+Each test checks the oracle against something other than itself: the values
+printed in the pages' worked example, brute force on tiny integer inputs,
+closed forms, library routines (scipy's normal CDF and logistic function),
+and invariants that the pages state (column shards concatenate to the
+unsharded product; row-shard contributions sum to it). A plausible mistake in
+the oracle (a dropped shard, a wrong block index, a transposed operand, a
+swapped gate/up, a bias added per shard) fails at least one of them; the
+``test_planted_*`` cases plant such mistakes in the oracle and check that.
+"""
+import itertools
+
+import numpy as np
+import pytest
+from scipy.special import expit
+from scipy.stats import norm
+
+from oracle import tp_oracle as O
+import synth_inputs as S
+
+
+# ---------------------------------------------------------------------------
+# Helpers independent of the oracle
+# ---------------------------------------------------------------------------
+
+def brute_matmul(X, W):
+    """Pure-Python triple loop: y[t][n] = sum_k x[t][k] * w[k][n]."""
+    T, K = len(X), len(X[0])
+    N = len(W[0])
+    return [[sum(X[t][k] * W[k][n] for k in range(K)) for n in range(N)]
+            for t in range(T)]
+
+
+def brute_mlp(X, W1, W2, act):
+    h = [[act(v) for v in row] for row in brute_matmul(X, W1)]
+    return brute_matmul(h, W2)
+
+
+def divisors(n):
+    return [d for d in range(1, n + 1) if n % d == 0]
+
+
+def rand_ints(rng, shape, lo=-2, hi=2):
+    return rng.integers(lo, hi + 1, size=shape).astype(np.int64)
+
+
+# ---------------------------------------------------------------------------
+# 1. The worked example, values as printed on the page
+# ---------------------------------------------------------------------------
+
+def test_worked_example_unsharded(golden_worked_example):
+    g = golden_worked_example
+    X = np.array(g["X"], np.int64)
+    W = np.array(g["W"], np.int64)
+    assert O.linear(X, W).tolist() == g["XW"]
+
+
+def test_worked_example_column_parallel(golden_worked_example):
+    g = golden_worked_example
+    X, W = np.array(g["X"], np.int64), np.array(g["W"], np.int64)
+    W0, W1 = O.column_shards(W, 2)
+    assert W0.tolist() == g["col_W0"] and W1.tolist() == g["col_W1"]
+    Y0, Y1 = O.column_parallel(X, W, 2)
+    assert Y0.tolist() == g["col_Y0"] and Y1.tolist() == g["col_Y1"]
+    assert O.all_gather([Y0, Y1]).tolist() == g["all_gather"]
+
+
+def test_worked_example_row_parallel(golden_worked_example):
+    g = golden_worked_example
+    X, W = np.array(g["X"], np.int64), np.array(g["W"], np.int64)
+    X0, X1 = O.split_columns(X, 2)
+    assert X0.tolist() == g["row_X0"] and X1.tolist() == g["row_X1"]
+    W0, W1 = O.row_shards(W, 2)
+    assert W0.tolist() == g["row_W0"] and W1.tolist() == g["row_W1"]
+    P0, P1 = O.row_parallel_partials([X0, X1], W, 2)
+    assert P0.tolist() == g["row_P0"] and P1.tolist() == g["row_P1"]
+    assert O.all_reduce([P0, P1]).tolist() == g["all_reduce"]
+
+
+def test_worked_example_from_input_generator(golden_worked_example):
+    X, W = S.worked_example()
+    assert X.astype(np.int64).tolist() == golden_worked_example["X"]
+    assert W.astype(np.int64).tolist() == golden_worked_example["W"]
+
+
+# ---------------------------------------------------------------------------
+# 2. Brute force on tiny integer inputs, every tp that divides the dims
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(6))
+def test_column_parallel_concat_equals_bruteforce(seed):
+    rng = np.random.default_rng(seed)
+    T, K, N = 2, 3, 12
+    X, W = rand_ints(rng, (T, K)), rand_ints(rng, (K, N))
+    ref = brute_matmul(X.tolist(), W.tolist())
+    for tp in divisors(N):
+        parts = O.column_parallel(X, W, tp)
+        assert [p.shape for p in parts] == [(T, N // tp)] * tp
+        assert O.all_gather(parts).tolist() == ref
+        # shard s holds exactly output columns [s*N/tp, (s+1)*N/tp)
+        for s, p in enumerate(parts):
+            assert p.tolist() == [row[s * N // tp:(s + 1) * N // tp] for row in ref]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_row_parallel_sum_equals_bruteforce(seed):
+    rng = np.random.default_rng(100 + seed)
+    T, K, N = 2, 12, 3
+    X, W = rand_ints(rng, (T, K)), rand_ints(rng, (K, N))
+    ref = brute_matmul(X.tolist(), W.tolist())
+    for tp in divisors(K):
+        Xs = O.split_columns(X, tp)
+        P = O.row_parallel_partials(Xs, W, tp)
+        assert O.all_reduce(P).tolist() == ref
+        # each partial is the contribution of its own K block only
+        k = K // tp
+        for s in range(tp):
+            sub = brute_matmul(X[:, s * k:(s + 1) * k].tolist(), W[s * k:(s + 1) * k].tolist())
+            assert P[s].tolist() == sub
+
+
+def test_enumerated_2x2_all_values():
+    """Every X in {-1,0,1}^2 against a fixed W, column and row splits."""
+    W = np.array([[1, -2], [3, 2]], np.int64)
+    for xs in itertools.product([-1, 0, 1], repeat=2):
+        X = np.array([xs], np.int64)
+        ref = brute_matmul(X.tolist(), W.tolist())
+        assert O.all_gather(O.column_parallel(X, W, 2)).tolist() == ref
+        assert O.all_reduce(O.row_parallel_partials(O.split_columns(X, 2), W, 2)).tolist() == ref
+
+
+def test_indivisible_dims_rejected():
+    W = np.zeros((4, 6), np.int64)
+    with pytest.raises(ValueError):
+        O.column_shards(W, 4)
+    with pytest.raises(ValueError):
+        O.row_shards(W, 3)
+
+
+# ---------------------------------------------------------------------------
+# 3. The MLP block: column -> local act -> row -> sum == unsharded, all tp
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(4))
+def test_mlp_relu_int_all_tp_bruteforce(seed):
+    rng = np.random.default_rng(200 + seed)
+    T, H, I = 3, 4, 12
+    X, W1, W2 = rand_ints(rng, (T, H)), rand_ints(rng, (H, I)), rand_ints(rng, (I, H))
+    ref = brute_mlp(X.tolist(), W1.tolist(), W2.tolist(), lambda v: max(v, 0))
+    for tp in divisors(I):
+        Hs, Y = O.mlp_block(X, W1, W2, tp, "relu")
+        assert Y.tolist() == ref
+        assert len(Hs) == tp
+
+
+@pytest.mark.parametrize("act", ["gelu", "silu", "none"])
+def test_mlp_float_acts_all_tp(act):
+    rng = np.random.default_rng(7)
+    T, H, I = 3, 4, 8
+    X = rng.standard_normal((T, H))
+    W1, W2 = rng.standard_normal((H, I)), rng.standard_normal((I, H))
+    f = {"gelu": lambda v: v * norm.cdf(v), "silu": lambda v: v * expit(v),
+         "none": lambda v: v}[act]
+    ref = np.array(brute_mlp(X.tolist(), W1.tolist(), W2.tolist(), f))
+    for tp in divisors(I):
+        _, Y = O.mlp_block(X, W1, W2, tp, act)
+        np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_mlp_swiglu_all_tp():
+    rng = np.random.default_rng(8)
+    T, H, I = 2, 4, 8
+    X = rng.standard_normal((T, H))
+    Wg, Wu, Wd = (rng.standard_normal(s) for s in [(H, I), (H, I), (I, H)])
+    g = np.array(brute_matmul(X.tolist(), Wg.tolist()))
+    u = np.array(brute_matmul(X.tolist(), Wu.tolist()))
+    h = g * expit(g) * u
+    ref = np.array(brute_matmul(h.tolist(), Wd.tolist()))
+    for tp in divisors(I):
+        _, Y = O.mlp_block(X, Wg, Wd, tp, "swiglu", W_up=Wu)
+        np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_mlp_bias_once_and_residual():
+    """Row bias enters once after the sum (not once per shard); the column
+    bias is split with its columns; the residual adds once."""
+    X = np.array([[1, 0]], np.int64)
+    W1 = np.array([[1, 2, 3, 4], [0, 0, 0, 0]], np.int64)
+    W2 = np.eye(4, 2, dtype=np.int64)  # picks h[0], h[1]
+    b1 = np.array([10, 20, 30, 40], np.int64)
+    b2 = np.array([100, 200], np.int64)
+    R = np.array([[1000, 2000]], np.int64)
+    for tp in (1, 2, 4):
+        Hs, Y = O.mlp_block(X, W1, W2, tp, "none", b1=b1, b2=b2, residual=R)
+        assert O.all_gather(Hs).tolist() == [[11, 22, 33, 44]]
+        assert Y.tolist() == [[1111, 2222]]
+
+
+# ---------------------------------------------------------------------------
+# 4. Closed forms
+# ---------------------------------------------------------------------------
+
+def test_closed_forms():
+    rng = np.random.default_rng(3)
+    K, N = 6, 8
+    W = rand_ints(rng, (K, N), -5, 5)
+    for tp in (1, 2, 4, 8):
+        for k in range(K):  # X = e_k picks row k of W
+            e = np.zeros((1, K), np.int64)
+            e[0, k] = 1
+            assert O.all_gather(O.column_parallel(e, W, tp)).tolist() == [W[k].tolist()]
+        ones = np.ones((1, K), np.int64)  # X = ones gives column sums
+        assert O.all_gather(O.column_parallel(ones, W, tp)).tolist() == [
+            [int(sum(W[k, n] for k in range(K))) for n in range(N)]]
+    X = rand_ints(rng, (3, N))
+    for tp in (1, 2, 4, 8):  # W = I returns X, in both splits
+        Ieye = np.eye(N, dtype=np.int64)
+        assert O.all_gather(O.column_parallel(X, Ieye, tp)).tolist() == X.tolist()
+        assert O.all_reduce(O.row_parallel_partials(O.split_columns(X, tp), Ieye, tp)).tolist() == X.tolist()
+
+
+def test_tp1_is_plain_product():
+    rng = np.random.default_rng(4)
+    X, W = rand_ints(rng, (3, 5)), rand_ints(rng, (5, 7))
+    ref = brute_matmul(X.tolist(), W.tolist())
+    assert O.column_parallel(X, W, 1)[0].tolist() == ref
+    assert O.row_parallel_partials([X], W, 1)[0].tolist() == ref
+
+
+# ---------------------------------------------------------------------------
+# 5. Combine operators
+# ---------------------------------------------------------------------------
+
+def test_reduce_scatter_explicit():
+    P0 = np.array([[1, 2], [3, 4], [5, 6], [7, 8]], np.int64)
+    P1 = np.array([[10, 20], [30, 40], [50, 60], [70, 80]], np.int64)
+    out = O.reduce_scatter([P0, P1], 2)
+    assert [o.tolist() for o in out] == [[[11, 22], [33, 44]], [[55, 66], [77, 88]]]
+    out4 = O.reduce_scatter([P0, P1], 4)
+    assert [o.tolist() for o in out4] == [[[11, 22]], [[33, 44]], [[55, 66]], [[77, 88]]]
+    with pytest.raises(ValueError):
+        O.reduce_scatter([P0, P1], 3)
+
+
+def test_all_reduce_worked_partials_in_order():
+    # the page's two contributions; and a three-way sum checked by hand
+    assert O.all_reduce([np.array([10, 20, 30, 40]), np.array([100, 120, 140, 160])]).tolist() == [110, 140, 170, 200]
+    assert O.all_reduce([np.array([1]), np.array([2]), np.array([4])]).tolist() == [7]
+
+
+# ---------------------------------------------------------------------------
+# 6. Activations against library routines and special values
+# ---------------------------------------------------------------------------
+
+def test_activations_against_library():
+    x = np.linspace(-6, 6, 97)
+    np.testing.assert_allclose(O.gelu(x), x * norm.cdf(x), rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(O.silu(x), x * expit(x), rtol=1e-14, atol=1e-15)
+    assert O.relu(np.array([-3, 0, 2])).tolist() == [0, 0, 2]
+    assert O.gelu(np.array([0.0]))[0] == 0.0 and O.silu(np.array([0.0]))[0] == 0.0
+    # GELU(1) = Phi(1); SiLU(1) = 1/(1+e^-1)
+    assert abs(O.gelu(np.array([1.0]))[0] - 0.8413447460685429) < 1e-15
+    assert abs(O.silu(np.array([1.0]))[0] - 0.7310585786300049) < 1e-15
+
+
+def test_swiglu_gate_is_the_silu_operand():
+    g, u = np.array([1.0]), np.array([2.0])
+    assert abs(O.swiglu(g, u)[0] - 2 * 0.7310585786300049) < 1e-15
+    assert abs(O.swiglu(u, g)[0] - 1.7615941559557646) < 1e-15  # silu(2)*1
+
+
+# ---------------------------------------------------------------------------
+# 7. Attention projections: heads, KV replication, the single-key context
+# ---------------------------------------------------------------------------
+
+def test_qkv_head_layout_explicit():
+    # 32 q / 8 kv heads: tp=2 splits both; tp=16 replicates each kv head twice
+    L2 = O.qkv_head_layout(32, 8, 2)
+    assert L2[0] == (list(range(16)), [0, 1, 2, 3])
+    assert L2[1] == (list(range(16, 32)), [4, 5, 6, 7])
+    L8 = O.qkv_head_layout(32, 8, 8)
+    assert [kv for _, kv in L8] == [[s] for s in range(8)]
+    L16 = O.qkv_head_layout(32, 8, 16)
+    assert [q for q, _ in L16] == [[2 * s, 2 * s + 1] for s in range(16)]
+    assert [kv for _, kv in L16] == [[s // 2] for s in range(16)]
+    # every q head's kv head (h // 4) sits on the q head's shard
+    for tp in (1, 2, 4, 8, 16, 32):
+        for q, kv in O.qkv_head_layout(32, 8, tp):
+            assert all(h // 4 in kv for h in q)
+    with pytest.raises(ValueError):
+        O.qkv_head_layout(32, 8, 3)
+    with pytest.raises(ValueError):
+        O.qkv_head_layout(32, 6, 4)  # hq not a multiple of hkv
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4, 8, 16])
+def test_qkv_shards_dedup_equals_unsharded(tp):
+    rng = np.random.default_rng(tp)
+    H, hq, hkv, hd, T = 4, 16, 8, 2, 3
+    Wq = rand_ints(rng, (H, hq * hd))
+    Wk, Wv = rand_ints(rng, (H, hkv * hd)), rand_ints(rng, (H, hkv * hd))
+    X = rand_ints(rng, (T, H))
+    ref = np.array(brute_matmul(X.tolist(), np.concatenate([Wq, Wk, Wv], 1).tolist()))
+    layout = O.qkv_head_layout(hq, hkv, tp)
+    shards = O.qkv_shards(Wq, Wk, Wv, hq, hkv, hd, tp)
+    q_seen, kv_seen = {}, {}
+    for s in range(tp):
+        y = O.linear(X, shards[s])
+        q, kv = layout[s]
+        for j, h in enumerate(q):
+            q_seen[h] = y[:, j * hd:(j + 1) * hd]
+        base = len(q) * hd
+        for j, h in enumerate(kv):
+            k = y[:, base + j * hd: base + (j + 1) * hd]
+            v = y[:, base + (len(kv) + j) * hd: base + (len(kv) + j + 1) * hd]
+            if h in kv_seen:  # a replica must equal the first copy
+                assert (kv_seen[h][0] == k).all() and (kv_seen[h][1] == v).all()
+            kv_seen[h] = (k, v)
+    assert sorted(q_seen) == list(range(hq)) and sorted(kv_seen) == list(range(hkv))
+    Q = np.concatenate([q_seen[h] for h in range(hq)], 1)
+    K = np.concatenate([kv_seen[h][0] for h in range(hkv)], 1)
+    V = np.concatenate([kv_seen[h][1] for h in range(hkv)], 1)
+    assert np.concatenate([Q, K, V], 1).tolist() == ref.tolist()
+
+
+def brute_attention_self_only(Q, K, V, hq, hkv, hd):
+    """Scaled dot-product attention per head with a mask that lets token t
+    see only key t: the softmax runs over a single score."""
+    T = Q.shape[0]
+    group = hq // hkv
+    out = np.zeros((T, hq * hd))
+    for h in range(hq):
+        g = h // group
+        for t in range(T):
+            scores = {}
+            for j in range(T):
+                if j == t:  # the only unmasked key
+                    scores[j] = float(Q[t, h * hd:(h + 1) * hd] @ K[j, g * hd:(g + 1) * hd]) / np.sqrt(hd)
+            m = max(scores.values())
+            z = sum(np.exp(v - m) for v in scores.values())
+            for j, v in scores.items():
+                out[t, h * hd:(h + 1) * hd] += np.exp(v - m) / z * V[j, g * hd:(g + 1) * hd]
+    return out
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4, 8, 16])
+def test_context_standin_is_single_key_attention(tp):
+    rng = np.random.default_rng(50 + tp)
+    H, hq, hkv, hd, T = 6, 16, 8, 2, 3
+    Wq, Wk, Wv = (rng.standard_normal(s) for s in [(H, hq * hd), (H, hkv * hd), (H, hkv * hd)])
+    Wo = rng.standard_normal((hq * hd, H))
+    X = rng.standard_normal((T, H))
+    Q, K, V = X @ Wq, X @ Wk, X @ Wv
+    ctx_ref = brute_attention_self_only(Q, K, V, hq, hkv, hd)
+    qkv, ctx, Y = O.attn_proj(X, Wq, Wk, Wv, Wo, hq, hkv, hd, tp)
+    np.testing.assert_allclose(O.all_gather(ctx), ctx_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(Y, ctx_ref @ Wo, rtol=1e-11, atol=1e-11)
+
+
+def test_attn_proj_int_residual_and_explicit_ctx():
+    rng = np.random.default_rng(9)
+    H, hq, hkv, hd, T, tp = 4, 4, 2, 2, 2, 4
+    Wq, Wk, Wv = rand_ints(rng, (H, 8)), rand_ints(rng, (H, 4)), rand_ints(rng, (H, 4))
+    Wo = rand_ints(rng, (8, H))
+    X, R = rand_ints(rng, (T, H)), rand_ints(rng, (T, H))
+    ctx = [rand_ints(rng, (T, 2)) for _ in range(tp)]
+    _, _, Y = O.attn_proj(X, Wq, Wk, Wv, Wo, hq, hkv, hd, tp, ctx=ctx, residual=R)
+    full_ctx = np.concatenate(ctx, 1)
+    assert Y.tolist() == (np.array(brute_matmul(full_ctx.tolist(), Wo.tolist())) + R).tolist()
+
+
+# ---------------------------------------------------------------------------
+# 8. RMSNorm and the stack
+# ---------------------------------------------------------------------------
+
+def test_rmsnorm_values():
+    x = np.array([[3.0, 4.0]])
+    y = O.rmsnorm(x, None, eps=0.0)
+    np.testing.assert_allclose(y, [[3 / np.sqrt(12.5), 4 / np.sqrt(12.5)]], rtol=1e-15)
+    y = O.rmsnorm(x, np.array([2.0, -1.0]), eps=1e-5)
+    d = np.sqrt(12.5 + 1e-5)
+    np.testing.assert_allclose(y, [[6 / d, -4 / d]], rtol=1e-15)
+    c = np.full((1, 8), -2.5)
+    np.testing.assert_allclose(O.rmsnorm(c, None, eps=0.0), -np.ones((1, 8)), rtol=1e-15)
+
+
+def _tiny_stack(rng, H=8, I=16, hq=4, hkv=2, hd=2, V=8, layers=2):
+    f = lambda *s: rng.standard_normal(s) * 0.3
+    Ls = [dict(Wq=f(H, hq * hd), Wk=f(H, hkv * hd), Wv=f(H, hkv * hd), Wo=f(hq * hd, H),
+               Wg=f(H, I), Wu=f(H, I), Wd=f(I, H)) for _ in range(layers)]
+    return Ls, f(H, V), f(3, H)
+
+
+def test_stack_tp_invariant():
+    rng = np.random.default_rng(11)
+    Ls, Wlm, X = _tiny_stack(rng)
+    ref = O.stack_forward(X, Ls, Wlm, 1, 4, 2, 2)
+    for tp in (2, 4):
+        np.testing.assert_allclose(O.stack_forward(X, Ls, Wlm, tp, 4, 2, 2), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_stack_block_wiring_against_explicit_steps():
+    """One block written out step by step with library primitives only."""
+    rng = np.random.default_rng(12)
+    Ls, Wlm, X = _tiny_stack(rng, layers=1)
+    L = Ls[0]
+    eps = 1e-5
+    nrm = lambda x: x / np.sqrt((x ** 2).mean(-1, keepdims=True) + eps)
+    h = nrm(X)
+    V = h @ L["Wv"]
+    ctx = np.concatenate([V[:, (q // 2) * 2:(q // 2) * 2 + 2] for q in range(4)], 1)
+    x = X + ctx @ L["Wo"]
+    h = nrm(x)
+    g, u = h @ L["Wg"], h @ L["Wu"]
+    x = x + (g * expit(g) * u) @ L["Wd"]
+    ref = nrm(x) @ Wlm
+    np.testing.assert_allclose(O.stack_forward(X, Ls, Wlm, 2, 4, 2, 2), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_stack_zero_weights_is_norm_then_head():
+    rng = np.random.default_rng(13)
+    Ls, Wlm, X = _tiny_stack(rng)
+    for L in Ls:
+        for k in L:
+            L[k] = np.zeros_like(L[k])
+    out = O.stack_forward(X, Ls, Wlm, 2, 4, 2, 2)
+    np.testing.assert_allclose(out, O.rmsnorm(X) @ Wlm, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# 9. Input generator properties (the values both sides start from)
+# ---------------------------------------------------------------------------
+
+def test_input_generator_deterministic_and_bf16():
+    a = S.normal(3, (257, 129), 0.02)
+    b = S.normal(3, (257, 129), 0.02)
+    assert (a == b).all() and a.dtype == np.float32
+    assert (a.view(np.uint32) & 0xFFFF == 0).all()  # bf16-representable
+    assert abs(a.std() - 0.02) < 0.002
+    i = S.uniform_ints(0, (16, 64))
+    assert set(np.unique(i).tolist()) <= set(range(-3, 4)) and len(np.unique(i)) == 7
+
+
+def test_int_config_fits_fp32_exactly():
+    d = S.int_mlp()
+    X, W1, W2 = (d[k].astype(np.int64) for k in ("X", "W1", "W2"))
+    for tp in (1, 2):
+        _, Y = O.mlp_block(X, W1, W2, tp, "relu")
+        assert np.abs(Y).max() < 2 ** 24
+
+
+# ---------------------------------------------------------------------------
+# 10. Planted mistakes: the pins above must catch them
+# ---------------------------------------------------------------------------
+
+def test_planted_dropped_shard_is_caught(monkeypatch, golden_worked_example):
+    monkeypatch.setattr(O, "all_reduce", lambda parts: sum(parts[:-1]))
+    with pytest.raises(AssertionError):
+        test_worked_example_row_parallel(golden_worked_example)
+
+
+def test_planted_wrong_column_block_is_caught(monkeypatch):
+    def bad(W, tp):
+        n = W.shape[1] // tp
+        return [W[:, ((s + 1) % tp) * n:((s + 1) % tp + 1) * n] for s in range(tp)]
+    monkeypatch.setattr(O, "column_shards", bad)
+    with pytest.raises(AssertionError):
+        test_column_parallel_concat_equals_bruteforce(0)
+
+
+def test_planted_swapped_swiglu_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "swiglu", lambda g, u: O.silu(u) * g)
+    with pytest.raises(AssertionError):
+        test_mlp_swiglu_all_tp()
+
+
+def test_planted_bias_per_shard_is_caught(monkeypatch):
+    orig = O.all_reduce
+    monkeypatch.setattr(O, "all_reduce", lambda parts: orig(parts) + 0)
+    real_mlp = O.mlp_block
+
+    def bad_mlp(X, W1, W2, tp, act="relu", W_up=None, b1=None, b1_up=None, b2=None, residual=None):
+        Hs, Y = real_mlp(X, W1, W2, tp, act, W_up, b1, b1_up, None, residual)
+        return Hs, Y + (tp * b2.reshape(1, -1) if b2 is not None else 0)
+    monkeypatch.setattr(O, "mlp_block", bad_mlp)
+    with pytest.raises(AssertionError):
+        test_mlp_bias_once_and_residual()
+
+
+def test_planted_transposed_operand_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "linear", lambda X, W: (W.T @ X.T).T if X.shape[1] == W.shape[0] else None)
+    # (W^T X^T)^T is the same product: a correct rewrite must still pass
+    test_column_parallel_concat_equals_bruteforce(1)
+    monkeypatch.setattr(O, "linear", lambda X, W: X @ W[::-1])
+    with pytest.raises(AssertionError):
+        test_column_parallel_concat_equals_bruteforce(1)
