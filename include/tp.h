@@ -1,0 +1,292 @@
+/*
+ * tp.h - C ABI of the tensor-parallel sharded linear pipeline, B300 (sm_103a).
+ *
+ * The pipeline (a Transformer block's linears under tensor parallelism) as
+ * described on the "CUDA tensor parallel computations" learning-notes page
+ * (jokeuncle.github.io) and the "Tensor parallelism: splitting Transformer
+ * layers" tutorial (freeguideonline.com):
+ *   - a column-parallel linear splits W by output columns; shard s computes
+ *     X @ W_s from a replicated X; results are CONCATENATED (all-gather);
+ *   - a row-parallel linear splits W by input rows and X by the matching
+ *     columns; shard s computes X_s @ W_s, a contribution to the full output;
+ *     contributions are SUMMED (all-reduce) or summed and split
+ *     (reduce-scatter);
+ *   - activations, gates and biases between them are shard-local;
+ *   - the MLP is column -> local activation -> row -> sum; attention is QKV
+ *     column-split by heads (KV heads replicated when there are fewer than
+ *     tp, per the "Parallel strategies in TensorRT LLM" page), local heads,
+ *     and an O projection row-split then summed.
+ *
+ * All tp shards live in ONE device's memory. Each "communication" step is
+ * an on-device combine: a reduction folded into a GEMM accumulator, a
+ * reduction kernel, or a strided copy.
+ *
+ * Conventions for every entry point:
+ *   - Every data pointer is a DEVICE pointer owned by the caller. The
+ *     library keeps no pointer after a call returns and allocates nothing.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). Arguments are validated before anything is launched:
+ *     a validation error returns a non-zero status and leaves every output
+ *     untouched.
+ *   - Row-major layouts. Weights are given as W[K][N] ("[in, out]",
+ *     Y = X @ W). Sharded weights are stored K-major per shard (see
+ *     tp_shards).
+ *   - dtype TP_BF16: bf16 storage, fp32 accumulation, fp32 epilogue math,
+ *     one rounding to bf16 at the output. Pointers must be 16-byte aligned
+ *     and every row width (K, K/tp, N/tp, N) a multiple of 8 elements
+ *     (TP_ERR_ALIGN otherwise). Runs on tcgen05 tensor cores fed by TMA.
+ *   - dtype TP_F32: fp32 storage and FFMA arithmetic in a fixed summation
+ *     order (exact for integer-valued data whose partial sums stay below
+ *     2^24). Pointers 4-byte aligned; any widths.
+ *   - T == 0 is a valid empty call (returns TP_OK, launches nothing).
+ *   - A failed CUDA launch returns TP_ERR_CUDA. Every device-side wait is
+ *     bounded; an expired wait is reported by tp_get_error().
+ */
+#ifndef TP_B300_TP_H
+#define TP_B300_TP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+  TP_OK = 0,
+  TP_ERR_NULL = 1,        /* a required pointer is NULL */
+  TP_ERR_SHAPE = 2,       /* bad size: < 1, not divisible by tp, or mismatched */
+  TP_ERR_DTYPE = 3,       /* unknown dtype or dtypes that disagree */
+  TP_ERR_MODE = 4,        /* unknown/wrong shard mode, activation, reduce op or flag */
+  TP_ERR_ALIGN = 5,       /* pointer or row width breaks the alignment rule */
+  TP_ERR_WORKSPACE = 6,   /* workspace or output buffer too small */
+  TP_ERR_CUDA = 7,        /* a CUDA runtime/driver call failed */
+  TP_ERR_TIMEOUT = 8,     /* a bounded device-side wait expired */
+  TP_ERR_UNSUPPORTED = 9  /* valid request outside this build's limits */
+};
+
+/* Storage types. */
+enum { TP_F32 = 0, TP_BF16 = 1 };
+
+/* Shard modes ("partition dim" of the [in, out] weight). */
+enum { TP_COL = 0, TP_ROW = 1 };
+
+/* Shard-local activations (TP_ACT_SWIGLU = silu(gate) * up). */
+enum { TP_ACT_NONE = 0, TP_ACT_RELU = 1, TP_ACT_GELU = 2, TP_ACT_SILU = 3, TP_ACT_SWIGLU = 4 };
+
+/* Combine of row-parallel partials. */
+enum { TP_REDUCE_SUM = 0, TP_REDUCE_SCATTER = 1 };
+
+/*
+ * Non-owning view of sharded weights, filled in by tp_shard_weights /
+ * tp_shard_qkv. K and N are the FULL weight's in/out features.
+ *   mode TP_COL: data is [tp][N/tp][K]: shard s is W[:, s*N/tp:(s+1)*N/tp]
+ *                transposed (K contiguous). The whole buffer equals W^T.
+ *   mode TP_ROW: data is [tp][N][K/tp]: shard s is W[s*K/tp:(s+1)*K/tp, :]
+ *                transposed.
+ *   hq, hkv, hd: non-zero only for QKV views (tp_shard_qkv); then N is
+ *                tp * (hq/tp + 2*nkv) * hd, with nkv = hkv/tp if hkv >= tp,
+ *                else 1 (a replicated kv head).
+ */
+typedef struct tp_shards {
+  void* data;
+  int64_t K;
+  int64_t N;
+  int32_t tp;
+  int32_t mode;
+  int32_t dtype;
+  int32_t hq;
+  int32_t hkv;
+  int32_t hd;
+} tp_shards;
+
+/* Human-readable name of a status code. Never NULL. */
+const char* tp_status_string(int status);
+
+/* ABI version of this header (increments on incompatible change). */
+int tp_abi_version(void);
+
+/*
+ * tp_shard_weights - re-shard a full weight into tp column or row shards.
+ * Weight re-sharding and distribution, step 3 of the "AutoTP" page's
+ * automatic derivation; the split itself is the Column Parallel / Row
+ * Parallel split of the "CUDA tensor parallel computations" page.
+ *   W        [K][N] row-major, dtype `dtype`.
+ *   mode     TP_COL (N % tp == 0) or TP_ROW (K % tp == 0).
+ *   out      K*N elements; layout as in tp_shards. out_bytes is its size.
+ *   view     filled on success (may be NULL).
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE (K, N < 1 or not divisible),
+ * TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_WORKSPACE (out_bytes < K*N*elem),
+ * TP_ERR_ALIGN (bf16: K/tp, N/tp must be multiples of 8; 16-byte pointers).
+ */
+int tp_shard_weights(const void* W, int64_t K, int64_t N, int dtype, int tp, int mode, void* out,
+                     size_t out_bytes, tp_shards* view, void* stream);
+
+/*
+ * tp_shard_qkv - shard the Q, K, V projections by whole heads.
+ * QKV projection split across GPUs by attention heads ("CUDA tensor parallel
+ * computations" page, QKV projection section; tutorial page, self-attention
+ * block sharding); KV heads replicated when hkv < tp ("Parallel strategies
+ * in TensorRT LLM" page, attention tensor parallelism, GQA/MQA exception).
+ *   Wq [H][hq*hd], Wk [H][hkv*hd], Wv [H][hkv*hd], row-major.
+ *   Shard s holds q heads [s*hq/tp, (s+1)*hq/tp); kv heads [s*hkv/tp, ...)
+ *   when hkv >= tp, else the single kv head floor(s*hkv/tp). Its storage is
+ *   [Nqkv_s][H] (K-major) with rows: its q heads, then its kv heads' K
+ *   columns, then their V columns; out is [tp][Nqkv_s][H].
+ *   Requires hq % tp == 0, hq % hkv == 0, and hkv % tp == 0 (hkv >= tp) or
+ *   tp % hkv == 0 (hkv < tp).
+ * Errors as tp_shard_weights.
+ */
+int tp_shard_qkv(const void* Wq, const void* Wk, const void* Wv, int64_t H, int hq, int hkv, int hd,
+                 int tp, int dtype, void* out, size_t out_bytes, tp_shards* view, void* stream);
+
+/* Elements of tp_shard_qkv's output, or 0 if the head counts are invalid. */
+size_t tp_qkv_shard_elems(int64_t H, int hq, int hkv, int hd, int tp);
+
+/*
+ * tp_column_linear - column-parallel linear with the shard-local epilogue.
+ * Y_s = act(X @ W_s + b_s) for s = 0..tp-1 ("CUDA tensor parallel
+ * computations" page: Column Parallel, local elementwise computation).
+ *   X       [T][K], replicated input, dtype W->dtype.
+ *   W       TP_COL shards. W_up: TP_COL shards of the up projection, required
+ *           iff act == TP_ACT_SWIGLU (then Y_s = silu(X@Wg_s + b_s) *
+ *           (X@Wu_s + bu_s)), same K, N, tp, dtype.
+ *   bias    [N] or NULL (shard s uses bias[s*N/tp ...]); bias_up likewise.
+ *   concat  0: Y is [tp][T][N/tp] (each shard's own output);
+ *           1: Y is [T][N], the all-gather result, written in place.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN,
+ * TP_ERR_CUDA.
+ */
+int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shards* W_up,
+                     const void* bias, const void* bias_up, int act, int concat, void* Y,
+                     void* stream);
+
+/*
+ * tp_row_linear - row-parallel linear with the combine fused:
+ * Y = sum_{s=0..tp-1} Xs[s] @ W_s (+ bias, once) (+ residual).
+ * ("CUDA tensor parallel computations" page: Row Parallel, all-reduce.)
+ * The shard sum is accumulated in fp32 inside the GEMM; partials never
+ * reach memory.
+ *   Xs        [tp][T][K/tp] (shard s's input block), dtype W->dtype.
+ *   W         TP_ROW shards.
+ *   bias      [N] or NULL.  residual [T][N] or NULL.  Y [T][N].
+ * Errors as tp_column_linear.
+ */
+int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
+                  const void* residual, void* Y, void* stream);
+
+/*
+ * tp_row_linear_partials - the per-shard contributions P_s = Xs[s] @ W_s,
+ * kept apart ("Row Parallel": each GPU computes one contribution).
+ *   partials  [tp][T][N] fp32 (always fp32, whatever W->dtype).
+ * Errors as tp_column_linear.
+ */
+int tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float* partials,
+                           void* stream);
+
+/*
+ * tp_shard_reduce - combine row-parallel partials.
+ *   op TP_REDUCE_SUM:     out[T][N] = sum_s partials[s] (+ bias) (+ residual)
+ *                         (all-reduce: every shard's copy is this one buffer).
+ *   op TP_REDUCE_SCATTER: the same sum, read as out[tp][T/tp][N]: shard s
+ *                         keeps token rows [s*T/tp, (s+1)*T/tp). Requires
+ *                         T % tp == 0. (The split axis, tokens, is a reading:
+ *                         the page says only "sum, then split".)
+ *   The sum is taken in fp32 in shard order 0..tp-1; bias [N] is added once;
+ *   residual is [T][N]. bias, residual and out have dtype out_dtype.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN
+ * (16-byte pointers when N % 4 == 0), TP_ERR_CUDA.
+ */
+int tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op, const void* bias,
+                    const void* residual, int out_dtype, void* out, void* stream);
+
+/*
+ * tp_shard_gather - all-gather by concatenation:
+ * out[t][s*N/tp + j] = shards[s][t][j] ("Column Parallel": concatenate, do
+ * not add). shards [tp][T][N/tp], out [T][N], dtype `dtype`.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_CUDA.
+ */
+int tp_shard_gather(const void* shards, int tp, int64_t T, int64_t N, int dtype, void* out,
+                    void* stream);
+
+/* Workspace bytes tp_mlp_block needs for T tokens, hidden H, intermediate I. */
+size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype);
+
+/*
+ * tp_mlp_block - the MLP block: column -> local activation -> row -> sum
+ * ("CUDA tensor parallel computations" page, MLP section; tutorial page,
+ * MLP block sharding steps 1-4):
+ *   Hs[s] = act(X @ W1_s + b1_s)            (SwiGLU: silu(X@Wg_s+b) * (X@Wu_s+bu))
+ *   Y     = sum_s Hs[s] @ W2_s (+ b2, once) (+ residual)
+ *   X [T][H]; W1, W_up: TP_COL shards (K=H, N=I); W2: TP_ROW shards (K=I,
+ *   N=H); all the same tp and dtype. Y [T][H].
+ *   workspace: >= tp_mlp_workspace_bytes(T, H, I, tp, dtype) bytes, 256-byte
+ *   aligned; holds Hs ([tp][T][I/tp], dtype) and, for small T on bf16, the
+ *   split-K scratch of the weight-streaming path. Its contents on return are
+ *   unspecified.
+ * Errors: as tp_column_linear, plus TP_ERR_WORKSPACE.
+ */
+int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                 const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
+                 const void* residual, int act, void* workspace, size_t ws_bytes, void* Y,
+                 void* stream);
+
+/* Workspace bytes tp_attn_proj needs. */
+size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype);
+
+/*
+ * tp_attn_proj - attention projections under TP: QKV column-parallel by
+ * heads, the local attention heads, O row-parallel then summed ("CUDA tensor
+ * parallel computations" page, QKV projection, attention heads and output
+ * projection sections).
+ *   X        [T][H]. Wqkv: the view from tp_shard_qkv (K=H). Wo: TP_ROW
+ *            shards of the O projection (K = hq*hd, N = H), same tp/dtype.
+ *   ctx      [tp][T][hq/tp*hd]: the attention output of each shard's heads,
+ *            or NULL for the single-key stand-in (each query attends only to
+ *            its own token, so the context of q head h is V of its kv head).
+ *   residual [T][H] or NULL.
+ *   qkv_out  [tp][T][Nqkv_s] (each shard's q | k | v), or NULL to keep it in
+ *            the workspace.
+ *   Y        [T][H] = sum_s ctx[s] @ Wo_s (+ residual).
+ * Errors: as tp_mlp_block.
+ */
+int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
+                 const void* ctx, const void* residual, void* qkv_out, void* workspace,
+                 size_t ws_bytes, void* Y, void* stream);
+
+/*
+ * tp_rmsnorm - RMSNorm on the replicated hidden ("CUDA tensor parallel
+ * computations" page, local elementwise section: a norm is local when it
+ * runs on the replicated hidden): Y = X * gamma / sqrt(mean(X^2) + eps),
+ * fp32 statistics. X, Y [T][H]; gamma [H] or NULL (= 1).
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_CUDA.
+ */
+int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype,
+               void* Y, void* stream);
+
+/*
+ * tp_get_error - synchronise `stream`, then report and clear the device
+ * error word: TP_ERR_TIMEOUT if a kernel's bounded wait expired since the
+ * last call (that kernel's outputs are then undefined), TP_ERR_CUDA if the
+ * stream reported an error, else TP_OK.
+ */
+int tp_get_error(void* stream);
+
+/*
+ * Test hooks (synchronous; they change device-global state used by every
+ * later launch on the current device):
+ *   tp_debug_set_wait_limit_ns: limit of every bounded device wait
+ *     (default 2e9 ns).
+ *   tp_debug_inject(1): the next tensor-core GEMM launch's first block
+ *     withholds one operand load, so its consumer's wait expires and the
+ *     kernel takes its abort path. tp_debug_inject(0) disarms.
+ */
+int tp_debug_set_wait_limit_ns(uint64_t ns);
+int tp_debug_inject(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_B300_TP_H */

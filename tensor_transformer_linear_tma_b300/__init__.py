@@ -1,0 +1,292 @@
+"""Python binding of the tensor-parallel sharded linear library (libtp_b300.so).
+
+Argument marshalling only: torch tensors supply device memory and the
+current CUDA stream; each function passes pointers and sizes to the C entry
+point of the same name (declared in include/tp.h) and raises TpError on a
+non-zero status. Every step of the computation runs in the library's CUDA
+kernels. There is no CPU fallback: importing this package fails if the
+library has not been built, and the kernels need a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "TpError", "Shards", "lib", "LIB_PATH",
+    "TP_F32", "TP_BF16", "TP_COL", "TP_ROW", "ACTS", "REDUCE_OPS",
+    "tp_shard_weights", "tp_shard_qkv", "tp_qkv_shard_elems", "tp_column_linear",
+    "tp_row_linear", "tp_row_linear_partials", "tp_shard_reduce", "tp_shard_gather",
+    "tp_mlp_workspace_bytes", "tp_mlp_block", "tp_attn_workspace_bytes", "tp_attn_proj",
+    "tp_rmsnorm", "tp_get_error", "tp_debug_set_wait_limit_ns", "tp_debug_inject",
+    "tp_status_string",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp_b300.so")
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m tensor_transformer_linear_tma_b300.build`")
+lib = ctypes.CDLL(LIB_PATH)
+
+TP_F32, TP_BF16 = 0, 1
+TP_COL, TP_ROW = 0, 1
+ACTS = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "swiglu": 4}
+REDUCE_OPS = {"sum": 0, "scatter": 1}
+
+_vp, _i64, _i32, _sz, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+
+
+class TpShardsC(ctypes.Structure):
+    _fields_ = [("data", _vp), ("K", _i64), ("N", _i64), ("tp", ctypes.c_int32),
+                ("mode", ctypes.c_int32), ("dtype", ctypes.c_int32), ("hq", ctypes.c_int32),
+                ("hkv", ctypes.c_int32), ("hd", ctypes.c_int32)]
+
+
+_P = ctypes.POINTER(TpShardsC)
+_SIGS = {
+    "tp_status_string": (ctypes.c_char_p, [_i32]),
+    "tp_abi_version": (_i32, []),
+    "tp_shard_weights": (_i32, [_vp, _i64, _i64, _i32, _i32, _i32, _vp, _sz, _P, _vp]),
+    "tp_shard_qkv": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _P, _vp]),
+    "tp_qkv_shard_elems": (_sz, [_i64, _i32, _i32, _i32, _i32]),
+    "tp_column_linear": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _i32, _i32, _vp, _vp]),
+    "tp_row_linear": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp]),
+    "tp_row_linear_partials": (_i32, [_vp, _i64, _P, _vp, _vp]),
+    "tp_shard_reduce": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _i32, _vp, _vp]),
+    "tp_shard_gather": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp]),
+    "tp_mlp_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
+    "tp_mlp_block": (_i32, [_vp, _i64, _P, _P, _P, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp, _vp]),
+    "tp_attn_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
+    "tp_attn_proj": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "tp_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _f32, _i32, _vp, _vp]),
+    "tp_get_error": (_i32, [_vp]),
+    "tp_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
+    "tp_debug_inject": (_i32, [_i32]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype, _f.argtypes = _res, _args
+
+
+class TpError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: status {status} ({tp_status_string(status)})")
+
+
+def tp_status_string(status: int) -> str:
+    return lib.tp_status_string(status).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise TpError(fn, status)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return TP_BF16
+    if t.dtype == torch.float32:
+        return TP_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _torch_dt(code: int):
+    return torch.bfloat16 if code == TP_BF16 else torch.float32
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(device=None):
+    if not torch.cuda.is_available():
+        return None
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class Shards:
+    """Sharded weights: the storage tensor plus its C view (tp_shards)."""
+
+    def __init__(self, storage: torch.Tensor, view: TpShardsC):
+        self.storage = storage
+        self.view = view
+
+    @property
+    def tp(self):
+        return self.view.tp
+
+    @property
+    def K(self):
+        return self.view.K
+
+    @property
+    def N(self):
+        return self.view.N
+
+    @property
+    def shard_width(self):
+        """Output columns per shard (column mode) or N (row mode)."""
+        return self.view.N // self.view.tp if self.view.mode == TP_COL else self.view.N
+
+    def ref(self):
+        return ctypes.byref(self.view)
+
+
+def tp_shard_weights(W: torch.Tensor, tp: int, mode: str) -> Shards:
+    """Shard W [K, N] (in, out) into tp column ("col") or row ("row") shards."""
+    K, N = W.shape
+    m = TP_COL if mode == "col" else TP_ROW
+    out = torch.empty(K * N, dtype=W.dtype, device=W.device)
+    view = TpShardsC()
+    _check("tp_shard_weights", lib.tp_shard_weights(
+        _ptr(W), K, N, _dt(W), tp, m, _ptr(out), out.numel() * out.element_size(),
+        ctypes.byref(view), _stream(W.device)))
+    return Shards(out, view)
+
+
+def tp_qkv_shard_elems(H: int, hq: int, hkv: int, hd: int, tp: int) -> int:
+    return lib.tp_qkv_shard_elems(H, hq, hkv, hd, tp)
+
+
+def tp_shard_qkv(Wq, Wk, Wv, hq: int, hkv: int, hd: int, tp: int) -> Shards:
+    H = Wq.shape[0]
+    n = tp_qkv_shard_elems(H, hq, hkv, hd, tp)
+    out = torch.empty(max(n, 1), dtype=Wq.dtype, device=Wq.device)
+    view = TpShardsC()
+    _check("tp_shard_qkv", lib.tp_shard_qkv(
+        _ptr(Wq), _ptr(Wk), _ptr(Wv), H, hq, hkv, hd, tp, _dt(Wq), _ptr(out),
+        out.numel() * out.element_size(), ctypes.byref(view), _stream(Wq.device)))
+    return Shards(out, view)
+
+
+def tp_column_linear(X, W: Shards, W_up: Shards | None = None, bias=None, bias_up=None,
+                     act: str = "none", concat: bool = False, out=None):
+    """Column-parallel linear; returns [tp, T, N/tp] or, with concat, [T, N]."""
+    T = X.shape[0]
+    Ns = W.shard_width
+    if out is None:
+        shape = (T, W.N) if concat else (W.tp, T, Ns)
+        out = torch.empty(shape, dtype=X.dtype, device=X.device)
+    _check("tp_column_linear", lib.tp_column_linear(
+        _ptr(X), T, W.ref(), W_up.ref() if W_up is not None else None, _ptr(bias), _ptr(bias_up),
+        ACTS[act], int(concat), _ptr(out), _stream(X.device)))
+    return out
+
+
+def tp_row_linear(Xs, W: Shards, bias=None, residual=None, out=None):
+    """Row-parallel linear with the shard sum fused; Xs is [tp, T, K/tp]."""
+    T = Xs.shape[1]
+    if out is None:
+        out = torch.empty((T, W.N), dtype=Xs.dtype, device=Xs.device)
+    _check("tp_row_linear", lib.tp_row_linear(
+        _ptr(Xs), T, W.ref(), _ptr(bias), _ptr(residual), _ptr(out), _stream(Xs.device)))
+    return out
+
+
+def tp_row_linear_partials(Xs, W: Shards, out=None):
+    """Per-shard fp32 contributions [tp, T, N]."""
+    T = Xs.shape[1]
+    if out is None:
+        out = torch.empty((W.tp, T, W.N), dtype=torch.float32, device=Xs.device)
+    _check("tp_row_linear_partials", lib.tp_row_linear_partials(
+        _ptr(Xs), T, W.ref(), _ptr(out), _stream(Xs.device)))
+    return out
+
+
+def tp_shard_reduce(partials, op: str = "sum", bias=None, residual=None, out_dtype=None, out=None):
+    """Sum [tp, T, N] fp32 partials; "scatter" returns the [tp, T/tp, N] view."""
+    tp, T, N = partials.shape
+    odt = out_dtype if out_dtype is not None else (out.dtype if out is not None else torch.float32)
+    if out is None:
+        out = torch.empty((T, N), dtype=odt, device=partials.device)
+    _check("tp_shard_reduce", lib.tp_shard_reduce(
+        _ptr(partials), tp, T, N, REDUCE_OPS[op], _ptr(bias), _ptr(residual),
+        TP_BF16 if odt == torch.bfloat16 else TP_F32, _ptr(out), _stream(partials.device)))
+    return out.view(tp, T // tp, N) if op == "scatter" else out
+
+
+def tp_shard_gather(shards, out=None):
+    """Concatenate [tp, T, N/tp] shards into [T, N]."""
+    tp, T, Ns = shards.shape
+    if out is None:
+        out = torch.empty((T, tp * Ns), dtype=shards.dtype, device=shards.device)
+    _check("tp_shard_gather", lib.tp_shard_gather(
+        _ptr(shards), tp, T, tp * Ns, _dt(shards), _ptr(out), _stream(shards.device)))
+    return out
+
+
+def tp_mlp_workspace_bytes(T: int, H: int, I: int, tp: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (TP_BF16 if dtype == torch.bfloat16 else TP_F32)
+    return lib.tp_mlp_workspace_bytes(T, H, I, tp, code)
+
+
+def _workspace(nbytes: int, device):
+    # 256-byte aligned by the caching allocator; at least one element
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def tp_mlp_block(X, W1: Shards, W2: Shards, W_up: Shards | None = None, b1=None, b1_up=None,
+                 b2=None, residual=None, act: str = "relu", workspace=None, out=None):
+    """column -> local activation -> row -> sum; returns Y [T, H]."""
+    T, H = X.shape
+    need = tp_mlp_workspace_bytes(T, H, W1.N, W1.tp, _dt(X))
+    if workspace is None:
+        workspace = _workspace(need, X.device)
+    if out is None:
+        out = torch.empty((T, W2.N), dtype=X.dtype, device=X.device)
+    _check("tp_mlp_block", lib.tp_mlp_block(
+        _ptr(X), T, W1.ref(), W_up.ref() if W_up is not None else None, W2.ref(), _ptr(b1),
+        _ptr(b1_up), _ptr(b2), _ptr(residual), ACTS[act], _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _stream(X.device)))
+    return out
+
+
+def tp_attn_workspace_bytes(T: int, hq: int, hkv: int, hd: int, tp: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (TP_BF16 if dtype == torch.bfloat16 else TP_F32)
+    return lib.tp_attn_workspace_bytes(T, hq, hkv, hd, tp, code)
+
+
+def tp_attn_proj(X, Wqkv: Shards, Wo: Shards, ctx=None, residual=None, qkv_out=None,
+                 workspace=None, out=None):
+    """QKV by heads -> local heads (ctx, or the single-key stand-in) -> O + sum."""
+    T = X.shape[0]
+    v = Wqkv.view
+    need = tp_attn_workspace_bytes(T, v.hq, v.hkv, v.hd, v.tp, _dt(X))
+    if workspace is None:
+        workspace = _workspace(need, X.device)
+    if out is None:
+        out = torch.empty((T, Wo.N), dtype=X.dtype, device=X.device)
+    _check("tp_attn_proj", lib.tp_attn_proj(
+        _ptr(X), T, Wqkv.ref(), Wo.ref(), _ptr(ctx), _ptr(residual), _ptr(qkv_out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _stream(X.device)))
+    return out
+
+
+def tp_rmsnorm(X, gamma=None, eps: float = 1e-5, out=None):
+    T, H = X.shape
+    if out is None:
+        out = torch.empty_like(X)
+    _check("tp_rmsnorm", lib.tp_rmsnorm(
+        _ptr(X), _ptr(gamma), T, H, eps, _dt(X), _ptr(out), _stream(X.device)))
+    return out
+
+
+def tp_get_error(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device status."""
+    return lib.tp_get_error(_stream(device))
+
+
+def tp_debug_set_wait_limit_ns(ns: int) -> None:
+    _check("tp_debug_set_wait_limit_ns", lib.tp_debug_set_wait_limit_ns(ns))
+
+
+def tp_debug_inject(kind: int) -> None:
+    _check("tp_debug_inject", lib.tp_debug_inject(kind))

@@ -1,0 +1,609 @@
+// C ABI of the tensor-parallel sharded linear pipeline (declared in tp.h).
+//
+// Each entry point validates its arguments on the host (no CUDA call before
+// validation passes), then launches the kernels of its step on the caller's
+// stream. Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+
+#include "tp.h"
+#include "tp_elementwise.cuh"
+#include "tp_gemm_tc.cuh"
+#include "tp_simt.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------------------
+// Host helpers
+// ---------------------------------------------------------------------------
+inline size_t elem_size(int dtype) { return dtype == TP_BF16 ? 2 : 4; }
+inline bool dtype_ok(int dtype) { return dtype == TP_F32 || dtype == TP_BF16; }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Pointer alignment each dtype path needs (bf16 feeds TMA / 16-byte vectors).
+inline bool ptr_ok(const void* p, int dtype) {
+  return p == nullptr || aligned(p, dtype == TP_BF16 ? 16 : 4);
+}
+
+int launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+int num_sms() {
+  static int cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 128) return 0;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+int grid_for(int64_t work, int threads) {
+  const int sms = std::max(1, num_sms());
+  const int64_t want = cdiv(std::max<int64_t>(work, 1), threads);
+  return static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 16));
+}
+
+// --- TMA tensor maps ---------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D bf16 map over [d2][d1][d0] (d0 contiguous), box {64, box1, 1}, 128-byte
+// swizzle, zero fill outside the tensor.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint32_t box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {64, box1, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// --- shard-view checks -------------------------------------------------------
+int check_view(const tp_shards* W, int mode) {
+  if (!W || !W->data) return TP_ERR_NULL;
+  if (W->mode != mode) return TP_ERR_MODE;
+  if (!dtype_ok(W->dtype)) return TP_ERR_DTYPE;
+  if (W->tp < 1 || W->K < 1 || W->N < 1) return TP_ERR_SHAPE;
+  if (mode == TP_COL && W->N % W->tp != 0) return TP_ERR_SHAPE;
+  if (mode == TP_ROW && W->K % W->tp != 0) return TP_ERR_SHAPE;
+  if (W->K > INT32_MAX || W->N > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  if (W->dtype == TP_BF16) {
+    const int64_t inner = mode == TP_COL ? W->K : W->K / W->tp;
+    const int64_t outw = mode == TP_COL ? W->N / W->tp : W->N;
+    if (inner % 8 != 0 || outw % 8 != 0 || !aligned(W->data, 16)) return TP_ERR_ALIGN;
+  } else if (!aligned(W->data, 4)) {
+    return TP_ERR_ALIGN;
+  }
+  return TP_OK;
+}
+
+bool same_shape(const tp_shards* a, const tp_shards* b) {
+  return a->K == b->K && a->N == b->N && a->tp == b->tp && a->mode == b->mode && a->dtype == b->dtype;
+}
+
+// ---------------------------------------------------------------------------
+// GEMM launchers
+// ---------------------------------------------------------------------------
+template <int KIND>
+int tc_launch(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
+              const tpk::TcArgs& args, cudaStream_t st) {
+  if (args.num_tiles <= 0) return TP_OK;
+  if (cudaFuncSetAttribute(tpk::tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           tpk::TC_SMEM_BYTES) != cudaSuccess)
+    return TP_ERR_CUDA;
+  const int grid = std::min(args.num_tiles, std::max(1, num_sms()));
+  tpk::tc_gemm_kernel<KIND><<<grid, tpk::TC_THREADS, tpk::TC_SMEM_BYTES, st>>>(ma, mb0, mb1, args);
+  return launch_status();
+}
+
+// Column-parallel bf16 GEMM on the tensor cores. Y layout per `concat`.
+int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
+             const void* bias_up, int act, int concat, void* Y, cudaStream_t st) {
+  const int tp = W->tp;
+  const int64_t K = W->K, Ns = W->N / tp;
+  const bool swiglu = act == TP_ACT_SWIGLU;
+  CUtensorMap ma, mb0, mb1;
+  if (!make_map_bf16(&ma, X, K, T, 1, tpk::TC_BM)) return TP_ERR_CUDA;
+  if (!make_map_bf16(&mb0, W->data, K, Ns, tp, swiglu ? tpk::TC_BN / 2 : tpk::TC_BN)) return TP_ERR_CUDA;
+  if (swiglu) {
+    if (!make_map_bf16(&mb1, Wu->data, K, Ns, tp, tpk::TC_BN / 2)) return TP_ERR_CUDA;
+  } else {
+    mb1 = mb0;
+  }
+  tpk::TcArgs a{};
+  a.M = static_cast<int>(T);
+  a.Ns = static_cast<int>(Ns);
+  a.tp = tp;
+  a.m_tiles = static_cast<int>(cdiv(T, tpk::TC_BM));
+  a.n_tiles = static_cast<int>(cdiv(Ns, swiglu ? tpk::TC_BN / 2 : tpk::TC_BN));
+  a.s_tiles = tp;
+  a.num_tiles = a.m_tiles * a.n_tiles * a.s_tiles;
+  a.kb_per_shard = static_cast<int>(cdiv(K, tpk::TC_BK));
+  a.k_shards = 1;
+  a.act = act;
+  a.out_concat = concat;
+  a.bias = static_cast<const bf16*>(bias);
+  a.bias_up = static_cast<const bf16*>(bias_up);
+  a.out = Y;
+  return swiglu ? tc_launch<tpk::TC_COL_SWIGLU>(ma, mb0, mb1, a, st)
+                : tc_launch<tpk::TC_COL>(ma, mb0, mb1, a, st);
+}
+
+// Row-parallel bf16 GEMM: fused shard sum (partials == nullptr) or per-shard
+// fp32 partials.
+int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
+             void* Y, float* partials, cudaStream_t st) {
+  const int tp = W->tp;
+  const int64_t Ks = W->K / tp, N = W->N;
+  CUtensorMap ma, mb;
+  if (!make_map_bf16(&ma, Xs, Ks, T, tp, tpk::TC_BM)) return TP_ERR_CUDA;
+  if (!make_map_bf16(&mb, W->data, Ks, N, tp, tpk::TC_BN)) return TP_ERR_CUDA;
+  tpk::TcArgs a{};
+  a.M = static_cast<int>(T);
+  a.Ns = static_cast<int>(N);
+  a.tp = tp;
+  a.m_tiles = static_cast<int>(cdiv(T, tpk::TC_BM));
+  a.n_tiles = static_cast<int>(cdiv(N, tpk::TC_BN));
+  a.kb_per_shard = static_cast<int>(cdiv(Ks, tpk::TC_BK));
+  a.bias = static_cast<const bf16*>(bias);
+  a.residual = static_cast<const bf16*>(residual);
+  if (partials) {
+    a.s_tiles = tp;
+    a.k_shards = 1;
+    a.out = partials;
+    a.num_tiles = a.m_tiles * a.n_tiles * a.s_tiles;
+    return tc_launch<tpk::TC_ROW_PARTIAL>(ma, mb, mb, a, st);
+  }
+  a.s_tiles = 1;
+  a.k_shards = tp;
+  a.out = Y;
+  a.num_tiles = a.m_tiles * a.n_tiles;
+  return tc_launch<tpk::TC_ROW_SUM>(ma, mb, mb, a, st);
+}
+
+template <int KIND>
+int simt_launch(const tpk::SimtArgs& a, int s_tiles, cudaStream_t st) {
+  const dim3 grid(static_cast<unsigned>(cdiv(a.Ns, tpk::SK_BN)), static_cast<unsigned>(cdiv(a.M, tpk::SK_BM)),
+                  static_cast<unsigned>(s_tiles));
+  tpk::simt_gemm_kernel<KIND><<<grid, tpk::SK_THREADS, 0, st>>>(a);
+  return launch_status();
+}
+
+int col_f32(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
+            const void* bias_up, int act, int concat, void* Y, cudaStream_t st) {
+  tpk::SimtArgs a{};
+  a.M = static_cast<int>(T);
+  a.Ns = static_cast<int>(W->N / W->tp);
+  a.Ks = static_cast<int>(W->K);
+  a.tp = W->tp;
+  a.k_shards = 1;
+  a.act = act;
+  a.out_concat = concat;
+  a.A = static_cast<const float*>(X);
+  a.a_shard_stride = 0;
+  a.B0 = static_cast<const float*>(W->data);
+  a.B1 = Wu ? static_cast<const float*>(Wu->data) : nullptr;
+  a.bias = static_cast<const float*>(bias);
+  a.bias_up = static_cast<const float*>(bias_up);
+  a.out = static_cast<float*>(Y);
+  return act == TP_ACT_SWIGLU ? simt_launch<tpk::SK_COL_SWIGLU>(a, W->tp, st)
+                              : simt_launch<tpk::SK_COL>(a, W->tp, st);
+}
+
+int row_f32(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
+            void* Y, float* partials, cudaStream_t st) {
+  tpk::SimtArgs a{};
+  a.M = static_cast<int>(T);
+  a.Ns = static_cast<int>(W->N);
+  a.Ks = static_cast<int>(W->K / W->tp);
+  a.tp = W->tp;
+  a.A = static_cast<const float*>(Xs);
+  a.a_shard_stride = T * a.Ks;
+  a.B0 = static_cast<const float*>(W->data);
+  a.bias = static_cast<const float*>(bias);
+  a.residual = static_cast<const float*>(residual);
+  if (partials) {
+    a.k_shards = 1;
+    a.out = partials;
+    return simt_launch<tpk::SK_ROW_PARTIAL>(a, W->tp, st);
+  }
+  a.k_shards = W->tp;
+  a.out = static_cast<float*>(Y);
+  return simt_launch<tpk::SK_ROW_SUM>(a, 1, st);
+}
+
+// Shared validation of a column-linear request.
+int check_col(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
+              const void* bias_up, int act, int concat, const void* Y) {
+  if ((!X || !Y) && T != 0) return TP_ERR_NULL;  // an empty call may pass empty (null) buffers
+  int r = check_view(W, TP_COL);
+  if (r) return r;
+  if (T < 0) return TP_ERR_SHAPE;
+  if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  if (act < TP_ACT_NONE || act > TP_ACT_SWIGLU) return TP_ERR_MODE;
+  if (concat != 0 && concat != 1) return TP_ERR_MODE;
+  if (act == TP_ACT_SWIGLU) {
+    if (!Wu) return TP_ERR_NULL;
+    if ((r = check_view(Wu, TP_COL))) return r;
+    if (!same_shape(W, Wu)) return TP_ERR_SHAPE;
+  } else if (Wu || bias_up) {
+    return TP_ERR_MODE;
+  }
+  const int dt = W->dtype;
+  if (!ptr_ok(X, dt) || !ptr_ok(Y, dt) || !ptr_ok(bias, dt) || !ptr_ok(bias_up, dt)) return TP_ERR_ALIGN;
+  return TP_OK;
+}
+
+int check_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
+              const void* out, int out_dt) {
+  if ((!Xs || !out) && T != 0) return TP_ERR_NULL;
+  int r = check_view(W, TP_ROW);
+  if (r) return r;
+  if (T < 0) return TP_ERR_SHAPE;
+  if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  const int dt = W->dtype;
+  if (!ptr_ok(Xs, dt) || !ptr_ok(bias, dt) || !ptr_ok(residual, dt) || !ptr_ok(out, out_dt))
+    return TP_ERR_ALIGN;
+  return TP_OK;
+}
+
+int run_col(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
+            const void* bias_up, int act, int concat, void* Y, cudaStream_t st) {
+  if (T == 0) return TP_OK;
+  return W->dtype == TP_BF16 ? col_bf16(X, T, W, Wu, bias, bias_up, act, concat, Y, st)
+                             : col_f32(X, T, W, Wu, bias, bias_up, act, concat, Y, st);
+}
+
+int run_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
+            void* Y, float* partials, cudaStream_t st) {
+  if (T == 0) return TP_OK;
+  return W->dtype == TP_BF16 ? row_bf16(Xs, T, W, bias, residual, Y, partials, st)
+                             : row_f32(Xs, T, W, bias, residual, Y, partials, st);
+}
+
+}  // namespace
+
+// ===========================================================================
+// Exported C ABI
+// ===========================================================================
+extern "C" {
+
+const char* tp_status_string(int s) {
+  switch (s) {
+    case TP_OK: return "ok";
+    case TP_ERR_NULL: return "null pointer";
+    case TP_ERR_SHAPE: return "bad shape (size < 1, not divisible by tp, or mismatched)";
+    case TP_ERR_DTYPE: return "bad or mismatched dtype";
+    case TP_ERR_MODE: return "bad mode, activation, reduce op or flag";
+    case TP_ERR_ALIGN: return "alignment rule broken (bf16: 16-byte pointers, widths % 8)";
+    case TP_ERR_WORKSPACE: return "workspace or output buffer too small";
+    case TP_ERR_CUDA: return "CUDA error";
+    case TP_ERR_TIMEOUT: return "bounded device wait expired";
+    case TP_ERR_UNSUPPORTED: return "unsupported size";
+    default: return "unknown status";
+  }
+}
+
+int tp_abi_version(void) { return 1; }
+
+int tp_shard_weights(const void* W, int64_t K, int64_t N, int dtype, int tp, int mode, void* out,
+                     size_t out_bytes, tp_shards* view, void* stream) {
+  if (!W || !out) return TP_ERR_NULL;
+  if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
+  if (mode != TP_COL && mode != TP_ROW) return TP_ERR_MODE;
+  if (tp < 1 || K < 1 || N < 1) return TP_ERR_SHAPE;
+  if ((mode == TP_COL && N % tp) || (mode == TP_ROW && K % tp)) return TP_ERR_SHAPE;
+  if (K > INT32_MAX || N > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  const size_t need = static_cast<size_t>(K) * static_cast<size_t>(N) * elem_size(dtype);
+  if (out_bytes < need) return TP_ERR_WORKSPACE;
+  if (dtype == TP_BF16) {
+    const int64_t inner = mode == TP_COL ? K : K / tp, outw = mode == TP_COL ? N / tp : N;
+    if (inner % 8 || outw % 8 || !aligned(W, 16) || !aligned(out, 16)) return TP_ERR_ALIGN;
+  } else if (!aligned(W, 4) || !aligned(out, 4)) {
+    return TP_ERR_ALIGN;
+  }
+  const dim3 grid(static_cast<unsigned>(cdiv(N, 32)), static_cast<unsigned>(cdiv(K, 32)));
+  const int64_t Ks = mode == TP_ROW ? K / tp : K;
+  if (dtype == TP_BF16)
+    tpk::shard_weights_kernel<bf16><<<grid, 256, 0, as_stream(stream)>>>(
+        static_cast<const bf16*>(W), K, N, Ks, mode == TP_ROW, static_cast<bf16*>(out));
+  else
+    tpk::shard_weights_kernel<float><<<grid, 256, 0, as_stream(stream)>>>(
+        static_cast<const float*>(W), K, N, Ks, mode == TP_ROW, static_cast<float*>(out));
+  const int r = launch_status();
+  if (r == TP_OK && view) {
+    *view = tp_shards{};
+    view->data = out;
+    view->K = K;
+    view->N = N;
+    view->tp = tp;
+    view->mode = mode;
+    view->dtype = dtype;
+  }
+  return r;
+}
+
+size_t tp_qkv_shard_elems(int64_t H, int hq, int hkv, int hd, int tp) {
+  if (H < 1 || hq < 1 || hkv < 1 || hd < 1 || tp < 1) return 0;
+  if (hq % tp || hq % hkv) return 0;
+  if (hkv >= tp ? (hkv % tp != 0) : (tp % hkv != 0)) return 0;
+  const int64_t nkv = hkv >= tp ? hkv / tp : 1;
+  return static_cast<size_t>(tp) * static_cast<size_t>((hq / tp + 2 * nkv) * hd) * static_cast<size_t>(H);
+}
+
+int tp_shard_qkv(const void* Wq, const void* Wk, const void* Wv, int64_t H, int hq, int hkv, int hd,
+                 int tp, int dtype, void* out, size_t out_bytes, tp_shards* view, void* stream) {
+  if (!Wq || !Wk || !Wv || !out) return TP_ERR_NULL;
+  if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
+  const size_t elems = tp_qkv_shard_elems(H, hq, hkv, hd, tp);
+  if (elems == 0) return TP_ERR_SHAPE;
+  if (H > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  if (out_bytes < elems * elem_size(dtype)) return TP_ERR_WORKSPACE;
+  const int64_t nkv = hkv >= tp ? hkv / tp : 1;
+  const int64_t Ns = (hq / tp + 2 * nkv) * hd;
+  if (dtype == TP_BF16) {
+    if (H % 8 || Ns % 8 || hd % 8) return TP_ERR_ALIGN;
+    for (const void* p : {Wq, Wk, Wv, static_cast<const void*>(out)})
+      if (!aligned(p, 16)) return TP_ERR_ALIGN;
+  } else {
+    for (const void* p : {Wq, Wk, Wv, static_cast<const void*>(out)})
+      if (!aligned(p, 4)) return TP_ERR_ALIGN;
+  }
+  const dim3 grid(static_cast<unsigned>(cdiv(Ns, 32)), static_cast<unsigned>(cdiv(H, 32)),
+                  static_cast<unsigned>(tp));
+  if (dtype == TP_BF16)
+    tpk::shard_qkv_kernel<bf16><<<grid, 256, 0, as_stream(stream)>>>(
+        static_cast<const bf16*>(Wq), static_cast<const bf16*>(Wk), static_cast<const bf16*>(Wv), H,
+        hq, hkv, hd, tp, static_cast<bf16*>(out));
+  else
+    tpk::shard_qkv_kernel<float><<<grid, 256, 0, as_stream(stream)>>>(
+        static_cast<const float*>(Wq), static_cast<const float*>(Wk), static_cast<const float*>(Wv),
+        H, hq, hkv, hd, tp, static_cast<float*>(out));
+  const int r = launch_status();
+  if (r == TP_OK && view) {
+    *view = tp_shards{};
+    view->data = out;
+    view->K = H;
+    view->N = tp * Ns;
+    view->tp = tp;
+    view->mode = TP_COL;
+    view->dtype = dtype;
+    view->hq = hq;
+    view->hkv = hkv;
+    view->hd = hd;
+  }
+  return r;
+}
+
+int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shards* W_up,
+                     const void* bias, const void* bias_up, int act, int concat, void* Y,
+                     void* stream) {
+  const int r = check_col(X, T, W, W_up, bias, bias_up, act, concat, Y);
+  if (r) return r;
+  return run_col(X, T, W, W_up, bias, bias_up, act, concat, Y, as_stream(stream));
+}
+
+int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
+                  const void* residual, void* Y, void* stream) {
+  const int r = check_row(Xs, T, W, bias, residual, Y, W ? W->dtype : TP_F32);
+  if (r) return r;
+  return run_row(Xs, T, W, bias, residual, Y, nullptr, as_stream(stream));
+}
+
+int tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float* partials,
+                           void* stream) {
+  const int r = check_row(Xs, T, W, nullptr, nullptr, partials, TP_BF16);
+  if (r) return r;
+  return run_row(Xs, T, W, nullptr, nullptr, nullptr, partials, as_stream(stream));
+}
+
+int tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op, const void* bias,
+                    const void* residual, int out_dtype, void* out, void* stream) {
+  if (!partials || !out) return TP_ERR_NULL;
+  if (op != TP_REDUCE_SUM && op != TP_REDUCE_SCATTER) return TP_ERR_MODE;
+  if (!dtype_ok(out_dtype)) return TP_ERR_DTYPE;
+  if (tp < 1 || T < 0 || N < 1) return TP_ERR_SHAPE;
+  if (op == TP_REDUCE_SCATTER && T % tp) return TP_ERR_SHAPE;
+  if (T == 0) return TP_OK;
+  const bool vec = (N % 4 == 0);
+  if (vec) {
+    if (!aligned(partials, 16)) return TP_ERR_ALIGN;
+  } else if (!aligned(partials, 4)) {
+    return TP_ERR_ALIGN;
+  }
+  for (const void* p : {bias, residual, static_cast<const void*>(out)})
+    if (p && !aligned(p, elem_size(out_dtype))) return TP_ERR_ALIGN;
+  const cudaStream_t st = as_stream(stream);
+  const int64_t work = vec ? T * N / 4 : T * N;
+  const int grid = grid_for(work, 256);
+  if (out_dtype == TP_BF16) {
+    auto b = static_cast<const bf16*>(bias);
+    auto rr = static_cast<const bf16*>(residual);
+    auto o = static_cast<bf16*>(out);
+    if (vec) tpk::reduce_kernel<bf16><<<grid, 256, 0, st>>>(partials, tp, T, N, b, rr, o);
+    else tpk::reduce_kernel_scalar<bf16><<<grid, 256, 0, st>>>(partials, tp, T, N, b, rr, o);
+  } else {
+    auto b = static_cast<const float*>(bias);
+    auto rr = static_cast<const float*>(residual);
+    auto o = static_cast<float*>(out);
+    if (vec) tpk::reduce_kernel<float><<<grid, 256, 0, st>>>(partials, tp, T, N, b, rr, o);
+    else tpk::reduce_kernel_scalar<float><<<grid, 256, 0, st>>>(partials, tp, T, N, b, rr, o);
+  }
+  return launch_status();
+}
+
+int tp_shard_gather(const void* shards, int tp, int64_t T, int64_t N, int dtype, void* out,
+                    void* stream) {
+  if (!shards || !out) return TP_ERR_NULL;
+  if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
+  if (tp < 1 || T < 0 || N < 1 || N % tp) return TP_ERR_SHAPE;
+  if (T == 0) return TP_OK;
+  const int64_t Ns = N / tp;
+  const size_t es = elem_size(dtype);
+  const bool vec = (Ns * es) % 16 == 0 && aligned(shards, 16) && aligned(out, 16);
+  if (!aligned(shards, es) || !aligned(out, es)) return TP_ERR_ALIGN;
+  const cudaStream_t st = as_stream(stream);
+  if (dtype == TP_BF16) {
+    auto in = static_cast<const bf16*>(shards);
+    auto o = static_cast<bf16*>(out);
+    if (vec) tpk::gather_kernel<bf16, 8><<<grid_for(tp * T * Ns / 8, 256), 256, 0, st>>>(in, tp, T, Ns, o);
+    else tpk::gather_kernel<bf16, 1><<<grid_for(tp * T * Ns, 256), 256, 0, st>>>(in, tp, T, Ns, o);
+  } else {
+    auto in = static_cast<const float*>(shards);
+    auto o = static_cast<float*>(out);
+    if (vec) tpk::gather_kernel<float, 4><<<grid_for(tp * T * Ns / 4, 256), 256, 0, st>>>(in, tp, T, Ns, o);
+    else tpk::gather_kernel<float, 1><<<grid_for(tp * T * Ns, 256), 256, 0, st>>>(in, tp, T, Ns, o);
+  }
+  return launch_status();
+}
+
+size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype) {
+  if (T < 0 || H < 1 || I < 1 || tp < 1 || !dtype_ok(dtype)) return 0;
+  return align256(static_cast<size_t>(T) * static_cast<size_t>(I) * elem_size(dtype));
+}
+
+int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                 const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
+                 const void* residual, int act, void* workspace, size_t ws_bytes, void* Y,
+                 void* stream) {
+  if (!workspace || !W2) return TP_ERR_NULL;
+  int r = check_col(X, T, W1, W_up, b1, b1_up, act, 0, Y);
+  if (r) return r;
+  if ((r = check_view(W2, TP_ROW))) return r;
+  if (W2->dtype != W1->dtype) return TP_ERR_DTYPE;
+  if (W2->tp != W1->tp || W2->K != W1->N || W2->N != W1->K) return TP_ERR_SHAPE;
+  const int dt = W1->dtype;
+  if (!ptr_ok(b2, dt) || !ptr_ok(residual, dt) || !aligned(workspace, 256)) return TP_ERR_ALIGN;
+  if (ws_bytes < tp_mlp_workspace_bytes(T, W1->K, W1->N, W1->tp, dt)) return TP_ERR_WORKSPACE;
+  if (T == 0) return TP_OK;
+  const cudaStream_t st = as_stream(stream);
+  void* Hs = workspace;  // [tp][T][I/tp]
+  if ((r = run_col(X, T, W1, W_up, b1, b1_up, act, 0, Hs, st))) return r;
+  return run_row(Hs, T, W2, b2, residual, Y, nullptr, st);
+}
+
+size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype) {
+  if (T < 0 || !dtype_ok(dtype)) return 0;
+  const size_t qkv = tp_qkv_shard_elems(1, hq, hkv, hd, tp);  // per token, all shards
+  if (qkv == 0) return 0;
+  const size_t es = elem_size(dtype);
+  const size_t ctx = static_cast<size_t>(hq) * hd;  // per token, all shards
+  return align256(static_cast<size_t>(T) * qkv * es) + align256(static_cast<size_t>(T) * ctx * es);
+}
+
+int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
+                 const void* ctx, const void* residual, void* qkv_out, void* workspace,
+                 size_t ws_bytes, void* Y, void* stream) {
+  if (!workspace || !Wo || !Wqkv) return TP_ERR_NULL;
+  int r = check_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, Y);
+  if (r) return r;
+  if (Wqkv->hd < 1 || Wqkv->hq < 1 || Wqkv->hkv < 1) return TP_ERR_MODE;  // not a QKV view
+  const int tp = Wqkv->tp, hq = Wqkv->hq, hkv = Wqkv->hkv, hd = Wqkv->hd;
+  if (tp_qkv_shard_elems(Wqkv->K, hq, hkv, hd, tp) != static_cast<size_t>(Wqkv->K) * Wqkv->N)
+    return TP_ERR_SHAPE;
+  if ((r = check_view(Wo, TP_ROW))) return r;
+  if (Wo->dtype != Wqkv->dtype) return TP_ERR_DTYPE;
+  if (Wo->tp != tp || Wo->K != static_cast<int64_t>(hq) * hd || Wo->N != Wqkv->K) return TP_ERR_SHAPE;
+  const int dt = Wqkv->dtype;
+  if (!ptr_ok(ctx, dt) || !ptr_ok(residual, dt) || !ptr_ok(qkv_out, dt) || !aligned(workspace, 256))
+    return TP_ERR_ALIGN;
+  if (dt == TP_BF16 && hd % 8) return TP_ERR_ALIGN;
+  if (ws_bytes < tp_attn_workspace_bytes(T, hq, hkv, hd, tp, dt)) return TP_ERR_WORKSPACE;
+  if (T == 0) return TP_OK;
+  const cudaStream_t st = as_stream(stream);
+  const size_t es = elem_size(dt);
+  const size_t qkv_bytes = align256(static_cast<size_t>(T) * tp_qkv_shard_elems(1, hq, hkv, hd, tp) * es);
+  void* qkv = qkv_out ? qkv_out : workspace;
+  void* ctx_ws = static_cast<char*>(workspace) + qkv_bytes;
+  if ((r = run_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, qkv, st))) return r;
+  if (!ctx) {
+    const int64_t total = static_cast<int64_t>(tp) * T * (hq / tp) * hd / 8;
+    if (dt == TP_BF16)
+      tpk::ctx_standin_kernel<bf16><<<grid_for(total, 256), 256, 0, st>>>(
+          static_cast<const bf16*>(qkv), tp, T, hq, hkv, hd, static_cast<bf16*>(ctx_ws));
+    else
+      tpk::ctx_standin_kernel<float><<<grid_for(total, 256), 256, 0, st>>>(
+          static_cast<const float*>(qkv), tp, T, hq, hkv, hd, static_cast<float*>(ctx_ws));
+    if ((r = launch_status())) return r;
+    ctx = ctx_ws;
+  }
+  return run_row(ctx, T, Wo, nullptr, residual, Y, nullptr, st);
+}
+
+int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
+               void* stream) {
+  if (!X || !Y) return TP_ERR_NULL;
+  if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
+  if (T < 0 || H < 1 || !(eps >= 0.0f)) return TP_ERR_SHAPE;
+  if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  const size_t es = elem_size(dtype);
+  for (const void* p : {X, gamma, static_cast<const void*>(Y)})
+    if (p && !aligned(p, es)) return TP_ERR_ALIGN;
+  if (T == 0) return TP_OK;
+  const cudaStream_t st = as_stream(stream);
+  if (dtype == TP_BF16)
+    tpk::rmsnorm_kernel<bf16><<<static_cast<unsigned>(T), 256, 0, st>>>(
+        static_cast<const bf16*>(X), static_cast<const bf16*>(gamma), H, eps, static_cast<bf16*>(Y));
+  else
+    tpk::rmsnorm_kernel<float><<<static_cast<unsigned>(T), 256, 0, st>>>(
+        static_cast<const float*>(X), static_cast<const float*>(gamma), H, eps, static_cast<float*>(Y));
+  return launch_status();
+}
+
+int tp_get_error(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return TP_ERR_CUDA;
+  int err = 0;
+  if (cudaMemcpyFromSymbol(&err, tpk::g_tp_error, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
+  if (err != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(tpk::g_tp_error, &zero, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
+    return err == tpk::TP_DEVERR_WAIT_TIMEOUT ? TP_ERR_TIMEOUT : TP_ERR_CUDA;
+  }
+  return TP_OK;
+}
+
+int tp_debug_set_wait_limit_ns(uint64_t ns) {
+  const unsigned long long v = ns;
+  return cudaMemcpyToSymbol(tpk::g_tp_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+int tp_debug_inject(int kind) {
+  if (kind < 0 || kind > 1) return TP_ERR_MODE;
+  return cudaMemcpyToSymbol(tpk::g_tp_inject, &kind, sizeof(int)) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // extern "C"

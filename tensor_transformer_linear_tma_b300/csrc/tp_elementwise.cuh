@@ -1,0 +1,226 @@
+// Memory-bound kernels of the pipeline: weight sharding, the on-device
+// combines (concatenation = all-gather, sum = all-reduce, reduce-scatter),
+// RMSNorm on the replicated hidden, and the attention-context stand-in.
+#pragma once
+
+#include "tp_epilogue.cuh"
+
+namespace tpk {
+
+// ---------------------------------------------------------------------------
+// Weight sharding. Input W is [K][N] row-major (the [in, out] orientation,
+// Y = X @ W). Output shards are stored K-major so that a GEMM tile of one
+// shard is a block of contiguous rows:
+//   column mode: shard s = W[:, s*N/tp:(s+1)*N/tp]^T, stored [tp][N/tp][K]
+//                (the whole output equals W^T);
+//   row mode:    shard s = W[s*K/tp:(s+1)*K/tp, :]^T, stored [tp][N][K/tp].
+// A 32x32 shared-memory transpose; grid (ceil(N/32), ceil(K/32)).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void shard_weights_kernel(const T* __restrict__ W, int64_t K, int64_t N, int64_t Ks,
+                                     int row_mode, T* __restrict__ out) {
+  __shared__ T tile[32][33];
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 32, k0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  for (int r = ty; r < 32; r += 8) {
+    const int64_t k = k0 + r, n = n0 + tx;
+    if (k < K && n < N) tile[r][tx] = W[k * N + n];
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int64_t n = n0 + r, k = k0 + tx;
+    if (k < K && n < N) {
+      int64_t dst;
+      if (!row_mode) {
+        dst = n * K + k;
+      } else {
+        const int64_t s = k / Ks, kl = k - s * Ks;
+        dst = (s * N + n) * Ks + kl;
+      }
+      out[dst] = tile[tx][r];
+    }
+  }
+}
+
+// QKV sharded by heads. Shard s holds its q heads, then its kv heads' K
+// columns, then their V columns, stored K-major: out [tp][Nqkv_s][H].
+// kv_first(s) is s*nkv when hkv >= tp, else the replicated head
+// floor(s*hkv/tp). grid (ceil(Nqkv_s/32), ceil(H/32), tp).
+template <typename T>
+__global__ void shard_qkv_kernel(const T* __restrict__ Wq, const T* __restrict__ Wk,
+                                 const T* __restrict__ Wv, int64_t H, int hq, int hkv, int hd, int tp,
+                                 T* __restrict__ out) {
+  __shared__ T tile[32][33];
+  const int s = blockIdx.z;
+  const int nq = hq / tp;
+  const int nkv = hkv >= tp ? hkv / tp : 1;
+  const int kv0 = hkv >= tp ? s * nkv : (s * hkv) / tp;
+  const int64_t Nq = static_cast<int64_t>(nq) * hd, Nkv = static_cast<int64_t>(nkv) * hd;
+  const int64_t Ns = Nq + 2 * Nkv;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32, k0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t k = k0 + i, r = r0 + tx;
+    if (k < H && r < Ns) {
+      T v;
+      if (r < Nq) {
+        v = Wq[k * hq * hd + static_cast<int64_t>(s) * Nq + r];
+      } else if (r < Nq + Nkv) {
+        v = Wk[k * hkv * hd + static_cast<int64_t>(kv0) * hd + (r - Nq)];
+      } else {
+        v = Wv[k * hkv * hd + static_cast<int64_t>(kv0) * hd + (r - Nq - Nkv)];
+      }
+      tile[i][tx] = v;
+    }
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int64_t r = r0 + i, k = k0 + tx;
+    if (k < H && r < Ns) out[(static_cast<int64_t>(s) * Ns + r) * H + k] = tile[tx][i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Gather (all-gather semantics): shards [tp][T][Ns] -> Y[T][tp*Ns].
+// VEC elements per thread (16-byte copies when the widths allow).
+// ---------------------------------------------------------------------------
+template <typename T, int VEC>
+__global__ void gather_kernel(const T* __restrict__ in, int tp, int64_t Tn, int64_t Ns,
+                              T* __restrict__ out) {
+  const int64_t nv = Ns / VEC;
+  const int64_t total = static_cast<int64_t>(tp) * Tn * nv;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t j = i % nv;
+    const int64_t t = (i / nv) % Tn;
+    const int64_t s = i / (nv * Tn);
+    const T* src = in + (s * Tn + t) * Ns + j * VEC;
+    T* dst = out + t * tp * Ns + s * Ns + j * VEC;
+    if constexpr (VEC * sizeof(T) == 16) {
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    } else {
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) dst[v] = src[v];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Reduce (all-reduce / reduce-scatter semantics): out[t][n] = sum over
+// s = 0..tp-1 of P[s][t][n], in that order, in fp32, then + bias[n] once and
+// + residual[t][n]. For reduce-scatter the output buffer is read as
+// [tp][T/tp][N]: shard s's slice holds token rows [s*T/tp, (s+1)*T/tp),
+// which is the same memory as [T][N]. 4 elements per thread.
+// ---------------------------------------------------------------------------
+template <typename TO>
+__global__ void reduce_kernel(const float* __restrict__ P, int tp, int64_t Tn, int64_t N,
+                              const TO* __restrict__ bias, const TO* __restrict__ residual,
+                              TO* __restrict__ out) {
+  const int64_t total4 = Tn * N / 4;
+  const int64_t plane = Tn * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i * 4;
+    float4 acc = *reinterpret_cast<const float4*>(P + e);
+    for (int s = 1; s < tp; ++s) {
+      const float4 p = *reinterpret_cast<const float4*>(P + s * plane + e);
+      acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+    }
+    float v[4] = {acc.x, acc.y, acc.z, acc.w};
+    const int64_t n = e % N;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (bias) v[j] += to_f32(bias[n + j]);
+      if (residual) v[j] += to_f32(residual[e + j]);
+      out[e + j] = from_f32<TO>(v[j]);
+    }
+  }
+}
+
+// Scalar variant for widths that are not a multiple of 4.
+template <typename TO>
+__global__ void reduce_kernel_scalar(const float* __restrict__ P, int tp, int64_t Tn, int64_t N,
+                                     const TO* __restrict__ bias, const TO* __restrict__ residual,
+                                     TO* __restrict__ out) {
+  const int64_t total = Tn * N;
+  for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float v = P[e];
+    for (int s = 1; s < tp; ++s) v += P[s * total + e];
+    if (bias) v += to_f32(bias[e % N]);
+    if (residual) v += to_f32(residual[e]);
+    out[e] = from_f32<TO>(v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm over the replicated hidden: y = x * g / sqrt(mean(x^2) + eps),
+// fp32 statistics. One 256-thread block per token row.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void rmsnorm_kernel(const T* __restrict__ X, const T* __restrict__ gamma, int64_t H,
+                               float eps, T* __restrict__ Y) {
+  const int64_t row = blockIdx.x;
+  const T* x = X + row * H;
+  T* y = Y + row * H;
+  float ss = 0.0f;
+  for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
+    const float v = to_f32(x[i]);
+    ss = fmaf(v, v, ss);
+  }
+  __shared__ float red[32];
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.0f;
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (threadIdx.x == 0) red[0] = t;
+  }
+  __syncthreads();
+  const float inv = rsqrtf(red[0] / static_cast<float>(H) + eps);
+  for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
+    float v = to_f32(x[i]) * inv;
+    if (gamma) v *= to_f32(gamma[i]);
+    y[i] = from_f32<T>(v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Attention-context stand-in: with each query attending only to its own
+// token, the softmax weight is 1 and the context of local q head j is V of
+// its kv head. qkv [tp][T][Nqkv_s] (q | k | v per shard) -> ctx
+// [tp][T][nq*hd]. One thread per 8 elements (hd % 8 == 0).
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void ctx_standin_kernel(const T* __restrict__ qkv, int tp, int64_t Tn, int hq, int hkv,
+                                   int hd, T* __restrict__ ctx) {
+  const int nq = hq / tp;
+  const int nkv = hkv >= tp ? hkv / tp : 1;
+  const int group = hq / hkv;
+  const int64_t Nqkv = static_cast<int64_t>(nq + 2 * nkv) * hd;
+  const int64_t Nc = static_cast<int64_t>(nq) * hd;
+  const int64_t per = Nc / 8;
+  const int64_t total = static_cast<int64_t>(tp) * Tn * per;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t c = (i % per) * 8;
+    const int64_t t = (i / per) % Tn;
+    const int s = static_cast<int>(i / (per * Tn));
+    const int j = static_cast<int>(c / hd), d = static_cast<int>(c % hd);
+    const int h = s * nq + j;  // global q head
+    const int g = h / group;   // its kv head
+    const int kv0 = hkv >= tp ? s * nkv : (s * hkv) / tp;
+    const int64_t src = (static_cast<int64_t>(s) * Tn + t) * Nqkv +
+                        static_cast<int64_t>(nq + nkv) * hd + static_cast<int64_t>(g - kv0) * hd + d;
+    const int64_t dst = (static_cast<int64_t>(s) * Tn + t) * Nc + c;
+    if constexpr (sizeof(T) == 2) {
+      *reinterpret_cast<uint4*>(ctx + dst) = *reinterpret_cast<const uint4*>(qkv + src);
+    } else {
+#pragma unroll
+      for (int v = 0; v < 8; ++v) ctx[dst + v] = qkv[src + v];
+    }
+  }
+}
+
+}  // namespace tpk

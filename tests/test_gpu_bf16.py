@@ -1,0 +1,150 @@
+"""GPU parity of the bf16 tensor-core path against the fp64 oracle, element by
+element, at sizes the oracle finishes in seconds. Shapes are chosen to span
+several 128x256 tiles and 64-wide k-blocks and to leave ragged tails in every
+dimension (tokens, output columns per shard, K per shard).
+Tolerance: max|gpu - oracle| <= 2e-2 * RMS(oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as S
+from oracle import tp_oracle as O
+from tests._util import TOL_BF16, TOL_F32, assert_close, assert_close_stored, dev, f64, host
+
+pytestmark = pytest.mark.gpu
+
+tpl = pytest.importorskip("tensor_transformer_linear_tma_b300")
+
+B = torch.bfloat16
+
+
+def nb(seed, shape, std=1.0):
+    return S.normal(seed, shape, std)
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu", "silu"])
+@pytest.mark.parametrize("concat", [False, True])
+def test_column_linear_acts_tails(act, concat):
+    T, K, N, tp = 300, 200, 3 * 344, 3      # M tail 44, K tail 8, shard tail 88
+    X, W, b = nb(1, (T, K)), nb(2, (K, N), 0.05), nb(3, (N,), 0.5)
+    Sc = tpl.tp_shard_weights(dev(W), tp, "col")
+    Y = tpl.tp_column_linear(dev(X), Sc, bias=dev(b), act=act, concat=concat)
+    ref = O.column_parallel(f64(X), f64(W), tp, f64(b), O.ACTIVATIONS[act])
+    assert_close(Y, O.all_gather(ref) if concat else np.stack(ref), TOL_BF16, f"col {act}")
+
+
+@pytest.mark.parametrize("T,K,I,tp", [(257, 256, 2 * 1376, 2), (129, 64, 8 * 136, 8), (64, 512, 4 * 256, 4)])
+def test_column_swiglu(T, K, I, tp):
+    X, Wg, Wu = nb(4, (T, K)), nb(5, (K, I), 0.05), nb(6, (K, I), 0.05)
+    bg, bu = nb(7, (I,), 0.3), nb(8, (I,), 0.3)
+    Sg = tpl.tp_shard_weights(dev(Wg), tp, "col")
+    Su = tpl.tp_shard_weights(dev(Wu), tp, "col")
+    Y = tpl.tp_column_linear(dev(X), Sg, W_up=Su, bias=dev(bg), bias_up=dev(bu), act="swiglu")
+    G = O.column_parallel(f64(X), f64(Wg), tp, f64(bg))
+    U = O.column_parallel(f64(X), f64(Wu), tp, f64(bu))
+    assert_close_stored(Y, np.stack([O.swiglu(G[s], U[s]) for s in range(tp)]), TOL_BF16, "swiglu")
+
+
+@pytest.mark.parametrize("T,K,N,tp", [(200, 3 * 344, 264, 3), (130, 8 * 72, 512, 8), (5, 2 * 64, 256, 2)])
+def test_row_linear_fused_and_partials(T, K, N, tp):
+    Xf, W = nb(9, (T, K)), nb(10, (K, N), 0.05)
+    b, R = nb(11, (N,), 0.5), nb(12, (T, N))
+    Xs_np = np.ascontiguousarray(Xf.reshape(T, tp, K // tp).transpose(1, 0, 2))  # [tp][T][K/tp]
+    Sr = tpl.tp_shard_weights(dev(W), tp, "row")
+    Xs = dev(Xs_np)
+    parts = O.row_parallel_partials([f64(x) for x in Xs_np], f64(W), tp)
+    ref = O.all_reduce(parts) + f64(b) + f64(R)
+    assert_close(tpl.tp_row_linear(Xs, Sr, bias=dev(b), residual=dev(R)), ref, TOL_BF16, "row fused")
+    P = tpl.tp_row_linear_partials(Xs, Sr)
+    assert_close(P, np.stack(parts), TOL_F32, "row partials (fp32 accumulation of bf16 products)")
+    assert_close(tpl.tp_shard_reduce(P, bias=dev(b), residual=dev(R), out_dtype=B), ref, TOL_BF16, "reduce")
+    if T % tp == 0:
+        rs = tpl.tp_shard_reduce(P, op="scatter", out_dtype=torch.float32)
+        assert_close(rs, np.stack(O.reduce_scatter(parts, tp)), TOL_F32, "reduce-scatter")
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4, 8])
+def test_mlp_block_swiglu_small(tp):
+    T, H, I = 333, 256, 8 * 344
+    d = S.swiglu_mlp(T, H, I, seeds=(21, 22, 23, 24))
+    R = nb(25, (T, H))
+    Sg, Su = (tpl.tp_shard_weights(dev(d[k]), tp, "col") for k in ("Wg", "Wu"))
+    Sd = tpl.tp_shard_weights(dev(d["Wd"]), tp, "row")
+    Y = tpl.tp_mlp_block(dev(d["X"]), Sg, Sd, W_up=Su, residual=dev(R), act="swiglu")
+    _, ref = O.mlp_block(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, "swiglu", W_up=f64(d["Wu"]), residual=f64(R))
+    assert_close(Y, ref, TOL_BF16, f"mlp swiglu tp={tp}")
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu"])
+def test_mlp_block_plain_acts_bias(act):
+    T, H, I, tp = 150, 128, 4 * 96, 4
+    X, W1, W2 = nb(31, (T, H)), nb(32, (H, I), 0.05), nb(33, (I, H), 0.05)
+    b1, b2 = nb(34, (I,), 0.3), nb(35, (H,), 0.3)
+    S1 = tpl.tp_shard_weights(dev(W1), tp, "col")
+    S2 = tpl.tp_shard_weights(dev(W2), tp, "row")
+    Y = tpl.tp_mlp_block(dev(X), S1, S2, b1=dev(b1), b2=dev(b2), act=act)
+    _, ref = O.mlp_block(f64(X), f64(W1), f64(W2), tp, act, b1=f64(b1), b2=f64(b2))
+    assert_close(Y, ref, TOL_BF16, f"mlp {act}")
+
+
+@pytest.mark.parametrize("tp", [1, 2, 4, 8, 16])
+def test_attn_proj_gqa_small(tp):
+    T, H, hq, hkv, hd = 260, 256, 16, 4, 64   # hkv < tp replicates KV at tp 8, 16
+    d = S.gqa_proj(T, H, hq, hkv, hd, seeds=(41, 42, 43, 44, 45))
+    R = nb(46, (T, H))
+    Sqkv = tpl.tp_shard_qkv(dev(d["Wq"]), dev(d["Wk"]), dev(d["Wv"]), hq, hkv, hd, tp)
+    So = tpl.tp_shard_weights(dev(d["Wo"]), tp, "row")
+    qkv_ref, ctx_ref, Y_ref = O.attn_proj(*(f64(d[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo")), hq, hkv, hd, tp,
+                                          residual=f64(R))
+    qkv = torch.empty((tp, T, qkv_ref[0].shape[1]), dtype=B, device="cuda")
+    Y = tpl.tp_attn_proj(dev(d["X"]), Sqkv, So, residual=dev(R), qkv_out=qkv)
+    assert_close(qkv, np.stack(qkv_ref), TOL_BF16, f"qkv tp={tp}")
+    assert_close(Y, Y_ref, TOL_BF16, f"attn tp={tp}")
+    # an explicit per-shard context replaces the stand-in
+    ctx = nb(47, (tp, T, hq // tp * hd))
+    Y2 = tpl.tp_attn_proj(dev(d["X"]), Sqkv, So, ctx=dev(ctx))
+    _, _, Y2_ref = O.attn_proj(*(f64(d[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo")), hq, hkv, hd, tp,
+                               ctx=[f64(c) for c in ctx])
+    assert_close(Y2, Y2_ref, TOL_BF16, "attn explicit ctx")
+
+
+def test_rmsnorm_and_gather():
+    X, g = nb(51, (77, 4096)), nb(52, (4096,), 1.0)
+    assert_close_stored(tpl.tp_rmsnorm(dev(X), dev(g)), O.rmsnorm(f64(X), f64(g)), TOL_BF16, "rmsnorm bf16")
+    assert_close(tpl.tp_rmsnorm(dev(X)), O.rmsnorm(f64(X)), TOL_BF16, "rmsnorm bf16, unit gain")
+    assert_close(tpl.tp_rmsnorm(dev(X, torch.float32)), O.rmsnorm(f64(X)), TOL_F32, "rmsnorm f32")
+    sh = nb(53, (4, 33, 80))
+    ref = O.all_gather(list(sh))
+    np.testing.assert_array_equal(host(tpl.tp_shard_gather(dev(sh))), ref)
+    np.testing.assert_array_equal(host(tpl.tp_shard_gather(dev(sh, torch.float32))), ref)
+
+
+def test_shard_layouts_bitwise():
+    """Sharded storage is a pure copy: compare bits with the oracle's shards."""
+    K, N, tp = 96, 160, 4
+    W = nb(54, (K, N))
+    c = host(tpl.tp_shard_weights(dev(W), tp, "col").storage).reshape(tp, N // tp, K)
+    r = host(tpl.tp_shard_weights(dev(W), tp, "row").storage).reshape(tp, N, K // tp)
+    for s in range(tp):
+        np.testing.assert_array_equal(c[s], O.column_shards(f64(W), tp)[s].T)
+        np.testing.assert_array_equal(r[s], O.row_shards(f64(W), tp)[s].T)
+    H, hq, hkv, hd = 64, 8, 2, 16
+    Wq, Wk, Wv = nb(55, (H, hq * hd)), nb(56, (H, hkv * hd)), nb(57, (H, hkv * hd))
+    for tp in (1, 2, 4, 8):
+        q = tpl.tp_shard_qkv(dev(Wq), dev(Wk), dev(Wv), hq, hkv, hd, tp)
+        got = host(q.storage).reshape(tp, -1, H)
+        for s, ws in enumerate(O.qkv_shards(f64(Wq), f64(Wk), f64(Wv), hq, hkv, hd, tp)):
+            np.testing.assert_array_equal(got[s], ws.T)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64, 100])
+def test_small_token_counts(T):
+    H, I, tp = 512, 8 * 136, 8
+    d = S.decode_mlp(T, H, I, seed=60)
+    Sg, Su = (tpl.tp_shard_weights(dev(d[k]), tp, "col") for k in ("Wg", "Wu"))
+    Sd = tpl.tp_shard_weights(dev(d["Wd"]), tp, "row")
+    R = nb(61, (T, H))
+    Y = tpl.tp_mlp_block(dev(d["X"]), Sg, Sd, W_up=Su, residual=dev(R), act="swiglu")
+    _, ref = O.mlp_block(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, "swiglu", W_up=f64(d["Wu"]), residual=f64(R))
+    assert_close(Y, ref, TOL_BF16, f"decode-shaped T={T}")
+    assert tpl.tp_get_error() == 0
