@@ -149,53 +149,77 @@ class OracleLeg:
 # GPU side
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while running."""
-    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
-               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
-               0x100: "display_clock_setting"}
+    """Samples SM clocks and clock-event (throttle) reasons while the timed
+    region runs, with `nvidia-smi --query-gpu ... -lms 20` in a child process
+    (the same fields as the profiling recipe's clocks line). Only samples
+    whose timestamps fall inside the marked timed window are summarised."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,power.draw")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, index: int, period_s: float = 0.01):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
-        self.period, self.index = period_s, index
-        self._stop = threading.Event()
-        self._t = None
+    def __init__(self, local_index: int, period_ms: int = 20):
+        self.rows, self.error, self.window = [], None, None
+        self.proc, self._t = None, None
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.target = vis.split(",")[local_index] if vis else str(local_index)
+        self.period_ms = period_ms
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append((time.perf_counter(), parts))
+
+    def start(self):
+        import subprocess
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self.nv = None
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                mask = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for bit, nm in self.REASONS.items():
-                    if mask & bit and nm != "gpu_idle":
-                        self.reasons.add(nm)
-            except Exception:
-                pass
-            time.sleep(self.period)
-
-    def __enter__(self):
-        if self.nv is not None:
-            self._t = threading.Thread(target=self._run, daemon=True)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.target, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._reader, daemon=True)
             self._t.start()
-        return self
+            time.sleep(0.5)  # nvidia-smi's first sample arrives a few hundred ms after start
+        except Exception as e:  # no nvidia-smi: the line then says so
+            self.error = repr(e)
 
-    def __exit__(self, *a):
-        self._stop.set()
-        if self._t:
-            self._t.join()
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(2 * self.period_ms / 1000.0)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self._t.join(timeout=5)
 
     def summary(self):
-        med = statistics.median(self.samples) if self.samples else None
-        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+        rows = self.rows
+        if self.window:
+            t0, t1 = self.window
+            inside = [r for r in rows if t0 <= r[0] <= t1 + 0.03]
+            rows = inside
+        mhz, mx, reasons, watts = [], None, set(), []
+        for _, p in rows:
+            try:
+                mhz.append(float(p[0]))
+                mx = float(p[1])
+                watts.append(float(p[6]))
+            except ValueError:
+                continue
+            for nm, v in zip(self.NAMES, p[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        out = {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": mx,
+               "reasons": sorted(reasons), "samples": len(mhz),
+               "power_w_median": statistics.median(watts) if watts else None}
+        if self.error:
+            out["sampler_error"] = self.error
+        return out
 
 
 def load_peaks():
@@ -249,17 +273,20 @@ def setup_workload(spec, torch, tpl):
         Hs = torch.empty((tp, T, I // tp), dtype=B, device="cuda")
         Y = torch.empty((T, H), dtype=B, device="cuda")
         ws = torch.empty(max(tpl.tp_mlp_workspace_bytes(T, H, I, tp, B), 256), dtype=torch.uint8, device="cuda")
+        gws = torch.empty(max(tpl.tp_gemm_workspace_bytes(T, Sg), tpl.tp_gemm_workspace_bytes(T, Sd), 256),
+                          dtype=torch.uint8, device="cuda")
 
+        # the two launches of tp_mlp_block, as two calls so each can be timed
         def part_a():
-            tpl.tp_column_linear(X, Sg, W_up=Su, act="swiglu", out=Hs)
+            tpl.tp_column_linear(X, Sg, W_up=Su, act="swiglu", out=Hs, workspace=gws)
 
         def part_b():
-            tpl.tp_row_linear(Hs, Sd, out=Y)
+            tpl.tp_row_linear(Hs, Sd, out=Y, workspace=gws)
 
         def api_call(Xin, Yout):
             tpl.tp_mlp_block(Xin, Sg, Sd, W_up=Su, act="swiglu", workspace=ws, out=Yout)
         st.update(parts=[part_a, part_b], X=X, Y=Y, api=api_call, launches_per_step=2,
-                  keep=[Sg, Su, Sd, Hs, ws])
+                  keep=[Sg, Su, Sd, Hs, ws, gws])
     elif name.startswith("gqa"):
         H, hq, hkv, hd = spec["H"], spec["hq"], spec["hkv"], spec["hd"]
         d = S.gqa_proj(T, H, hq, hkv, hd)
@@ -274,14 +301,16 @@ def setup_workload(spec, torch, tpl):
         ws = torch.empty(max(tpl.tp_attn_workspace_bytes(T, hq, hkv, hd, tp, B), 256), dtype=torch.uint8,
                          device="cuda")
 
-        def part_a():
-            tpl.tp_column_linear(X, Sqkv, out=qkv)
+        gws = torch.empty(max(tpl.tp_gemm_workspace_bytes(T, Sqkv), 256), dtype=torch.uint8, device="cuda")
+
+        def part_a():  # the QKV launch of tp_attn_proj, timed alone
+            tpl.tp_column_linear(X, Sqkv, out=qkv, workspace=gws)
 
         def api_call(Xin, Yout):
             # QKV by heads -> single-key context (V by the GQA head map) -> O + shard sum
             tpl.tp_attn_proj(Xin, Sqkv, So, qkv_out=qkv, workspace=ws, out=Yout)
         st.update(parts=[lambda: api_call(X, Y)], X=X, Y=Y, api=api_call, launches_per_step=3,
-                  keep=[Sqkv, So, qkv, ctx, ws], dominant_part=part_a)
+                  keep=[Sqkv, So, qkv, ctx, ws, gws], dominant_part=part_a)
     else:
         H, I, hq, hkv, hd, V, L = (spec[k] for k in ("H", "I", "hq", "hkv", "hd", "V", "L"))
         d = S.stack(T, H, I, hq, hkv, hd, V, L)
@@ -341,6 +370,9 @@ def run_gpu(args, spec):
             dist.barrier()
         torch.cuda.synchronize()
 
+    clk = ClockSampler(local)
+    if rank == 0:
+        clk.start()
     for _ in range(args.warmup):
         for p in st["parts"]:
             p()
@@ -350,17 +382,19 @@ def run_gpu(args, spec):
     nparts = len(st["parts"])
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nparts + 1)] for _ in range(args.steps)]
     barrier()
-    with ClockSampler(local) as clk:
-        t_wall = time.perf_counter()
-        for k in range(args.steps):
-            flush.fill_(float(k))
-            e = evs[k]
-            e[0].record(stream)
-            for i, p in enumerate(st["parts"]):
-                p()
-                e[i + 1].record(stream)
-        barrier()
-        t_wall = time.perf_counter() - t_wall
+    t_begin = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(float(k))
+        e = evs[k]
+        e[0].record(stream)
+        for i, p in enumerate(st["parts"]):
+            p()
+            e[i + 1].record(stream)
+    barrier()
+    t_end = time.perf_counter()
+    t_wall = t_end - t_begin
+    clk.mark(t_begin, t_end)
+    clk.stop()
     status = tpl.tp_get_error()
     if status != 0:
         raise SystemExit(f"device error in timed region: {tpl.tp_status_string(status)}")
@@ -478,7 +512,7 @@ def cpu_baseline_obj(spec, unit, target_s):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mlp", choices=["mlp", "gqa", "decode", "stack"])
     ap.add_argument("--tp", type=int, default=None)

@@ -155,12 +155,22 @@ size_t tp_qkv_shard_elems(int64_t H, int hq, int hkv, int hd, int tp);
  *   bias    [N] or NULL (shard s uses bias[s*N/tp ...]); bias_up likewise.
  *   concat  0: Y is [tp][T][N/tp] (each shard's own output);
  *           1: Y is [T][N], the all-gather result, written in place.
+ *   For a QKV view (tp_shard_qkv) with replicated kv heads and no bias, the
+ *   K|V columns of each group of tp/hkv shards are computed once and stored
+ *   to every shard of the group (they are identical).
+ *   workspace, ws_bytes: optional scratch (NULL/0 allowed) of at least
+ *           tp_gemm_workspace_bytes(T, W) bytes, 256-byte aligned. With it, a
+ *           bf16 call with T <= 64 uses the weight-streaming arrangement
+ *           (weights as the 128-row MMA operand, their K loops split evenly
+ *           over all SMs, split tiles combined in a fixed order so results do
+ *           not depend on timing); without it, and for T > 64, every tile
+ *           runs whole on one SM. The two agree within rounding.
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN,
- * TP_ERR_CUDA.
+ * TP_ERR_WORKSPACE, TP_ERR_CUDA.
  */
 int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shards* W_up,
                      const void* bias, const void* bias_up, int act, int concat, void* Y,
-                     void* stream);
+                     void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * tp_row_linear - row-parallel linear with the combine fused:
@@ -170,11 +180,18 @@ int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shar
  * reach memory.
  *   Xs        [tp][T][K/tp] (shard s's input block), dtype W->dtype.
  *   W         TP_ROW shards.
- *   bias      [N] or NULL.  residual [T][N] or NULL.  Y [T][N].
+ *   bias      [N] or NULL.  residual [T][N] or NULL (may alias Y: each
+ *             element is read before it is written, by the same thread).
+ *   Y         [T][N].  workspace, ws_bytes: as tp_column_linear.
  * Errors as tp_column_linear.
  */
 int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
-                  const void* residual, void* Y, void* stream);
+                  const void* residual, void* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/* Scratch bytes that make tp_column_linear / tp_row_linear over W at T
+ * tokens use the balanced (stream-K) schedule; 0 for fp32 views or invalid
+ * arguments. */
+size_t tp_gemm_workspace_bytes(int64_t T, const tp_shards* W);
 
 /*
  * tp_row_linear_partials - the per-shard contributions P_s = Xs[s] @ W_s,
@@ -194,7 +211,8 @@ int tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float*
  *                         T % tp == 0. (The split axis, tokens, is a reading:
  *                         the page says only "sum, then split".)
  *   The sum is taken in fp32 in shard order 0..tp-1; bias [N] is added once;
- *   residual is [T][N]. bias, residual and out have dtype out_dtype.
+ *   residual is [T][N] and may alias out. bias, residual and out have dtype
+ *   out_dtype.
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN
  * (16-byte pointers when N % 4 == 0), TP_ERR_CUDA.
  */
@@ -220,10 +238,10 @@ size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype
  *   Hs[s] = act(X @ W1_s + b1_s)            (SwiGLU: silu(X@Wg_s+b) * (X@Wu_s+bu))
  *   Y     = sum_s Hs[s] @ W2_s (+ b2, once) (+ residual)
  *   X [T][H]; W1, W_up: TP_COL shards (K=H, N=I); W2: TP_ROW shards (K=I,
- *   N=H); all the same tp and dtype. Y [T][H].
+ *   N=H); all the same tp and dtype. Y [T][H]; residual may alias Y.
  *   workspace: >= tp_mlp_workspace_bytes(T, H, I, tp, dtype) bytes, 256-byte
- *   aligned; holds Hs ([tp][T][I/tp], dtype) and, for small T on bf16, the
- *   split-K scratch of the weight-streaming path. Its contents on return are
+ *   aligned; holds Hs ([tp][T][I/tp], dtype) and, for bf16, the scratch of
+ *   the balanced schedule (see tp_column_linear). Its contents on return are
  *   unspecified.
  * Errors: as tp_column_linear, plus TP_ERR_WORKSPACE.
  */
@@ -245,10 +263,13 @@ size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int d
  *   ctx      [tp][T][hq/tp*hd]: the attention output of each shard's heads,
  *            or NULL for the single-key stand-in (each query attends only to
  *            its own token, so the context of q head h is V of its kv head).
- *   residual [T][H] or NULL.
+ *   residual [T][H] or NULL; may alias Y.
  *   qkv_out  [tp][T][Nqkv_s] (each shard's q | k | v), or NULL to keep it in
  *            the workspace.
  *   Y        [T][H] = sum_s ctx[s] @ Wo_s (+ residual).
+ *   When kv heads are replicated (hkv < tp) the K|V columns of each group of
+ *   tp/hkv shards are computed once and stored to every shard of the group.
+ *   Requires H <= 4 * hq * hd (TP_ERR_UNSUPPORTED otherwise).
  * Errors: as tp_mlp_block.
  */
 int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,

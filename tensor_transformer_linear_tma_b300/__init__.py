@@ -18,7 +18,7 @@ __all__ = [
     "TpError", "Shards", "lib", "LIB_PATH",
     "TP_F32", "TP_BF16", "TP_COL", "TP_ROW", "ACTS", "REDUCE_OPS",
     "tp_shard_weights", "tp_shard_qkv", "tp_qkv_shard_elems", "tp_column_linear",
-    "tp_row_linear", "tp_row_linear_partials", "tp_shard_reduce", "tp_shard_gather",
+    "tp_row_linear", "tp_row_linear_partials", "tp_gemm_workspace_bytes", "tp_shard_reduce", "tp_shard_gather",
     "tp_mlp_workspace_bytes", "tp_mlp_block", "tp_attn_workspace_bytes", "tp_attn_proj",
     "tp_rmsnorm", "tp_get_error", "tp_debug_set_wait_limit_ns", "tp_debug_inject",
     "tp_status_string",
@@ -27,7 +27,7 @@ __all__ = [
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp_b300.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m tensor_transformer_linear_tma_b300.build`")
+        f"{LIB_PATH} is missing: build it with `python tensor_transformer_linear_tma_b300/build.py`")
 lib = ctypes.CDLL(LIB_PATH)
 
 TP_F32, TP_BF16 = 0, 1
@@ -51,8 +51,9 @@ _SIGS = {
     "tp_shard_weights": (_i32, [_vp, _i64, _i64, _i32, _i32, _i32, _vp, _sz, _P, _vp]),
     "tp_shard_qkv": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _P, _vp]),
     "tp_qkv_shard_elems": (_sz, [_i64, _i32, _i32, _i32, _i32]),
-    "tp_column_linear": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _i32, _i32, _vp, _vp]),
-    "tp_row_linear": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp]),
+    "tp_column_linear": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "tp_row_linear": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tp_gemm_workspace_bytes": (_sz, [_i64, _P]),
     "tp_row_linear_partials": (_i32, [_vp, _i64, _P, _vp, _vp]),
     "tp_shard_reduce": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _i32, _vp, _vp]),
     "tp_shard_gather": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp]),
@@ -166,27 +167,40 @@ def tp_shard_qkv(Wq, Wk, Wv, hq: int, hkv: int, hd: int, tp: int) -> Shards:
     return Shards(out, view)
 
 
+def tp_gemm_workspace_bytes(T: int, W: Shards) -> int:
+    return lib.tp_gemm_workspace_bytes(T, W.ref())
+
+
+def _ws_args(workspace):
+    if workspace is None:
+        return None, 0
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
 def tp_column_linear(X, W: Shards, W_up: Shards | None = None, bias=None, bias_up=None,
-                     act: str = "none", concat: bool = False, out=None):
-    """Column-parallel linear; returns [tp, T, N/tp] or, with concat, [T, N]."""
+                     act: str = "none", concat: bool = False, out=None, workspace=None):
+    """Column-parallel linear; returns [tp, T, N/tp] or, with concat, [T, N].
+    `workspace` (optional, tp_gemm_workspace_bytes) enables the balanced schedule."""
     T = X.shape[0]
     Ns = W.shard_width
     if out is None:
         shape = (T, W.N) if concat else (W.tp, T, Ns)
         out = torch.empty(shape, dtype=X.dtype, device=X.device)
+    ws, wsb = _ws_args(workspace)
     _check("tp_column_linear", lib.tp_column_linear(
         _ptr(X), T, W.ref(), W_up.ref() if W_up is not None else None, _ptr(bias), _ptr(bias_up),
-        ACTS[act], int(concat), _ptr(out), _stream(X.device)))
+        ACTS[act], int(concat), _ptr(out), ws, wsb, _stream(X.device)))
     return out
 
 
-def tp_row_linear(Xs, W: Shards, bias=None, residual=None, out=None):
+def tp_row_linear(Xs, W: Shards, bias=None, residual=None, out=None, workspace=None):
     """Row-parallel linear with the shard sum fused; Xs is [tp, T, K/tp]."""
     T = Xs.shape[1]
     if out is None:
         out = torch.empty((T, W.N), dtype=Xs.dtype, device=Xs.device)
+    ws, wsb = _ws_args(workspace)
     _check("tp_row_linear", lib.tp_row_linear(
-        _ptr(Xs), T, W.ref(), _ptr(bias), _ptr(residual), _ptr(out), _stream(Xs.device)))
+        _ptr(Xs), T, W.ref(), _ptr(bias), _ptr(residual), _ptr(out), ws, wsb, _stream(Xs.device)))
     return out
 
 

@@ -1,6 +1,8 @@
 """Build step: compile the CUDA sources into the in-tree shared library.
 
-    python -m tensor_transformer_linear_tma_b300.build [--force] [--verbose]
+    python tensor_transformer_linear_tma_b300/build.py [--force] [--verbose]
+
+(Run it as a file, not with -m: importing the package loads the library.)
 
 Produces libtp_b300.so next to this file, for sm_103a only. The library
 links the CUDA runtime statically and reaches the driver's tensor-map

@@ -12,7 +12,7 @@
 
 #include "tp.h"
 #include "tp_elementwise.cuh"
-#include "tp_gemm_tc.cuh"
+#include "tp_gemm.cuh"
 #include "tp_simt.cuh"
 
 namespace {
@@ -116,83 +116,170 @@ bool same_shape(const tp_shards* a, const tp_shards* b) {
 }
 
 // ---------------------------------------------------------------------------
-// GEMM launchers
+// Tensor-core GEMM launchers (bf16)
 // ---------------------------------------------------------------------------
-template <int KIND>
-int tc_launch(const CUtensorMap& ma, const CUtensorMap& mb0, const CUtensorMap& mb1,
-              const tpk::TcArgs& args, cudaStream_t st) {
+// Scratch for the stream-K schedule: fp32 workspace slots for split tiles
+// and one counter per split tile. Without scratch every tile runs whole.
+struct Scratch {
+  float* partials;
+  size_t partial_bytes;
+  int* counters;
+  size_t ncounters;
+};
+
+constexpr int SK_MAX_CTAS = 160;  // grid cap of the stream-K schedule (>= SMs of a B300)
+constexpr int SWAP_MAX_T = 64;    // token counts served by the weight-streaming (swap) arrangement
+
+size_t sk_partial_bytes(bool swap) {
+  return static_cast<size_t>(2) * SK_MAX_CTAS * 128 * (swap ? 128 : 256) * sizeof(float);
+}
+
+// Work split. Token-major tiles (normal arrangement) run whole, round-robin:
+// CTAs of one wave then walk the same K range in step, so the weight blocks
+// they share are read from L2 rather than HBM (splitting their K loops
+// measured a 4x rise in DRAM reads on the row GEMM). The weight-streaming
+// arrangement reads each weight byte once whatever the order, so there the
+// k-iterations of all tiles are spread evenly over the SMs (stream-K).
+// Returns the grid size.
+int plan_schedule(tpk::GemmArgs& a, bool swap, const Scratch* sc) {
+  const int sms = std::max(1, std::min(num_sms(), SK_MAX_CTAS));
+  a.dp_tiles = a.num_tiles;
+  a.sk_iters = 0;
+  const int grid = std::min(a.num_tiles, sms);
+  if (!sc || !swap) return grid;
+  const int dp = 0;
+  const long long sk = static_cast<long long>(a.num_tiles - dp) * a.kpt;
+  if (sk < 2 || static_cast<size_t>(a.num_tiles - dp) > sc->ncounters) return grid;
+  a.dp_tiles = dp;
+  a.sk_iters = sk;
+  a.partials = sc->partials;
+  a.counters = sc->counters;
+  return sms;  // the launcher clamps it to sk_iters so that no stream-K range is empty
+}
+
+template <int KIND, bool SWAP>
+int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
+                tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
+  using Cfg = tpk::GemmCfg<KIND, SWAP>;
   if (args.num_tiles <= 0) return TP_OK;
-  if (cudaFuncSetAttribute(tpk::tc_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           tpk::TC_SMEM_BYTES) != cudaSuccess)
+  int grid = plan_schedule(args, SWAP, sc);
+  if (args.sk_iters > 0) {
+    // every stream-K range must be non-empty: grid <= sk_iters
+    grid = static_cast<int>(std::min<long long>(grid, args.sk_iters));
+    if (cudaMemsetAsync(args.counters, 0, sizeof(int) * (args.num_tiles - args.dp_tiles), st) != cudaSuccess)
+      return TP_ERR_CUDA;
+  }
+  if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg::SMEM_BYTES) != cudaSuccess)
     return TP_ERR_CUDA;
-  const int grid = std::min(args.num_tiles, std::max(1, num_sms()));
-  tpk::tc_gemm_kernel<KIND><<<grid, tpk::TC_THREADS, tpk::TC_SMEM_BYTES, st>>>(ma, mb0, mb1, args);
+  tpk::tp_gemm_kernel<KIND, SWAP><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(a0, a1, b0, b1, args);
   return launch_status();
 }
 
-// Column-parallel bf16 GEMM on the tensor cores. Y layout per `concat`.
+inline int tpad_of(int64_t T) { return static_cast<int>(cdiv(std::max<int64_t>(T, 1), 16) * 16); }
+
+// Column-parallel bf16 GEMM. `rep` > 1 computes replicated K|V column blocks
+// once per group of rep shards (QKV views with kv heads < tp).
 int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
-             const void* bias_up, int act, int concat, void* Y, cudaStream_t st) {
+             const void* bias_up, int act, int concat, void* Y, const Scratch* sc, int rep, int64_t kv_col0,
+             cudaStream_t st) {
   const int tp = W->tp;
   const int64_t K = W->K, Ns = W->N / tp;
   const bool swiglu = act == TP_ACT_SWIGLU;
-  CUtensorMap ma, mb0, mb1;
-  if (!make_map_bf16(&ma, X, K, T, 1, tpk::TC_BM)) return TP_ERR_CUDA;
-  if (!make_map_bf16(&mb0, W->data, K, Ns, tp, swiglu ? tpk::TC_BN / 2 : tpk::TC_BN)) return TP_ERR_CUDA;
-  if (swiglu) {
-    if (!make_map_bf16(&mb1, Wu->data, K, Ns, tp, tpk::TC_BN / 2)) return TP_ERR_CUDA;
-  } else {
-    mb1 = mb0;
-  }
-  tpk::TcArgs a{};
+  const bool swap = sc != nullptr && T <= SWAP_MAX_T;
+  tpk::GemmArgs a{};
   a.M = static_cast<int>(T);
   a.Ns = static_cast<int>(Ns);
   a.tp = tp;
-  a.m_tiles = static_cast<int>(cdiv(T, tpk::TC_BM));
-  a.n_tiles = static_cast<int>(cdiv(Ns, swiglu ? tpk::TC_BN / 2 : tpk::TC_BN));
-  a.s_tiles = tp;
-  a.num_tiles = a.m_tiles * a.n_tiles * a.s_tiles;
-  a.kb_per_shard = static_cast<int>(cdiv(K, tpk::TC_BK));
-  a.k_shards = 1;
+  a.rep = 1;
+  a.kb_per_shard = static_cast<int>(cdiv(K, 64));
+  a.kpt = a.kb_per_shard;
   a.act = act;
   a.out_concat = concat;
   a.bias = static_cast<const bf16*>(bias);
   a.bias_up = static_cast<const bf16*>(bias_up);
   a.out = Y;
-  return swiglu ? tc_launch<tpk::TC_COL_SWIGLU>(ma, mb0, mb1, a, st)
-                : tc_launch<tpk::TC_COL>(ma, mb0, mb1, a, st);
+  CUtensorMap mx, mw, mu;
+  if (swap) {
+    a.Tpad = tpad_of(T);
+    if (!make_map_bf16(&mx, X, K, T, 1, a.Tpad)) return TP_ERR_CUDA;
+    if (!make_map_bf16(&mw, W->data, K, Ns, tp, 128)) return TP_ERR_CUDA;
+    if (swiglu && !make_map_bf16(&mu, Wu->data, K, Ns, tp, 128)) return TP_ERR_CUDA;
+    if (!swiglu) mu = mw;
+    a.m_tiles = static_cast<int>(cdiv(Ns, 128));
+    a.n_tiles = 1;
+    a.num_tiles = a.m_tiles * tp;
+    a.r1_tiles = a.num_tiles;
+    return swiglu ? gemm_launch<tpk::GK_COL_SWIGLU, true>(mw, mu, mx, mx, a, sc, st)
+                  : gemm_launch<tpk::GK_COL, true>(mw, mu, mx, mx, a, sc, st);
+  }
+  const int nout = swiglu ? 128 : 256;
+  if (!make_map_bf16(&mx, X, K, T, 1, 128)) return TP_ERR_CUDA;
+  if (!make_map_bf16(&mw, W->data, K, Ns, tp, swiglu ? 128 : 256)) return TP_ERR_CUDA;
+  if (swiglu && !make_map_bf16(&mu, Wu->data, K, Ns, tp, 128)) return TP_ERR_CUDA;
+  if (!swiglu) mu = mw;
+  a.m_tiles = static_cast<int>(cdiv(T, 128));
+  a.n_tiles = static_cast<int>(cdiv(Ns, nout));
+  int nq = a.n_tiles;
+  if (rep > 1 && !swiglu && tp % rep == 0) {
+    nq = static_cast<int>(cdiv(kv_col0, nout));
+    if (nq < a.n_tiles) {
+      a.rep = rep;
+      a.n_q_tiles = nq;
+    } else {
+      nq = a.n_tiles;
+    }
+  }
+  a.r1_tiles = a.m_tiles * nq * tp;
+  a.num_tiles = a.r1_tiles + (a.rep > 1 ? a.m_tiles * (a.n_tiles - nq) * (tp / a.rep) : 0);
+  return swiglu ? gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mw, mu, a, sc, st)
+                : gemm_launch<tpk::GK_COL, false>(mx, mx, mw, mu, a, sc, st);
 }
 
-// Row-parallel bf16 GEMM: fused shard sum (partials == nullptr) or per-shard
-// fp32 partials.
+// Row-parallel bf16 GEMM: fused shard sum (partials_out == nullptr) or
+// per-shard fp32 contributions.
 int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
-             void* Y, float* partials, cudaStream_t st) {
+             void* Y, float* partials_out, const Scratch* sc, cudaStream_t st) {
   const int tp = W->tp;
   const int64_t Ks = W->K / tp, N = W->N;
-  CUtensorMap ma, mb;
-  if (!make_map_bf16(&ma, Xs, Ks, T, tp, tpk::TC_BM)) return TP_ERR_CUDA;
-  if (!make_map_bf16(&mb, W->data, Ks, N, tp, tpk::TC_BN)) return TP_ERR_CUDA;
-  tpk::TcArgs a{};
+  const bool swap = sc != nullptr && T <= SWAP_MAX_T && partials_out == nullptr;
+  tpk::GemmArgs a{};
   a.M = static_cast<int>(T);
   a.Ns = static_cast<int>(N);
   a.tp = tp;
-  a.m_tiles = static_cast<int>(cdiv(T, tpk::TC_BM));
-  a.n_tiles = static_cast<int>(cdiv(N, tpk::TC_BN));
-  a.kb_per_shard = static_cast<int>(cdiv(Ks, tpk::TC_BK));
+  a.rep = 1;
+  a.kb_per_shard = static_cast<int>(cdiv(Ks, 64));
   a.bias = static_cast<const bf16*>(bias);
   a.residual = static_cast<const bf16*>(residual);
-  if (partials) {
-    a.s_tiles = tp;
-    a.k_shards = 1;
-    a.out = partials;
-    a.num_tiles = a.m_tiles * a.n_tiles * a.s_tiles;
-    return tc_launch<tpk::TC_ROW_PARTIAL>(ma, mb, mb, a, st);
+  CUtensorMap mx, mw;
+  if (swap) {
+    a.Tpad = tpad_of(T);
+    if (!make_map_bf16(&mx, Xs, Ks, T, tp, a.Tpad)) return TP_ERR_CUDA;
+    if (!make_map_bf16(&mw, W->data, Ks, N, tp, 128)) return TP_ERR_CUDA;
+    a.m_tiles = static_cast<int>(cdiv(N, 128));
+    a.n_tiles = 1;
+    a.num_tiles = a.m_tiles;
+    a.r1_tiles = a.num_tiles;
+    a.kpt = a.kb_per_shard * tp;
+    a.out = Y;
+    return gemm_launch<tpk::GK_ROW_SUM, true>(mw, mw, mx, mx, a, sc, st);
   }
-  a.s_tiles = 1;
-  a.k_shards = tp;
-  a.out = Y;
+  if (!make_map_bf16(&mx, Xs, Ks, T, tp, 128)) return TP_ERR_CUDA;
+  if (!make_map_bf16(&mw, W->data, Ks, N, tp, 256)) return TP_ERR_CUDA;
+  a.m_tiles = static_cast<int>(cdiv(T, 128));
+  a.n_tiles = static_cast<int>(cdiv(N, 256));
+  if (partials_out) {
+    a.num_tiles = a.m_tiles * a.n_tiles * tp;
+    a.kpt = a.kb_per_shard;
+    a.r1_tiles = a.num_tiles;
+    a.out = partials_out;
+    return gemm_launch<tpk::GK_ROW_PARTIAL, false>(mx, mx, mw, mw, a, sc, st);
+  }
   a.num_tiles = a.m_tiles * a.n_tiles;
-  return tc_launch<tpk::TC_ROW_SUM>(ma, mb, mb, a, st);
+  a.kpt = a.kb_per_shard * tp;
+  a.r1_tiles = a.num_tiles;
+  a.out = Y;
+  return gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, a, sc, st);
 }
 
 template <int KIND>
@@ -282,17 +369,53 @@ int check_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, c
 }
 
 int run_col(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
-            const void* bias_up, int act, int concat, void* Y, cudaStream_t st) {
+            const void* bias_up, int act, int concat, void* Y, cudaStream_t st, const Scratch* sc = nullptr) {
   if (T == 0) return TP_OK;
-  return W->dtype == TP_BF16 ? col_bf16(X, T, W, Wu, bias, bias_up, act, concat, Y, st)
-                             : col_f32(X, T, W, Wu, bias, bias_up, act, concat, Y, st);
+  if (W->dtype != TP_BF16) return col_f32(X, T, W, Wu, bias, bias_up, act, concat, Y, st);
+  // A QKV view whose kv heads are replicated (hkv < tp): without a bias the
+  // replicas' K|V columns are identical, so each group of tp/hkv shards
+  // computes them once and stores them to every shard of the group.
+  int rep = 1;
+  int64_t kv_col0 = 0;
+  if (W->hd > 0 && W->hkv > 0 && W->hkv < W->tp && !bias && !bias_up) {
+    rep = W->tp / W->hkv;
+    kv_col0 = static_cast<int64_t>(W->hq / W->tp) * W->hd;
+  }
+  return col_bf16(X, T, W, Wu, bias, bias_up, act, concat, Y, sc, rep, kv_col0, st);
 }
 
 int run_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
-            void* Y, float* partials, cudaStream_t st) {
+            void* Y, float* partials, cudaStream_t st, const Scratch* sc = nullptr) {
   if (T == 0) return TP_OK;
-  return W->dtype == TP_BF16 ? row_bf16(Xs, T, W, bias, residual, Y, partials, st)
+  return W->dtype == TP_BF16 ? row_bf16(Xs, T, W, bias, residual, Y, partials, sc, st)
                              : row_f32(Xs, T, W, bias, residual, Y, partials, st);
+}
+
+// Stream-K scratch carved from a caller workspace after `used` bytes.
+size_t scratch_bytes(int64_t T, size_t max_tiles) {
+  return align256(sk_partial_bytes(T <= SWAP_MAX_T)) + align256(sizeof(int) * max_tiles);
+}
+Scratch carve_scratch(void* ws, size_t used, int64_t T, size_t max_tiles) {
+  Scratch sc{};
+  char* base = static_cast<char*>(ws) + used;
+  sc.partial_bytes = sk_partial_bytes(T <= SWAP_MAX_T);
+  sc.partials = reinterpret_cast<float*>(base);
+  sc.counters = reinterpret_cast<int*>(base + align256(sc.partial_bytes));
+  sc.ncounters = max_tiles;
+  return sc;
+}
+// Counters the MLP's two GEMMs can need: the stream-K part of a normal
+// schedule stays under 2 * SK_MAX_CTAS tiles; the swap schedule splits all
+// of its tiles.
+size_t mlp_max_tiles(int64_t H, int64_t I, int tp) {
+  const size_t swap_col = static_cast<size_t>(tp) * cdiv(I / std::max(tp, 1), 128);
+  const size_t swap_row = cdiv(H, 128);
+  return std::max<size_t>(2 * SK_MAX_CTAS, std::max(swap_col, swap_row));
+}
+size_t attn_max_tiles(int64_t H, int hq, int hkv, int hd, int tp) {
+  const int64_t nkv = hkv >= tp ? hkv / tp : 1;
+  const size_t swap_col = static_cast<size_t>(tp) * cdiv((hq / tp + 2 * nkv) * hd, 128);
+  return std::max<size_t>(2 * SK_MAX_CTAS, std::max(swap_col, static_cast<size_t>(cdiv(H, 128))));
 }
 
 }  // namespace
@@ -409,19 +532,48 @@ int tp_shard_qkv(const void* Wq, const void* Wk, const void* Wv, int64_t H, int 
   return r;
 }
 
+size_t tp_gemm_workspace_bytes(int64_t T, const tp_shards* W) {
+  if (!W || T < 0 || W->dtype != TP_BF16 || W->tp < 1 || W->K < 1 || W->N < 1) return 0;
+  size_t tiles;
+  if (W->mode == TP_COL) tiles = static_cast<size_t>(W->tp) * cdiv(W->N / W->tp, 128);
+  else if (W->mode == TP_ROW) tiles = cdiv(W->N, 128);
+  else return 0;
+  return scratch_bytes(T, std::max<size_t>(2 * SK_MAX_CTAS, tiles));
+}
+
+// Optional caller scratch for a single linear: NULL -> whole tiles only.
+int linear_scratch(const tp_shards* W, int64_t T, void* ws, size_t ws_bytes, Scratch* sc, const Scratch** scp) {
+  *scp = nullptr;
+  if (!ws || W->dtype != TP_BF16) return TP_OK;
+  if (!aligned(ws, 256)) return TP_ERR_ALIGN;
+  const size_t need = tp_gemm_workspace_bytes(T, W);
+  if (ws_bytes < need) return TP_ERR_WORKSPACE;
+  const size_t tiles = W->mode == TP_COL ? static_cast<size_t>(W->tp) * cdiv(W->N / W->tp, 128)
+                                         : static_cast<size_t>(cdiv(W->N, 128));
+  *sc = carve_scratch(ws, 0, T, std::max<size_t>(2 * SK_MAX_CTAS, tiles));
+  *scp = sc;
+  return TP_OK;
+}
+
 int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shards* W_up,
                      const void* bias, const void* bias_up, int act, int concat, void* Y,
-                     void* stream) {
-  const int r = check_col(X, T, W, W_up, bias, bias_up, act, concat, Y);
+                     void* workspace, size_t ws_bytes, void* stream) {
+  int r = check_col(X, T, W, W_up, bias, bias_up, act, concat, Y);
   if (r) return r;
-  return run_col(X, T, W, W_up, bias, bias_up, act, concat, Y, as_stream(stream));
+  Scratch sc{};
+  const Scratch* scp;
+  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return r;
+  return run_col(X, T, W, W_up, bias, bias_up, act, concat, Y, as_stream(stream), scp);
 }
 
 int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
-                  const void* residual, void* Y, void* stream) {
-  const int r = check_row(Xs, T, W, bias, residual, Y, W ? W->dtype : TP_F32);
+                  const void* residual, void* Y, void* workspace, size_t ws_bytes, void* stream) {
+  int r = check_row(Xs, T, W, bias, residual, Y, W ? W->dtype : TP_F32);
   if (r) return r;
-  return run_row(Xs, T, W, bias, residual, Y, nullptr, as_stream(stream));
+  Scratch sc{};
+  const Scratch* scp;
+  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return r;
+  return run_row(Xs, T, W, bias, residual, Y, nullptr, as_stream(stream), scp);
 }
 
 int tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float* partials,
@@ -493,14 +645,16 @@ int tp_shard_gather(const void* shards, int tp, int64_t T, int64_t N, int dtype,
 
 size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype) {
   if (T < 0 || H < 1 || I < 1 || tp < 1 || !dtype_ok(dtype)) return 0;
-  return align256(static_cast<size_t>(T) * static_cast<size_t>(I) * elem_size(dtype));
+  size_t b = align256(static_cast<size_t>(T) * static_cast<size_t>(I) * elem_size(dtype));
+  if (dtype == TP_BF16) b += scratch_bytes(T, mlp_max_tiles(H, I, tp));
+  return b;
 }
 
 int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
                  const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
                  const void* residual, int act, void* workspace, size_t ws_bytes, void* Y,
                  void* stream) {
-  if (!workspace || !W2) return TP_ERR_NULL;
+  if (!W2 || (!workspace && T != 0)) return TP_ERR_NULL;
   int r = check_col(X, T, W1, W_up, b1, b1_up, act, 0, Y);
   if (r) return r;
   if ((r = check_view(W2, TP_ROW))) return r;
@@ -512,8 +666,15 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
   if (T == 0) return TP_OK;
   const cudaStream_t st = as_stream(stream);
   void* Hs = workspace;  // [tp][T][I/tp]
-  if ((r = run_col(X, T, W1, W_up, b1, b1_up, act, 0, Hs, st))) return r;
-  return run_row(Hs, T, W2, b2, residual, Y, nullptr, st);
+  const size_t hs_bytes = align256(static_cast<size_t>(T) * W1->N * elem_size(dt));
+  Scratch sc{};
+  const Scratch* scp = nullptr;
+  if (dt == TP_BF16) {
+    sc = carve_scratch(workspace, hs_bytes, T, mlp_max_tiles(W1->K, W1->N, W1->tp));
+    scp = &sc;
+  }
+  if ((r = run_col(X, T, W1, W_up, b1, b1_up, act, 0, Hs, st, scp))) return r;
+  return run_row(Hs, T, W2, b2, residual, Y, nullptr, st, scp);
 }
 
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype) {
@@ -522,13 +683,16 @@ size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int d
   if (qkv == 0) return 0;
   const size_t es = elem_size(dtype);
   const size_t ctx = static_cast<size_t>(hq) * hd;  // per token, all shards
-  return align256(static_cast<size_t>(T) * qkv * es) + align256(static_cast<size_t>(T) * ctx * es);
+  size_t b = align256(static_cast<size_t>(T) * qkv * es) + align256(static_cast<size_t>(T) * ctx * es);
+  // the stream-K scratch is sized for the largest hidden size the O projection may have
+  if (dtype == TP_BF16) b += scratch_bytes(T, attn_max_tiles(static_cast<int64_t>(hq) * hd * 4, hq, hkv, hd, tp));
+  return b;
 }
 
 int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
                  const void* ctx, const void* residual, void* qkv_out, void* workspace,
                  size_t ws_bytes, void* Y, void* stream) {
-  if (!workspace || !Wo || !Wqkv) return TP_ERR_NULL;
+  if (!Wo || !Wqkv || (!workspace && T != 0)) return TP_ERR_NULL;
   int r = check_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, Y);
   if (r) return r;
   if (Wqkv->hd < 1 || Wqkv->hq < 1 || Wqkv->hkv < 1) return TP_ERR_MODE;  // not a QKV view
@@ -542,14 +706,23 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
   if (!ptr_ok(ctx, dt) || !ptr_ok(residual, dt) || !ptr_ok(qkv_out, dt) || !aligned(workspace, 256))
     return TP_ERR_ALIGN;
   if (dt == TP_BF16 && hd % 8) return TP_ERR_ALIGN;
+  if (Wqkv->K > static_cast<int64_t>(hq) * hd * 4) return TP_ERR_UNSUPPORTED;  // scratch sizing bound
   if (ws_bytes < tp_attn_workspace_bytes(T, hq, hkv, hd, tp, dt)) return TP_ERR_WORKSPACE;
   if (T == 0) return TP_OK;
   const cudaStream_t st = as_stream(stream);
   const size_t es = elem_size(dt);
   const size_t qkv_bytes = align256(static_cast<size_t>(T) * tp_qkv_shard_elems(1, hq, hkv, hd, tp) * es);
+  const size_t ctx_bytes = align256(static_cast<size_t>(T) * hq * hd * es);
   void* qkv = qkv_out ? qkv_out : workspace;
   void* ctx_ws = static_cast<char*>(workspace) + qkv_bytes;
-  if ((r = run_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, qkv, st))) return r;
+  Scratch sc{};
+  const Scratch* scp = nullptr;
+  if (dt == TP_BF16) {
+    sc = carve_scratch(workspace, qkv_bytes + ctx_bytes, T,
+                       attn_max_tiles(static_cast<int64_t>(hq) * hd * 4, hq, hkv, hd, tp));
+    scp = &sc;
+  }
+  if ((r = run_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, qkv, st, scp))) return r;
   if (!ctx) {
     const int64_t total = static_cast<int64_t>(tp) * T * (hq / tp) * hd / 8;
     if (dt == TP_BF16)
@@ -561,7 +734,7 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
     if ((r = launch_status())) return r;
     ctx = ctx_ws;
   }
-  return run_row(ctx, T, Wo, nullptr, residual, Y, nullptr, st);
+  return run_row(ctx, T, Wo, nullptr, residual, Y, nullptr, st, scp);
 }
 
 int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,

@@ -1,0 +1,668 @@
+// Persistent tcgen05 GEMM for the sharded column / row linears (bf16 in,
+// fp32 accumulation in tensor memory, fused epilogues).
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: streams operand tiles through an mbarrier ring;
+//   warp 1      TMEM owner and MMA issuer (one thread issues tcgen05.mma into
+//               one of two TMEM accumulators, so the epilogue of one work
+//               unit overlaps the main loop of the next);
+//   warps 2..5  epilogue (tcgen05.ld, fused elementwise work, stores).
+//
+// Two operand arrangements:
+//   normal   A = 128 token rows, B = 256 weight rows (MMA 128x256x16). For
+//            large token counts.
+//   SWAP     A = 128 weight rows (two tiles, gate and up, for SwiGLU), B = the
+//            token rows padded to Tpad in {16,32,48,64} (MMA 128xTpadx16). For
+//            few tokens: the weights are the big operand and are streamed
+//            once, so this regime is bound by HBM bandwidth, not the MMA.
+//
+// Tile kinds (what one output tile is and how its K loop runs):
+//   COL         column-parallel linear, Y_s = act(X @ W_s + b_s) for each
+//               output-column shard s ("CUDA tensor parallel computations"
+//               page, Column Parallel and local elementwise sections); X is
+//               replicated, so every shard's tiles read the same A rows.
+//   COL_SWIGLU  gate and up shards together; the epilogue writes
+//               silu(gate) * up ("Tensor parallelism" tutorial page, MLP block).
+//   ROW_SUM     row-parallel linear with the all-reduce folded into the
+//               accumulator: the K loop runs over (shard, k-block), so
+//               sum_s X_s @ W_s never leaves TMEM; bias once, then residual
+//               ("Row Parallel": contributions are added).
+//   ROW_PARTIAL per-shard contributions P_s = X_s @ W_s stored as fp32.
+//
+// Work schedule. A work unit is a tile's K loop or a contiguous piece of it.
+// The first dp_tiles tiles go round-robin to the CTAs, whole. The remaining
+// tiles' k-iterations are split evenly over the grid (stream-K), which
+// removes the last-wave imbalance. A tile split over several CTAs is
+// combined deterministically: each piece is stored as fp32 in a workspace
+// slot, and the CTA that finishes last (an atomic counter per tile) sums the
+// pieces in k order and runs the tile's epilogue. No CTA ever waits for
+// another, so the schedule cannot deadlock.
+//
+// QKV replica dedup (normal COL): when kv heads are replicated across rep
+// consecutive shards, the tiles holding only replicated K|V columns are
+// computed once, on the first shard of each group, and stored to all rep
+// shards.
+#pragma once
+
+#include "tp_epilogue.cuh"
+#include "tp_ptx.cuh"
+
+namespace tpk {
+
+enum GemmKind : int { GK_COL = 0, GK_COL_SWIGLU = 1, GK_ROW_SUM = 2, GK_ROW_PARTIAL = 3 };
+
+template <int KIND_, bool SWAP_>
+struct GemmCfg {
+  static constexpr int KIND = KIND_;
+  static constexpr bool SWAP = SWAP_;
+  static constexpr bool SWIGLU = KIND_ == GK_COL_SWIGLU;
+  static constexpr bool IS_COL = KIND_ == GK_COL || KIND_ == GK_COL_SWIGLU;
+  static constexpr int NACC = (SWAP_ && SWIGLU) ? 2 : 1;  // A tiles per stage in swap mode
+  static constexpr int BM = 128;
+  static constexpr int BK = 64;
+  static constexpr int A_TILE = BM * BK * 2;               // 16 KB
+  static constexpr int A_BYTES = NACC * A_TILE;
+  static constexpr int B_ROWS = SWAP_ ? 64 : 256;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = SWAP_ ? (NACC == 2 ? 5 : 8) : 4;
+  static constexpr int ACC_COLS = SWAP_ ? 128 : 256;      // TMEM columns per accumulator buffer
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+  static constexpr int SLOT_FLOATS = 128 * ACC_COLS;       // one fp32 partial tile
+  static constexpr int THREADS = 192;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 512;
+};
+
+struct GemmArgs {
+  int M;             // tokens
+  int Ns;            // normal: output columns of a tile's shard; swap: weight rows per shard
+  int tp;
+  int Tpad;          // swap: MMA N (tokens padded to a multiple of 16)
+  int m_tiles;       // normal: token blocks; swap: weight-row blocks
+  int n_tiles;       // normal: output-column blocks per shard; swap: 1
+  int num_tiles;
+  int r1_tiles;      // tiles enumerated over all shards (the rest: first shard of each replica group)
+  int n_q_tiles;     // with rep > 1: column blocks before the replicated K|V columns
+  int rep;           // shards sharing one computed K|V tile (1 = no dedup)
+  int kb_per_shard;  // ceil(K extent of one shard / 64)
+  int kpt;           // k-iterations per tile: kb_per_shard * (ROW_SUM ? tp : 1)
+  int dp_tiles;      // tiles processed whole, round-robin
+  long long sk_iters;  // k-iterations of tiles [dp_tiles, num_tiles), split evenly over the grid
+  int act;
+  int out_concat;    // COL: 1 -> Y[T][tp*Ns]; 0 -> Y[tp][T][Ns]
+  const __nv_bfloat16* bias;      // COL: [tp*Ns]; ROW_SUM: [N]; may be null
+  const __nv_bfloat16* bias_up;   // COL_SWIGLU up bias [tp*Ns]; may be null
+  const __nv_bfloat16* residual;  // ROW_SUM: [M][N]; may be null
+  void* out;
+  float* partials;   // [2 * gridDim.x][SLOT_FLOATS] when sk_iters > 0
+  int* counters;     // [num_tiles - dp_tiles], zero on entry; reset to zero by the kernel
+};
+
+// ---------------------------------------------------------------------------
+// Schedule helpers (identical in every role, so all roles see one sequence)
+// ---------------------------------------------------------------------------
+struct Seg {
+  int tile, kb0, kb1;
+};
+
+__device__ __forceinline__ long long sk_begin(const GemmArgs& a, int c) {
+  return a.sk_iters * c / gridDim.x;
+}
+// The CTA whose stream-K range holds iteration i (every range is non-empty).
+__device__ __forceinline__ int sk_cta_of(const GemmArgs& a, long long i) {
+  return static_cast<int>(((i + 1) * gridDim.x - 1) / a.sk_iters);
+}
+
+struct SegIter {
+  int dp_next;
+  long long i, i_end;
+  __device__ explicit SegIter(const GemmArgs& a) {
+    dp_next = blockIdx.x;
+    i = sk_begin(a, blockIdx.x);
+    i_end = sk_begin(a, blockIdx.x + 1);
+  }
+  __device__ bool next(const GemmArgs& a, Seg& s) {
+    if (dp_next < a.dp_tiles) {
+      s.tile = dp_next;
+      s.kb0 = 0;
+      s.kb1 = a.kpt;
+      dp_next += gridDim.x;
+      return true;
+    }
+    if (i < i_end) {
+      const long long t = i / a.kpt;
+      s.tile = a.dp_tiles + static_cast<int>(t);
+      s.kb0 = static_cast<int>(i - t * a.kpt);
+      const long long left = i_end - i;
+      s.kb1 = static_cast<int>(left < a.kpt - s.kb0 ? s.kb0 + left : a.kpt);
+      i += s.kb1 - s.kb0;
+      return true;
+    }
+    return false;
+  }
+};
+
+// normal mode: tile -> (token block m, column block n, shard s)
+__device__ __forceinline__ void decode_tile_normal(const GemmArgs& a, int tile, int& m, int& n, int& s) {
+  if (tile < a.r1_tiles) {
+    const int nq = a.rep > 1 ? a.n_q_tiles : a.n_tiles;
+    m = tile % a.m_tiles;
+    const int r = tile / a.m_tiles;
+    n = r % nq;
+    s = r / nq;
+  } else {
+    const int t2 = tile - a.r1_tiles;
+    const int nk = a.n_tiles - a.n_q_tiles;
+    m = t2 % a.m_tiles;
+    const int r = t2 / a.m_tiles;
+    n = a.n_q_tiles + r % nk;
+    s = (r / nk) * a.rep;
+  }
+}
+
+// swap mode: tile -> (weight-row block m, shard s); ROW_SUM has s = 0
+__device__ __forceinline__ void decode_tile_swap(const GemmArgs& a, int tile, int& m, int& s) {
+  m = tile % a.m_tiles;
+  s = tile / a.m_tiles;
+}
+
+// Named barrier 1 over the 128 epilogue threads (warps 2..5).
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Barrier over the 128 epilogue threads that also ORs a predicate across
+// them, so every epilogue warp takes the same branch (no warp can be left
+// waiting at a later named barrier for one that gave up).
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void load_bf16x8_f(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+  v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
+  v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
+}
+__device__ __forceinline__ void store_bf16x8_f(__nv_bfloat16* p, const float* v) {
+  uint4 q;
+  q.x = pack_bf16x2(v[0], v[1]); q.y = pack_bf16x2(v[2], v[3]);
+  q.z = pack_bf16x2(v[4], v[5]); q.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = q;
+}
+
+// ---------------------------------------------------------------------------
+// Accumulator sources for the epilogue: TMEM, or the sum of workspace pieces.
+// Partial slot layout: float4 index (col/4) * 128 + row, so a warp's 32 rows
+// read and write 512 contiguous bytes.
+// ---------------------------------------------------------------------------
+struct TmemSrc {
+  uint32_t t_acc;  // lane quadrant + accumulator buffer already applied
+  template <int N>
+  __device__ __forceinline__ void fetch(int col, float* v) const {
+    if constexpr (N == 32) {
+      uint32_t r[32];
+      tmem_ld32(t_acc + col, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    } else {
+      uint32_t r[16];
+      tmem_ld16(t_acc + col, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+    }
+  }
+};
+
+struct PartialSrc {
+  const float* ws;  // partial workspace base
+  int slot_floats;
+  int c_first, c_last;  // CTAs whose pieces make up this tile, in k order
+  int row;              // this thread's row within the tile
+  const GemmArgs* a;
+  int tile_local;       // tile - dp_tiles
+  __device__ __forceinline__ const float4* slot_ptr(int c) const {
+    const long long f = a->sk_iters * c / gridDim.x;
+    const int first_local = static_cast<int>(f / a->kpt);
+    const int slot = 2 * c + (first_local == tile_local ? 0 : 1);
+    return reinterpret_cast<const float4*>(ws + static_cast<size_t>(slot) * slot_floats);
+  }
+  template <int N>
+  __device__ __forceinline__ void fetch(int col, float* v) const {
+#pragma unroll
+    for (int j = 0; j < N; ++j) v[j] = 0.0f;
+    for (int c = c_first; c <= c_last; ++c) {
+      const float4* p = slot_ptr(c);
+#pragma unroll
+      for (int j4 = 0; j4 < N / 4; ++j4) {
+        const float4 q = __ldcg(p + static_cast<size_t>(col / 4 + j4) * 128 + row);
+        v[4 * j4 + 0] += q.x; v[4 * j4 + 1] += q.y; v[4 * j4 + 2] += q.z; v[4 * j4 + 3] += q.w;
+      }
+    }
+  }
+};
+
+// Store this thread's accumulator row (ncols columns) from TMEM into a slot.
+template <int CHUNK>
+__device__ __forceinline__ void store_partial(uint32_t t_acc, float* slot, int row, int ncols) {
+  float4* p = reinterpret_cast<float4*>(slot);
+  for (int c = 0; c < ncols; c += CHUNK) {
+    float v[CHUNK];
+    TmemSrc{t_acc}.template fetch<CHUNK>(c, v);
+#pragma unroll
+    for (int j4 = 0; j4 < CHUNK / 4; ++j4)
+      __stcg(p + static_cast<size_t>(c / 4 + j4) * 128 + row,
+             make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Tile epilogues
+// ---------------------------------------------------------------------------
+// normal mode: this thread owns token row `row`; columns are output features.
+template <class Cfg, class Src>
+__device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& src, int row, int n_blk,
+                                                int s) {
+  const bool row_ok = row < a.M;
+  if constexpr (Cfg::IS_COL) {
+    constexpr int NOUT = Cfg::SWIGLU ? 128 : 256;
+    const int n0 = n_blk * NOUT;
+    const int copies = (a.rep > 1 && n_blk >= a.n_q_tiles) ? a.rep : 1;
+    __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.out);
+    const __nv_bfloat16* bias = a.bias ? a.bias + static_cast<size_t>(s) * a.Ns : nullptr;
+    const __nv_bfloat16* bias_up = a.bias_up ? a.bias_up + static_cast<size_t>(s) * a.Ns : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < NOUT; c += 32) {
+      float g[32];
+      src.template fetch<32>(c, g);
+      float u[Cfg::SWIGLU ? 32 : 1];
+      if constexpr (Cfg::SWIGLU) src.template fetch<32>(NOUT + c, u);
+#pragma unroll
+      for (int j8 = 0; j8 < 32; j8 += 8) {
+        const int n = n0 + c + j8;
+        if (!row_ok || n >= a.Ns) continue;
+        float v[8], b[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = g[j8 + j];
+        if (bias) {
+          load_bf16x8_f(bias + n, b);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] += b[j];
+        }
+        if constexpr (Cfg::SWIGLU) {
+          float w[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[j] = u[j8 + j];
+          if (bias_up) {
+            load_bf16x8_f(bias_up + n, b);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] += b[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = act_silu(v[j]) * w[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = apply_act(a.act, v[j]);
+        }
+        for (int r = 0; r < copies; ++r) {
+          const size_t sr = static_cast<size_t>(s + r);
+          const size_t off = a.out_concat
+                                 ? static_cast<size_t>(row) * (static_cast<size_t>(a.tp) * a.Ns) + sr * a.Ns + n
+                                 : (sr * a.M + row) * static_cast<size_t>(a.Ns) + n;
+          store_bf16x8_f(Y + off, v);
+        }
+      }
+    }
+  } else if constexpr (Cfg::KIND == GK_ROW_SUM) {
+    const int n0 = n_blk * 256;
+    __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.out);
+    const size_t row_off = static_cast<size_t>(row) * a.Ns;
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      float g[32];
+      src.template fetch<32>(c, g);
+#pragma unroll
+      for (int j8 = 0; j8 < 32; j8 += 8) {
+        const int n = n0 + c + j8;
+        if (!row_ok || n >= a.Ns) continue;
+        float v[8], b[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = g[j8 + j];
+        if (a.bias) {
+          load_bf16x8_f(a.bias + n, b);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] += b[j];
+        }
+        if (a.residual) {
+          load_bf16x8_f(a.residual + row_off + n, b);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] += b[j];
+        }
+        store_bf16x8_f(Y + row_off + n, v);
+      }
+    }
+  } else {  // GK_ROW_PARTIAL
+    const int n0 = n_blk * 256;
+    float* P = static_cast<float*>(a.out);
+    const size_t row_off = (static_cast<size_t>(s) * a.M + row) * static_cast<size_t>(a.Ns);
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      float g[32];
+      src.template fetch<32>(c, g);
+#pragma unroll
+      for (int j4 = 0; j4 < 32; j4 += 4) {
+        const int n = n0 + c + j4;
+        if (row_ok && n < a.Ns)
+          *reinterpret_cast<float4*>(P + row_off + n) = make_float4(g[j4], g[j4 + 1], g[j4 + 2], g[j4 + 3]);
+      }
+    }
+  }
+}
+
+// swap mode: this thread owns weight row `wrow` (an output feature); the
+// accumulator columns are tokens (gate at [0, Tpad), up at [Tpad, 2*Tpad)).
+template <class Cfg, class Src>
+__device__ __forceinline__ void epilogue_swap(const GemmArgs& a, const Src& src, int wrow, int s) {
+  const bool ok = wrow < a.Ns;
+  __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.out);
+  float bg = 0.0f, bu = 0.0f;
+  if constexpr (Cfg::IS_COL) {
+    if (ok && a.bias) bg = __bfloat162float(a.bias[static_cast<size_t>(s) * a.Ns + wrow]);
+    if constexpr (Cfg::SWIGLU)
+      if (ok && a.bias_up) bu = __bfloat162float(a.bias_up[static_cast<size_t>(s) * a.Ns + wrow]);
+  } else {
+    if (ok && a.bias) bg = __bfloat162float(a.bias[wrow]);
+  }
+#pragma unroll 1
+  for (int t0 = 0; t0 < a.M; t0 += 16) {
+    float g[16];
+    src.template fetch<16>(t0, g);
+    float u[Cfg::SWIGLU ? 16 : 1];
+    if constexpr (Cfg::SWIGLU) src.template fetch<16>(a.Tpad + t0, u);
+    if (!ok) continue;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int t = t0 + j;
+      if (t >= a.M) break;
+      float v = g[j] + bg;
+      if constexpr (Cfg::IS_COL) {
+        if constexpr (Cfg::SWIGLU) v = act_silu(v) * (u[j] + bu);
+        else v = apply_act(a.act, v);
+        const size_t off = a.out_concat
+                               ? static_cast<size_t>(t) * (static_cast<size_t>(a.tp) * a.Ns) +
+                                     static_cast<size_t>(s) * a.Ns + wrow
+                               : (static_cast<size_t>(s) * a.M + t) * static_cast<size_t>(a.Ns) + wrow;
+        Y[off] = __float2bfloat16_rn(v);
+      } else {  // ROW_SUM
+        const size_t off = static_cast<size_t>(t) * a.Ns + wrow;
+        if (a.residual) v += __bfloat162float(a.residual[off]);
+        Y[off] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int KIND, bool SWAP>
+__global__ void __launch_bounds__(192, 1)
+    tp_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
+                   const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
+                   const GemmArgs args) {
+  using Cfg = GemmCfg<KIND, SWAP>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+  uint64_t* full = bars;                        // [STAGES]  TMA -> MMA
+  uint64_t* empty = bars + Cfg::STAGES;         // [STAGES]  MMA -> TMA
+  uint64_t* tfull = bars + 2 * Cfg::STAGES;     // [2]       MMA -> epilogue
+  uint64_t* tempty = tfull + 2;                 // [2]       epilogue -> MMA
+  uint64_t* drain = tempty + 2;                 // [1]       abort path only
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Cfg::STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&mapA0);
+    tma_prefetch_desc(&mapB0);
+    if (Cfg::SWIGLU) {
+      tma_prefetch_desc(&mapA1);
+      tma_prefetch_desc(&mapB1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------ TMA producer ------------------------------
+      const uint32_t stage_tx = SWAP ? static_cast<uint32_t>(Cfg::A_BYTES + args.Tpad * 128)
+                                     : static_cast<uint32_t>(Cfg::STAGE_BYTES);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued[Cfg::STAGES];
+#pragma unroll
+      for (int i = 0; i < Cfg::STAGES; ++i) issued[i] = -1;
+      // test-only: withhold one load (the flag is consumed by the first launch that sees it)
+      bool skip_one = blockIdx.x == 0 && g_tp_inject == 1 && atomicExch(&g_tp_inject, 0) == 1;
+      bool ok = true;
+      SegIter it(args);
+      Seg sg;
+      while (ok && it.next(args, sg)) {
+        int m, n = 0, s;
+        if constexpr (SWAP) decode_tile_swap(args, sg.tile, m, s);
+        else decode_tile_normal(args, sg.tile, m, n, s);
+        for (int kb_i = sg.kb0; kb_i < sg.kb1; ++kb_i) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (skip_one) {
+            skip_one = false;
+          } else {
+            int ks, kb;
+            if constexpr (KIND == GK_ROW_SUM) {
+              ks = kb_i / args.kb_per_shard;
+              kb = kb_i - ks * args.kb_per_shard;
+            } else {
+              ks = s;
+              kb = kb_i;
+            }
+            uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
+            uint8_t* sb = sa + Cfg::A_BYTES;
+            mbar_arrive_expect_tx(&full[stage], stage_tx);
+            if constexpr (SWAP) {
+              // A: weight rows of shard ks; B: token rows (X for COL, Hs[ks] for ROW)
+              tma_load_3d(sa, &mapA0, &full[stage], kb * 64, m * 128, ks);
+              if constexpr (Cfg::NACC == 2) tma_load_3d(sa + Cfg::A_TILE, &mapA1, &full[stage], kb * 64, m * 128, ks);
+              tma_load_3d(sb, &mapB0, &full[stage], kb * 64, 0, Cfg::IS_COL ? 0 : ks);
+            } else {
+              tma_load_3d(sa, &mapA0, &full[stage], kb * 64, m * 128, Cfg::IS_COL ? 0 : ks);
+              if constexpr (Cfg::SWIGLU) {
+                tma_load_3d(sb, &mapB0, &full[stage], kb * 64, n * 128, ks);
+                tma_load_3d(sb + Cfg::B_BYTES / 2, &mapB1, &full[stage], kb * 64, n * 128, ks);
+              } else {
+                tma_load_3d(sb, &mapB0, &full[stage], kb * 64, n * 256, ks);
+              }
+            }
+            issued[stage] = static_cast<int>(phase);
+          }
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {  // let every copy this block started land before it exits
+        for (int i = 0; i < Cfg::STAGES; ++i)
+          if (issued[i] >= 0) mbar_wait_drain(&full[i], static_cast<uint32_t>(issued[i]));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------ MMA issuer ------------------------------
+      const uint32_t idesc = SWAP ? idesc_bf16_f32(128, args.Tpad) : idesc_bf16_f32(128, 256);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, issued_any = false;
+      SegIter it(args);
+      Seg sg;
+      while (ok && it.next(args, sg)) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_COLS);
+        for (int kb_i = sg.kb0; kb_i < sg.kb1; ++kb_i) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
+          const uint64_t bdesc = smem_desc_k_sw128(sa + Cfg::A_BYTES);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t accumulate = (kb_i > sg.kb0 || k > 0) ? 1u : 0u;
+#pragma unroll
+            for (int q = 0; q < Cfg::NACC; ++q) {
+              const uint64_t adesc = smem_desc_k_sw128(sa + q * Cfg::A_TILE);
+              // +32 bytes along K per step: +2 in the descriptor's 16-byte address units
+              tc_mma_bf16(d_tmem + static_cast<uint32_t>(q * args.Tpad), adesc + 2 * k, bdesc + 2 * k,
+                          idesc, accumulate);
+            }
+          }
+          tc_commit(&empty[stage]);
+          issued_any = true;
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok && issued_any) {  // wait for MMAs in flight before TMEM is freed
+        tc_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;        // TMEM lane quadrant this warp may access
+    const int row = q * 32 + lane; // row of the 128-row tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    SegIter it(args);
+    Seg sg;
+    while (it.next(args, sg)) {
+      const bool waited = mbar_wait(&tfull[acc], acc_phase, abort_flag);
+      if (epi_any(!waited || *abort_flag)) break;  // uniform over the four epilogue warps
+      tc_fence_after();
+      const uint32_t t_acc =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * Cfg::ACC_COLS);
+      int m, n = 0, s;
+      if constexpr (SWAP) decode_tile_swap(args, sg.tile, m, s);
+      else decode_tile_normal(args, sg.tile, m, n, s);
+      const bool whole = sg.kb0 == 0 && sg.kb1 == args.kpt;
+      if (whole) {
+        TmemSrc src{t_acc};
+        if constexpr (SWAP) epilogue_swap<Cfg>(args, src, m * 128 + row, s);
+        else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else {
+        // a piece of a split tile: park it in this CTA's workspace slot
+        const int tile_local = sg.tile - args.dp_tiles;
+        const long long f = sk_begin(args, blockIdx.x);
+        const int slot = 2 * blockIdx.x + (static_cast<int>(f / args.kpt) == tile_local ? 0 : 1);
+        float* slot_ptr = args.partials + static_cast<size_t>(slot) * Cfg::SLOT_FLOATS;
+        if constexpr (SWAP) store_partial<16>(t_acc, slot_ptr, row, Cfg::NACC * args.Tpad);
+        else store_partial<32>(t_acc, slot_ptr, row, 256);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        // count the pieces; the CTA adding the last one combines them
+        const long long i0 = static_cast<long long>(tile_local) * args.kpt;
+        const int c_first = sk_cta_of(args, i0);
+        const int c_last = sk_cta_of(args, i0 + args.kpt - 1);
+        __threadfence();
+        epi_bar();
+        if (threadIdx.x == 64) {
+          const int prev = atomicAdd(&args.counters[tile_local], 1);
+          *last_flag = (prev == c_last - c_first) ? 1 : 0;
+        }
+        epi_bar();
+        if (*last_flag) {
+          __threadfence();
+          PartialSrc src{args.partials, Cfg::SLOT_FLOATS, c_first, c_last, row, &args, tile_local};
+          if constexpr (SWAP) epilogue_swap<Cfg>(args, src, m * 128 + row, s);
+          else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s);
+          if (threadIdx.x == 64) args.counters[tile_local] = 0;
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace tpk

@@ -55,7 +55,7 @@ def view(K=64, N=256, tp=2, mode=COL, dtype=F32, data=FAKE, hq=0, hkv=0, hd=0):
 def col(X=FAKE, T=16, W=None, Wu=None, bias=None, bias_up=None, act=0, concat=0, Y=FAKE):
     W = view() if W is None else W
     return tpl.lib.tp_column_linear(X, T, ctypes.byref(W), ctypes.byref(Wu) if Wu else None,
-                                    bias, bias_up, act, concat, Y, None)
+                                    bias, bias_up, act, concat, Y, None, 0, None)
 
 
 def test_column_linear_validation():
@@ -83,14 +83,19 @@ def test_column_linear_validation():
 def test_row_linear_validation():
     W = view(K=256, N=64, tp=2, mode=ROW)
     f = tpl.lib.tp_row_linear
-    assert f(None, 16, ctypes.byref(W), None, None, FAKE, None) == NULL
-    assert f(FAKE, 16, ctypes.byref(view(K=255, N=64, tp=2, mode=ROW)), None, None, FAKE, None) == SHAPE
-    assert f(FAKE, 16, ctypes.byref(view(mode=COL)), None, None, FAKE, None) == MODE
-    assert f(FAKE, -3, ctypes.byref(W), None, None, FAKE, None) == SHAPE
+    assert f(None, 16, ctypes.byref(W), None, None, FAKE, None, 0, None) == NULL
+    assert f(FAKE, 16, ctypes.byref(view(K=255, N=64, tp=2, mode=ROW)), None, None, FAKE, None, 0, None) == SHAPE
+    assert f(FAKE, 16, ctypes.byref(view(mode=COL)), None, None, FAKE, None, 0, None) == MODE
+    assert f(FAKE, -3, ctypes.byref(W), None, None, FAKE, None, 0, None) == SHAPE
     Wb = view(K=256, N=64, tp=4, mode=ROW, dtype=BF16)   # K/tp = 64
-    assert f(FAKE, 16, ctypes.byref(Wb), FAKE + 8, None, FAKE, None) == ALIGN
+    assert f(FAKE, 16, ctypes.byref(Wb), FAKE + 8, None, FAKE, None, 0, None) == ALIGN
     Wb = view(K=4 * 12, N=64, tp=4, mode=ROW, dtype=BF16)  # K/tp = 12, not % 8
-    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, None) == ALIGN
+    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, None, 0, None) == ALIGN
+    Wb = view(K=256, N=64, tp=4, mode=ROW, dtype=BF16)
+    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, FAKE + 16, 1 << 40, None) == ALIGN      # workspace 256-aligned
+    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, FAKE, 1024, None) == WORKSPACE          # too small
+    assert tpl.lib.tp_gemm_workspace_bytes(16, ctypes.byref(Wb)) > 0
+    assert tpl.lib.tp_gemm_workspace_bytes(16, ctypes.byref(W)) == 0                              # fp32: none
     g = tpl.lib.tp_row_linear_partials
     assert g(FAKE, 16, ctypes.byref(W), None, None) == NULL
 

@@ -148,3 +148,76 @@ def test_small_token_counts(T):
     _, ref = O.mlp_block(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, "swiglu", W_up=f64(d["Wu"]), residual=f64(R))
     assert_close(Y, ref, TOL_BF16, f"decode-shaped T={T}")
     assert tpl.tp_get_error() == 0
+
+
+@pytest.mark.parametrize("hq,hkv,tp", [(32, 8, 16), (32, 2, 32), (32, 4, 8)])
+def test_attn_proj_replica_dedup(hq, hkv, tp):
+    """kv heads replicated over tp/hkv shards: their K|V tiles are computed once
+    and stored to every shard of the group (hd 128 makes whole K|V tiles)."""
+    T, H, hd = 260, 256, 128
+    d = S.gqa_proj(T, H, hq, hkv, hd, seeds=(71, 72, 73, 74, 75))
+    Sqkv = tpl.tp_shard_qkv(dev(d["Wq"]), dev(d["Wk"]), dev(d["Wv"]), hq, hkv, hd, tp)
+    So = tpl.tp_shard_weights(dev(d["Wo"]), tp, "row")
+    qkv_ref, _, Y_ref = O.attn_proj(*(f64(d[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo")), hq, hkv, hd, tp)
+    qkv = torch.full((tp, T, qkv_ref[0].shape[1]), float("nan"), dtype=B, device="cuda")
+    Y = tpl.tp_attn_proj(dev(d["X"]), Sqkv, So, qkv_out=qkv)
+    assert_close(qkv, np.stack(qkv_ref), TOL_BF16, "qkv with replicas")
+    g = qkv.float().cpu().numpy()
+    rep = tp // hkv
+    kv0 = hq // tp * hd
+    c0 = -(-kv0 // 256) * 256   # first column of the whole-K|V tiles (computed once per group)
+    for s in range(0, tp, rep):  # deduped tiles: replicas hold bitwise the primary's values
+        for r in range(1, rep):
+            np.testing.assert_array_equal(g[s][:, c0:], g[s + r][:, c0:])
+    assert_close(Y, Y_ref, TOL_BF16, "attn with replicas")
+    # the standalone call (whole tiles, no workspace) dedups the same way; its
+    # summation order differs from the split-tile schedule, so compare within rounding
+    qkv2 = tpl.tp_column_linear(dev(d["X"]), Sqkv)
+    assert_close(qkv2, np.stack(qkv_ref), TOL_BF16, "standalone qkv with replicas")
+    g2 = qkv2.float().cpu().numpy()
+    for s in range(0, tp, rep):
+        for r in range(1, rep):
+            np.testing.assert_array_equal(g2[s][:, c0:], g2[s + r][:, c0:])
+
+
+@pytest.mark.parametrize("T", [1, 17, 64, 65, 300])
+def test_linears_with_workspace_schedules(T):
+    """With a workspace the column/row linears split their last wave (and use
+    the weight-streaming arrangement for T <= 64); results match the oracle and
+    agree with the whole-tile schedule within rounding."""
+    K, N, tp = 512, 4 * 520, 4          # shard width 520: a 8-column tail past two 256 tiles
+    X, W, b = nb(81, (T, K)), nb(82, (K, N), 0.05), nb(83, (N,), 0.5)
+    Sc = tpl.tp_shard_weights(dev(W), tp, "col")
+    ws = torch.empty(tpl.tp_gemm_workspace_bytes(T, Sc), dtype=torch.uint8, device="cuda")
+    ref = np.stack(O.column_parallel(f64(X), f64(W), tp, f64(b), O.gelu))
+    Y1 = tpl.tp_column_linear(dev(X), Sc, bias=dev(b), act="gelu", workspace=ws)
+    Y0 = tpl.tp_column_linear(dev(X), Sc, bias=dev(b), act="gelu")
+    assert_close(Y1, ref, TOL_BF16, f"col T={T} with workspace")
+    assert_close(Y0, ref, TOL_BF16, f"col T={T} whole tiles")
+    Wr = nb(84, (N, 264), 0.05)
+    Sr = tpl.tp_shard_weights(dev(Wr), tp, "row")
+    R = nb(85, (T, 264))
+    wsr = torch.empty(tpl.tp_gemm_workspace_bytes(T, Sr), dtype=torch.uint8, device="cuda")
+    parts = O.row_parallel_partials([f64(x) for x in np.ascontiguousarray(
+        host(Y1).reshape(tp, T, N // tp))], f64(Wr), tp)
+    refr = O.all_reduce(parts) + f64(R)
+    Z1 = tpl.tp_row_linear(Y1, Sr, residual=dev(R), workspace=wsr)
+    Z0 = tpl.tp_row_linear(Y1, Sr, residual=dev(R))
+    assert_close(Z1, refr, TOL_BF16, f"row T={T} with workspace")
+    assert_close(Z0, refr, TOL_BF16, f"row T={T} whole tiles")
+    Zi = dev(R)                                       # residual aliasing the output
+    tpl.tp_row_linear(Y1, Sr, residual=Zi, out=Zi, workspace=wsr)
+    assert_close(Zi, refr, TOL_BF16, "row residual in place")
+    assert tpl.tp_get_error() == 0
+
+
+def test_swiglu_swap_many_shards_and_tails():
+    """Weight-streaming arrangement with a shard width that is not a multiple
+    of 128 and a K that is not a multiple of 64."""
+    T, H, I, tp = 5, 200, 16 * 104, 16
+    d = S.swiglu_mlp(T, H, I, seeds=(86, 87, 88, 89))
+    Sg, Su = (tpl.tp_shard_weights(dev(d[k]), tp, "col") for k in ("Wg", "Wu"))
+    Sd = tpl.tp_shard_weights(dev(d["Wd"]), tp, "row")
+    Y = tpl.tp_mlp_block(dev(d["X"]), Sg, Sd, W_up=Su, act="swiglu")
+    _, ref = O.mlp_block(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, "swiglu", W_up=f64(d["Wu"]))
+    assert_close(Y, ref, TOL_BF16, "swap swiglu tails")
