@@ -188,9 +188,9 @@ int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shar
 int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
                   const void* residual, void* Y, void* workspace, size_t ws_bytes, void* stream);
 
-/* Scratch bytes that make tp_column_linear / tp_row_linear over W at T
- * tokens use the balanced (stream-K) schedule; 0 for fp32 views or invalid
- * arguments. */
+/* Scratch bytes that let tp_column_linear / tp_row_linear over W at T
+ * tokens use the weight-streaming arrangement; 0 when none is used (T > 64,
+ * fp32 views) or for invalid arguments. */
 size_t tp_gemm_workspace_bytes(int64_t T, const tp_shards* W);
 
 /*
@@ -240,9 +240,9 @@ size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype
  *   X [T][H]; W1, W_up: TP_COL shards (K=H, N=I); W2: TP_ROW shards (K=I,
  *   N=H); all the same tp and dtype. Y [T][H]; residual may alias Y.
  *   workspace: >= tp_mlp_workspace_bytes(T, H, I, tp, dtype) bytes, 256-byte
- *   aligned; holds Hs ([tp][T][I/tp], dtype) and, for bf16, the scratch of
- *   the balanced schedule (see tp_column_linear). Its contents on return are
- *   unspecified.
+ *   aligned; holds Hs ([tp][T][I/tp], dtype) and, for bf16 with T <= 64, the
+ *   scratch of the weight-streaming arrangement (see tp_column_linear). Its
+ *   contents on return are unspecified.
  * Errors: as tp_column_linear, plus TP_ERR_WORKSPACE.
  */
 int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,

@@ -130,9 +130,9 @@ struct Scratch {
 constexpr int SK_MAX_CTAS = 160;  // grid cap of the stream-K schedule (>= SMs of a B300)
 constexpr int SWAP_MAX_T = 64;    // token counts served by the weight-streaming (swap) arrangement
 
-size_t sk_partial_bytes(bool swap) {
-  return static_cast<size_t>(2) * SK_MAX_CTAS * 128 * (swap ? 128 : 256) * sizeof(float);
-}
+// fp32 slots for split tiles of the weight-streaming arrangement: two per CTA,
+// each 128 rows x up to 128 accumulator columns.
+constexpr size_t SK_PARTIAL_BYTES = static_cast<size_t>(2) * SK_MAX_CTAS * 128 * 128 * sizeof(float);
 
 // Work split. Token-major tiles (normal arrangement) run whole, round-robin:
 // CTAs of one wave then walk the same K range in step, so the weight blocks
@@ -391,14 +391,17 @@ int run_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, con
                              : row_f32(Xs, T, W, bias, residual, Y, partials, st);
 }
 
-// Stream-K scratch carved from a caller workspace after `used` bytes.
+// Stream-K scratch carved from a caller workspace after `used` bytes. Only
+// the weight-streaming arrangement (T <= SWAP_MAX_T) splits tiles; larger T
+// needs none.
 size_t scratch_bytes(int64_t T, size_t max_tiles) {
-  return align256(sk_partial_bytes(T <= SWAP_MAX_T)) + align256(sizeof(int) * max_tiles);
+  if (T > SWAP_MAX_T) return 0;
+  return align256(SK_PARTIAL_BYTES) + align256(sizeof(int) * max_tiles);
 }
-Scratch carve_scratch(void* ws, size_t used, int64_t T, size_t max_tiles) {
+Scratch carve_scratch(void* ws, size_t used, size_t max_tiles) {
   Scratch sc{};
   char* base = static_cast<char*>(ws) + used;
-  sc.partial_bytes = sk_partial_bytes(T <= SWAP_MAX_T);
+  sc.partial_bytes = SK_PARTIAL_BYTES;
   sc.partials = reinterpret_cast<float*>(base);
   sc.counters = reinterpret_cast<int*>(base + align256(sc.partial_bytes));
   sc.ncounters = max_tiles;
@@ -548,9 +551,10 @@ int linear_scratch(const tp_shards* W, int64_t T, void* ws, size_t ws_bytes, Scr
   if (!aligned(ws, 256)) return TP_ERR_ALIGN;
   const size_t need = tp_gemm_workspace_bytes(T, W);
   if (ws_bytes < need) return TP_ERR_WORKSPACE;
+  if (need == 0) return TP_OK;  // large T: whole tiles, no scratch
   const size_t tiles = W->mode == TP_COL ? static_cast<size_t>(W->tp) * cdiv(W->N / W->tp, 128)
                                          : static_cast<size_t>(cdiv(W->N, 128));
-  *sc = carve_scratch(ws, 0, T, std::max<size_t>(2 * SK_MAX_CTAS, tiles));
+  *sc = carve_scratch(ws, 0, std::max<size_t>(2 * SK_MAX_CTAS, tiles));
   *scp = sc;
   return TP_OK;
 }
@@ -669,8 +673,8 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
   const size_t hs_bytes = align256(static_cast<size_t>(T) * W1->N * elem_size(dt));
   Scratch sc{};
   const Scratch* scp = nullptr;
-  if (dt == TP_BF16) {
-    sc = carve_scratch(workspace, hs_bytes, T, mlp_max_tiles(W1->K, W1->N, W1->tp));
+  if (dt == TP_BF16 && T <= SWAP_MAX_T) {
+    sc = carve_scratch(workspace, hs_bytes, mlp_max_tiles(W1->K, W1->N, W1->tp));
     scp = &sc;
   }
   if ((r = run_col(X, T, W1, W_up, b1, b1_up, act, 0, Hs, st, scp))) return r;
@@ -717,8 +721,8 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
   void* ctx_ws = static_cast<char*>(workspace) + qkv_bytes;
   Scratch sc{};
   const Scratch* scp = nullptr;
-  if (dt == TP_BF16) {
-    sc = carve_scratch(workspace, qkv_bytes + ctx_bytes, T,
+  if (dt == TP_BF16 && T <= SWAP_MAX_T) {
+    sc = carve_scratch(workspace, qkv_bytes + ctx_bytes,
                        attn_max_tiles(static_cast<int64_t>(hq) * hd * 4, hq, hkv, hd, tp));
     scp = &sc;
   }

@@ -33,7 +33,7 @@ def test_llama7b_swiglu_mlp_full(mlp7b, tp):
     Sd = tpl.tp_shard_weights(g["Wd"], tp, "row")
     Y = tpl.tp_mlp_block(g["X"], Sg, Sd, W_up=Su, act="swiglu")
     # the bench's two timed calls (same kernels, same schedule)
-    ws = torch.empty(max(tpl.tp_gemm_workspace_bytes(T, Sg), tpl.tp_gemm_workspace_bytes(T, Sd)),
+    ws = torch.empty(max(tpl.tp_gemm_workspace_bytes(T, Sg), tpl.tp_gemm_workspace_bytes(T, Sd), 256),
                      dtype=torch.uint8, device="cuda")
     Hs = tpl.tp_column_linear(g["X"], Sg, W_up=Su, act="swiglu", workspace=ws)
     Y2 = tpl.tp_row_linear(Hs, Sd, workspace=ws)

@@ -34,15 +34,16 @@ def short_wait_limit():
     tpl.tp_get_error()
 
 
-@pytest.mark.parametrize("path", ["whole_tiles", "stream_k", "weight_streaming"])
+@pytest.mark.parametrize("path", ["whole_tiles", "weight_streaming"])
 def test_expired_wait_is_reported_and_context_survives(short_wait_limit, path):
     T = 8 if path == "weight_streaming" else 300
     K, N, tp = 256, 2 * 1024, 2
     X, W = S.normal(101, (T, K)), S.normal(102, (K, N), 0.05)
     Sc = tpl.tp_shard_weights(dev(W), tp, "col")
     ws = None
-    if path != "whole_tiles":
+    if path == "weight_streaming":  # T <= 64 with a workspace: split tiles, stream-K schedule
         ws = torch.empty(tpl.tp_gemm_workspace_bytes(T, Sc), dtype=torch.uint8, device="cuda")
+        assert ws.numel() > 0
     ref = np.stack(O.column_parallel(f64(X), f64(W), tp))
     Xd = dev(X)
     torch.cuda.synchronize()
