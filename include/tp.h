@@ -250,6 +250,36 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
                  const void* residual, int act, void* workspace, size_t ws_bytes, void* Y,
                  void* stream);
 
+/*
+ * tp_mlp_block_static - tp_mlp_block without a caller workspace.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory at the point of the call -- for example a
+ * plug-in whose host process owns the whole device-memory budget and forbids
+ * further cudaMalloc calls, or a caller on a path where the driver's
+ * allocator must not be entered. It takes the same arguments as tp_mlp_block
+ * minus workspace/ws_bytes; Hs and the weight-streaming scratch live in one
+ * array of TP_STATIC_WORKSPACE_BYTES in the library's static device memory,
+ * which every GPU that loads the library holds until the process exits.
+ *   Limit: tp_mlp_workspace_bytes(T, H, I, tp, dtype) must not exceed
+ *   TP_STATIC_WORKSPACE_BYTES (32 MiB), else TP_ERR_WORKSPACE and nothing is
+ *   launched. For bf16 that covers T <= 64 with T * I up to about 5.7M
+ *   (e.g. the 70B-shaped decode block at T = 64), and larger T with
+ *   T * I * 2 bytes up to 32 MiB.
+ *   The first call on each device looks up the array's device address
+ *   (with that device current) and caches it; make that first call before
+ *   any stream capture. The call allocates nothing: no cudaMalloc/cudaFree
+ *   and no allocating library routine.
+ *   Every call shares the one array and the array keeps the last call's
+ *   contents (each call clears what must start at zero). Calls that overlap
+ *   on the GPU -- on different streams, or from different host threads
+ *   without ordering -- race on the array; serialise them.
+ * Errors: as tp_mlp_block.
+ */
+#define TP_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
+int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                        const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
+                        const void* residual, int act, void* Y, void* stream);
+
 /* Workspace bytes tp_attn_proj needs. */
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype);
 

@@ -19,7 +19,8 @@ __all__ = [
     "TP_F32", "TP_BF16", "TP_COL", "TP_ROW", "ACTS", "REDUCE_OPS",
     "tp_shard_weights", "tp_shard_qkv", "tp_qkv_shard_elems", "tp_column_linear",
     "tp_row_linear", "tp_row_linear_partials", "tp_gemm_workspace_bytes", "tp_shard_reduce", "tp_shard_gather",
-    "tp_mlp_workspace_bytes", "tp_mlp_block", "tp_attn_workspace_bytes", "tp_attn_proj",
+    "tp_mlp_workspace_bytes", "tp_mlp_block", "tp_mlp_block_static", "tp_attn_workspace_bytes",
+    "tp_attn_proj", "TP_STATIC_WORKSPACE_BYTES",
     "tp_rmsnorm", "tp_get_error", "tp_debug_set_wait_limit_ns", "tp_debug_inject",
     "tp_status_string",
 ]
@@ -59,6 +60,7 @@ _SIGS = {
     "tp_shard_gather": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp]),
     "tp_mlp_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
     "tp_mlp_block": (_i32, [_vp, _i64, _P, _P, _P, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp, _vp]),
+    "tp_mlp_block_static": (_i32, [_vp, _i64, _P, _P, _P, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
     "tp_attn_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
     "tp_attn_proj": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "tp_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _f32, _i32, _vp, _vp]),
@@ -259,6 +261,22 @@ def tp_mlp_block(X, W1: Shards, W2: Shards, W_up: Shards | None = None, b1=None,
         _ptr(X), T, W1.ref(), W_up.ref() if W_up is not None else None, W2.ref(), _ptr(b1),
         _ptr(b1_up), _ptr(b2), _ptr(residual), ACTS[act], _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _stream(X.device)))
+    return out
+
+
+TP_STATIC_WORKSPACE_BYTES = 32 << 20
+
+
+def tp_mlp_block_static(X, W1: Shards, W2: Shards, W_up: Shards | None = None, b1=None, b1_up=None,
+                        b2=None, residual=None, act: str = "relu", out=None):
+    """tp_mlp_block with the library's static device workspace (no caller
+    workspace; sizes beyond TP_STATIC_WORKSPACE_BYTES are refused)."""
+    T = X.shape[0]
+    if out is None:
+        out = torch.empty((T, W2.N), dtype=X.dtype, device=X.device)
+    _check("tp_mlp_block_static", lib.tp_mlp_block_static(
+        _ptr(X), T, W1.ref(), W_up.ref() if W_up is not None else None, W2.ref(), _ptr(b1),
+        _ptr(b1_up), _ptr(b2), _ptr(residual), ACTS[act], _ptr(out), _stream(X.device)))
     return out
 
 

@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "tp.h"
 #include "tp_elementwise.cuh"
@@ -679,6 +680,51 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
   }
   if ((r = run_col(X, T, W1, W_up, b1, b1_up, act, 0, Hs, st, scp))) return r;
   return run_row(Hs, T, W2, b2, residual, Y, nullptr, st, scp);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Static workspace for tp_mlp_block_static (callers that cannot allocate)
+// ---------------------------------------------------------------------------
+// The array lives in this module's static device memory. In host code its
+// name is only a host-side stand-in, so its device address is looked up with
+// cudaGetSymbolAddress once per device (with that device current) and cached.
+static __device__ __align__(256) unsigned char g_static_workspace[TP_STATIC_WORKSPACE_BYTES];
+
+namespace {
+std::mutex g_static_mu;
+void* g_static_ptr[128] = {};
+
+int static_workspace(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  if (dev < 0 || dev >= 128) return TP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return TP_ERR_CUDA;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return TP_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                        const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
+                        const void* residual, int act, void* Y, void* stream) {
+  if (!W1 || !W2) return TP_ERR_NULL;
+  // sizes beyond the static array are refused before anything else happens
+  if (tp_mlp_workspace_bytes(T, W1->K, W1->N, W1->tp, W1->dtype) > TP_STATIC_WORKSPACE_BYTES)
+    return TP_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const int r = static_workspace(&ws);
+  if (r) return r;
+  return tp_mlp_block(X, T, W1, W_up, W2, b1, b1_up, b2, residual, act, ws, TP_STATIC_WORKSPACE_BYTES, Y,
+                      stream);
 }
 
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype) {
