@@ -182,11 +182,16 @@ int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shar
  *   W         TP_ROW shards.
  *   bias      [N] or NULL.  residual [T][N] or NULL (may alias Y: each
  *             element is read before it is written, by the same thread).
- *   Y         [T][N].  workspace, ws_bytes: as tp_column_linear.
+ *   Y         [T][N].
+ *   out_dtype dtype of bias, residual and Y: W->dtype, or TP_F32 with bf16
+ *             shards (an fp32 residual stream; the shard sum, bias and
+ *             residual are added in fp32 and stored without rounding to bf16).
+ *   workspace, ws_bytes: as tp_column_linear.
  * Errors as tp_column_linear.
  */
 int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
-                  const void* residual, void* Y, void* workspace, size_t ws_bytes, void* stream);
+                  const void* residual, void* Y, int out_dtype, void* workspace, size_t ws_bytes,
+                  void* stream);
 
 /* Scratch bytes that let tp_column_linear / tp_row_linear over W at T
  * tokens use the weight-streaming arrangement; 0 when none is used (T > 64,
@@ -239,6 +244,7 @@ size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype
  *   Y     = sum_s Hs[s] @ W2_s (+ b2, once) (+ residual)
  *   X [T][H]; W1, W_up: TP_COL shards (K=H, N=I); W2: TP_ROW shards (K=I,
  *   N=H); all the same tp and dtype. Y [T][H]; residual may alias Y.
+ *   out_dtype: dtype of b2, residual and Y (as tp_row_linear).
  *   workspace: >= tp_mlp_workspace_bytes(T, H, I, tp, dtype) bytes, 256-byte
  *   aligned; holds Hs ([tp][T][I/tp], dtype) and, for bf16 with T <= 64, the
  *   scratch of the weight-streaming arrangement (see tp_column_linear). Its
@@ -247,8 +253,8 @@ size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype
  */
 int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
                  const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
-                 const void* residual, int act, void* workspace, size_t ws_bytes, void* Y,
-                 void* stream);
+                 const void* residual, int act, int out_dtype, void* workspace, size_t ws_bytes,
+                 void* Y, void* stream);
 
 /*
  * tp_mlp_block_static - tp_mlp_block without a caller workspace.
@@ -278,7 +284,7 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
 #define TP_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
 int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
                         const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
-                        const void* residual, int act, void* Y, void* stream);
+                        const void* residual, int act, int out_dtype, void* Y, void* stream);
 
 /* Workspace bytes tp_attn_proj needs. */
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype);
@@ -293,7 +299,8 @@ size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int d
  *   ctx      [tp][T][hq/tp*hd]: the attention output of each shard's heads,
  *            or NULL for the single-key stand-in (each query attends only to
  *            its own token, so the context of q head h is V of its kv head).
- *   residual [T][H] or NULL; may alias Y.
+ *   residual [T][H] or NULL; may alias Y. out_dtype: dtype of residual and Y
+ *            (as tp_row_linear).
  *   qkv_out  [tp][T][Nqkv_s] (each shard's q | k | v), or NULL to keep it in
  *            the workspace.
  *   Y        [T][H] = sum_s ctx[s] @ Wo_s (+ residual).
@@ -303,18 +310,20 @@ size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int d
  * Errors: as tp_mlp_block.
  */
 int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
-                 const void* ctx, const void* residual, void* qkv_out, void* workspace,
+                 const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
                  size_t ws_bytes, void* Y, void* stream);
 
 /*
  * tp_rmsnorm - RMSNorm on the replicated hidden ("CUDA tensor parallel
  * computations" page, local elementwise section: a norm is local when it
  * runs on the replicated hidden): Y = X * gamma / sqrt(mean(X^2) + eps),
- * fp32 statistics. X, Y [T][H]; gamma [H] or NULL (= 1).
- * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_CUDA.
+ * fp32 statistics. X [T][H] and gamma [H] (or NULL = 1) in `dtype`; Y [T][H]
+ * in `out_dtype` (e.g. an fp32 residual stream normalised into bf16 GEMM
+ * input).
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_ALIGN, TP_ERR_CUDA.
  */
-int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype,
-               void* Y, void* stream);
+int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
+               int out_dtype, void* stream);
 
 /*
  * tp_get_error - synchronise `stream`, then report and clear the device

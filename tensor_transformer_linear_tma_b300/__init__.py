@@ -53,17 +53,17 @@ _SIGS = {
     "tp_shard_qkv": (_i32, [_vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _P, _vp]),
     "tp_qkv_shard_elems": (_sz, [_i64, _i32, _i32, _i32, _i32]),
     "tp_column_linear": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _i32, _i32, _vp, _vp, _sz, _vp]),
-    "tp_row_linear": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tp_row_linear": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
     "tp_gemm_workspace_bytes": (_sz, [_i64, _P]),
     "tp_row_linear_partials": (_i32, [_vp, _i64, _P, _vp, _vp]),
     "tp_shard_reduce": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _i32, _vp, _vp]),
     "tp_shard_gather": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp]),
     "tp_mlp_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
-    "tp_mlp_block": (_i32, [_vp, _i64, _P, _P, _P, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp, _vp]),
-    "tp_mlp_block_static": (_i32, [_vp, _i64, _P, _P, _P, _vp, _vp, _vp, _vp, _i32, _vp, _vp]),
+    "tp_mlp_block": (_i32, [_vp, _i64, _P, _P, _P, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _sz, _vp, _vp]),
+    "tp_mlp_block_static": (_i32, [_vp, _i64, _P, _P, _P, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
     "tp_attn_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
-    "tp_attn_proj": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
-    "tp_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _f32, _i32, _vp, _vp]),
+    "tp_attn_proj": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _i32, _vp, _vp, _sz, _vp, _vp]),
+    "tp_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _f32, _i32, _vp, _i32, _vp]),
     "tp_get_error": (_i32, [_vp]),
     "tp_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "tp_debug_inject": (_i32, [_i32]),
@@ -98,6 +98,17 @@ def _dt(t: torch.Tensor) -> int:
 
 def _torch_dt(code: int):
     return torch.bfloat16 if code == TP_BF16 else torch.float32
+
+
+def _out_dtype(default, out=None, residual=None, out_dtype=None):
+    """Output dtype: explicit, else that of `out`, else of `residual`, else `default`."""
+    if out_dtype is not None:
+        return out_dtype
+    if out is not None:
+        return out.dtype
+    if residual is not None:
+        return residual.dtype
+    return default
 
 
 def _ptr(t):
@@ -195,14 +206,17 @@ def tp_column_linear(X, W: Shards, W_up: Shards | None = None, bias=None, bias_u
     return out
 
 
-def tp_row_linear(Xs, W: Shards, bias=None, residual=None, out=None, workspace=None):
-    """Row-parallel linear with the shard sum fused; Xs is [tp, T, K/tp]."""
+def tp_row_linear(Xs, W: Shards, bias=None, residual=None, out=None, workspace=None, out_dtype=None):
+    """Row-parallel linear with the shard sum fused; Xs is [tp, T, K/tp].
+    bias, residual and the output share out_dtype (default Xs.dtype)."""
     T = Xs.shape[1]
+    odt = _out_dtype(Xs.dtype, out, residual, out_dtype)
     if out is None:
-        out = torch.empty((T, W.N), dtype=Xs.dtype, device=Xs.device)
+        out = torch.empty((T, W.N), dtype=odt, device=Xs.device)
     ws, wsb = _ws_args(workspace)
     _check("tp_row_linear", lib.tp_row_linear(
-        _ptr(Xs), T, W.ref(), _ptr(bias), _ptr(residual), _ptr(out), ws, wsb, _stream(Xs.device)))
+        _ptr(Xs), T, W.ref(), _ptr(bias), _ptr(residual), _ptr(out), _dt(out), ws, wsb,
+        _stream(Xs.device)))
     return out
 
 
@@ -249,17 +263,19 @@ def _workspace(nbytes: int, device):
 
 
 def tp_mlp_block(X, W1: Shards, W2: Shards, W_up: Shards | None = None, b1=None, b1_up=None,
-                 b2=None, residual=None, act: str = "relu", workspace=None, out=None):
-    """column -> local activation -> row -> sum; returns Y [T, H]."""
+                 b2=None, residual=None, act: str = "relu", workspace=None, out=None, out_dtype=None):
+    """column -> local activation -> row -> sum; returns Y [T, H] (b2, residual
+    and Y in out_dtype, default X.dtype)."""
     T, H = X.shape
     need = tp_mlp_workspace_bytes(T, H, W1.N, W1.tp, _dt(X))
     if workspace is None:
         workspace = _workspace(need, X.device)
+    odt = _out_dtype(X.dtype, out, residual, out_dtype)
     if out is None:
-        out = torch.empty((T, W2.N), dtype=X.dtype, device=X.device)
+        out = torch.empty((T, W2.N), dtype=odt, device=X.device)
     _check("tp_mlp_block", lib.tp_mlp_block(
         _ptr(X), T, W1.ref(), W_up.ref() if W_up is not None else None, W2.ref(), _ptr(b1),
-        _ptr(b1_up), _ptr(b2), _ptr(residual), ACTS[act], _ptr(workspace),
+        _ptr(b1_up), _ptr(b2), _ptr(residual), ACTS[act], _dt(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _stream(X.device)))
     return out
 
@@ -268,15 +284,16 @@ TP_STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 def tp_mlp_block_static(X, W1: Shards, W2: Shards, W_up: Shards | None = None, b1=None, b1_up=None,
-                        b2=None, residual=None, act: str = "relu", out=None):
+                        b2=None, residual=None, act: str = "relu", out=None, out_dtype=None):
     """tp_mlp_block with the library's static device workspace (no caller
     workspace; sizes beyond TP_STATIC_WORKSPACE_BYTES are refused)."""
     T = X.shape[0]
+    odt = _out_dtype(X.dtype, out, residual, out_dtype)
     if out is None:
-        out = torch.empty((T, W2.N), dtype=X.dtype, device=X.device)
+        out = torch.empty((T, W2.N), dtype=odt, device=X.device)
     _check("tp_mlp_block_static", lib.tp_mlp_block_static(
         _ptr(X), T, W1.ref(), W_up.ref() if W_up is not None else None, W2.ref(), _ptr(b1),
-        _ptr(b1_up), _ptr(b2), _ptr(residual), ACTS[act], _ptr(out), _stream(X.device)))
+        _ptr(b1_up), _ptr(b2), _ptr(residual), ACTS[act], _dt(out), _ptr(out), _stream(X.device)))
     return out
 
 
@@ -286,28 +303,31 @@ def tp_attn_workspace_bytes(T: int, hq: int, hkv: int, hd: int, tp: int, dtype) 
 
 
 def tp_attn_proj(X, Wqkv: Shards, Wo: Shards, ctx=None, residual=None, qkv_out=None,
-                 workspace=None, out=None):
-    """QKV by heads -> local heads (ctx, or the single-key stand-in) -> O + sum."""
+                 workspace=None, out=None, out_dtype=None):
+    """QKV by heads -> local heads (ctx, or the single-key stand-in) -> O + sum.
+    residual and the output share out_dtype (default X.dtype)."""
     T = X.shape[0]
     v = Wqkv.view
     need = tp_attn_workspace_bytes(T, v.hq, v.hkv, v.hd, v.tp, _dt(X))
     if workspace is None:
         workspace = _workspace(need, X.device)
+    odt = _out_dtype(X.dtype, out, residual, out_dtype)
     if out is None:
-        out = torch.empty((T, Wo.N), dtype=X.dtype, device=X.device)
+        out = torch.empty((T, Wo.N), dtype=odt, device=X.device)
     _check("tp_attn_proj", lib.tp_attn_proj(
-        _ptr(X), T, Wqkv.ref(), Wo.ref(), _ptr(ctx), _ptr(residual), _ptr(qkv_out),
+        _ptr(X), T, Wqkv.ref(), Wo.ref(), _ptr(ctx), _ptr(residual), _dt(out), _ptr(qkv_out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _stream(X.device)))
     return out
 
 
-def tp_rmsnorm(X, gamma=None, eps: float = 1e-5, out=None):
+def tp_rmsnorm(X, gamma=None, eps: float = 1e-5, out=None, out_dtype=None):
+    """RMSNorm over the hidden; the output dtype may differ from X's."""
     T, H = X.shape
     if out is None:
-        out = torch.empty_like(X)
+        out = torch.empty((T, H), dtype=out_dtype or X.dtype, device=X.device)
     _check("tp_rmsnorm", lib.tp_rmsnorm(
-        _ptr(X), _ptr(gamma), T, H, eps, _dt(X), _ptr(out), _stream(X.device)))
+        _ptr(X), _ptr(gamma), T, H, eps, _dt(X), _ptr(out), _dt(out), _stream(X.device)))
     return out
 
 

@@ -197,7 +197,7 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
   a.kpt = a.kb_per_shard;
   a.act = act;
   a.out_concat = concat;
-  a.bias = static_cast<const bf16*>(bias);
+  a.bias = bias;
   a.bias_up = static_cast<const bf16*>(bias_up);
   a.out = Y;
   CUtensorMap mx, mw, mu;
@@ -240,7 +240,7 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
 // Row-parallel bf16 GEMM: fused shard sum (partials_out == nullptr) or
 // per-shard fp32 contributions.
 int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
-             void* Y, float* partials_out, const Scratch* sc, cudaStream_t st) {
+             void* Y, int out_dtype, float* partials_out, const Scratch* sc, cudaStream_t st) {
   const int tp = W->tp;
   const int64_t Ks = W->K / tp, N = W->N;
   const bool swap = sc != nullptr && T <= SWAP_MAX_T && partials_out == nullptr;
@@ -250,8 +250,9 @@ int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, co
   a.tp = tp;
   a.rep = 1;
   a.kb_per_shard = static_cast<int>(cdiv(Ks, 64));
-  a.bias = static_cast<const bf16*>(bias);
-  a.residual = static_cast<const bf16*>(residual);
+  a.bias = bias;
+  a.residual = residual;
+  a.out_f32 = (out_dtype == TP_F32 && partials_out == nullptr) ? 1 : 0;
   CUtensorMap mx, mw;
   if (swap) {
     a.Tpad = tpad_of(T);
@@ -356,16 +357,25 @@ int check_col(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu,
   return TP_OK;
 }
 
+// bias, residual and out are in out_dt: bf16, or fp32 (a residual stream kept
+// in fp32 while the GEMM operands are bf16); the fp32 path writes fp32 only.
+int check_out_dtype(const tp_shards* W, int out_dt) {
+  if (!dtype_ok(out_dt)) return TP_ERR_DTYPE;
+  if (W->dtype == TP_F32 && out_dt != TP_F32) return TP_ERR_DTYPE;
+  return TP_OK;
+}
+
 int check_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
               const void* out, int out_dt) {
   if ((!Xs || !out) && T != 0) return TP_ERR_NULL;
   int r = check_view(W, TP_ROW);
   if (r) return r;
+  if ((r = check_out_dtype(W, out_dt))) return r;
   if (T < 0) return TP_ERR_SHAPE;
   if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
   const int dt = W->dtype;
-  if (!ptr_ok(Xs, dt) || !ptr_ok(bias, dt) || !ptr_ok(residual, dt) || !ptr_ok(out, out_dt))
-    return TP_ERR_ALIGN;
+  if (!ptr_ok(Xs, dt) || !ptr_ok(bias, dt) || !ptr_ok(residual, dt) || !ptr_ok(out, dt))
+    return TP_ERR_ALIGN;  // bf16 path: 16-byte vectors for every dtype of out
   return TP_OK;
 }
 
@@ -386,9 +396,9 @@ int run_col(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, c
 }
 
 int run_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
-            void* Y, float* partials, cudaStream_t st, const Scratch* sc = nullptr) {
+            void* Y, int out_dtype, float* partials, cudaStream_t st, const Scratch* sc = nullptr) {
   if (T == 0) return TP_OK;
-  return W->dtype == TP_BF16 ? row_bf16(Xs, T, W, bias, residual, Y, partials, sc, st)
+  return W->dtype == TP_BF16 ? row_bf16(Xs, T, W, bias, residual, Y, out_dtype, partials, sc, st)
                              : row_f32(Xs, T, W, bias, residual, Y, partials, st);
 }
 
@@ -572,20 +582,21 @@ int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shar
 }
 
 int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
-                  const void* residual, void* Y, void* workspace, size_t ws_bytes, void* stream) {
-  int r = check_row(Xs, T, W, bias, residual, Y, W ? W->dtype : TP_F32);
+                  const void* residual, void* Y, int out_dtype, void* workspace, size_t ws_bytes,
+                  void* stream) {
+  int r = check_row(Xs, T, W, bias, residual, Y, out_dtype);
   if (r) return r;
   Scratch sc{};
   const Scratch* scp;
   if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return r;
-  return run_row(Xs, T, W, bias, residual, Y, nullptr, as_stream(stream), scp);
+  return run_row(Xs, T, W, bias, residual, Y, out_dtype, nullptr, as_stream(stream), scp);
 }
 
 int tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float* partials,
                            void* stream) {
-  const int r = check_row(Xs, T, W, nullptr, nullptr, partials, TP_BF16);
+  const int r = check_row(Xs, T, W, nullptr, nullptr, partials, TP_F32);
   if (r) return r;
-  return run_row(Xs, T, W, nullptr, nullptr, nullptr, partials, as_stream(stream));
+  return run_row(Xs, T, W, nullptr, nullptr, nullptr, TP_F32, partials, as_stream(stream));
 }
 
 int tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op, const void* bias,
@@ -657,12 +668,13 @@ size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype
 
 int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
                  const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
-                 const void* residual, int act, void* workspace, size_t ws_bytes, void* Y,
-                 void* stream) {
+                 const void* residual, int act, int out_dtype, void* workspace, size_t ws_bytes,
+                 void* Y, void* stream) {
   if (!W2 || (!workspace && T != 0)) return TP_ERR_NULL;
   int r = check_col(X, T, W1, W_up, b1, b1_up, act, 0, Y);
   if (r) return r;
   if ((r = check_view(W2, TP_ROW))) return r;
+  if ((r = check_out_dtype(W2, out_dtype))) return r;
   if (W2->dtype != W1->dtype) return TP_ERR_DTYPE;
   if (W2->tp != W1->tp || W2->K != W1->N || W2->N != W1->K) return TP_ERR_SHAPE;
   const int dt = W1->dtype;
@@ -679,7 +691,7 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
     scp = &sc;
   }
   if ((r = run_col(X, T, W1, W_up, b1, b1_up, act, 0, Hs, st, scp))) return r;
-  return run_row(Hs, T, W2, b2, residual, Y, nullptr, st, scp);
+  return run_row(Hs, T, W2, b2, residual, Y, out_dtype, nullptr, st, scp);
 }
 
 }  // extern "C"
@@ -715,7 +727,7 @@ extern "C" {
 
 int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
                         const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
-                        const void* residual, int act, void* Y, void* stream) {
+                        const void* residual, int act, int out_dtype, void* Y, void* stream) {
   if (!W1 || !W2) return TP_ERR_NULL;
   // sizes beyond the static array are refused before anything else happens
   if (tp_mlp_workspace_bytes(T, W1->K, W1->N, W1->tp, W1->dtype) > TP_STATIC_WORKSPACE_BYTES)
@@ -723,8 +735,8 @@ int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_
   void* ws = nullptr;
   const int r = static_workspace(&ws);
   if (r) return r;
-  return tp_mlp_block(X, T, W1, W_up, W2, b1, b1_up, b2, residual, act, ws, TP_STATIC_WORKSPACE_BYTES, Y,
-                      stream);
+  return tp_mlp_block(X, T, W1, W_up, W2, b1, b1_up, b2, residual, act, out_dtype, ws,
+                      TP_STATIC_WORKSPACE_BYTES, Y, stream);
 }
 
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype) {
@@ -740,7 +752,7 @@ size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int d
 }
 
 int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
-                 const void* ctx, const void* residual, void* qkv_out, void* workspace,
+                 const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
                  size_t ws_bytes, void* Y, void* stream) {
   if (!Wo || !Wqkv || (!workspace && T != 0)) return TP_ERR_NULL;
   int r = check_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, Y);
@@ -751,6 +763,7 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
     return TP_ERR_SHAPE;
   if ((r = check_view(Wo, TP_ROW))) return r;
   if (Wo->dtype != Wqkv->dtype) return TP_ERR_DTYPE;
+  if ((r = check_out_dtype(Wo, out_dtype))) return r;
   if (Wo->tp != tp || Wo->K != static_cast<int64_t>(hq) * hd || Wo->N != Wqkv->K) return TP_ERR_SHAPE;
   const int dt = Wqkv->dtype;
   if (!ptr_ok(ctx, dt) || !ptr_ok(residual, dt) || !ptr_ok(qkv_out, dt) || !aligned(workspace, 256))
@@ -784,25 +797,32 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
     if ((r = launch_status())) return r;
     ctx = ctx_ws;
   }
-  return run_row(ctx, T, Wo, nullptr, residual, Y, nullptr, st, scp);
+  return run_row(ctx, T, Wo, nullptr, residual, Y, out_dtype, nullptr, st, scp);
 }
 
 int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
-               void* stream) {
-  if (!X || !Y) return TP_ERR_NULL;
-  if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
+               int out_dtype, void* stream) {
+  if ((!X || !Y) && T != 0) return TP_ERR_NULL;
+  if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return TP_ERR_DTYPE;
   if (T < 0 || H < 1 || !(eps >= 0.0f)) return TP_ERR_SHAPE;
   if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
-  const size_t es = elem_size(dtype);
-  for (const void* p : {X, gamma, static_cast<const void*>(Y)})
-    if (p && !aligned(p, es)) return TP_ERR_ALIGN;
+  for (const void* p : {X, gamma})
+    if (p && !aligned(p, elem_size(dtype))) return TP_ERR_ALIGN;
+  if (Y && !aligned(Y, elem_size(out_dtype))) return TP_ERR_ALIGN;
   if (T == 0) return TP_OK;
   const cudaStream_t st = as_stream(stream);
-  if (dtype == TP_BF16)
-    tpk::rmsnorm_kernel<bf16><<<static_cast<unsigned>(T), 256, 0, st>>>(
+  const unsigned grid = static_cast<unsigned>(T);
+  if (dtype == TP_BF16 && out_dtype == TP_BF16)
+    tpk::rmsnorm_kernel<bf16, bf16><<<grid, 256, 0, st>>>(
         static_cast<const bf16*>(X), static_cast<const bf16*>(gamma), H, eps, static_cast<bf16*>(Y));
+  else if (dtype == TP_BF16)
+    tpk::rmsnorm_kernel<bf16, float><<<grid, 256, 0, st>>>(
+        static_cast<const bf16*>(X), static_cast<const bf16*>(gamma), H, eps, static_cast<float*>(Y));
+  else if (out_dtype == TP_BF16)
+    tpk::rmsnorm_kernel<float, bf16><<<grid, 256, 0, st>>>(
+        static_cast<const float*>(X), static_cast<const float*>(gamma), H, eps, static_cast<bf16*>(Y));
   else
-    tpk::rmsnorm_kernel<float><<<static_cast<unsigned>(T), 256, 0, st>>>(
+    tpk::rmsnorm_kernel<float, float><<<grid, 256, 0, st>>>(
         static_cast<const float*>(X), static_cast<const float*>(gamma), H, eps, static_cast<float*>(Y));
   return launch_status();
 }

@@ -157,12 +157,12 @@ __global__ void reduce_kernel_scalar(const float* __restrict__ P, int tp, int64_
 // RMSNorm over the replicated hidden: y = x * g / sqrt(mean(x^2) + eps),
 // fp32 statistics. One 256-thread block per token row.
 // ---------------------------------------------------------------------------
-template <typename T>
+template <typename T, typename TO>
 __global__ void rmsnorm_kernel(const T* __restrict__ X, const T* __restrict__ gamma, int64_t H,
-                               float eps, T* __restrict__ Y) {
+                               float eps, TO* __restrict__ Y) {
   const int64_t row = blockIdx.x;
   const T* x = X + row * H;
-  T* y = Y + row * H;
+  TO* y = Y + row * H;
   float ss = 0.0f;
   for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
     const float v = to_f32(x[i]);
@@ -182,7 +182,7 @@ __global__ void rmsnorm_kernel(const T* __restrict__ X, const T* __restrict__ ga
   for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
     float v = to_f32(x[i]) * inv;
     if (gamma) v *= to_f32(gamma[i]);
-    y[i] = from_f32<T>(v);
+    y[i] = from_f32<TO>(v);
   }
 }
 

@@ -90,9 +90,10 @@ struct GemmArgs {
   long long sk_iters;  // k-iterations of tiles [dp_tiles, num_tiles), split evenly over the grid
   int act;
   int out_concat;    // COL: 1 -> Y[T][tp*Ns]; 0 -> Y[tp][T][Ns]
-  const __nv_bfloat16* bias;      // COL: [tp*Ns]; ROW_SUM: [N]; may be null
+  int out_f32;       // ROW_SUM: bias, residual and Y are fp32 (else bf16)
+  const void* bias;               // COL: [tp*Ns]; ROW_SUM: [N]; may be null
   const __nv_bfloat16* bias_up;   // COL_SWIGLU up bias [tp*Ns]; may be null
-  const __nv_bfloat16* residual;  // ROW_SUM: [M][N]; may be null
+  const void* residual;           // ROW_SUM: [M][N]; may be null
   void* out;
   float* partials;   // [2 * gridDim.x][SLOT_FLOATS] when sk_iters > 0
   int* counters;     // [num_tiles - dp_tiles], zero on entry; reset to zero by the kernel
@@ -287,7 +288,8 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
     const int n0 = n_blk * NOUT;
     const int copies = (a.rep > 1 && n_blk >= a.n_q_tiles) ? a.rep : 1;
     __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.out);
-    const __nv_bfloat16* bias = a.bias ? a.bias + static_cast<size_t>(s) * a.Ns : nullptr;
+    const __nv_bfloat16* bias =
+        a.bias ? static_cast<const __nv_bfloat16*>(a.bias) + static_cast<size_t>(s) * a.Ns : nullptr;
     const __nv_bfloat16* bias_up = a.bias_up ? a.bias_up + static_cast<size_t>(s) * a.Ns : nullptr;
 #pragma unroll 1
     for (int c = 0; c < NOUT; c += 32) {
@@ -333,7 +335,6 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
     }
   } else if constexpr (Cfg::KIND == GK_ROW_SUM) {
     const int n0 = n_blk * 256;
-    __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.out);
     const size_t row_off = static_cast<size_t>(row) * a.Ns;
 #pragma unroll 1
     for (int c = 0; c < 256; c += 32) {
@@ -346,17 +347,37 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
         float v[8], b[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = g[j8 + j];
-        if (a.bias) {
-          load_bf16x8_f(a.bias + n, b);
+        if (a.out_f32) {  // fp32 bias / residual / output (an fp32 residual stream)
+          const float* bias = static_cast<const float*>(a.bias);
+          const float* res = static_cast<const float*>(a.residual);
+          if (bias) {
+            const float4 p = __ldg(reinterpret_cast<const float4*>(bias + n));
+            const float4 q = __ldg(reinterpret_cast<const float4*>(bias + n + 4));
+            v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+            v[4] += q.x; v[5] += q.y; v[6] += q.z; v[7] += q.w;
+          }
+          if (res) {
+            const float4 p = *reinterpret_cast<const float4*>(res + row_off + n);
+            const float4 q = *reinterpret_cast<const float4*>(res + row_off + n + 4);
+            v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
+            v[4] += q.x; v[5] += q.y; v[6] += q.z; v[7] += q.w;
+          }
+          float* Y = static_cast<float*>(a.out) + row_off + n;
+          *reinterpret_cast<float4*>(Y) = make_float4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<float4*>(Y + 4) = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+          if (a.bias) {
+            load_bf16x8_f(static_cast<const __nv_bfloat16*>(a.bias) + n, b);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] += b[j];
+            for (int j = 0; j < 8; ++j) v[j] += b[j];
+          }
+          if (a.residual) {  // plain load: the residual may alias Y (read before written, same thread)
+            const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.residual) + row_off + n);
+            v[0] += bf16_lo(q.x); v[1] += bf16_hi(q.x); v[2] += bf16_lo(q.y); v[3] += bf16_hi(q.y);
+            v[4] += bf16_lo(q.z); v[5] += bf16_hi(q.z); v[6] += bf16_lo(q.w); v[7] += bf16_hi(q.w);
+          }
+          store_bf16x8_f(static_cast<__nv_bfloat16*>(a.out) + row_off + n, v);
         }
-        if (a.residual) {
-          load_bf16x8_f(a.residual + row_off + n, b);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] += b[j];
-        }
-        store_bf16x8_f(Y + row_off + n, v);
       }
     }
   } else {  // GK_ROW_PARTIAL
@@ -385,11 +406,14 @@ __device__ __forceinline__ void epilogue_swap(const GemmArgs& a, const Src& src,
   __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.out);
   float bg = 0.0f, bu = 0.0f;
   if constexpr (Cfg::IS_COL) {
-    if (ok && a.bias) bg = __bfloat162float(a.bias[static_cast<size_t>(s) * a.Ns + wrow]);
+    if (ok && a.bias)
+      bg = __bfloat162float(static_cast<const __nv_bfloat16*>(a.bias)[static_cast<size_t>(s) * a.Ns + wrow]);
     if constexpr (Cfg::SWIGLU)
       if (ok && a.bias_up) bu = __bfloat162float(a.bias_up[static_cast<size_t>(s) * a.Ns + wrow]);
   } else {
-    if (ok && a.bias) bg = __bfloat162float(a.bias[wrow]);
+    if (ok && a.bias)
+      bg = a.out_f32 ? static_cast<const float*>(a.bias)[wrow]
+                     : __bfloat162float(static_cast<const __nv_bfloat16*>(a.bias)[wrow]);
   }
 #pragma unroll 1
   for (int t0 = 0; t0 < a.M; t0 += 16) {
@@ -413,8 +437,13 @@ __device__ __forceinline__ void epilogue_swap(const GemmArgs& a, const Src& src,
         Y[off] = __float2bfloat16_rn(v);
       } else {  // ROW_SUM
         const size_t off = static_cast<size_t>(t) * a.Ns + wrow;
-        if (a.residual) v += __bfloat162float(a.residual[off]);
-        Y[off] = __float2bfloat16_rn(v);
+        if (a.out_f32) {
+          if (a.residual) v += static_cast<const float*>(a.residual)[off];
+          static_cast<float*>(a.out)[off] = v;
+        } else {
+          if (a.residual) v += __bfloat162float(static_cast<const __nv_bfloat16*>(a.residual)[off]);
+          Y[off] = __float2bfloat16_rn(v);
+        }
       }
     }
   }

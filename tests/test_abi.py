@@ -83,17 +83,19 @@ def test_column_linear_validation():
 def test_row_linear_validation():
     W = view(K=256, N=64, tp=2, mode=ROW)
     f = tpl.lib.tp_row_linear
-    assert f(None, 16, ctypes.byref(W), None, None, FAKE, None, 0, None) == NULL
-    assert f(FAKE, 16, ctypes.byref(view(K=255, N=64, tp=2, mode=ROW)), None, None, FAKE, None, 0, None) == SHAPE
-    assert f(FAKE, 16, ctypes.byref(view(mode=COL)), None, None, FAKE, None, 0, None) == MODE
-    assert f(FAKE, -3, ctypes.byref(W), None, None, FAKE, None, 0, None) == SHAPE
+    assert f(None, 16, ctypes.byref(W), None, None, FAKE, F32, None, 0, None) == NULL
+    assert f(FAKE, 16, ctypes.byref(view(K=255, N=64, tp=2, mode=ROW)), None, None, FAKE, F32, None, 0, None) == SHAPE
+    assert f(FAKE, 16, ctypes.byref(view(mode=COL)), None, None, FAKE, F32, None, 0, None) == MODE
+    assert f(FAKE, -3, ctypes.byref(W), None, None, FAKE, F32, None, 0, None) == SHAPE
     Wb = view(K=256, N=64, tp=4, mode=ROW, dtype=BF16)   # K/tp = 64
-    assert f(FAKE, 16, ctypes.byref(Wb), FAKE + 8, None, FAKE, None, 0, None) == ALIGN
+    assert f(FAKE, 16, ctypes.byref(Wb), FAKE + 8, None, FAKE, BF16, None, 0, None) == ALIGN
     Wb = view(K=4 * 12, N=64, tp=4, mode=ROW, dtype=BF16)  # K/tp = 12, not % 8
-    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, None, 0, None) == ALIGN
+    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, BF16, None, 0, None) == ALIGN
     Wb = view(K=256, N=64, tp=4, mode=ROW, dtype=BF16)
-    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, FAKE + 16, 1 << 40, None) == ALIGN      # workspace 256-aligned
-    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, FAKE, 1024, None) == WORKSPACE          # too small
+    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, BF16, FAKE + 16, 1 << 40, None) == ALIGN      # workspace 256-aligned
+    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, BF16, FAKE, 1024, None) == WORKSPACE
+    assert f(FAKE, 16, ctypes.byref(Wb), None, None, FAKE, 7, None, 0, None) == DTYPE             # bad out dtype
+    assert f(FAKE, 16, ctypes.byref(W), None, None, FAKE, BF16, None, 0, None) == DTYPE            # fp32 path writes fp32          # too small
     assert tpl.lib.tp_gemm_workspace_bytes(16, ctypes.byref(Wb)) > 0
     assert tpl.lib.tp_gemm_workspace_bytes(16, ctypes.byref(W)) == 0                              # fp32: none
     g = tpl.lib.tp_row_linear_partials
@@ -155,33 +157,37 @@ def test_mlp_and_attn_validation_and_workspace():
     def call(**k):
         a = args(**k)
         return f(a["X"], a["T"], ctypes.byref(a["W1"]), ctypes.byref(a["Wu"]) if a["Wu"] else None,
-                 ctypes.byref(a["W2"]), None, None, None, None, a["act"], a["ws"], a["wsb"], a["Y"], None)
+                 ctypes.byref(a["W2"]), None, None, None, None, a["act"], a.get("odt", F32), a["ws"], a["wsb"],
+                 a["Y"], None)
     assert call(ws=None) == NULL
     assert call(wsb=16) == WORKSPACE
     assert call(W2=view(K=256, N=64, tp=4, mode=ROW)) == SHAPE        # tp mismatch
     assert call(W2=view(K=128, N=64, mode=ROW)) == SHAPE              # K of W2 != I
     assert call(W2=view(K=256, N=64, mode=COL)) == MODE
     assert call(ws=FAKE + 16) == ALIGN                                # workspace 256-aligned
+    assert call(odt=BF16) == DTYPE                                    # fp32 path writes fp32
     aw = tpl.lib.tp_attn_workspace_bytes(4096, 32, 8, 128, 16, BF16)
     assert aw >= 4096 * (16 * 4 * 128) * 2 + 4096 * 4096 * 2
     Wqkv = view(K=4096, N=16 * 4 * 128, tp=16, mode=COL, dtype=BF16, hq=32, hkv=8, hd=128)
     Wo = view(K=4096, N=4096, tp=16, mode=ROW, dtype=BF16)
     a = tpl.lib.tp_attn_proj
-    assert a(FAKE, 64, ctypes.byref(Wqkv), ctypes.byref(Wo), None, None, None, None, 1 << 40, FAKE, None) == NULL
-    assert a(FAKE, 64, ctypes.byref(Wqkv), ctypes.byref(Wo), None, None, None, FAKE, 10, FAKE, None) == WORKSPACE
+    assert a(FAKE, 64, ctypes.byref(Wqkv), ctypes.byref(Wo), None, None, BF16, None, None, 1 << 40, FAKE, None) == NULL
+    assert a(FAKE, 64, ctypes.byref(Wqkv), ctypes.byref(Wo), None, None, BF16, None, FAKE, 10, FAKE, None) == WORKSPACE
     Wplain = view(K=4096, N=16 * 4 * 128, tp=16, mode=COL, dtype=BF16)
-    assert a(FAKE, 64, ctypes.byref(Wplain), ctypes.byref(Wo), None, None, None, FAKE, 1 << 40, FAKE, None) == MODE
+    assert a(FAKE, 64, ctypes.byref(Wplain), ctypes.byref(Wo), None, None, BF16, None, FAKE, 1 << 40, FAKE, None) == MODE
     Wo_bad = view(K=2048, N=4096, tp=16, mode=ROW, dtype=BF16)
-    assert a(FAKE, 64, ctypes.byref(Wqkv), ctypes.byref(Wo_bad), None, None, None, FAKE, 1 << 40, FAKE, None) == SHAPE
+    assert a(FAKE, 64, ctypes.byref(Wqkv), ctypes.byref(Wo_bad), None, None, BF16, None, FAKE, 1 << 40, FAKE, None) == SHAPE
 
 
 def test_rmsnorm_validation():
     f = tpl.lib.tp_rmsnorm
-    assert f(None, None, 4, 8, 1e-5, F32, FAKE, None) == NULL
-    assert f(FAKE, None, 4, 0, 1e-5, F32, FAKE, None) == SHAPE
-    assert f(FAKE, None, 4, 8, -1.0, F32, FAKE, None) == SHAPE
-    assert f(FAKE, None, 4, 8, 1e-5, 5, FAKE, None) == DTYPE
-    assert f(FAKE, None, 0, 8, 1e-5, F32, FAKE, None) == OK
+    assert f(None, None, 4, 8, 1e-5, F32, FAKE, F32, None) == NULL
+    assert f(FAKE, None, 4, 0, 1e-5, F32, FAKE, F32, None) == SHAPE
+    assert f(FAKE, None, 4, 8, -1.0, F32, FAKE, F32, None) == SHAPE
+    assert f(FAKE, None, 4, 8, 1e-5, 5, FAKE, F32, None) == DTYPE
+    assert f(FAKE, None, 4, 8, 1e-5, F32, FAKE, 5, None) == DTYPE
+    assert f(FAKE + 2, None, 4, 8, 1e-5, F32, FAKE, BF16, None) == ALIGN
+    assert f(FAKE, None, 0, 8, 1e-5, F32, FAKE, BF16, None) == OK
 
 
 def test_binding_raises_on_error_status():

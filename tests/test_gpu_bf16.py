@@ -221,3 +221,47 @@ def test_swiglu_swap_many_shards_and_tails():
     Y = tpl.tp_mlp_block(dev(d["X"]), Sg, Sd, W_up=Su, act="swiglu")
     _, ref = O.mlp_block(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, "swiglu", W_up=f64(d["Wu"]))
     assert_close(Y, ref, TOL_BF16, "swap swiglu tails")
+
+
+def test_fp32_residual_stream_outputs():
+    """bf16 GEMM operands with fp32 bias / residual / output: the row linear's
+    output is not rounded to bf16, so it meets the fp32 tolerance; blocks whose
+    intermediate (Hs, qkv) is bf16 meet the bf16 tolerance."""
+    F = torch.float32
+    rng = np.random.default_rng(120)
+    for T in (200, 9):   # whole tiles; weight-streaming arrangement (with workspace)
+        K, N, tp = 4 * 344, 264, 4
+        Xf, W = nb(121, (T, K)), nb(122, (K, N), 0.05)
+        b = rng.standard_normal(N).astype(np.float32)          # not bf16-representable
+        R = rng.standard_normal((T, N)).astype(np.float32)
+        Xs = np.ascontiguousarray(Xf.reshape(T, tp, K // tp).transpose(1, 0, 2))
+        Sr = tpl.tp_shard_weights(dev(W), tp, "row")
+        ws = torch.empty(max(tpl.tp_gemm_workspace_bytes(T, Sr), 256), dtype=torch.uint8, device="cuda")
+        ref = O.all_reduce(O.row_parallel_partials([f64(x) for x in Xs], f64(W), tp)) + f64(b) + f64(R)
+        Rd = dev(R, F)
+        Y = tpl.tp_row_linear(dev(Xs), Sr, bias=dev(b, F), residual=Rd, workspace=ws)
+        assert Y.dtype == F
+        assert_close(Y, ref, TOL_F32, f"row linear fp32 out T={T}")
+        tpl.tp_row_linear(dev(Xs), Sr, bias=dev(b, F), residual=Rd, out=Rd, workspace=ws)  # in place
+        assert_close(Rd, ref, TOL_F32, f"row linear fp32 in place T={T}")
+    T, H, I, tp = 130, 256, 4 * 344, 4
+    d = S.swiglu_mlp(T, H, I, seeds=(123, 124, 125, 126))
+    R = rng.standard_normal((T, H)).astype(np.float32)
+    Sg, Su = (tpl.tp_shard_weights(dev(d[k]), tp, "col") for k in ("Wg", "Wu"))
+    Sd = tpl.tp_shard_weights(dev(d["Wd"]), tp, "row")
+    Y = tpl.tp_mlp_block(dev(d["X"]), Sg, Sd, W_up=Su, residual=dev(R, F), act="swiglu")
+    assert Y.dtype == F
+    _, ref = O.mlp_block(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, "swiglu", W_up=f64(d["Wu"]), residual=f64(R))
+    assert_close(Y, ref, TOL_BF16, "mlp fp32 residual")
+    hq, hkv, hd = 8, 2, 32
+    g = S.gqa_proj(T, H, hq, hkv, hd, seeds=(127, 128, 129, 130, 131))
+    Sq = tpl.tp_shard_qkv(dev(g["Wq"]), dev(g["Wk"]), dev(g["Wv"]), hq, hkv, hd, tp)
+    So = tpl.tp_shard_weights(dev(g["Wo"]), tp, "row")
+    Ya = tpl.tp_attn_proj(dev(g["X"]), Sq, So, residual=dev(R, F))
+    _, _, ref = O.attn_proj(*(f64(g[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo")), hq, hkv, hd, tp, residual=f64(R))
+    assert Ya.dtype == F
+    assert_close(Ya, ref, TOL_BF16, "attn fp32 residual")
+    h = tpl.tp_rmsnorm(dev(R, F), out_dtype=B)     # fp32 stream -> bf16 GEMM input
+    assert h.dtype == B
+    assert_close(h, O.rmsnorm(f64(R)), TOL_BF16, "rmsnorm fp32 -> bf16")
+    assert tpl.tp_get_error() == 0

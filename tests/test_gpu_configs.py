@@ -99,9 +99,9 @@ def test_stack4_lmhead_full():
             g=tpl.tp_shard_weights(dev(L["Wg"]), tp, "col"), u=tpl.tp_shard_weights(dev(L["Wu"]), tp, "col"),
             d=tpl.tp_shard_weights(dev(L["Wd"]), tp, "row")))
     lm = tpl.tp_shard_weights(dev(d["W_lm"]), tp, "col")
-    x = dev(d["X"])
+    x = torch.from_numpy(d["X"]).to("cuda")          # fp32 residual stream
     x1 = torch.empty_like(x)
-    h = torch.empty_like(x)
+    h = torch.empty(x.shape, dtype=B, device="cuda")  # bf16 GEMM input
     for Lw in layers:   # the same call sequence bench.py times
         tpl.tp_rmsnorm(x, out=h)
         tpl.tp_attn_proj(h, Lw["qkv"], Lw["o"], residual=x, out=x1)
@@ -114,4 +114,34 @@ def test_stack4_lmhead_full():
     rows = sample_rows(T, 48)
     Ls = [{k: f64(v) for k, v in L.items()} for L in d["layers"]]
     ref = O.stack_forward(f64(d["X"][rows]), Ls, f64(d["W_lm"]), tp, hq, hkv, hd)
-    assert_close(logits[rows], ref, TOL_BF16, "4-block stack + LM head")
+    # Four blocks compound the bf16 rounding of every GEMM input (the normed
+    # activations, V, Hs; logits are stored bf16). The model below rounds just
+    # those tensors on the same rows, with no GPU involved: it lands above 2e-2
+    # on its own, so the end-to-end bound is 5e-2 (each block alone meets 2e-2
+    # in the block tests).
+    model_err = bf16_storage_model_error(f64(d["X"][rows]), Ls, f64(d["W_lm"]), ref, hq, hkv, hd)
+    assert model_err > TOL_BF16
+    assert_close(logits[rows], ref, TOL_STACK, "4-block stack + LM head")
+
+
+TOL_STACK = 5e-2
+
+
+def bf16_storage_model_error(X, Ls, Wlm, ref, hq, hkv, hd):
+    """max|model - oracle| / RMS(oracle) for a model that computes exactly but
+    rounds to bf16 the tensors a bf16 pipeline must store in bf16."""
+    def bf(a):
+        a = np.asarray(a, np.float32).copy()
+        return S.to_bf16_inplace(a).astype(np.float64)
+    x = X.copy()
+    group = hq // hkv
+    for L in Ls:
+        h = bf(O.rmsnorm(x))
+        V = bf(h @ L["Wv"])
+        ctx = np.concatenate([V[:, (q // group) * hd:(q // group + 1) * hd] for q in range(hq)], 1)
+        x = x + ctx @ L["Wo"]
+        h = bf(O.rmsnorm(x))
+        g, u = h @ L["Wg"], h @ L["Wu"]
+        x = x + bf(O.silu(g) * u) @ L["Wd"]
+    y = bf(bf(O.rmsnorm(x)) @ Wlm)
+    return float(np.abs(y - ref).max() / np.sqrt(np.mean(ref ** 2)))

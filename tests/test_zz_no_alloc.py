@@ -28,13 +28,14 @@ tpl = pytest.importorskip("tensor_transformer_linear_tma_b300")
 
 TP_ERR_WORKSPACE = 6
 ACT_SWIGLU = 4
+TP_BF16 = 1
 
 
 def call_static(X, T, Sg, Su, Sd, R, Y):
     """Direct C-ABI call of tp_mlp_block_static."""
     f = tpl.lib.tp_mlp_block_static
     return f(ctypes.c_void_p(X.data_ptr()), T, Sg.ref(), Su.ref(), Sd.ref(), None, None, None,
-             ctypes.c_void_p(R.data_ptr()), ACT_SWIGLU, ctypes.c_void_p(Y.data_ptr()),
+             ctypes.c_void_p(R.data_ptr()), ACT_SWIGLU, TP_BF16, ctypes.c_void_p(Y.data_ptr()),
              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
