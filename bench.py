@@ -258,16 +258,16 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, workload: str):
+def ncu_traffic(kernel: str, workload: str, T: int):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources (null otherwise)."""
+    the current kernel sources and at this token count (null otherwise)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(f"{workload}:{kernel}")
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != kernel_source_sha() or e.get("T") != T:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -539,7 +539,7 @@ def run_gpu(args, spec):
                                                  if peak == peaks.get("bf16_tflops_sustained") else
                                                  "(bf16_tflops burst)"),
                 "unit": unit, "frac": round(achieved / peak, 4) if achieved else None,
-                "traffic": ncu_traffic(spec["dominant"], spec["name"]),
+                "traffic": ncu_traffic(spec["dominant"], spec["name"], spec["T"]),
                 "kernel_ms": round(dom_ms, 5) if dom_ms else None,
             },
             "part_ms": [round(float(np.mean(p)), 5) for p in part_ms],
@@ -547,7 +547,8 @@ def run_gpu(args, spec):
                     "h2d_bytes_per_step": int(st["X"].numel() * st["X"].element_size()),
                     "d2h_bytes_per_step": int(st["Y"].numel() * st["Y"].element_size()),
                     "ms_per_step": round(e2e_ms, 5),
-                    "copies": "pinned host buffers; upload/compute/download pipelined on 3 streams"},
+                    "copies": "pinned host buffers; upload/compute/download pipelined on 3 streams",
+                    "l2": "not flushed between e2e steps; each step touches more than the 126 MB L2"},
             "gpu_launches": st["launches_per_step"] * args.steps,
             "clocks": clocks,
             "wall_s_timed": round(t_wall, 4),

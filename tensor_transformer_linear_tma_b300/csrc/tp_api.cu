@@ -787,12 +787,13 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
   }
   if ((r = run_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, qkv, st, scp))) return r;
   if (!ctx) {
-    const int64_t total = static_cast<int64_t>(tp) * T * (hq / tp) * hd / 8;
+    const dim3 block(32, 8);
+    const dim3 grid(static_cast<unsigned>(cdiv(static_cast<int64_t>(tp) * T, 8)));
     if (dt == TP_BF16)
-      tpk::ctx_standin_kernel<bf16><<<grid_for(total, 256), 256, 0, st>>>(
+      tpk::ctx_standin_kernel<bf16><<<grid, block, 0, st>>>(
           static_cast<const bf16*>(qkv), tp, T, hq, hkv, hd, static_cast<bf16*>(ctx_ws));
     else
-      tpk::ctx_standin_kernel<float><<<grid_for(total, 256), 256, 0, st>>>(
+      tpk::ctx_standin_kernel<float><<<grid, block, 0, st>>>(
           static_cast<const float*>(qkv), tp, T, hq, hkv, hd, static_cast<float*>(ctx_ws));
     if ((r = launch_status())) return r;
     ctx = ctx_ws;

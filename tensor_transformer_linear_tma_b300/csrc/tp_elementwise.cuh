@@ -190,35 +190,33 @@ __global__ void rmsnorm_kernel(const T* __restrict__ X, const T* __restrict__ ga
 // Attention-context stand-in: with each query attending only to its own
 // token, the softmax weight is 1 and the context of local q head j is V of
 // its kv head. qkv [tp][T][Nqkv_s] (q | k | v per shard) -> ctx
-// [tp][T][nq*hd]. One thread per 8 elements (hd % 8 == 0).
+// [tp][T][nq*hd]. Block (32, 8): eight (shard, token) rows per block, the 32
+// lanes stride over the row in 16-byte chunks (bf16, hd % 8 == 0) or single
+// elements (fp32); 32-bit index math inside a row.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void ctx_standin_kernel(const T* __restrict__ qkv, int tp, int64_t Tn, int hq, int hkv,
                                    int hd, T* __restrict__ ctx) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.y + threadIdx.y;  // s * T + t
+  if (row >= static_cast<int64_t>(tp) * Tn) return;
+  const int s = static_cast<int>(row / Tn);
   const int nq = hq / tp;
   const int nkv = hkv >= tp ? hkv / tp : 1;
   const int group = hq / hkv;
-  const int64_t Nqkv = static_cast<int64_t>(nq + 2 * nkv) * hd;
-  const int64_t Nc = static_cast<int64_t>(nq) * hd;
-  const int64_t per = Nc / 8;
-  const int64_t total = static_cast<int64_t>(tp) * Tn * per;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t c = (i % per) * 8;
-    const int64_t t = (i / per) % Tn;
-    const int s = static_cast<int>(i / (per * Tn));
-    const int j = static_cast<int>(c / hd), d = static_cast<int>(c % hd);
-    const int h = s * nq + j;  // global q head
-    const int g = h / group;   // its kv head
-    const int kv0 = hkv >= tp ? s * nkv : (s * hkv) / tp;
-    const int64_t src = (static_cast<int64_t>(s) * Tn + t) * Nqkv +
-                        static_cast<int64_t>(nq + nkv) * hd + static_cast<int64_t>(g - kv0) * hd + d;
-    const int64_t dst = (static_cast<int64_t>(s) * Tn + t) * Nc + c;
-    if constexpr (sizeof(T) == 2) {
-      *reinterpret_cast<uint4*>(ctx + dst) = *reinterpret_cast<const uint4*>(qkv + src);
+  const int kv0 = hkv >= tp ? s * nkv : (s * hkv) / tp;
+  const int Nqkv = (nq + 2 * nkv) * hd;
+  const int Nc = nq * hd;
+  const T* src_row = qkv + row * Nqkv + (nq + nkv) * hd;  // start of this shard-row's V block
+  T* dst_row = ctx + row * Nc;
+  constexpr int CH = sizeof(T) == 2 ? 8 : 1;  // bf16: 16-byte chunks (hd % 8 == 0); fp32: elements
+  for (int c = threadIdx.x * CH; c < Nc; c += 32 * CH) {
+    const int j = c / hd;
+    const int g = (s * nq + j) / group;  // kv head of global q head s*nq + j
+    const T* src = src_row + (g - kv0) * hd + (c - j * hd);
+    if constexpr (CH == 8) {
+      *reinterpret_cast<uint4*>(dst_row + c) = *reinterpret_cast<const uint4*>(src);
     } else {
-#pragma unroll
-      for (int v = 0; v < 8; ++v) ctx[dst + v] = qkv[src + v];
+      dst_row[c] = *src;
     }
   }
 }
