@@ -325,8 +325,8 @@ def setup_workload(spec, torch, tpl):
             tpl.tp_column_linear(X, Sqkv, out=qkv, workspace=gws)
 
         def api_call(Xin, Yout):
-            # QKV by heads, then O + shard sum reading each query head's V block
-            # (the single-key context) straight from qkv: two launches
+            # QKV by heads (its epilogue also writes the single-key context),
+            # then O + shard sum: two launches
             tpl.tp_attn_proj(Xin, Sqkv, So, qkv_out=qkv, workspace=ws, out=Yout)
         st.update(parts=[lambda: api_call(X, Y)], X=X, Y=Y, api=api_call, launches_per_step=2,
                   keep=[Sqkv, So, qkv, ctx, ws, gws], dominant_part=part_a)

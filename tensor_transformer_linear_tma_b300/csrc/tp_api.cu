@@ -158,11 +158,77 @@ int plan_schedule(tpk::GemmArgs& a, bool swap, const Scratch* sc) {
   return sms;  // the launcher clamps it to sk_iters so that no stream-K range is empty
 }
 
+// CTA pairs of the 2-SM kernel that fit on the device at once (the
+// persistent grid of a paired launch), looked up once per device.
+template <int KIND>
+int max_cluster_pairs() {
+  using Cfg = tpk::GemmCfg<KIND, false, true>;
+  static int cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  if (cache[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2));
+    cfg.blockDim = dim3(Cfg::THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tpk::tp_gemm_kernel<KIND, false, true>, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = -1;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Paired launch: clusters of two CTAs, one pair per two SMs, each pair
+// walking the 256-token tile units round-robin.
+template <int KIND>
+int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
+                tpk::GemmArgs args, cudaStream_t st) {
+  using Cfg = tpk::GemmCfg<KIND, false, true>;
+  if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg::SMEM_BYTES) != cudaSuccess)
+    return TP_ERR_CUDA;
+  const int pairs = max_cluster_pairs<KIND>();
+  if (pairs < 1) return TP_ERR_UNSUPPORTED;
+  args.dp_tiles = args.num_tiles;
+  args.sk_iters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(args.num_tiles, pairs)));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, false, true>, a0, a1, b0, b1, args) != cudaSuccess)
+    return TP_ERR_CUDA;
+  return launch_status();
+}
+
 template <int KIND, bool SWAP>
 int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
                 tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
   using Cfg = tpk::GemmCfg<KIND, SWAP>;
   if (args.num_tiles <= 0) return TP_OK;
+  if constexpr (!SWAP) {
+    if (args.cluster > 1) return pair_launch<KIND>(a0, a1, b0, b1, args, st);
+  }
+  if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg::SMEM_BYTES) != cudaSuccess)
+    return TP_ERR_CUDA;
   int grid = plan_schedule(args, SWAP, sc);
   if (args.sk_iters > 0) {
     // every stream-K range must be non-empty: grid <= sk_iters
@@ -170,20 +236,25 @@ int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
     if (cudaMemsetAsync(args.counters, 0, sizeof(int) * (args.num_tiles - args.dp_tiles), st) != cudaSuccess)
       return TP_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg::SMEM_BYTES) != cudaSuccess)
-    return TP_ERR_CUDA;
-  tpk::tp_gemm_kernel<KIND, SWAP><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(a0, a1, b0, b1, args);
+  tpk::tp_gemm_kernel<KIND, SWAP, false><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(a0, a1, b0, b1, args);
   return launch_status();
+}
+
+// Token-major launches run as CTA pairs (2-SM MMA, 256-token units) when
+// there are at least two token blocks and pairing wastes little: an even
+// count, or enough blocks that one empty half-unit is a small fraction.
+inline int cluster_for(int64_t m_blocks) {
+  return (m_blocks >= 2 && (m_blocks % 2 == 0 || m_blocks >= 8)) ? 2 : 1;
 }
 
 inline int tpad_of(int64_t T) { return static_cast<int>(cdiv(std::max<int64_t>(T, 1), 16) * 16); }
 
 // Column-parallel bf16 GEMM. `rep` > 1 computes replicated K|V column blocks
-// once per group of rep shards (QKV views with kv heads < tp).
+// once per group of rep shards (QKV views with kv heads < tp). A non-null
+// `ctx` (QKV views only) also receives the single-key attention context.
 int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
              const void* bias_up, int act, int concat, void* Y, const Scratch* sc, int rep, int64_t kv_col0,
-             cudaStream_t st) {
+             void* ctx, cudaStream_t st) {
   const int tp = W->tp;
   const int64_t K = W->K, Ns = W->N / tp;
   const bool swiglu = act == TP_ACT_SWIGLU;
@@ -193,6 +264,7 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
   a.Ns = static_cast<int>(Ns);
   a.tp = tp;
   a.rep = 1;
+  a.cluster = 1;
   a.kb_per_shard = static_cast<int>(cdiv(K, 64));
   a.kpt = a.kb_per_shard;
   a.act = act;
@@ -200,6 +272,12 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
   a.bias = bias;
   a.bias_up = static_cast<const bf16*>(bias_up);
   a.out = Y;
+  if (ctx) {
+    a.ctx = static_cast<bf16*>(ctx);
+    a.hq = W->hq;
+    a.hkv = W->hkv;
+    a.hd = W->hd;
+  }
   CUtensorMap mx, mw, mu;
   if (swap) {
     a.Tpad = tpad_of(T);
@@ -215,11 +293,13 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
                   : gemm_launch<tpk::GK_COL, true>(mw, mu, mx, mx, a, sc, st);
   }
   const int nout = swiglu ? 128 : 256;
+  a.cluster = cluster_for(cdiv(T, 128));
+  // each CTA of a pair stages half of each 256-row B block
   if (!make_map_bf16(&mx, X, K, T, 1, 128)) return TP_ERR_CUDA;
-  if (!make_map_bf16(&mw, W->data, K, Ns, tp, swiglu ? 128 : 256)) return TP_ERR_CUDA;
+  if (!make_map_bf16(&mw, W->data, K, Ns, tp, (swiglu || a.cluster > 1) ? 128 : 256)) return TP_ERR_CUDA;
   if (swiglu && !make_map_bf16(&mu, Wu->data, K, Ns, tp, 128)) return TP_ERR_CUDA;
   if (!swiglu) mu = mw;
-  a.m_tiles = static_cast<int>(cdiv(T, 128));
+  a.m_tiles = static_cast<int>(cdiv(cdiv(T, 128), a.cluster));
   a.n_tiles = static_cast<int>(cdiv(Ns, nout));
   int nq = a.n_tiles;
   if (rep > 1 && !swiglu && tp % rep == 0) {
@@ -249,6 +329,7 @@ int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, co
   a.Ns = static_cast<int>(N);
   a.tp = tp;
   a.rep = 1;
+  a.cluster = 1;
   a.kb_per_shard = static_cast<int>(cdiv(Ks, 64));
   a.bias = bias;
   a.residual = residual;
@@ -266,9 +347,10 @@ int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, co
     a.out = Y;
     return gemm_launch<tpk::GK_ROW_SUM, true>(mw, mw, mx, mx, a, sc, st);
   }
+  a.cluster = cluster_for(cdiv(T, 128));
   if (!make_map_bf16(&mx, Xs, Ks, T, tp, 128)) return TP_ERR_CUDA;
-  if (!make_map_bf16(&mw, W->data, Ks, N, tp, 256)) return TP_ERR_CUDA;
-  a.m_tiles = static_cast<int>(cdiv(T, 128));
+  if (!make_map_bf16(&mw, W->data, Ks, N, tp, a.cluster > 1 ? 128 : 256)) return TP_ERR_CUDA;
+  a.m_tiles = static_cast<int>(cdiv(cdiv(T, 128), a.cluster));
   a.n_tiles = static_cast<int>(cdiv(N, 256));
   if (partials_out) {
     a.num_tiles = a.m_tiles * a.n_tiles * tp;
@@ -380,7 +462,8 @@ int check_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, c
 }
 
 int run_col(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
-            const void* bias_up, int act, int concat, void* Y, cudaStream_t st, const Scratch* sc = nullptr) {
+            const void* bias_up, int act, int concat, void* Y, cudaStream_t st, const Scratch* sc = nullptr,
+            void* ctx = nullptr) {
   if (T == 0) return TP_OK;
   if (W->dtype != TP_BF16) return col_f32(X, T, W, Wu, bias, bias_up, act, concat, Y, st);
   // A QKV view whose kv heads are replicated (hkv < tp): without a bias the
@@ -392,7 +475,7 @@ int run_col(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, c
     rep = W->tp / W->hkv;
     kv_col0 = static_cast<int64_t>(W->hq / W->tp) * W->hd;
   }
-  return col_bf16(X, T, W, Wu, bias, bias_up, act, concat, Y, sc, rep, kv_col0, st);
+  return col_bf16(X, T, W, Wu, bias, bias_up, act, concat, Y, sc, rep, kv_col0, ctx, st);
 }
 
 int run_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, const void* residual,
@@ -785,19 +868,21 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
                        attn_max_tiles(static_cast<int64_t>(hq) * hd * 4, hq, hkv, hd, tp));
     scp = &sc;
   }
-  if ((r = run_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, qkv, st, scp))) return r;
-  if (!ctx) {
+  // Without a caller context the single-key stand-in is used: on the bf16
+  // path the QKV epilogue writes it from the V columns it has just computed;
+  // the fp32 path copies it from qkv with a separate kernel.
+  const bool fused_ctx = !ctx && dt == TP_BF16;
+  if ((r = run_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, qkv, st, scp,
+                   fused_ctx ? ctx_ws : nullptr)))
+    return r;
+  if (!ctx && !fused_ctx) {
     const dim3 block(32, 8);
     const dim3 grid(static_cast<unsigned>(cdiv(static_cast<int64_t>(tp) * T, 8)));
-    if (dt == TP_BF16)
-      tpk::ctx_standin_kernel<bf16><<<grid, block, 0, st>>>(
-          static_cast<const bf16*>(qkv), tp, T, hq, hkv, hd, static_cast<bf16*>(ctx_ws));
-    else
-      tpk::ctx_standin_kernel<float><<<grid, block, 0, st>>>(
-          static_cast<const float*>(qkv), tp, T, hq, hkv, hd, static_cast<float*>(ctx_ws));
+    tpk::ctx_standin_kernel<float><<<grid, block, 0, st>>>(
+        static_cast<const float*>(qkv), tp, T, hq, hkv, hd, static_cast<float*>(ctx_ws));
     if ((r = launch_status())) return r;
-    ctx = ctx_ws;
   }
+  if (!ctx) ctx = ctx_ws;
   return run_row(ctx, T, Wo, nullptr, residual, Y, out_dtype, nullptr, st, scp);
 }
 

@@ -187,12 +187,13 @@ __global__ void rmsnorm_kernel(const T* __restrict__ X, const T* __restrict__ ga
 }
 
 // ---------------------------------------------------------------------------
-// Attention-context stand-in: with each query attending only to its own
-// token, the softmax weight is 1 and the context of local q head j is V of
-// its kv head. qkv [tp][T][Nqkv_s] (q | k | v per shard) -> ctx
-// [tp][T][nq*hd]. Block (32, 8): eight (shard, token) rows per block, the 32
-// lanes stride over the row in 16-byte chunks (bf16, hd % 8 == 0) or single
-// elements (fp32); 32-bit index math inside a row.
+// Attention-context stand-in as a separate copy (the fp32 path; the bf16
+// QKV GEMM writes the same context from its epilogue): with each query
+// attending only to its own token, the softmax weight is 1 and the context
+// of local q head j is V of its kv head. qkv [tp][T][Nqkv_s] (q | k | v per
+// shard) -> ctx [tp][T][nq*hd]. Block (32, 8): eight (shard, token) rows per
+// block, the 32 lanes stride over the row in 16-byte chunks (bf16, hd % 8 ==
+// 0) or single elements (fp32); 32-bit index math inside a row.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void ctx_standin_kernel(const T* __restrict__ qkv, int tp, int64_t Tn, int hq, int hkv,

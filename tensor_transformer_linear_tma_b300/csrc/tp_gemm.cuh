@@ -38,6 +38,17 @@
 // pieces in k order and runs the tile's epilogue. No CTA ever waits for
 // another, so the schedule cannot deadlock.
 //
+// CTA pairs (normal mode, PAIR): a cluster of two CTAs on two SMs computes a
+// 256 x 256 tile with the 2-SM MMA. The even CTA holds token block 2u, the
+// odd one block 2u+1 (A), and each holds one 128-row half of the weight
+// block (B: gate / up for SwiGLU, else rows [128 r, 128 r + 128)). Per SM a
+// k-step then stages 32 KB instead of 48 KB and the tensor core reads half
+// of B from each SM's shared memory, which leaves room for six stages. One
+// thread of the even CTA issues the MMAs; both CTAs' TMA loads count on the
+// even CTA's "full" barrier; its commits release the stage in both CTAs and
+// hand each CTA's accumulator half (its own tensor memory) to that CTA's
+// epilogue; both epilogues report a drained accumulator to the even CTA.
+//
 // QKV replica dedup (normal COL): when kv heads are replicated across rep
 // consecutive shards, the tiles holding only replicated K|V columns are
 // computed once, on the first shard of each group, and stored to all rep
@@ -51,10 +62,11 @@ namespace tpk {
 
 enum GemmKind : int { GK_COL = 0, GK_COL_SWIGLU = 1, GK_ROW_SUM = 2, GK_ROW_PARTIAL = 3 };
 
-template <int KIND_, bool SWAP_>
+template <int KIND_, bool SWAP_, bool PAIR_ = false>
 struct GemmCfg {
   static constexpr int KIND = KIND_;
   static constexpr bool SWAP = SWAP_;
+  static constexpr bool PAIR = PAIR_;  // normal mode only: 2-SM MMA over a CTA pair
   static constexpr bool SWIGLU = KIND_ == GK_COL_SWIGLU;
   static constexpr bool IS_COL = KIND_ == GK_COL || KIND_ == GK_COL_SWIGLU;
   static constexpr int NACC = (SWAP_ && SWIGLU) ? 2 : 1;  // A tiles per stage in swap mode
@@ -62,10 +74,10 @@ struct GemmCfg {
   static constexpr int BK = 64;
   static constexpr int A_TILE = BM * BK * 2;               // 16 KB
   static constexpr int A_BYTES = NACC * A_TILE;
-  static constexpr int B_ROWS = SWAP_ ? 64 : 256;
+  static constexpr int B_ROWS = SWAP_ ? 64 : (PAIR_ ? 128 : 256);  // rows staged by this CTA
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = SWAP_ ? (NACC == 2 ? 5 : 8) : 4;
+  static constexpr int STAGES = SWAP_ ? (NACC == 2 ? 5 : 8) : (PAIR_ ? 6 : 4);
   static constexpr int ACC_COLS = SWAP_ ? 128 : 256;      // TMEM columns per accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
   static constexpr int SLOT_FLOATS = 128 * ACC_COLS;       // one fp32 partial tile
@@ -78,7 +90,7 @@ struct GemmArgs {
   int Ns;            // normal: output columns of a tile's shard; swap: weight rows per shard
   int tp;
   int Tpad;          // swap: MMA N (tokens padded to a multiple of 16)
-  int m_tiles;       // normal: token blocks; swap: weight-row blocks
+  int m_tiles;       // normal: token-block units (pairs of blocks when cluster = 2); swap: weight-row blocks
   int n_tiles;       // normal: output-column blocks per shard; swap: 1
   int num_tiles;
   int r1_tiles;      // tiles enumerated over all shards (the rest: first shard of each replica group)
@@ -88,6 +100,7 @@ struct GemmArgs {
   int kpt;           // k-iterations per tile: kb_per_shard * (ROW_SUM ? tp : 1)
   int dp_tiles;      // tiles processed whole, round-robin
   long long sk_iters;  // k-iterations of tiles [dp_tiles, num_tiles), split evenly over the grid
+  int cluster;       // CTAs per cluster: 2 for a CTA-pair launch, else 1
   int act;
   int out_concat;    // COL: 1 -> Y[T][tp*Ns]; 0 -> Y[tp][T][Ns]
   int out_f32;       // ROW_SUM: bias, residual and Y are fp32 (else bf16)
@@ -97,6 +110,10 @@ struct GemmArgs {
   void* out;
   float* partials;   // [2 * gridDim.x][SLOT_FLOATS] when sk_iters > 0
   int* counters;     // [num_tiles - dp_tiles], zero on entry; reset to zero by the kernel
+  // COL on a QKV view: also write the single-key attention context
+  // ctx [tp][M][hq/tp * hd] from the V columns (null: no context)
+  __nv_bfloat16* ctx;
+  int hq, hkv, hd;   // the view's heads (global) and head size
 };
 
 // ---------------------------------------------------------------------------
@@ -118,7 +135,7 @@ struct SegIter {
   int dp_next;
   long long i, i_end;
   __device__ explicit SegIter(const GemmArgs& a) {
-    dp_next = blockIdx.x;
+    dp_next = blockIdx.x / a.cluster;  // the CTAs of a cluster walk the same tiles
     i = sk_begin(a, blockIdx.x);
     i_end = sk_begin(a, blockIdx.x + 1);
   }
@@ -127,7 +144,7 @@ struct SegIter {
       s.tile = dp_next;
       s.kb0 = 0;
       s.kb1 = a.kpt;
-      dp_next += gridDim.x;
+      dp_next += gridDim.x / a.cluster;
       return true;
     }
     if (i < i_end) {
@@ -143,8 +160,10 @@ struct SegIter {
   }
 };
 
-// normal mode: tile -> (token block m, column block n, shard s)
-__device__ __forceinline__ void decode_tile_normal(const GemmArgs& a, int tile, int& m, int& n, int& s) {
+// normal mode: tile -> (token block m, column block n, shard s); `rank` is
+// the CTA's rank in its cluster (token block m = unit * cluster + rank)
+__device__ __forceinline__ void decode_tile_normal(const GemmArgs& a, int tile, int rank, int& m, int& n,
+                                                   int& s) {
   if (tile < a.r1_tiles) {
     const int nq = a.rep > 1 ? a.n_q_tiles : a.n_tiles;
     m = tile % a.m_tiles;
@@ -159,6 +178,7 @@ __device__ __forceinline__ void decode_tile_normal(const GemmArgs& a, int tile, 
     n = a.n_q_tiles + r % nk;
     s = (r / nk) * a.rep;
   }
+  m = m * a.cluster + rank;
 }
 
 // swap mode: tile -> (weight-row block m, shard s); ROW_SUM has s = 0
@@ -276,6 +296,48 @@ __device__ __forceinline__ void store_partial(uint32_t t_acc, float* slot, int r
 }
 
 // ---------------------------------------------------------------------------
+// Single-key attention context, written from the QKV epilogue. With every
+// query attending only to its own token the softmax weight is 1, so the
+// context of query head g is V of its kv head g / (hq / hkv). A V column of
+// shard s (shard-local column n in the V block) is copied to each query head
+// that reads it, on each of the `copies` shards s, s+1, ... that hold it.
+// ---------------------------------------------------------------------------
+struct CtxMap {
+  int nq, nkv, group, vcol0, hd;
+  __device__ explicit CtxMap(const GemmArgs& a) {
+    nq = a.hq / a.tp;
+    nkv = a.hkv >= a.tp ? a.hkv / a.tp : 1;
+    group = a.hq / a.hkv;
+    vcol0 = (nq + nkv) * a.hd;
+    hd = a.hd;
+  }
+  __device__ int kv_first(const GemmArgs& a, int s) const {
+    return a.hkv >= a.tp ? s * nkv : (s * a.hkv) / a.tp;
+  }
+};
+
+// W elements (W = 8: one 16-byte vector; W = 1: one element) at V column n.
+template <int W>
+__device__ __forceinline__ void store_ctx(const GemmArgs& a, const CtxMap& cm, int s, int copies, int row,
+                                          int n, const float* v) {
+  const int i = (n - cm.vcol0) / cm.hd;        // kv head within the shard's V block
+  const int d = n - cm.vcol0 - i * cm.hd;      // position in the head
+  const int kvh = cm.kv_first(a, s) + i;       // global kv head (the same on every replica)
+  const size_t nc = static_cast<size_t>(cm.nq) * cm.hd;
+  for (int r = 0; r < copies; ++r) {
+    const int s2 = s + r;
+    const int g0 = max(s2 * cm.nq, kvh * cm.group);
+    const int g1 = min((s2 + 1) * cm.nq, (kvh + 1) * cm.group);
+    __nv_bfloat16* base = a.ctx + (static_cast<size_t>(s2) * a.M + row) * nc + d;
+    for (int g = g0; g < g1; ++g) {
+      __nv_bfloat16* p = base + static_cast<size_t>(g - s2 * cm.nq) * cm.hd;
+      if constexpr (W == 8) store_bf16x8_f(p, v);
+      else *p = __float2bfloat16_rn(v[0]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Tile epilogues
 // ---------------------------------------------------------------------------
 // normal mode: this thread owns token row `row`; columns are output features.
@@ -330,6 +392,12 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
                                  ? static_cast<size_t>(row) * (static_cast<size_t>(a.tp) * a.Ns) + sr * a.Ns + n
                                  : (sr * a.M + row) * static_cast<size_t>(a.Ns) + n;
           store_bf16x8_f(Y + off, v);
+        }
+        if constexpr (!Cfg::SWIGLU) {
+          if (a.ctx) {
+            const CtxMap cm(a);
+            if (n >= cm.vcol0) store_ctx<8>(a, cm, s, copies, row, n, v);
+          }
         }
       }
     }
@@ -435,6 +503,12 @@ __device__ __forceinline__ void epilogue_swap(const GemmArgs& a, const Src& src,
                                      static_cast<size_t>(s) * a.Ns + wrow
                                : (static_cast<size_t>(s) * a.M + t) * static_cast<size_t>(a.Ns) + wrow;
         Y[off] = __float2bfloat16_rn(v);
+        if constexpr (!Cfg::SWIGLU) {
+          if (a.ctx) {
+            const CtxMap cm(a);
+            if (wrow >= cm.vcol0) store_ctx<1>(a, cm, s, 1, t, wrow, &v);
+          }
+        }
       } else {  // ROW_SUM
         const size_t off = static_cast<size_t>(t) * a.Ns + wrow;
         if (a.out_f32) {
@@ -452,12 +526,13 @@ __device__ __forceinline__ void epilogue_swap(const GemmArgs& a, const Src& src,
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int KIND, bool SWAP>
+template <int KIND, bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(192, 1)
     tp_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
                    const GemmArgs args) {
-  using Cfg = GemmCfg<KIND, SWAP>;
+  using Cfg = GemmCfg<KIND, SWAP, PAIR>;
+  static_assert(!(PAIR && SWAP), "CTA pairs are a token-major arrangement");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -473,6 +548,7 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;  // 0: the pair's MMA issuer
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Cfg::STAGES; ++i) {
@@ -481,7 +557,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], PAIR ? 8 : 4);  // the epilogue warps of both CTAs of a pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -495,19 +571,26 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------ TMA producer ------------------------------
+      // The pair's full barrier counts both CTAs' bytes; only the even CTA arms it.
       const uint32_t stage_tx = SWAP ? static_cast<uint32_t>(Cfg::A_BYTES + args.Tpad * 128)
-                                     : static_cast<uint32_t>(Cfg::STAGE_BYTES);
+                                     : static_cast<uint32_t>((PAIR ? 2 : 1) * Cfg::STAGE_BYTES);
       int stage = 0;
       uint32_t phase = 0;
       int issued[Cfg::STAGES];
@@ -521,7 +604,7 @@ __global__ void __launch_bounds__(192, 1)
       while (ok && it.next(args, sg)) {
         int m, n = 0, s;
         if constexpr (SWAP) decode_tile_swap(args, sg.tile, m, s);
-        else decode_tile_normal(args, sg.tile, m, n, s);
+        else decode_tile_normal(args, sg.tile, rank, m, n, s);
         for (int kb_i = sg.kb0; kb_i < sg.kb1; ++kb_i) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -540,19 +623,30 @@ __global__ void __launch_bounds__(192, 1)
             }
             uint8_t* sa = smem + stage * Cfg::STAGE_BYTES;
             uint8_t* sb = sa + Cfg::A_BYTES;
-            mbar_arrive_expect_tx(&full[stage], stage_tx);
-            if constexpr (SWAP) {
-              // A: weight rows of shard ks; B: token rows (X for COL, Hs[ks] for ROW)
-              tma_load_3d(sa, &mapA0, &full[stage], kb * 64, m * 128, ks);
-              if constexpr (Cfg::NACC == 2) tma_load_3d(sa + Cfg::A_TILE, &mapA1, &full[stage], kb * 64, m * 128, ks);
-              tma_load_3d(sb, &mapB0, &full[stage], kb * 64, 0, Cfg::IS_COL ? 0 : ks);
+            if constexpr (PAIR) {
+              if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
+              const uint32_t fb = mapa_shared(&full[stage], 0);
+              tma_load_3d_pair(sa, &mapA0, fb, kb * 64, m * 128, Cfg::IS_COL ? 0 : ks);
+              if constexpr (Cfg::SWIGLU)
+                tma_load_3d_pair(sb, rank ? &mapB1 : &mapB0, fb, kb * 64, n * 128, ks);
+              else
+                tma_load_3d_pair(sb, &mapB0, fb, kb * 64, n * 256 + rank * 128, ks);
             } else {
-              tma_load_3d(sa, &mapA0, &full[stage], kb * 64, m * 128, Cfg::IS_COL ? 0 : ks);
-              if constexpr (Cfg::SWIGLU) {
-                tma_load_3d(sb, &mapB0, &full[stage], kb * 64, n * 128, ks);
-                tma_load_3d(sb + Cfg::B_BYTES / 2, &mapB1, &full[stage], kb * 64, n * 128, ks);
+              mbar_arrive_expect_tx(&full[stage], stage_tx);
+              if constexpr (SWAP) {
+                // A: weight rows of shard ks; B: token rows (X for COL, Hs[ks] for ROW)
+                tma_load_3d(sa, &mapA0, &full[stage], kb * 64, m * 128, ks);
+                if constexpr (Cfg::NACC == 2)
+                  tma_load_3d(sa + Cfg::A_TILE, &mapA1, &full[stage], kb * 64, m * 128, ks);
+                tma_load_3d(sb, &mapB0, &full[stage], kb * 64, 0, Cfg::IS_COL ? 0 : ks);
               } else {
-                tma_load_3d(sb, &mapB0, &full[stage], kb * 64, n * 256, ks);
+                tma_load_3d(sa, &mapA0, &full[stage], kb * 64, m * 128, Cfg::IS_COL ? 0 : ks);
+                if constexpr (Cfg::SWIGLU) {
+                  tma_load_3d(sb, &mapB0, &full[stage], kb * 64, n * 128, ks);
+                  tma_load_3d(sb + Cfg::B_BYTES / 2, &mapB1, &full[stage], kb * 64, n * 128, ks);
+                } else {
+                  tma_load_3d(sb, &mapB0, &full[stage], kb * 64, n * 256, ks);
+                }
               }
             }
             issued[stage] = static_cast<int>(phase);
@@ -563,15 +657,34 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      if constexpr (PAIR) {
+        // wait until the pair's MMAs have released every stage, so that no
+        // commit from the even CTA is still on its way to this CTA's barriers
+        for (int i = 0; ok && i < Cfg::STAGES; ++i) {
+          ok = mbar_wait(&empty[stage], phase ^ 1u, abort_flag);
+          if (++stage == Cfg::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
       if (!ok) {  // let every copy this block started land before it exits
-        for (int i = 0; i < Cfg::STAGES; ++i)
-          if (issued[i] >= 0) mbar_wait_drain(&full[i], static_cast<uint32_t>(issued[i]));
+        if (!PAIR || rank == 0) {
+          for (int i = 0; i < Cfg::STAGES; ++i)
+            if (issued[i] >= 0) mbar_wait_drain(&full[i], static_cast<uint32_t>(issued[i]));
+        } else {
+          // the odd CTA's copies count on the even CTA's barrier, which it
+          // cannot poll: give them a fixed 50 us to land
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 50000) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ------------------------------ MMA issuer ------------------------------
-      const uint32_t idesc = SWAP ? idesc_bf16_f32(128, args.Tpad) : idesc_bf16_f32(128, 256);
+      const uint32_t idesc = SWAP ? idesc_bf16_f32(128, args.Tpad) : idesc_bf16_f32(PAIR ? 256 : 128, 256);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -601,11 +714,15 @@ __global__ void __launch_bounds__(192, 1)
             for (int q = 0; q < Cfg::NACC; ++q) {
               const uint64_t adesc = smem_desc_k_sw128(sa + q * Cfg::A_TILE);
               // +32 bytes along K per step: +2 in the descriptor's 16-byte address units
-              tc_mma_bf16(d_tmem + static_cast<uint32_t>(q * args.Tpad), adesc + 2 * k, bdesc + 2 * k,
-                          idesc, accumulate);
+              if constexpr (PAIR)
+                tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, accumulate);
+              else
+                tc_mma_bf16(d_tmem + static_cast<uint32_t>(q * args.Tpad), adesc + 2 * k, bdesc + 2 * k,
+                            idesc, accumulate);
             }
           }
-          tc_commit(&empty[stage]);
+          if constexpr (PAIR) tc_commit_pair_both(&empty[stage]);
+          else tc_commit(&empty[stage]);
           issued_any = true;
           if (++stage == Cfg::STAGES) {
             stage = 0;
@@ -613,14 +730,16 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         if (!ok) break;
-        tc_commit(&tfull[acc]);
+        if constexpr (PAIR) tc_commit_pair_both(&tfull[acc]);
+        else tc_commit(&tfull[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       if (!ok && issued_any) {  // wait for MMAs in flight before TMEM is freed
-        tc_commit(drain);
+        if constexpr (PAIR) tc_commit_pair_local(drain);
+        else tc_commit(drain);
         mbar_wait_drain(drain, 0);
       }
     }
@@ -640,15 +759,18 @@ __global__ void __launch_bounds__(192, 1)
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * Cfg::ACC_COLS);
       int m, n = 0, s;
       if constexpr (SWAP) decode_tile_swap(args, sg.tile, m, s);
-      else decode_tile_normal(args, sg.tile, m, n, s);
+      else decode_tile_normal(args, sg.tile, rank, m, n, s);
       const bool whole = sg.kb0 == 0 && sg.kb1 == args.kpt;
-      if (whole) {
+      if (PAIR || whole) {
         TmemSrc src{t_acc};
         if constexpr (SWAP) epilogue_swap<Cfg>(args, src, m * 128 + row, s);
         else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
+        if (lane == 0) {
+          if (PAIR && rank != 0) mbar_arrive_cluster(mapa_shared(&tempty[acc], 0));
+          else mbar_arrive(&tempty[acc]);
+        }
       } else {
         // a piece of a split tile: park it in this CTA's workspace slot
         const int tile_local = sg.tile - args.dp_tiles;
@@ -688,9 +810,11 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // neither CTA leaves while the other may still signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    else tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
 }
 

@@ -265,3 +265,65 @@ def test_fp32_residual_stream_outputs():
     assert h.dtype == B
     assert_close(h, O.rmsnorm(f64(R)), TOL_BF16, "rmsnorm fp32 -> bf16")
     assert tpl.tp_get_error() == 0
+
+
+@pytest.mark.parametrize("T,hq,hkv,hd,tp", [(260, 32, 8, 128, 16), (260, 16, 4, 64, 4), (130, 32, 2, 128, 32),
+                                            (24, 32, 8, 128, 16), (64, 16, 16, 64, 4), (1, 8, 2, 64, 8)])
+def test_attn_fused_context(T, hq, hkv, hd, tp):
+    """Without a caller context the bf16 QKV epilogue writes the single-key
+    stand-in itself: every query head's block of the context (in the caller
+    workspace, after the qkv region) holds bitwise the V columns of its kv
+    head on the same shard. T <= 64 runs the weight-streaming arrangement,
+    hkv < tp the replica-dedup tiles."""
+    H = 256
+    d = S.gqa_proj(T, H, hq, hkv, hd, seeds=(81, 82, 83, 84, 85))
+    Sqkv = tpl.tp_shard_qkv(dev(d["Wq"]), dev(d["Wk"]), dev(d["Wv"]), hq, hkv, hd, tp)
+    So = tpl.tp_shard_weights(dev(d["Wo"]), tp, "row")
+    Ns = Sqkv.shard_width
+    ws = torch.zeros(tpl.tp_attn_workspace_bytes(T, hq, hkv, hd, tp, B), dtype=torch.uint8, device="cuda")
+    qkv = torch.empty((tp, T, Ns), dtype=B, device="cuda")
+    Y = tpl.tp_attn_proj(dev(d["X"]), Sqkv, So, qkv_out=qkv, workspace=ws)
+    assert tpl.tp_get_error() == 0
+    c0 = -(-(T * tp * Ns * 2) // 256) * 256   # the context follows the (256-aligned) qkv region
+    nc = hq // tp * hd
+    ctx = ws[c0:c0 + tp * T * nc * 2].view(B).view(tp, T, nc)
+    g = host(qkv)
+    layout = O.qkv_head_layout(hq, hkv, tp)
+    for s in range(tp):
+        want = O.context_standin(g[s], layout[s][0], layout[s][1], hq, hkv, hd)
+        np.testing.assert_array_equal(host(ctx[s]), want, err_msg=f"context of shard {s}")
+    qkv_ref, _, Y_ref = O.attn_proj(*(f64(d[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo")), hq, hkv, hd, tp)
+    assert_close(qkv, np.stack(qkv_ref), TOL_BF16, "qkv")
+    assert_close(Y, Y_ref, TOL_BF16, "attn with the fused context")
+
+
+@pytest.mark.parametrize("T", [256, 1100])
+def test_cluster_pairs(T):
+    """Token-major launches with an even number of token blocks, or at least
+    eight, run as CTA pairs (2-SM MMA, 256-token units, each CTA staging half
+    of every weight tile). 1100 tokens make 9 blocks, so the odd CTA of the
+    last unit has no token rows (its A tile is zero fill, it stores nothing)."""
+    H, I, tp = 384, 4 * 320, 4
+    d = S.swiglu_mlp(T, H, I, seeds=(91, 92, 93, 94))
+    Sg, Su = (tpl.tp_shard_weights(dev(d[k]), tp, "col") for k in ("Wg", "Wu"))
+    Sd = tpl.tp_shard_weights(dev(d["Wd"]), tp, "row")
+    Hs_ref, Y_ref = O.mlp_block(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, "swiglu", W_up=f64(d["Wu"]))
+    Hs = tpl.tp_column_linear(dev(d["X"]), Sg, W_up=Su, act="swiglu")
+    assert_close_stored(Hs, np.stack(Hs_ref), TOL_BF16, f"paired SwiGLU column T={T}")
+    assert_close(tpl.tp_row_linear(Hs, Sd), Y_ref, TOL_BF16, f"paired row sum T={T}")
+    P = tpl.tp_row_linear_partials(Hs, Sd)
+    P_ref = O.row_parallel_partials([f64(h) for h in host(Hs)], f64(d["Wd"]), tp)
+    assert_close(P, np.stack(P_ref), TOL_F32, f"paired row partials T={T}")
+    b = nb(95, (I,), 0.3)
+    Yc = tpl.tp_column_linear(dev(d["X"]), Sg, bias=dev(b), act="gelu", concat=True)
+    ref = np.concatenate(O.column_parallel(f64(d["X"]), f64(d["Wg"]), tp, bias=f64(b), act=O.gelu), axis=1)
+    assert_close_stored(Yc, ref, TOL_BF16, f"paired column, bias + GELU, concatenated T={T}")
+    g = S.gqa_proj(T, H, 16, 2, 128, seeds=(96, 97, 98, 99, 100))   # kv replicated over 4 shards of 8
+    Sqkv = tpl.tp_shard_qkv(dev(g["Wq"]), dev(g["Wk"]), dev(g["Wv"]), 16, 2, 128, 8)
+    So = tpl.tp_shard_weights(dev(g["Wo"]), 8, "row")
+    qkv_ref, _, Ya_ref = O.attn_proj(*(f64(g[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo")), 16, 2, 128, 8)
+    qkv = torch.empty((8, T, qkv_ref[0].shape[1]), dtype=B, device="cuda")
+    Ya = tpl.tp_attn_proj(dev(g["X"]), Sqkv, So, qkv_out=qkv)
+    assert_close(qkv, np.stack(qkv_ref), TOL_BF16, f"paired QKV with replicas T={T}")
+    assert_close(Ya, Ya_ref, TOL_BF16, f"paired attention projections T={T}")
+    assert tpl.tp_get_error() == 0
