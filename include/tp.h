@@ -162,9 +162,11 @@ size_t tp_qkv_shard_elems(int64_t H, int hq, int hkv, int hd, int tp);
  *           tp_gemm_workspace_bytes(T, W) bytes, 256-byte aligned. With it, a
  *           bf16 call with T <= 64 uses the weight-streaming arrangement
  *           (weights as the 128-row MMA operand, their K loops split evenly
- *           over all SMs, split tiles combined in a fixed order so results do
- *           not depend on timing); without it, and for T > 64, every tile
- *           runs whole on one SM. The two agree within rounding.
+ *           over all SMs), and a larger row-parallel call whose last round
+ *           of 256-token units leaves pairs of SMs idle cuts those units
+ *           along K into pieces run side by side. Split tiles and pieces are combined in a
+ *           fixed order, so results do not depend on timing. Without it every
+ *           tile runs whole. The two agree within rounding.
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN,
  * TP_ERR_WORKSPACE, TP_ERR_CUDA.
  */
@@ -194,8 +196,8 @@ int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bia
                   void* stream);
 
 /* Scratch bytes that let tp_column_linear / tp_row_linear over W at T
- * tokens use the weight-streaming arrangement; 0 when none is used (T > 64,
- * fp32 views) or for invalid arguments. */
+ * tokens split tiles (the weight-streaming arrangement at T <= 64, the split
+ * last round above): about 21 MB; 0 for fp32 views or invalid arguments. */
 size_t tp_gemm_workspace_bytes(int64_t T, const tp_shards* W);
 
 /*
@@ -246,9 +248,8 @@ size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype
  *   N=H); all the same tp and dtype. Y [T][H]; residual may alias Y.
  *   out_dtype: dtype of b2, residual and Y (as tp_row_linear).
  *   workspace: >= tp_mlp_workspace_bytes(T, H, I, tp, dtype) bytes, 256-byte
- *   aligned; holds Hs ([tp][T][I/tp], dtype) and, for bf16 with T <= 64, the
- *   scratch of the weight-streaming arrangement (see tp_column_linear). Its
- *   contents on return are unspecified.
+ *   aligned; holds Hs ([tp][T][I/tp], dtype) and, for bf16, the split-tile
+ *   scratch (see tp_column_linear). Its contents on return are unspecified.
  * Errors: as tp_column_linear, plus TP_ERR_WORKSPACE.
  */
 int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
@@ -263,14 +264,14 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
  * plug-in whose host process owns the whole device-memory budget and forbids
  * further cudaMalloc calls, or a caller on a path where the driver's
  * allocator must not be entered. It takes the same arguments as tp_mlp_block
- * minus workspace/ws_bytes; Hs and the weight-streaming scratch live in one
+ * minus workspace/ws_bytes; Hs and the split-tile scratch live in one
  * array of TP_STATIC_WORKSPACE_BYTES in the library's static device memory,
  * which every GPU that loads the library holds until the process exits.
  *   Limit: tp_mlp_workspace_bytes(T, H, I, tp, dtype) must not exceed
  *   TP_STATIC_WORKSPACE_BYTES (32 MiB), else TP_ERR_WORKSPACE and nothing is
- *   launched. For bf16 that covers T <= 64 with T * I up to about 5.7M
- *   (e.g. the 70B-shaped decode block at T = 64), and larger T with
- *   T * I * 2 bytes up to 32 MiB.
+ *   launched. For bf16 that covers T * I up to about 6.2M, whatever T
+ *   (Hs plus about 21 MB of scratch; e.g. the 70B-shaped decode block at
+ *   T = 64).
  *   The first call on each device looks up the array's device address
  *   (with that device current) and caches it; make that first call before
  *   any stream capture. The call allocates nothing: no cudaMalloc/cudaFree

@@ -7,9 +7,12 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <random>
 
 #include "tp.h"
 #include "tp_elementwise.cuh"
@@ -158,6 +161,19 @@ int plan_schedule(tpk::GemmArgs& a, bool swap, const Scratch* sc) {
   return sms;  // the launcher clamps it to sk_iters so that no stream-K range is empty
 }
 
+// Flag value of a split launch: a per-process random high half and a launch
+// counter, so no earlier launch (and no leftover workspace contents, except
+// with probability 2^-64) carries the same value.
+unsigned long long next_split_epoch() {
+  static std::atomic<unsigned long long> counter{0};
+  static const unsigned long long salt = [] {
+    std::random_device rd;
+    return (static_cast<unsigned long long>(rd()) << 32) ^ static_cast<unsigned long long>(
+        std::chrono::steady_clock::now().time_since_epoch().count());
+  }();
+  return salt ^ (counter.fetch_add(1, std::memory_order_relaxed) + 1);
+}
+
 // CTA pairs of the 2-SM kernel that fit on the device at once (the
 // persistent grid of a paired launch), looked up once per device.
 template <int KIND>
@@ -188,11 +204,26 @@ int max_cluster_pairs() {
   return cache[dev];
 }
 
+// Pieces per unit of a split last round: as many as the idle pairs allow,
+// at most 4 (each piece beyond the owner costs a 128 KB fp32 round trip per
+// CTA), each at least 8 k-blocks long. 1: no split. Only row GEMMs split:
+// the column GEMMs' heavier epilogues (SwiGLU, QKV replicas and context)
+// make the owner's combine the longer tail, and splitting them measured
+// slower.
+template <int KIND>
+int split_ways_for(int rem_units, int pairs, int kpt) {
+  if (KIND != tpk::GK_ROW_SUM || rem_units <= 0) return 1;
+  int ways = std::min(4, pairs / rem_units);
+  while (ways > 1 && kpt / ways < 8) --ways;
+  return std::max(1, ways);
+}
+
 // Paired launch: clusters of two CTAs, one pair per two SMs, each pair
-// walking the 256-token tile units round-robin.
+// walking the 256-token tile units round-robin. With scratch, a partial last
+// round is split along K (see the kernel's header).
 template <int KIND>
 int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
-                tpk::GemmArgs args, cudaStream_t st) {
+                tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
   using Cfg = tpk::GemmCfg<KIND, false, true>;
   if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
@@ -201,8 +232,22 @@ int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   if (pairs < 1) return TP_ERR_UNSUPPORTED;
   args.dp_tiles = args.num_tiles;
   args.sk_iters = 0;
+  int grid_pairs = std::min(args.num_tiles, pairs);
+  const int rem = args.num_tiles % pairs;
+  const int ways = split_ways_for<KIND>(rem, pairs, args.kpt);
+  if (ways > 1 && sc != nullptr &&
+      static_cast<size_t>(rem) * (ways - 1) * 2 * (128 * 256 * sizeof(float)) <= sc->partial_bytes &&
+      static_cast<size_t>(rem) * (ways - 1) * 2 * sizeof(unsigned long long) <= sc->ncounters * sizeof(int)) {
+    args.dp_tiles = args.num_tiles - rem;
+    args.split_units = rem;
+    args.split_ways = ways;
+    args.partials = sc->partials;
+    args.split_flags = reinterpret_cast<unsigned long long*>(sc->counters);
+    args.split_epoch = next_split_epoch();
+    grid_pairs = args.dp_tiles > 0 ? pairs : rem * ways;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * std::min(args.num_tiles, pairs)));
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * grid_pairs));
   cfg.blockDim = dim3(Cfg::THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = st;
@@ -224,7 +269,7 @@ int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   using Cfg = tpk::GemmCfg<KIND, SWAP>;
   if (args.num_tiles <= 0) return TP_OK;
   if constexpr (!SWAP) {
-    if (args.cluster > 1) return pair_launch<KIND>(a0, a1, b0, b1, args, st);
+    if (args.cluster > 1) return pair_launch<KIND>(a0, a1, b0, b1, args, sc, st);
   }
   if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
@@ -485,11 +530,13 @@ int run_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, con
                              : row_f32(Xs, T, W, bias, residual, Y, partials, st);
 }
 
-// Stream-K scratch carved from a caller workspace after `used` bytes. Only
-// the weight-streaming arrangement (T <= SWAP_MAX_T) splits tiles; larger T
-// needs none.
+// Split-tile scratch carved from a caller workspace after `used` bytes:
+// fp32 slots and counters for the stream-K schedule of the weight-streaming
+// arrangement (T <= SWAP_MAX_T) and for the split last round of CTA-pair
+// launches (larger T). The counters must be zero before the first use; the
+// kernels leave them zero.
 size_t scratch_bytes(int64_t T, size_t max_tiles) {
-  if (T > SWAP_MAX_T) return 0;
+  (void)T;
   return align256(SK_PARTIAL_BYTES) + align256(sizeof(int) * max_tiles);
 }
 Scratch carve_scratch(void* ws, size_t used, size_t max_tiles) {
@@ -645,7 +692,6 @@ int linear_scratch(const tp_shards* W, int64_t T, void* ws, size_t ws_bytes, Scr
   if (!aligned(ws, 256)) return TP_ERR_ALIGN;
   const size_t need = tp_gemm_workspace_bytes(T, W);
   if (ws_bytes < need) return TP_ERR_WORKSPACE;
-  if (need == 0) return TP_OK;  // large T: whole tiles, no scratch
   const size_t tiles = W->mode == TP_COL ? static_cast<size_t>(W->tp) * cdiv(W->N / W->tp, 128)
                                          : static_cast<size_t>(cdiv(W->N, 128));
   *sc = carve_scratch(ws, 0, std::max<size_t>(2 * SK_MAX_CTAS, tiles));
@@ -769,7 +815,7 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
   const size_t hs_bytes = align256(static_cast<size_t>(T) * W1->N * elem_size(dt));
   Scratch sc{};
   const Scratch* scp = nullptr;
-  if (dt == TP_BF16 && T <= SWAP_MAX_T) {
+  if (dt == TP_BF16) {
     sc = carve_scratch(workspace, hs_bytes, mlp_max_tiles(W1->K, W1->N, W1->tp));
     scp = &sc;
   }
@@ -863,7 +909,7 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
   void* ctx_ws = static_cast<char*>(workspace) + qkv_bytes;
   Scratch sc{};
   const Scratch* scp = nullptr;
-  if (dt == TP_BF16 && T <= SWAP_MAX_T) {
+  if (dt == TP_BF16) {
     sc = carve_scratch(workspace, qkv_bytes + ctx_bytes,
                        attn_max_tiles(static_cast<int64_t>(hq) * hd * 4, hq, hkv, hd, tp));
     scp = &sc;

@@ -49,6 +49,20 @@
 // hand each CTA's accumulator half (its own tensor memory) to that CTA's
 // epilogue; both epilogues report a drained accumulator to the even CTA.
 //
+// Split last round (CTA pairs, row GEMMs): when the units do not fill the pairs evenly,
+// the first dp_tiles units run whole, round-robin, and each of the
+// split_units remaining ones is cut along K into split_ways equal pieces,
+// one piece per pair, so that the last round is 1/split_ways as long. Pair q
+// of that round takes piece j = q / split_units of unit q % split_units, so
+// the pieces running together cover the same K range of their operands.
+// Pieces j < split_ways - 1 park their fp32 accumulator in a workspace slot
+// and then set their flag (per unit, CTA rank and piece) to this launch's
+// epoch, a 64-bit value never used by an earlier launch, so the flags need
+// no clearing between launches. The last piece (the owner, every pair's
+// final item) waits for the others' flags, adds their slots in j order to
+// its own accumulator and runs the epilogue. The sum order is fixed, so
+// results do not depend on timing.
+//
 // QKV replica dedup (normal COL): when kv heads are replicated across rep
 // consecutive shards, the tiles holding only replicated K|V columns are
 // computed once, on the first shard of each group, and stored to all rep
@@ -108,8 +122,13 @@ struct GemmArgs {
   const __nv_bfloat16* bias_up;   // COL_SWIGLU up bias [tp*Ns]; may be null
   const void* residual;           // ROW_SUM: [M][N]; may be null
   void* out;
-  float* partials;   // [2 * gridDim.x][SLOT_FLOATS] when sk_iters > 0
-  int* counters;     // [num_tiles - dp_tiles], zero on entry; reset to zero by the kernel
+  float* partials;   // [2 * gridDim.x][SLOT_FLOATS] when sk_iters > 0; split pieces' slots
+  int* counters;     // [num_tiles - dp_tiles] (stream-K) or [2 * split_units] (split
+                     // pieces), zero on entry; reset to zero by the kernel
+  int split_units;   // CTA pairs: units after dp_tiles, each cut into split_ways K pieces
+  int split_ways;    // 0 or 1: no split
+  unsigned long long* split_flags;  // [split_units][2][split_ways - 1]
+  unsigned long long split_epoch;   // this launch's flag value
   // COL on a QKV view: also write the single-key attention context
   // ctx [tp][M][hq/tp * hd] from the V columns (null: no context)
   __nv_bfloat16* ctx;
@@ -133,9 +152,11 @@ __device__ __forceinline__ int sk_cta_of(const GemmArgs& a, long long i) {
 
 struct SegIter {
   int dp_next;
+  bool piece_left;
   long long i, i_end;
   __device__ explicit SegIter(const GemmArgs& a) {
     dp_next = blockIdx.x / a.cluster;  // the CTAs of a cluster walk the same tiles
+    piece_left = a.split_ways > 1 && static_cast<int>(blockIdx.x / a.cluster) < a.split_units * a.split_ways;
     i = sk_begin(a, blockIdx.x);
     i_end = sk_begin(a, blockIdx.x + 1);
   }
@@ -145,6 +166,15 @@ struct SegIter {
       s.kb0 = 0;
       s.kb1 = a.kpt;
       dp_next += gridDim.x / a.cluster;
+      return true;
+    }
+    if (piece_left) {  // this pair's piece of the split last round
+      piece_left = false;
+      const int q = static_cast<int>(blockIdx.x / a.cluster);
+      const int j = q / a.split_units;
+      s.tile = a.dp_tiles + q % a.split_units;
+      s.kb0 = static_cast<int>(static_cast<long long>(j) * a.kpt / a.split_ways);
+      s.kb1 = static_cast<int>(static_cast<long long>(j + 1) * a.kpt / a.split_ways);
       return true;
     }
     if (i < i_end) {
@@ -278,6 +308,32 @@ struct PartialSrc {
         v[4 * j4 + 0] += q.x; v[4 * j4 + 1] += q.y; v[4 * j4 + 2] += q.z; v[4 * j4 + 3] += q.w;
       }
     }
+  }
+};
+
+// The owner piece of a split unit: the other pieces' slots (j = 0..ways-2,
+// this CTA rank, in that order) summed, then this CTA's own accumulator.
+struct SplitSrc {
+  uint32_t t_acc;
+  const float* slot0;   // slot of piece 0; piece j's slot is 2 * j slots further
+  int row;
+  int others;           // split_ways - 1
+  template <int N>
+  __device__ __forceinline__ void fetch(int col, float* v) const {
+    float own[N];
+    TmemSrc{t_acc}.template fetch<N>(col, own);
+#pragma unroll
+    for (int j = 0; j < N; ++j) v[j] = 0.0f;
+    for (int p = 0; p < others; ++p) {
+      const float4* sp = reinterpret_cast<const float4*>(slot0 + static_cast<size_t>(2 * p) * (128 * 256));
+#pragma unroll
+      for (int j4 = 0; j4 < N / 4; ++j4) {
+        const float4 q = __ldcg(sp + static_cast<size_t>(col / 4 + j4) * 128 + row);
+        v[4 * j4 + 0] += q.x; v[4 * j4 + 1] += q.y; v[4 * j4 + 2] += q.z; v[4 * j4 + 3] += q.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < N; ++j) v[j] += own[j];
   }
 };
 
@@ -761,6 +817,63 @@ __global__ void __launch_bounds__(192, 1)
       if constexpr (SWAP) decode_tile_swap(args, sg.tile, m, s);
       else decode_tile_normal(args, sg.tile, rank, m, n, s);
       const bool whole = sg.kb0 == 0 && sg.kb1 == args.kpt;
+      if constexpr (PAIR && KIND == GK_ROW_SUM) {  // only row GEMMs split their last round
+        if (!whole) {
+          // a piece of a split unit: slots per (unit u, piece j < ways-1, rank),
+          // counters per (unit u, rank)
+          const int q = static_cast<int>(blockIdx.x / 2);
+          const int u = q % args.split_units, j = q / args.split_units;
+          const int others = args.split_ways - 1;
+          float* slot0 = args.partials + (static_cast<size_t>(u) * others * 2 + rank) * (128 * 256);
+          volatile unsigned long long* flags = args.split_flags + (static_cast<size_t>(u) * 2 + rank) * others;
+          if (j < others) {
+            store_partial<32>(t_acc, slot0 + static_cast<size_t>(2 * j) * (128 * 256), row, 256);
+            tc_fence_before();
+            __syncwarp();
+            __threadfence();
+            epi_bar();
+            if (threadIdx.x == 64) {
+              __threadfence();
+              flags[j] = args.split_epoch;
+            }
+          } else {
+            // the owner: wait (bounded) until the other pieces have parked their slots
+            if (threadIdx.x == 64) {
+              const uint64_t t0 = globaltimer_ns();
+              const uint64_t limit = g_tp_wait_limit_ns;
+              bool ok = true;
+              for (int p = 0; ok && p < others; ++p) {
+                while (flags[p] != args.split_epoch) {
+                  if (*abort_flag || globaltimer_ns() - t0 > limit) {
+                    atomicCAS(&g_tp_error, TP_DEVERR_NONE, TP_DEVERR_WAIT_TIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                  }
+                }
+              }
+              __threadfence();
+              *last_flag = ok ? 1 : 0;
+            }
+            epi_bar();
+            if (*last_flag) {
+              SplitSrc src{t_acc, slot0, row, others};
+              epilogue_normal<Cfg>(args, src, m * 128 + row, n, s);
+            }
+            tc_fence_before();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            if (rank != 0) mbar_arrive_cluster(mapa_shared(&tempty[acc], 0));
+            else mbar_arrive(&tempty[acc]);
+          }
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          continue;
+        }
+      }
       if (PAIR || whole) {
         TmemSrc src{t_acc};
         if constexpr (SWAP) epilogue_swap<Cfg>(args, src, m * 128 + row, s);

@@ -327,3 +327,56 @@ def test_cluster_pairs(T):
     assert_close(qkv, np.stack(qkv_ref), TOL_BF16, f"paired QKV with replicas T={T}")
     assert_close(Ya, Ya_ref, TOL_BF16, f"paired attention projections T={T}")
     assert tpl.tp_get_error() == 0
+
+
+@pytest.mark.parametrize("T", [256, 1100])
+def test_split_last_round(T):
+    """With a workspace, a paired row-GEMM launch whose units leave pairs of
+    SMs idle in the last round cuts those units along K into pieces (one per
+    pair) and combines them in a fixed order. Checked against the oracle; the
+    column launches (which run whole with or without a workspace) against the
+    oracle and the call without a workspace. Row GEMM: 6 units at 256 tokens,
+    cut 4 ways (and the O projection's 8); at 1100 tokens (5 token units, the
+    last one half empty) 30 units, cut 2 ways."""
+    tp, K, Nc = 2, 2048, 2 * 768         # column: 3 units of 256 columns per shard, per 256 tokens
+    X, W, b = nb(121, (T, K)), nb(122, (K, Nc), 0.02), nb(123, (Nc,), 0.3)
+    Sc = tpl.tp_shard_weights(dev(W), tp, "col")
+    ws = torch.empty(tpl.tp_gemm_workspace_bytes(T, Sc), dtype=torch.uint8, device="cuda")
+    ref = np.concatenate(O.column_parallel(f64(X), f64(W), tp, bias=f64(b), act=O.gelu), axis=1)
+    Y1 = tpl.tp_column_linear(dev(X), Sc, bias=dev(b), act="gelu", concat=True, workspace=ws)
+    Y0 = tpl.tp_column_linear(dev(X), Sc, bias=dev(b), act="gelu", concat=True)
+    assert_close_stored(Y1, ref, TOL_BF16, f"split column T={T}")
+    assert_close_stored(Y1, host(Y0), TOL_BF16, f"split vs whole column T={T}")
+
+    Wg, Wu = nb(124, (K, Nc), 0.02), nb(125, (K, Nc), 0.02)
+    Sg, Su = tpl.tp_shard_weights(dev(Wg), tp, "col"), tpl.tp_shard_weights(dev(Wu), tp, "col")
+    Hs = tpl.tp_column_linear(dev(X), Sg, W_up=Su, act="swiglu", workspace=ws)
+    Hs_ref = O.column_parallel(f64(X), f64(Wg), tp)
+    Up_ref = O.column_parallel(f64(X), f64(Wu), tp)
+    assert_close_stored(Hs, np.stack([O.swiglu(g, u) for g, u in zip(Hs_ref, Up_ref)]), TOL_BF16,
+                        f"split SwiGLU T={T}")
+    Kr, Nr = 2048, 1536                   # row: 6 column blocks of 256, per 256 tokens
+    Wr = nb(126, (Kr, Nr), 0.02)
+    Sr = tpl.tp_shard_weights(dev(Wr), tp, "row")
+    Xs = nb(127, (tp, T, Kr // tp))
+    br, R = nb(128, (Nr,), 0.3), nb(129, (T, Nr))
+    wsr = torch.empty(tpl.tp_gemm_workspace_bytes(T, Sr), dtype=torch.uint8, device="cuda")
+    Yr = tpl.tp_row_linear(dev(Xs), Sr, bias=dev(br, torch.float32), residual=dev(R, torch.float32),
+                           workspace=wsr)
+    ref_r = O.all_reduce(O.row_parallel_partials([f64(x) for x in Xs], f64(Wr), tp)) + f64(br) + f64(R)
+    assert_close(Yr, ref_r, TOL_BF16, f"split row sum, fp32 residual T={T}")
+    Yr2 = tpl.tp_row_linear(dev(Xs), Sr, bias=dev(br, torch.float32), residual=dev(R, torch.float32),
+                            workspace=wsr)
+    np.testing.assert_array_equal(host(Yr2), host(Yr))   # fixed combine order: run to run identical
+    Yr0 = tpl.tp_row_linear(dev(Xs), Sr, bias=dev(br, torch.float32), residual=dev(R, torch.float32))
+    assert_close(Yr, host(Yr0), TOL_F32 * 10, f"split vs whole row sum T={T}")
+    # attention projections: QKV (with replicas) and O both split
+    g = S.gqa_proj(T, 2048, 16, 4, 128, seeds=(130, 131, 132, 133, 134))
+    Sqkv = tpl.tp_shard_qkv(dev(g["Wq"]), dev(g["Wk"]), dev(g["Wv"]), 16, 4, 128, 8)
+    So = tpl.tp_shard_weights(dev(g["Wo"]), 8, "row")
+    qkv_ref, _, Ya_ref = O.attn_proj(*(f64(g[k]) for k in ("X", "Wq", "Wk", "Wv", "Wo")), 16, 4, 128, 8)
+    qkv = torch.empty((8, T, qkv_ref[0].shape[1]), dtype=B, device="cuda")
+    Ya = tpl.tp_attn_proj(dev(g["X"]), Sqkv, So, qkv_out=qkv)
+    assert_close(qkv, np.stack(qkv_ref), TOL_BF16, f"split QKV T={T}")
+    assert_close(Ya, Ya_ref, TOL_BF16, f"split attention projections T={T}")
+    assert tpl.tp_get_error() == 0
