@@ -96,6 +96,28 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map for bulk tensor stores of an output [d2][d1][d0] (d0 contiguous)
+// with byte strides s1 (dim 1) and s2 (dim 2): box {128 bytes of elements,
+// 32 rows, 1}, 128-byte swizzle (the epilogue's staging layout).
+bool make_store_map(CUtensorMap* m, void* base, bool f32, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                    uint64_t s2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {f32 ? 32u : 64u, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Output maps of a token-major launch (unused by the weight-streaming one).
+struct OutMaps {
+  CUtensorMap y;  // the output
+  CUtensorMap c;  // the attention context (QKV launches that write it)
+};
+
 // --- shard-view checks -------------------------------------------------------
 int check_view(const tp_shards* W, int mode) {
   if (!W || !W->data) return TP_ERR_NULL;
@@ -223,7 +245,7 @@ int split_ways_for(int rem_units, int pairs, int kpt) {
 // round is split along K (see the kernel's header).
 template <int KIND>
 int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
-                tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
+                const OutMaps& om, tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
   using Cfg = tpk::GemmCfg<KIND, false, true>;
   if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
@@ -258,18 +280,19 @@ int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, false, true>, a0, a1, b0, b1, args) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, false, true>, a0, a1, b0, b1, om.y, om.c, args) !=
+      cudaSuccess)
     return TP_ERR_CUDA;
   return launch_status();
 }
 
 template <int KIND, bool SWAP>
 int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
-                tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
+                const OutMaps& om, tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
   using Cfg = tpk::GemmCfg<KIND, SWAP>;
   if (args.num_tiles <= 0) return TP_OK;
   if constexpr (!SWAP) {
-    if (args.cluster > 1) return pair_launch<KIND>(a0, a1, b0, b1, args, sc, st);
+    if (args.cluster > 1) return pair_launch<KIND>(a0, a1, b0, b1, om, args, sc, st);
   }
   if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg::SMEM_BYTES) != cudaSuccess)
@@ -281,7 +304,8 @@ int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
     if (cudaMemsetAsync(args.counters, 0, sizeof(int) * (args.num_tiles - args.dp_tiles), st) != cudaSuccess)
       return TP_ERR_CUDA;
   }
-  tpk::tp_gemm_kernel<KIND, SWAP, false><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(a0, a1, b0, b1, args);
+  tpk::tp_gemm_kernel<KIND, SWAP, false><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(a0, a1, b0, b1, om.y, om.c,
+                                                                                     args);
   return launch_status();
 }
 
@@ -334,8 +358,9 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
     a.n_tiles = 1;
     a.num_tiles = a.m_tiles * tp;
     a.r1_tiles = a.num_tiles;
-    return swiglu ? gemm_launch<tpk::GK_COL_SWIGLU, true>(mw, mu, mx, mx, a, sc, st)
-                  : gemm_launch<tpk::GK_COL, true>(mw, mu, mx, mx, a, sc, st);
+    static const OutMaps none{};
+    return swiglu ? gemm_launch<tpk::GK_COL_SWIGLU, true>(mw, mu, mx, mx, none, a, sc, st)
+                  : gemm_launch<tpk::GK_COL, true>(mw, mu, mx, mx, none, a, sc, st);
   }
   const int nout = swiglu ? 128 : 256;
   a.cluster = cluster_for(cdiv(T, 128));
@@ -358,8 +383,21 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
   }
   a.r1_tiles = a.m_tiles * nq * tp;
   a.num_tiles = a.r1_tiles + (a.rep > 1 ? a.m_tiles * (a.n_tiles - nq) * (tp / a.rep) : 0);
-  return swiglu ? gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mw, mu, a, sc, st)
-                : gemm_launch<tpk::GK_COL, false>(mx, mx, mw, mu, a, sc, st);
+  // outputs through staging + bulk tensor stores: per shard [tp][T][Ns] or
+  // concatenated [T][tp*Ns] (the same (n, t, s) coordinates, other strides);
+  // a context needs whole 64-column chunks inside a head (hd % 64 == 0)
+  OutMaps om{};
+  const uint64_t es = 2;
+  bool ok = a.out_concat
+                ? make_store_map(&om.y, Y, false, Ns, T, tp, tp * Ns * es, Ns * es)
+                : make_store_map(&om.y, Y, false, Ns, T, tp, Ns * es, T * Ns * es);
+  if (ok && ctx) {
+    const uint64_t nc = static_cast<uint64_t>(W->hq / tp) * W->hd;
+    ok = W->hd % 64 == 0 && make_store_map(&om.c, ctx, false, nc, T, tp, nc * es, T * nc * es);
+  }
+  a.tma_store = ok ? 1 : 0;
+  return swiglu ? gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mw, mu, om, a, sc, st)
+                : gemm_launch<tpk::GK_COL, false>(mx, mx, mw, mu, om, a, sc, st);
 }
 
 // Row-parallel bf16 GEMM: fused shard sum (partials_out == nullptr) or
@@ -390,7 +428,8 @@ int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, co
     a.r1_tiles = a.num_tiles;
     a.kpt = a.kb_per_shard * tp;
     a.out = Y;
-    return gemm_launch<tpk::GK_ROW_SUM, true>(mw, mw, mx, mx, a, sc, st);
+    static const OutMaps none{};
+    return gemm_launch<tpk::GK_ROW_SUM, true>(mw, mw, mx, mx, none, a, sc, st);
   }
   a.cluster = cluster_for(cdiv(T, 128));
   if (!make_map_bf16(&mx, Xs, Ks, T, tp, 128)) return TP_ERR_CUDA;
@@ -402,13 +441,18 @@ int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, co
     a.kpt = a.kb_per_shard;
     a.r1_tiles = a.num_tiles;
     a.out = partials_out;
-    return gemm_launch<tpk::GK_ROW_PARTIAL, false>(mx, mx, mw, mw, a, sc, st);
+    OutMaps om{};
+    a.tma_store = make_store_map(&om.y, partials_out, true, N, T, tp, N * 4, T * N * 4) ? 1 : 0;
+    return gemm_launch<tpk::GK_ROW_PARTIAL, false>(mx, mx, mw, mw, om, a, sc, st);
   }
   a.num_tiles = a.m_tiles * a.n_tiles;
   a.kpt = a.kb_per_shard * tp;
   a.r1_tiles = a.num_tiles;
   a.out = Y;
-  return gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, a, sc, st);
+  OutMaps om{};
+  const uint64_t oes = a.out_f32 ? 4 : 2;
+  a.tma_store = make_store_map(&om.y, Y, a.out_f32 != 0, N, T, 1, N * oes, T * N * oes) ? 1 : 0;
+  return gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, om, a, sc, st);
 }
 
 template <int KIND>

@@ -96,7 +96,8 @@ struct GemmCfg {
   static constexpr int TMEM_COLS = 2 * ACC_COLS;
   static constexpr int SLOT_FLOATS = 128 * ACC_COLS;       // one fp32 partial tile
   static constexpr int THREADS = 192;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 512;
+  static constexpr int OUT_STAGE_BYTES = SWAP_ ? 0 : 4 * 2 * 4096;  // epilogue warps x 2 x (32 rows x 128 B)
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGE_BYTES + 1024 + 512;
 };
 
 struct GemmArgs {
@@ -118,6 +119,7 @@ struct GemmArgs {
   int act;
   int out_concat;    // COL: 1 -> Y[T][tp*Ns]; 0 -> Y[tp][T][Ns]
   int out_f32;       // ROW_SUM: bias, residual and Y are fp32 (else bf16)
+  int tma_store;     // normal mode: outputs go through staging + bulk tensor stores (mapY, mapC)
   const void* bias;               // COL: [tp*Ns]; ROW_SUM: [N]; may be null
   const __nv_bfloat16* bias_up;   // COL_SWIGLU up bias [tp*Ns]; may be null
   const void* residual;           // ROW_SUM: [M][N]; may be null
@@ -396,10 +398,46 @@ __device__ __forceinline__ void store_ctx(const GemmArgs& a, const CtxMap& cm, i
 // ---------------------------------------------------------------------------
 // Tile epilogues
 // ---------------------------------------------------------------------------
+// Output staging for TMA stores (normal mode). Each epilogue warp owns 32
+// token rows of the tile and two 4 KB buffers. A chunk of 128 bytes per row
+// (64 bf16 or 32 fp32 columns) is written by its 32 threads, one row each,
+// into a buffer in the 128-byte-swizzled layout of the output tensor map,
+// then one thread stores the 32 x 128 B box with a bulk tensor copy (to
+// every destination: replica shards, context slots). The copy engine writes
+// whole lines and clips rows and columns outside the output.
+struct OutStage {
+  uint8_t* buf;              // this warp's two staging buffers (null: per-thread stores)
+  const CUtensorMap* mapY;   // output
+  const CUtensorMap* mapC;   // attention context (COL with a context)
+  int next;                  // buffer filled next
+  int row0;                  // first token row of the warp's 32 rows
+  int lane;
+};
+
+// Wait until the buffer about to be filled has been read by its last store.
+__device__ __forceinline__ uint8_t* stage_acquire(OutStage& o) {
+  if (o.lane == 0) tma_store_wait_read<1>();
+  __syncwarp();
+  return o.buf + o.next * 4096;
+}
+// 16-byte piece c16 (0..7) of this thread's 128-byte row, swizzled.
+__device__ __forceinline__ void stage_put(uint8_t* b, int lane, int c16, uint4 v) {
+  *reinterpret_cast<uint4*>(b + lane * 128 + ((c16 ^ (lane & 7)) << 4)) = v;
+}
+// Make the warp's staged rows visible to the copy engine.
+__device__ __forceinline__ void stage_ready() {
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
 // normal mode: this thread owns token row `row`; columns are output features.
 template <class Cfg, class Src>
-__device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& src, int row, int n_blk,
-                                                int s) {
+__device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& src, int row, int n_blk, int s,
+                                                OutStage& os) {
   const bool row_ok = row < a.M;
   if constexpr (Cfg::IS_COL) {
     constexpr int NOUT = Cfg::SWIGLU ? 128 : 256;
@@ -409,114 +447,203 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
     const __nv_bfloat16* bias =
         a.bias ? static_cast<const __nv_bfloat16*>(a.bias) + static_cast<size_t>(s) * a.Ns : nullptr;
     const __nv_bfloat16* bias_up = a.bias_up ? a.bias_up + static_cast<size_t>(s) * a.Ns : nullptr;
+    const bool with_ctx = !Cfg::SWIGLU && a.ctx != nullptr;
 #pragma unroll 1
-    for (int c = 0; c < NOUT; c += 32) {
-      float g[32];
-      src.template fetch<32>(c, g);
-      float u[Cfg::SWIGLU ? 32 : 1];
-      if constexpr (Cfg::SWIGLU) src.template fetch<32>(NOUT + c, u);
+    for (int cc = 0; cc < NOUT; cc += 64) {  // one 128-byte chunk of bf16 per row
+      uint8_t* sb = os.buf ? stage_acquire(os) : nullptr;
+#pragma unroll 1
+      for (int h = 0; h < 64; h += 32) {
+        const int c = cc + h;
+        float g[32];
+        src.template fetch<32>(c, g);
+        float u[Cfg::SWIGLU ? 32 : 1];
+        if constexpr (Cfg::SWIGLU) src.template fetch<32>(NOUT + c, u);
 #pragma unroll
-      for (int j8 = 0; j8 < 32; j8 += 8) {
-        const int n = n0 + c + j8;
-        if (!row_ok || n >= a.Ns) continue;
-        float v[8], b[8];
+        for (int j8 = 0; j8 < 32; j8 += 8) {
+          const int n = n0 + c + j8;
+          const bool col_ok = n < a.Ns;
+          float v[8], b[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = g[j8 + j];
-        if (bias) {
-          load_bf16x8_f(bias + n, b);
+          for (int j = 0; j < 8; ++j) v[j] = g[j8 + j];
+          if (bias && col_ok) {
+            load_bf16x8_f(bias + n, b);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] += b[j];
-        }
-        if constexpr (Cfg::SWIGLU) {
-          float w[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) w[j] = u[j8 + j];
-          if (bias_up) {
-            load_bf16x8_f(bias_up + n, b);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] += b[j];
+            for (int j = 0; j < 8; ++j) v[j] += b[j];
           }
+          if constexpr (Cfg::SWIGLU) {
+            float w[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = act_silu(v[j]) * w[j];
-        } else {
+            for (int j = 0; j < 8; ++j) w[j] = u[j8 + j];
+            if (bias_up && col_ok) {
+              load_bf16x8_f(bias_up + n, b);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = apply_act(a.act, v[j]);
-        }
-        for (int r = 0; r < copies; ++r) {
-          const size_t sr = static_cast<size_t>(s + r);
-          const size_t off = a.out_concat
-                                 ? static_cast<size_t>(row) * (static_cast<size_t>(a.tp) * a.Ns) + sr * a.Ns + n
-                                 : (sr * a.M + row) * static_cast<size_t>(a.Ns) + n;
-          store_bf16x8_f(Y + off, v);
-        }
-        if constexpr (!Cfg::SWIGLU) {
-          if (a.ctx) {
-            const CtxMap cm(a);
-            if (n >= cm.vcol0) store_ctx<8>(a, cm, s, copies, row, n, v);
+              for (int j = 0; j < 8; ++j) w[j] += b[j];
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = act_silu(v[j]) * w[j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = apply_act(a.act, v[j]);
+          }
+          if (sb) {
+            stage_put(sb, os.lane, (h + j8) >> 3, pack_bf16x8(v));
+          } else if (row_ok && col_ok) {
+            for (int r = 0; r < copies; ++r) {
+              const size_t sr = static_cast<size_t>(s + r);
+              const size_t off = a.out_concat
+                                     ? static_cast<size_t>(row) * (static_cast<size_t>(a.tp) * a.Ns) + sr * a.Ns + n
+                                     : (sr * a.M + row) * static_cast<size_t>(a.Ns) + n;
+              store_bf16x8_f(Y + off, v);
+            }
+            if constexpr (!Cfg::SWIGLU) {
+              if (with_ctx) {
+                const CtxMap cm(a);
+                if (n >= cm.vcol0) store_ctx<8>(a, cm, s, copies, row, n, v);
+              }
+            }
           }
         }
+      }
+      if (sb) {
+        stage_ready();
+        if (os.lane == 0) {
+          const int n = n0 + cc;
+          if (n < a.Ns && os.row0 < a.M) {  // boxes wholly outside the output are not issued
+            for (int r = 0; r < copies; ++r) tma_store_3d(os.mapY, sb, n, os.row0, s + r);
+            if constexpr (!Cfg::SWIGLU) {
+              if (with_ctx) {
+                // the chunk lies in one head (hd % 64 == 0 on this path): store it to
+                // every query head that reads it, on every replica shard
+                const CtxMap cm(a);
+                if (n >= cm.vcol0) {
+                  const int i = (n - cm.vcol0) / cm.hd;
+                  const int d = n - cm.vcol0 - i * cm.hd;
+                  const int kvh = cm.kv_first(a, s) + i;
+                  for (int r = 0; r < copies; ++r) {
+                    const int s2 = s + r;
+                    const int g0 = max(s2 * cm.nq, kvh * cm.group);
+                    const int g1 = min((s2 + 1) * cm.nq, (kvh + 1) * cm.group);
+                    for (int gq = g0; gq < g1; ++gq)
+                      tma_store_3d(os.mapC, sb, (gq - s2 * cm.nq) * cm.hd + d, os.row0, s2);
+                  }
+                }
+              }
+            }
+          }
+          tma_store_commit();
+        }
+        os.next ^= 1;
       }
     }
   } else if constexpr (Cfg::KIND == GK_ROW_SUM) {
     const int n0 = n_blk * 256;
     const size_t row_off = static_cast<size_t>(row) * a.Ns;
+    if (a.out_f32) {  // fp32 bias / residual / output (an fp32 residual stream)
+      const float* bias = static_cast<const float*>(a.bias);
+      const float* res = static_cast<const float*>(a.residual);
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
-      float g[32];
-      src.template fetch<32>(c, g);
+      for (int c = 0; c < 256; c += 32) {  // one 128-byte chunk of fp32 per row
+        uint8_t* sb = os.buf ? stage_acquire(os) : nullptr;
+        float g[32];
+        src.template fetch<32>(c, g);
 #pragma unroll
-      for (int j8 = 0; j8 < 32; j8 += 8) {
-        const int n = n0 + c + j8;
-        if (!row_ok || n >= a.Ns) continue;
-        float v[8], b[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = g[j8 + j];
-        if (a.out_f32) {  // fp32 bias / residual / output (an fp32 residual stream)
-          const float* bias = static_cast<const float*>(a.bias);
-          const float* res = static_cast<const float*>(a.residual);
-          if (bias) {
+        for (int j4 = 0; j4 < 32; j4 += 4) {
+          const int n = n0 + c + j4;
+          const bool col_ok = n < a.Ns;
+          float4 v = make_float4(g[j4], g[j4 + 1], g[j4 + 2], g[j4 + 3]);
+          if (bias && col_ok) {
             const float4 p = __ldg(reinterpret_cast<const float4*>(bias + n));
-            const float4 q = __ldg(reinterpret_cast<const float4*>(bias + n + 4));
-            v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
-            v[4] += q.x; v[5] += q.y; v[6] += q.z; v[7] += q.w;
+            v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
           }
-          if (res) {
+          if (res && row_ok && col_ok) {  // may alias Y: read here, before this chunk is stored
             const float4 p = *reinterpret_cast<const float4*>(res + row_off + n);
-            const float4 q = *reinterpret_cast<const float4*>(res + row_off + n + 4);
-            v[0] += p.x; v[1] += p.y; v[2] += p.z; v[3] += p.w;
-            v[4] += q.x; v[5] += q.y; v[6] += q.z; v[7] += q.w;
+            v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
           }
-          float* Y = static_cast<float*>(a.out) + row_off + n;
-          *reinterpret_cast<float4*>(Y) = make_float4(v[0], v[1], v[2], v[3]);
-          *reinterpret_cast<float4*>(Y + 4) = make_float4(v[4], v[5], v[6], v[7]);
-        } else {
-          if (a.bias) {
-            load_bf16x8_f(static_cast<const __nv_bfloat16*>(a.bias) + n, b);
+          if (sb) {
+            stage_put(sb, os.lane, j4 >> 2,
+                      make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                                 __float_as_uint(v.w)));
+          } else if (row_ok && col_ok) {
+            *reinterpret_cast<float4*>(static_cast<float*>(a.out) + row_off + n) = v;
+          }
+        }
+        if (sb) {
+          stage_ready();
+          if (os.lane == 0) {
+            if (n0 + c < a.Ns && os.row0 < a.M) tma_store_3d(os.mapY, sb, n0 + c, os.row0, 0);
+            tma_store_commit();
+          }
+          os.next ^= 1;
+        }
+      }
+    } else {
+      const __nv_bfloat16* bias = static_cast<const __nv_bfloat16*>(a.bias);
+      const __nv_bfloat16* res = static_cast<const __nv_bfloat16*>(a.residual);
+#pragma unroll 1
+      for (int cc = 0; cc < 256; cc += 64) {  // one 128-byte chunk of bf16 per row
+        uint8_t* sb = os.buf ? stage_acquire(os) : nullptr;
+#pragma unroll 1
+        for (int h = 0; h < 64; h += 32) {
+          const int c = cc + h;
+          float g[32];
+          src.template fetch<32>(c, g);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] += b[j];
+          for (int j8 = 0; j8 < 32; j8 += 8) {
+            const int n = n0 + c + j8;
+            const bool col_ok = n < a.Ns;
+            float v[8], b[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = g[j8 + j];
+            if (bias && col_ok) {
+              load_bf16x8_f(bias + n, b);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] += b[j];
+            }
+            if (res && row_ok && col_ok) {  // plain load: may alias Y (read before this chunk is stored)
+              const uint4 q = *reinterpret_cast<const uint4*>(res + row_off + n);
+              v[0] += bf16_lo(q.x); v[1] += bf16_hi(q.x); v[2] += bf16_lo(q.y); v[3] += bf16_hi(q.y);
+              v[4] += bf16_lo(q.z); v[5] += bf16_hi(q.z); v[6] += bf16_lo(q.w); v[7] += bf16_hi(q.w);
+            }
+            if (sb) stage_put(sb, os.lane, (h + j8) >> 3, pack_bf16x8(v));
+            else if (row_ok && col_ok) store_bf16x8_f(static_cast<__nv_bfloat16*>(a.out) + row_off + n, v);
           }
-          if (a.residual) {  // plain load: the residual may alias Y (read before written, same thread)
-            const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.residual) + row_off + n);
-            v[0] += bf16_lo(q.x); v[1] += bf16_hi(q.x); v[2] += bf16_lo(q.y); v[3] += bf16_hi(q.y);
-            v[4] += bf16_lo(q.z); v[5] += bf16_hi(q.z); v[6] += bf16_lo(q.w); v[7] += bf16_hi(q.w);
+        }
+        if (sb) {
+          stage_ready();
+          if (os.lane == 0) {
+            if (n0 + cc < a.Ns && os.row0 < a.M) tma_store_3d(os.mapY, sb, n0 + cc, os.row0, 0);
+            tma_store_commit();
           }
-          store_bf16x8_f(static_cast<__nv_bfloat16*>(a.out) + row_off + n, v);
+          os.next ^= 1;
         }
       }
     }
-  } else {  // GK_ROW_PARTIAL
+  } else {  // GK_ROW_PARTIAL: fp32 [tp][M][N]
     const int n0 = n_blk * 256;
     float* P = static_cast<float*>(a.out);
     const size_t row_off = (static_cast<size_t>(s) * a.M + row) * static_cast<size_t>(a.Ns);
 #pragma unroll 1
     for (int c = 0; c < 256; c += 32) {
+      uint8_t* sb = os.buf ? stage_acquire(os) : nullptr;
       float g[32];
       src.template fetch<32>(c, g);
 #pragma unroll
       for (int j4 = 0; j4 < 32; j4 += 4) {
         const int n = n0 + c + j4;
-        if (row_ok && n < a.Ns)
+        if (sb)
+          stage_put(sb, os.lane, j4 >> 2,
+                    make_uint4(__float_as_uint(g[j4]), __float_as_uint(g[j4 + 1]), __float_as_uint(g[j4 + 2]),
+                               __float_as_uint(g[j4 + 3])));
+        else if (row_ok && n < a.Ns)
           *reinterpret_cast<float4*>(P + row_off + n) = make_float4(g[j4], g[j4 + 1], g[j4 + 2], g[j4 + 3]);
+      }
+      if (sb) {
+        stage_ready();
+        if (os.lane == 0) {
+          if (n0 + c < a.Ns && os.row0 < a.M) tma_store_3d(os.mapY, sb, n0 + c, os.row0, s);
+          tma_store_commit();
+        }
+        os.next ^= 1;
       }
     }
   }
@@ -586,13 +713,15 @@ template <int KIND, bool SWAP, bool PAIR>
 __global__ void __launch_bounds__(192, 1)
     tp_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
+                   const __grid_constant__ CUtensorMap mapY, const __grid_constant__ CUtensorMap mapC,
                    const GemmArgs args) {
   using Cfg = GemmCfg<KIND, SWAP, PAIR>;
   static_assert(!(PAIR && SWAP), "CTA pairs are a token-major arrangement");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::STAGES * Cfg::STAGE_BYTES);
+  uint8_t* out_stage = smem + Cfg::STAGES * Cfg::STAGE_BYTES;  // epilogue staging (normal mode)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + Cfg::OUT_STAGE_BYTES);
   uint64_t* full = bars;                        // [STAGES]  TMA -> MMA
   uint64_t* empty = bars + Cfg::STAGES;         // [STAGES]  MMA -> TMA
   uint64_t* tfull = bars + 2 * Cfg::STAGES;     // [2]       MMA -> epilogue
@@ -803,6 +932,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------ epilogue ------------------------------
     const int q = warp & 3;        // TMEM lane quadrant this warp may access
     const int row = q * 32 + lane; // row of the 128-row tile
+    OutStage os{(!SWAP && args.tma_store) ? out_stage + (warp - 2) * 8192 : nullptr, &mapY, &mapC, 0, 0, lane};
     int acc = 0;
     uint32_t acc_phase = 0;
     SegIter it(args);
@@ -816,6 +946,7 @@ __global__ void __launch_bounds__(192, 1)
       int m, n = 0, s;
       if constexpr (SWAP) decode_tile_swap(args, sg.tile, m, s);
       else decode_tile_normal(args, sg.tile, rank, m, n, s);
+      os.row0 = m * 128 + q * 32;
       const bool whole = sg.kb0 == 0 && sg.kb1 == args.kpt;
       if constexpr (PAIR && KIND == GK_ROW_SUM) {  // only row GEMMs split their last round
         if (!whole) {
@@ -858,7 +989,7 @@ __global__ void __launch_bounds__(192, 1)
             epi_bar();
             if (*last_flag) {
               SplitSrc src{t_acc, slot0, row, others};
-              epilogue_normal<Cfg>(args, src, m * 128 + row, n, s);
+              epilogue_normal<Cfg>(args, src, m * 128 + row, n, s, os);
             }
             tc_fence_before();
             __syncwarp();
@@ -877,7 +1008,7 @@ __global__ void __launch_bounds__(192, 1)
       if (PAIR || whole) {
         TmemSrc src{t_acc};
         if constexpr (SWAP) epilogue_swap<Cfg>(args, src, m * 128 + row, s);
-        else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s);
+        else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s, os);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -910,7 +1041,7 @@ __global__ void __launch_bounds__(192, 1)
           __threadfence();
           PartialSrc src{args.partials, Cfg::SLOT_FLOATS, c_first, c_last, row, &args, tile_local};
           if constexpr (SWAP) epilogue_swap<Cfg>(args, src, m * 128 + row, s);
-          else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s);
+          else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s, os);
           if (threadIdx.x == 64) args.counters[tile_local] = 0;
         }
       }
@@ -919,6 +1050,7 @@ __global__ void __launch_bounds__(192, 1)
         acc_phase ^= 1u;
       }
     }
+    if (os.buf && lane == 0) tma_store_wait_all();  // the staged outputs have landed
   }
 
   tc_fence_before();
