@@ -149,8 +149,8 @@ bool same_shape(const tp_shards* a, const tp_shards* b) {
 struct Scratch {
   float* partials;
   size_t partial_bytes;
-  int* counters;
-  size_t ncounters;
+  unsigned long long* words;  // epoch-tagged synchronisation words
+  size_t nwords;
 };
 
 constexpr int SK_MAX_CTAS = 160;  // grid cap of the stream-K schedule (>= SMs of a B300)
@@ -159,6 +159,19 @@ constexpr int SWAP_MAX_T = 64;    // token counts served by the weight-streaming
 // fp32 slots for split tiles of the weight-streaming arrangement: two per CTA,
 // each 128 rows x up to 128 accumulator columns.
 constexpr size_t SK_PARTIAL_BYTES = static_cast<size_t>(2) * SK_MAX_CTAS * 128 * 128 * sizeof(float);
+
+// Epoch of a launch that splits tiles: a per-process random value and a
+// launch counter, so no earlier launch (and no leftover workspace contents,
+// except with vanishing probability) carries the same value.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> counter{0};
+  static const unsigned long long salt = [] {
+    std::random_device rd;
+    return (static_cast<unsigned long long>(rd()) << 32) ^ static_cast<unsigned long long>(
+        std::chrono::steady_clock::now().time_since_epoch().count());
+  }();
+  return salt ^ (counter.fetch_add(1, std::memory_order_relaxed) + 1);
+}
 
 // Work split. Token-major tiles (normal arrangement) run whole, round-robin:
 // CTAs of one wave then walk the same K range in step, so the weight blocks
@@ -175,25 +188,13 @@ int plan_schedule(tpk::GemmArgs& a, bool swap, const Scratch* sc) {
   if (!sc || !swap) return grid;
   const int dp = 0;
   const long long sk = static_cast<long long>(a.num_tiles - dp) * a.kpt;
-  if (sk < 2 || static_cast<size_t>(a.num_tiles - dp) > sc->ncounters) return grid;
+  if (sk < 2 || static_cast<size_t>(a.num_tiles - dp) > sc->nwords) return grid;
   a.dp_tiles = dp;
   a.sk_iters = sk;
   a.partials = sc->partials;
-  a.counters = sc->counters;
+  a.sync_words = sc->words;
+  a.epoch = next_epoch();
   return sms;  // the launcher clamps it to sk_iters so that no stream-K range is empty
-}
-
-// Flag value of a split launch: a per-process random high half and a launch
-// counter, so no earlier launch (and no leftover workspace contents, except
-// with probability 2^-64) carries the same value.
-unsigned long long next_split_epoch() {
-  static std::atomic<unsigned long long> counter{0};
-  static const unsigned long long salt = [] {
-    std::random_device rd;
-    return (static_cast<unsigned long long>(rd()) << 32) ^ static_cast<unsigned long long>(
-        std::chrono::steady_clock::now().time_since_epoch().count());
-  }();
-  return salt ^ (counter.fetch_add(1, std::memory_order_relaxed) + 1);
 }
 
 // CTA pairs of the 2-SM kernel that fit on the device at once (the
@@ -259,13 +260,13 @@ int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   const int ways = split_ways_for<KIND>(rem, pairs, args.kpt);
   if (ways > 1 && sc != nullptr &&
       static_cast<size_t>(rem) * (ways - 1) * 2 * (128 * 256 * sizeof(float)) <= sc->partial_bytes &&
-      static_cast<size_t>(rem) * (ways - 1) * 2 * sizeof(unsigned long long) <= sc->ncounters * sizeof(int)) {
+      static_cast<size_t>(rem) * (ways - 1) * 2 <= sc->nwords) {
     args.dp_tiles = args.num_tiles - rem;
     args.split_units = rem;
     args.split_ways = ways;
     args.partials = sc->partials;
-    args.split_flags = reinterpret_cast<unsigned long long*>(sc->counters);
-    args.split_epoch = next_split_epoch();
+    args.sync_words = sc->words;
+    args.epoch = next_epoch();
     grid_pairs = args.dp_tiles > 0 ? pairs : rem * ways;
   }
   cudaLaunchConfig_t cfg = {};
@@ -273,13 +274,15 @@ int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   cfg.blockDim = dim3(Cfg::THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // setup may overlap the previous kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, false, true>, a0, a1, b0, b1, om.y, om.c, args) !=
       cudaSuccess)
     return TP_ERR_CUDA;
@@ -301,11 +304,20 @@ int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   if (args.sk_iters > 0) {
     // every stream-K range must be non-empty: grid <= sk_iters
     grid = static_cast<int>(std::min<long long>(grid, args.sk_iters));
-    if (cudaMemsetAsync(args.counters, 0, sizeof(int) * (args.num_tiles - args.dp_tiles), st) != cudaSuccess)
-      return TP_ERR_CUDA;
   }
-  tpk::tp_gemm_kernel<KIND, SWAP, false><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, st>>>(a0, a1, b0, b1, om.y, om.c,
-                                                                                     args);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // setup may overlap the previous kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, SWAP, false>, a0, a1, b0, b1, om.y, om.c, args) !=
+      cudaSuccess)
+    return TP_ERR_CUDA;
   return launch_status();
 }
 
@@ -575,21 +587,20 @@ int run_row(const void* Xs, int64_t T, const tp_shards* W, const void* bias, con
 }
 
 // Split-tile scratch carved from a caller workspace after `used` bytes:
-// fp32 slots and counters for the stream-K schedule of the weight-streaming
-// arrangement (T <= SWAP_MAX_T) and for the split last round of CTA-pair
-// launches (larger T). The counters must be zero before the first use; the
-// kernels leave them zero.
+// fp32 slots and epoch-tagged synchronisation words (no clearing needed) for
+// the stream-K schedule of the weight-streaming arrangement (T <= SWAP_MAX_T)
+// and for the split last round of paired row GEMMs (larger T).
 size_t scratch_bytes(int64_t T, size_t max_tiles) {
   (void)T;
-  return align256(SK_PARTIAL_BYTES) + align256(sizeof(int) * max_tiles);
+  return align256(SK_PARTIAL_BYTES) + align256(sizeof(unsigned long long) * max_tiles);
 }
 Scratch carve_scratch(void* ws, size_t used, size_t max_tiles) {
   Scratch sc{};
   char* base = static_cast<char*>(ws) + used;
   sc.partial_bytes = SK_PARTIAL_BYTES;
   sc.partials = reinterpret_cast<float*>(base);
-  sc.counters = reinterpret_cast<int*>(base + align256(sc.partial_bytes));
-  sc.ncounters = max_tiles;
+  sc.words = reinterpret_cast<unsigned long long*>(base + align256(sc.partial_bytes));
+  sc.nwords = max_tiles;
   return sc;
 }
 // Counters the MLP's two GEMMs can need: the stream-K part of a normal

@@ -57,8 +57,7 @@
 // the pieces running together cover the same K range of their operands.
 // Pieces j < split_ways - 1 park their fp32 accumulator in a workspace slot
 // and then set their flag (per unit, CTA rank and piece) to this launch's
-// epoch, a 64-bit value never used by an earlier launch, so the flags need
-// no clearing between launches. The last piece (the owner, every pair's
+// epoch (see GemmArgs::sync_words). The last piece (the owner, every pair's
 // final item) waits for the others' flags, adds their slots in j order to
 // its own accumulator and runs the epilogue. The sum order is fixed, so
 // results do not depend on timing.
@@ -125,12 +124,14 @@ struct GemmArgs {
   const void* residual;           // ROW_SUM: [M][N]; may be null
   void* out;
   float* partials;   // [2 * gridDim.x][SLOT_FLOATS] when sk_iters > 0; split pieces' slots
-  int* counters;     // [num_tiles - dp_tiles] (stream-K) or [2 * split_units] (split
-                     // pieces), zero on entry; reset to zero by the kernel
+  // Synchronisation words in the workspace, tagged with this launch's epoch
+  // (a 64-bit value no earlier launch used), so they need no clearing:
+  // stream-K: [num_tiles - dp_tiles] arrival counters, (epoch << 16) | count;
+  // split pieces: [split_units][2][split_ways - 1] flags, equal to epoch when set.
+  unsigned long long* sync_words;
+  unsigned long long epoch;
   int split_units;   // CTA pairs: units after dp_tiles, each cut into split_ways K pieces
   int split_ways;    // 0 or 1: no split
-  unsigned long long* split_flags;  // [split_units][2][split_ways - 1]
-  unsigned long long split_epoch;   // this launch's flag value
   // COL on a QKV view: also write the single-key attention context
   // ctx [tp][M][hq/tp * hd] from the V columns (null: no context)
   __nv_bfloat16* ctx;
@@ -217,6 +218,20 @@ __device__ __forceinline__ void decode_tile_normal(const GemmArgs& a, int tile, 
 __device__ __forceinline__ void decode_tile_swap(const GemmArgs& a, int tile, int& m, int& s) {
   m = tile % a.m_tiles;
   s = tile / a.m_tiles;
+}
+
+// Count one arrival on an epoch-tagged counter ((epoch << 16) | count; a
+// word left by any other launch reads as zero arrivals) and return the count
+// including this one.
+__device__ __forceinline__ int arrive_tagged(unsigned long long* word, unsigned long long epoch) {
+  const unsigned long long tag = epoch & ((1ull << 48) - 1);
+  unsigned long long cur = atomicAdd(word, 0ull);
+  for (;;) {
+    const unsigned long long nv = ((cur >> 16) == tag) ? cur + 1 : ((tag << 16) | 1ull);
+    const unsigned long long prev = atomicCAS(word, cur, nv);
+    if (prev == cur) return static_cast<int>(nv & 0xFFFFull);
+    cur = prev;
+  }
 }
 
 // Named barrier 1 over the 128 epilogue threads (warps 2..5).
@@ -769,6 +784,11 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before either signals the other
+  // Setup above may overlap the previous kernel of the stream; every global
+  // memory access below comes after it has completed. The next kernel may
+  // begin its own setup on SMs this launch leaves idle.
+  griddep_launch_dependents();
+  griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -956,7 +976,7 @@ __global__ void __launch_bounds__(192, 1)
           const int u = q % args.split_units, j = q / args.split_units;
           const int others = args.split_ways - 1;
           float* slot0 = args.partials + (static_cast<size_t>(u) * others * 2 + rank) * (128 * 256);
-          volatile unsigned long long* flags = args.split_flags + (static_cast<size_t>(u) * 2 + rank) * others;
+          volatile unsigned long long* flags = args.sync_words + (static_cast<size_t>(u) * 2 + rank) * others;
           if (j < others) {
             store_partial<32>(t_acc, slot0 + static_cast<size_t>(2 * j) * (128 * 256), row, 256);
             tc_fence_before();
@@ -965,7 +985,7 @@ __global__ void __launch_bounds__(192, 1)
             epi_bar();
             if (threadIdx.x == 64) {
               __threadfence();
-              flags[j] = args.split_epoch;
+              flags[j] = args.epoch;
             }
           } else {
             // the owner: wait (bounded) until the other pieces have parked their slots
@@ -974,7 +994,7 @@ __global__ void __launch_bounds__(192, 1)
               const uint64_t limit = g_tp_wait_limit_ns;
               bool ok = true;
               for (int p = 0; ok && p < others; ++p) {
-                while (flags[p] != args.split_epoch) {
+                while (flags[p] != args.epoch) {
                   if (*abort_flag || globaltimer_ns() - t0 > limit) {
                     atomicCAS(&g_tp_error, TP_DEVERR_NONE, TP_DEVERR_WAIT_TIMEOUT);
                     *abort_flag = 1;
@@ -1033,8 +1053,7 @@ __global__ void __launch_bounds__(192, 1)
         __threadfence();
         epi_bar();
         if (threadIdx.x == 64) {
-          const int prev = atomicAdd(&args.counters[tile_local], 1);
-          *last_flag = (prev == c_last - c_first) ? 1 : 0;
+          *last_flag = arrive_tagged(args.sync_words + tile_local, args.epoch) == c_last - c_first + 1 ? 1 : 0;
         }
         epi_bar();
         if (*last_flag) {
@@ -1042,7 +1061,6 @@ __global__ void __launch_bounds__(192, 1)
           PartialSrc src{args.partials, Cfg::SLOT_FLOATS, c_first, c_last, row, &args, tile_local};
           if constexpr (SWAP) epilogue_swap<Cfg>(args, src, m * 128 + row, s);
           else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s, os);
-          if (threadIdx.x == 64) args.counters[tile_local] = 0;
         }
       }
       if (++acc == 2) {

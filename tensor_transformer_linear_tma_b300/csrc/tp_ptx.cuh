@@ -220,6 +220,16 @@ __device__ __forceinline__ void tc_commit_pair_local(uint64_t* bar) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: the next kernel of the stream may start its
+// setup once every CTA of this one has signalled; griddep_wait() returns when
+// the previous kernel has completed and its writes are visible.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // Thread-block clusters
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
