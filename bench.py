@@ -406,8 +406,41 @@ def run_gpu(args, spec):
     for _ in range(args.warmup):
         for p in st["parts"]:
             p()
+        if "dominant_part" in st:
+            st["dominant_part"]()
     if tpl.tp_get_error() != 0:
         raise SystemExit("device error during warm-up")
+
+    # The device-timed steps replay a CUDA graph of each part, captured after
+    # warm-up (the same launches with the same arguments), so that host-side
+    # time between the start event and the first launch cannot enter the
+    # measurement when the host is slower than the GPU. The end-to-end leg
+    # below calls the public API directly.
+    launch_mode = "direct calls"
+    if not args.no_graph:
+        try:
+            graphs = {}
+            torch.cuda.synchronize()
+            for key, fn in [(i, p) for i, p in enumerate(st["parts"])] + (
+                    [("dominant", st["dominant_part"])] if "dominant_part" in st else []):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn()
+                graphs[key] = g
+            torch.cuda.synchronize()
+            if tpl.tp_get_error() != 0:
+                raise RuntimeError("device error during capture")
+            st["parts"] = [graphs[i].replay for i in range(len(st["parts"]))]
+            if "dominant" in graphs:
+                st["dominant_part"] = graphs["dominant"].replay
+            st["graphs"] = graphs
+            for p in st["parts"]:  # one replay of each before timing
+                p()
+            torch.cuda.synchronize()
+            launch_mode = "one CUDA graph replay per part (captured after warm-up)"
+        except Exception as e:  # capture unavailable: time the direct calls
+            launch_mode = f"direct calls (graph capture failed: {type(e).__name__})"
+            torch.cuda.synchronize()
 
     nparts = len(st["parts"])
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nparts + 1)] for _ in range(args.steps)]
@@ -519,7 +552,7 @@ def run_gpu(args, spec):
             achieved = spec["dominant_flops"] / (dom_ms * 1e-3) / 1e12 if dom_ms else None
         clocks = clk.summary()
         cfg = {k: v for k, v in spec.items() if k in ("T", "H", "I", "hq", "hkv", "hd", "V", "L", "tp")}
-        cfg.update(workload=spec["name"], tokens_per_step=spec["T"],
+        cfg.update(workload=spec["name"], tokens_per_step=spec["T"], launches=launch_mode,
                    l2="flushed before every timed step (256 MB write, then 256 MB read to evict it)",
                    layout=f"tp={spec['tp']} shards in one device's memory")
         out = {
@@ -580,6 +613,7 @@ def main():
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time direct calls instead of graph replays")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

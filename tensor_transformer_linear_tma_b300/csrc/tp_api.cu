@@ -197,6 +197,23 @@ int plan_schedule(tpk::GemmArgs& a, bool swap, const Scratch* sc) {
   return sms;  // the launcher clamps it to sk_iters so that no stream-K range is empty
 }
 
+// The kernel's dynamic shared memory limit, raised once per device (not on
+// every launch, so that launches can also be recorded into CUDA graphs).
+template <int KIND, bool SWAP, bool PAIR>
+bool smem_attr_set() {
+  using Cfg = tpk::GemmCfg<KIND, SWAP, PAIR>;
+  static bool done[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM_BYTES) != cudaSuccess)
+      return false;
+    done[dev] = true;
+  }
+  return true;
+}
+
 // CTA pairs of the 2-SM kernel that fit on the device at once (the
 // persistent grid of a paired launch), looked up once per device.
 template <int KIND>
@@ -248,9 +265,7 @@ template <int KIND>
 int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
                 const OutMaps& om, tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
   using Cfg = tpk::GemmCfg<KIND, false, true>;
-  if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg::SMEM_BYTES) != cudaSuccess)
-    return TP_ERR_CUDA;
+  if (!smem_attr_set<KIND, false, true>()) return TP_ERR_CUDA;
   const int pairs = max_cluster_pairs<KIND>();
   if (pairs < 1) return TP_ERR_UNSUPPORTED;
   args.dp_tiles = args.num_tiles;
@@ -297,9 +312,7 @@ int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   if constexpr (!SWAP) {
     if (args.cluster > 1) return pair_launch<KIND>(a0, a1, b0, b1, om, args, sc, st);
   }
-  if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg::SMEM_BYTES) != cudaSuccess)
-    return TP_ERR_CUDA;
+  if (!smem_attr_set<KIND, SWAP, false>()) return TP_ERR_CUDA;
   int grid = plan_schedule(args, SWAP, sc);
   if (args.sk_iters > 0) {
     // every stream-K range must be non-empty: grid <= sk_iters

@@ -125,7 +125,9 @@ struct GemmArgs {
   void* out;
   float* partials;   // [2 * gridDim.x][SLOT_FLOATS] when sk_iters > 0; split pieces' slots
   // Synchronisation words in the workspace, tagged with this launch's epoch
-  // (a 64-bit value no earlier launch used), so they need no clearing:
+  // (a 64-bit value no earlier launch used), so that leftover contents read
+  // as "not arrived"; the kernel also returns each word it used to zero, so a
+  // replayed launch (same epoch, e.g. from a CUDA graph) starts clean:
   // stream-K: [num_tiles - dp_tiles] arrival counters, (epoch << 16) | count;
   // split pieces: [split_units][2][split_ways - 1] flags, equal to epoch when set.
   unsigned long long* sync_words;
@@ -1010,6 +1012,8 @@ __global__ void __launch_bounds__(192, 1)
             if (*last_flag) {
               SplitSrc src{t_acc, slot0, row, others};
               epilogue_normal<Cfg>(args, src, m * 128 + row, n, s, os);
+              if (threadIdx.x == 64)
+                for (int p = 0; p < others; ++p) flags[p] = 0ull;  // every piece has arrived: clear for a replay
             }
             tc_fence_before();
             __syncwarp();
@@ -1061,6 +1065,7 @@ __global__ void __launch_bounds__(192, 1)
           PartialSrc src{args.partials, Cfg::SLOT_FLOATS, c_first, c_last, row, &args, tile_local};
           if constexpr (SWAP) epilogue_swap<Cfg>(args, src, m * 128 + row, s);
           else epilogue_normal<Cfg>(args, src, m * 128 + row, n, s, os);
+          if (threadIdx.x == 64) args.sync_words[tile_local] = 0ull;  // all pieces arrived: clear for a replay
         }
       }
       if (++acc == 2) {

@@ -380,3 +380,33 @@ def test_split_last_round(T):
     assert_close(qkv, np.stack(qkv_ref), TOL_BF16, f"split QKV T={T}")
     assert_close(Ya, Ya_ref, TOL_BF16, f"split attention projections T={T}")
     assert tpl.tp_get_error() == 0
+
+
+@pytest.mark.parametrize("T", [8, 256])
+def test_graph_replay_matches_direct_calls(T):
+    """The API calls can be recorded into a CUDA graph and replayed: launch
+    arguments (including the split-tile epoch) are then frozen, and every
+    launch returns its synchronisation words to zero, so each replay
+    recombines its own pieces. 8 tokens: weight streaming with stream-K
+    tiles; 256 tokens: the row GEMM's split last round. Each replay must
+    reproduce the direct call bit for bit (fixed combine order)."""
+    H, I, tp = 2048, 8 * 768, 8
+    d = S.swiglu_mlp(T, H, I, seeds=(141, 142, 143, 144))
+    Sg, Su = (tpl.tp_shard_weights(dev(d[k]), tp, "col") for k in ("Wg", "Wu"))
+    Sd = tpl.tp_shard_weights(dev(d["Wd"]), tp, "row")
+    X = dev(d["X"])
+    ws = torch.empty(tpl.tp_mlp_workspace_bytes(T, H, I, tp, B), dtype=torch.uint8, device="cuda")
+    Y_direct = tpl.tp_mlp_block(X, Sg, Sd, W_up=Su, act="swiglu", workspace=ws)
+    torch.cuda.synchronize()
+    Y = torch.empty_like(Y_direct)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        tpl.tp_mlp_block(X, Sg, Sd, W_up=Su, act="swiglu", workspace=ws, out=Y)
+    for rep in range(3):
+        Y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert tpl.tp_get_error() == 0
+        np.testing.assert_array_equal(host(Y), host(Y_direct), err_msg=f"replay {rep}")
+    _, ref = O.mlp_block(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, "swiglu", W_up=f64(d["Wu"]))
+    assert_close(Y, ref, TOL_BF16, f"graph replay T={T}")
