@@ -578,6 +578,9 @@ def run_gpu(args, spec):
                 "kernel_ms": round(dom_ms, 5) if dom_ms else None,
             },
             "part_ms": [round(float(np.mean(p)), 5) for p in part_ms],
+            # first and last tenth of the timed steps: the drift shows the power cap settling in
+            "step_ms_first_last_tenth": [round(float(np.mean(step_ms[:max(1, len(step_ms) // 10)])), 5),
+                                         round(float(np.mean(step_ms[-max(1, len(step_ms) // 10):])), 5)],
             "e2e": {"value": round(e2e_value, 3), "unit": unit,
                     "h2d_bytes_per_step": int(st["X"].numel() * st["X"].element_size()),
                     "d2h_bytes_per_step": int(st["Y"].numel() * st["Y"].element_size()),
