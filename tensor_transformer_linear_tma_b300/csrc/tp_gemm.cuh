@@ -75,6 +75,7 @@ namespace tpk {
 
 enum GemmKind : int { GK_COL = 0, GK_COL_SWIGLU = 1, GK_ROW_SUM = 2, GK_ROW_PARTIAL = 3 };
 
+
 template <int KIND_, bool SWAP_, bool PAIR_ = false>
 struct GemmCfg {
   static constexpr int KIND = KIND_;
@@ -806,6 +807,7 @@ __global__ void __launch_bounds__(192, 1)
       // test-only: withhold one load (the flag is consumed by the first launch that sees it)
       bool skip_one = blockIdx.x == 0 && g_tp_inject == 1 && atomicExch(&g_tp_inject, 0) == 1;
       bool ok = true;
+
       SegIter it(args);
       Seg sg;
       while (ok && it.next(args, sg)) {
@@ -842,10 +844,14 @@ __global__ void __launch_bounds__(192, 1)
               mbar_arrive_expect_tx(&full[stage], stage_tx);
               if constexpr (SWAP) {
                 // A: weight rows of shard ks; B: token rows (X for COL, Hs[ks] for ROW)
-                tma_load_3d(sa, &mapA0, &full[stage], kb * 64, m * 128, ks);
+                // L2 priorities: each weight byte is read once here, so its lines
+                // go first and the token rows stay (token-major tiles reuse both
+                // operands across a round; hints measured no gain there)
+                const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
+                tma_load_3d_hint(sa, &mapA0, &full[stage], kb * 64, m * 128, ks, pol_w);
                 if constexpr (Cfg::NACC == 2)
-                  tma_load_3d(sa + Cfg::A_TILE, &mapA1, &full[stage], kb * 64, m * 128, ks);
-                tma_load_3d(sb, &mapB0, &full[stage], kb * 64, 0, Cfg::IS_COL ? 0 : ks);
+                  tma_load_3d_hint(sa + Cfg::A_TILE, &mapA1, &full[stage], kb * 64, m * 128, ks, pol_w);
+                tma_load_3d_hint(sb, &mapB0, &full[stage], kb * 64, 0, Cfg::IS_COL ? 0 : ks, pol_x);
               } else {
                 tma_load_3d(sa, &mapA0, &full[stage], kb * 64, m * 128, Cfg::IS_COL ? 0 : ks);
                 if constexpr (Cfg::SWIGLU) {
