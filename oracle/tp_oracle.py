@@ -40,9 +40,12 @@ reason in the design notes of the repository):
   * reduce-scatter splits the summed result along tokens into tp equal slices.
   * KV heads are replicated when num_kv_heads < tp; q head h uses kv head
     floor(h / (hq / hkv)).
-  * Between QKV and O, the attention core is the single-key case: each query
-    attends only to its own token, so the softmax weight is 1 and the context
-    of q head h is V of its kv head.
+  * Between QKV and O, the default attention core is the single-key case:
+    each query attends only to its own token, so the softmax weight is 1 and
+    the context of q head h is V of its kv head. The full core is scaled
+    dot-product attention of each local head, softmax(q k^T / sqrt(hd)) v,
+    either causal (query t sees keys 0..t, the decoder reading) or
+    unmasked.
   * RMSNorm: x * g / sqrt(mean(x^2) + eps), eps = 1e-5, statistics over the
     full (replicated) hidden.
   * Block wiring: x += O(ctx(QKV(norm(x)))); x += MLP(norm(x)); after the
@@ -66,7 +69,8 @@ __all__ = [
     "column_parallel", "all_gather", "row_parallel_partials", "all_reduce",
     "reduce_scatter", "relu", "gelu", "silu", "swiglu", "ACTIVATIONS",
     "mlp_block", "qkv_head_layout", "qkv_shards", "context_standin",
-    "attn_proj", "rmsnorm", "transformer_block", "stack_forward",
+    "attention_head", "context_attention", "attn_proj", "rmsnorm",
+    "transformer_block", "stack_forward",
 ]
 
 
@@ -292,17 +296,56 @@ def context_standin(qkv_s, q_heads, kv_heads, hq, hkv, hd):
     return np.concatenate(cols, axis=1)
 
 
-def attn_proj(X, Wq, Wk, Wv, Wo, hq, hkv, hd, tp, ctx=None, residual=None):
+def attention_head(q, k, v, causal=True):
+    """Scaled dot-product attention of one head: softmax(q k^T / sqrt(hd)) v,
+    the softmax over keys, with query t restricted to keys 0..t when causal.
+    q, k, v are [T, hd]. [CTP] attention heads (each GPU runs the attention
+    of its own heads); [TUT] self-attention block sharding (heads are local
+    between the QKV and output projections)."""
+    T, hd = q.shape
+    s = (q @ k.T) / math.sqrt(hd)
+    if causal:
+        s = np.where(np.tril(np.ones((T, T), dtype=bool)), s, -np.inf)
+    s = s - s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    p = p / p.sum(axis=1, keepdims=True)
+    return p @ v
+
+
+def context_attention(qkv_s, q_heads, kv_heads, hq, hkv, hd, causal=True):
+    """Attention core of one shard: every local q head h attends with the
+    K and V of kv head floor(h / (hq / hkv)), which the shard holds (a
+    replica when hkv < tp). qkv_s is [T, (nq + 2*nkv) * hd] (q | k | v).
+    Returns [T, len(q_heads) * hd]."""
+    nq, nkv = len(q_heads), len(kv_heads)
+    k0, v0 = nq * hd, (nq + nkv) * hd
+    group = hq // hkv
+    cols = []
+    for i, h in enumerate(q_heads):
+        j = kv_heads.index(h // group)
+        cols.append(attention_head(qkv_s[:, i * hd:(i + 1) * hd],
+                                   qkv_s[:, k0 + j * hd:k0 + (j + 1) * hd],
+                                   qkv_s[:, v0 + j * hd:v0 + (j + 1) * hd], causal))
+    return np.concatenate(cols, axis=1)
+
+
+def attn_proj(X, Wq, Wk, Wv, Wo, hq, hkv, hd, tp, ctx=None, residual=None, attention=None):
     """[CTP] QKV projection (column parallel by heads), local attention
     heads, output projection (row parallel, then all-reduce); [TUT]
     self-attention block sharding.
 
     ctx, if given, is the per-shard attention output [tp][T, hq/tp*hd];
-    otherwise the single-key stand-in supplies it. Returns
+    otherwise attention = "causal" or "full" runs the attention core of each
+    shard's heads, and None the single-key stand-in. Returns
     (qkv per shard, ctx per shard, Y)."""
     layout = qkv_head_layout(hq, hkv, tp)
     Wqkv = qkv_shards(Wq, Wk, Wv, hq, hkv, hd, tp)
     qkv = [linear(X, Wqkv[s]) for s in range(tp)]
+    if ctx is None and attention is not None:
+        if attention not in ("causal", "full"):
+            raise ValueError("attention must be 'causal', 'full' or None")
+        ctx = [context_attention(qkv[s], layout[s][0], layout[s][1], hq, hkv, hd, attention == "causal")
+               for s in range(tp)]
     if ctx is None:
         ctx = [context_standin(qkv[s], layout[s][0], layout[s][1], hq, hkv, hd)
                for s in range(tp)]

@@ -10,6 +10,7 @@ swapped gate/up, a bias added per shard) fails at least one of them; the
 ``test_planted_*`` cases plant such mistakes in the oracle and check that.
 """
 import itertools
+import math
 
 import numpy as np
 import pytest
@@ -565,3 +566,122 @@ def test_property_qkv_dedup_every_layout(heads, seed):
     full = [sum((cols[("q", h)][t] for h in range(hq)), []) + sum((cols[("k", h)][t] for h in range(hkv)), [])
             + sum((cols[("v", h)][t] for h in range(hkv)), []) for t in range(T)]
     assert full == ref
+
+
+# ---------------------------------------------------------------------------
+# Attention core (scaled dot-product attention of each local head)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_single_key_is_v(causal):
+    """One token: the softmax over one score is 1, so the context is V exactly."""
+    rng = np.random.default_rng(201)
+    q, k, v = (rng.standard_normal((1, 8)) for _ in range(3))
+    np.testing.assert_array_equal(O.attention_head(q, k, v, causal), v)
+
+
+def test_attention_causal_first_query_sees_only_key_0():
+    rng = np.random.default_rng(202)
+    q, k, v = (rng.standard_normal((6, 4)) for _ in range(3))
+    np.testing.assert_array_equal(O.attention_head(q, k, v, True)[0], v[0])
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_equal_keys_average_values(causal):
+    """Equal keys give equal scores: uniform weights over the visible keys,
+    so the context is the mean of V over keys 0..t (causal) or all keys."""
+    rng = np.random.default_rng(203)
+    T, hd = 7, 4
+    q = rng.standard_normal((T, hd))
+    k = np.tile(rng.standard_normal((1, hd)), (T, 1))
+    v = rng.standard_normal((T, hd))
+    want = (np.cumsum(v, 0) / np.arange(1, T + 1)[:, None]) if causal else np.tile(v.mean(0), (T, 1))
+    np.testing.assert_allclose(O.attention_head(q, k, v, causal), want, rtol=0, atol=1e-13)
+
+
+def test_attention_two_keys_closed_form():
+    """hd = 2, q = (1, 0): scores are k[:,0] / sqrt(2). With k0 = 0 and
+    k1[0] = sqrt(2) ln 3 the weights are 1/4 and 3/4 (checks the 1/sqrt(hd)
+    scale and the softmax)."""
+    q = np.array([[1.0, 0.0], [1.0, 0.0]])
+    k = np.array([[0.0, 5.0], [math.sqrt(2.0) * math.log(3.0), -2.0]])
+    v = np.array([[4.0, 8.0], [-4.0, 12.0]])
+    out = O.attention_head(q, k, v, causal=False)
+    np.testing.assert_allclose(out, np.tile(0.25 * v[0] + 0.75 * v[1], (2, 1)), rtol=0, atol=1e-12)
+    out_c = O.attention_head(q, k, v, causal=True)    # row 0 sees key 0 only; row 1 as above
+    np.testing.assert_allclose(out_c, np.stack([v[0], 0.25 * v[0] + 0.75 * v[1]]), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_key_shift_invariance(causal):
+    """Adding one vector c to every key adds q.c/sqrt(hd) to all scores of a
+    query, which the softmax cancels."""
+    rng = np.random.default_rng(204)
+    q, k, v = (rng.standard_normal((9, 6)) for _ in range(3))
+    c = rng.standard_normal((1, 6))
+    np.testing.assert_allclose(O.attention_head(q, k + c, v, causal), O.attention_head(q, k, v, causal),
+                               rtol=0, atol=1e-12)
+
+
+def test_attention_causal_ignores_future_tokens():
+    rng = np.random.default_rng(205)
+    q, k, v = (rng.standard_normal((8, 4)) for _ in range(3))
+    k2, v2 = k.copy(), v.copy()
+    k2[5:] += 3.0
+    v2[5:] -= 7.0
+    a, b = O.attention_head(q, k, v, True), O.attention_head(q, k2, v2, True)
+    np.testing.assert_array_equal(a[:5], b[:5])
+    assert not np.allclose(a[5:], b[5:])
+
+
+def test_attention_full_is_key_permutation_invariant():
+    rng = np.random.default_rng(206)
+    q, k, v = (rng.standard_normal((8, 4)) for _ in range(3))
+    perm = rng.permutation(8)
+    np.testing.assert_allclose(O.attention_head(q, k[perm], v[perm], False), O.attention_head(q, k, v, False),
+                               rtol=0, atol=1e-12)
+
+
+def test_attention_gqa_head_map():
+    """hq = 4, hkv = 2 on one shard: q heads 0, 1 read kv head 0 and 2, 3 read
+    kv head 1. Zeroing kv head 1's V zeroes exactly heads 2 and 3; equal q
+    vectors within a group give equal contexts."""
+    rng = np.random.default_rng(207)
+    T, hd, hq, hkv = 5, 4, 4, 2
+    qkv = rng.standard_normal((T, (hq + 2 * hkv) * hd))
+    qkv[:, hd:2 * hd] = qkv[:, 0:hd]                       # q head 1 = q head 0
+    v1 = (hq + hkv + 1) * hd
+    qkv[:, v1:v1 + hd] = 0.0                               # V of kv head 1
+    (q, kv), = O.qkv_head_layout(hq, hkv, 1)
+    ctx = O.context_attention(qkv, q, kv, hq, hkv, hd, causal=True)
+    assert np.all(ctx[:, 2 * hd:] == 0.0) and not np.any(np.all(ctx[:, :2 * hd] == 0.0, axis=0))
+    np.testing.assert_array_equal(ctx[:, 0:hd], ctx[:, hd:2 * hd])
+
+
+def test_attention_sharded_equals_unsharded():
+    """Per-shard attention (kv heads replicated where hkv < tp) gives the same
+    context columns as running every head on one device."""
+    rng = np.random.default_rng(208)
+    T, H, hq, hkv, hd = 6, 8, 8, 2, 4
+    X = rng.standard_normal((T, H))
+    Wq, Wk, Wv = (rng.standard_normal((H, n * hd)) for n in (hq, hkv, hkv))
+    (q1, kv1), = O.qkv_head_layout(hq, hkv, 1)
+    full = O.context_attention(X @ np.concatenate([Wq, Wk, Wv], 1), q1, kv1, hq, hkv, hd)
+    for tp in (2, 4, 8):
+        layout = O.qkv_head_layout(hq, hkv, tp)
+        parts = [O.context_attention(X @ Ws, layout[s][0], layout[s][1], hq, hkv, hd)
+                 for s, Ws in enumerate(O.qkv_shards(Wq, Wk, Wv, hq, hkv, hd, tp))]
+        np.testing.assert_allclose(np.concatenate(parts, 1), full, rtol=0, atol=1e-12)
+
+
+def test_planted_missing_scale_is_caught(monkeypatch):
+    """A planted mistake (no 1/sqrt(hd)) fails the closed-form pin."""
+    def bad(q, k, v, causal=True):
+        s = q @ k.T
+        if causal:
+            s = np.where(np.tril(np.ones(s.shape, dtype=bool)), s, -np.inf)
+        p = np.exp(s - s.max(1, keepdims=True))
+        return (p / p.sum(1, keepdims=True)) @ v
+    monkeypatch.setattr(O, "attention_head", bad)
+    with pytest.raises(AssertionError):
+        test_attention_two_keys_closed_form()
