@@ -78,6 +78,11 @@ enum { TP_ACT_NONE = 0, TP_ACT_RELU = 1, TP_ACT_GELU = 2, TP_ACT_SILU = 3, TP_AC
 /* Combine of row-parallel partials. */
 enum { TP_REDUCE_SUM = 0, TP_REDUCE_SCATTER = 1 };
 
+/* Attention core between the QKV and O projections (tp_attn_block): the
+ * single-key stand-in (each query attends only to its own token), or scaled
+ * dot-product attention of each local head, causal or unmasked. */
+enum { TP_ATTN_SINGLE_KEY = 0, TP_ATTN_CAUSAL = 1, TP_ATTN_FULL = 2 };
+
 /*
  * Non-owning view of sharded weights, filled in by tp_shard_weights /
  * tp_shard_qkv. K and N are the FULL weight's in/out features.
@@ -313,6 +318,40 @@ size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int d
 int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
                  const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
                  size_t ws_bytes, void* Y, void* stream);
+
+/*
+ * tp_attention - the attention core of every local head of every shard
+ * ("CUDA tensor parallel computations" page, attention heads: each GPU runs
+ * the attention of its own heads; tutorial page, self-attention block
+ * sharding): for q head h of shard s and its kv head g = h / (hq / hkv)
+ * (a replica when hkv < tp),
+ *   ctx[s][:, h_local] = softmax(Q_h K_g^T / sqrt(hd)) V_g,
+ * with query t restricted to keys 0..t under TP_ATTN_CAUSAL (the decoder
+ * reading) and unmasked under TP_ATTN_FULL.
+ *   qkv   [tp][T][(nq + 2 nkv) * hd] bf16, the layout tp_column_linear writes
+ *         for a tp_shard_qkv view (q heads | k heads | v heads per shard).
+ *   ctx   [tp][T][nq * hd] bf16, written.
+ *   hd must be 128 (TP_ERR_UNSUPPORTED otherwise). Scores, the softmax and
+ *   the P V accumulation are fp32; P is rounded to bf16 before P V.
+ * Errors: TP_ERR_NULL, TP_ERR_MODE, TP_ERR_SHAPE (head counts that
+ * tp_shard_qkv rejects), TP_ERR_UNSUPPORTED, TP_ERR_ALIGN, TP_ERR_CUDA.
+ */
+int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, int mode, void* ctx, void* stream);
+
+/*
+ * tp_attn_block - tp_attn_proj with the attention core chosen by `mode`:
+ * TP_ATTN_SINGLE_KEY (as tp_attn_proj without ctx), TP_ATTN_CAUSAL or
+ * TP_ATTN_FULL (tp_attention between the QKV and O launches; bf16, hd 128).
+ * Arguments otherwise as tp_attn_proj; the workspace holds qkv (unless
+ * qkv_out is given), the context and the split-tile scratch
+ * (tp_attn_workspace_bytes).
+ * Errors: as tp_attn_proj, plus TP_ERR_MODE for an unknown mode and
+ * TP_ERR_UNSUPPORTED for a core other than the single-key one on fp32 views
+ * or hd != 128.
+ */
+int tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, int mode,
+                  const void* residual, int out_dtype, void* qkv_out, void* workspace, size_t ws_bytes, void* Y,
+                  void* stream);
 
 /*
  * tp_rmsnorm - RMSNorm on the replicated hidden ("CUDA tensor parallel

@@ -296,16 +296,18 @@ def context_standin(qkv_s, q_heads, kv_heads, hq, hkv, hd):
     return np.concatenate(cols, axis=1)
 
 
-def attention_head(q, k, v, causal=True):
+def attention_head(q, k, v, causal=True, q_offset=0):
     """Scaled dot-product attention of one head: softmax(q k^T / sqrt(hd)) v,
     the softmax over keys, with query t restricted to keys 0..t when causal.
-    q, k, v are [T, hd]. [CTP] attention heads (each GPU runs the attention
-    of its own heads); [TUT] self-attention block sharding (heads are local
+    q is [Tq, hd] holding the queries at positions q_offset..q_offset+Tq-1;
+    k, v are [T, hd]. [CTP] attention heads (each GPU runs the attention of
+    its own heads); [TUT] self-attention block sharding (heads are local
     between the QKV and output projections)."""
-    T, hd = q.shape
+    Tq, hd = q.shape
     s = (q @ k.T) / math.sqrt(hd)
     if causal:
-        s = np.where(np.tril(np.ones((T, T), dtype=bool)), s, -np.inf)
+        pos = np.arange(Tq)[:, None] + q_offset
+        s = np.where(np.arange(k.shape[0])[None, :] <= pos, s, -np.inf)
     s = s - s.max(axis=1, keepdims=True)
     p = np.exp(s)
     p = p / p.sum(axis=1, keepdims=True)

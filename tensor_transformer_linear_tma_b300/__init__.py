@@ -20,7 +20,7 @@ __all__ = [
     "tp_shard_weights", "tp_shard_qkv", "tp_qkv_shard_elems", "tp_column_linear",
     "tp_row_linear", "tp_row_linear_partials", "tp_gemm_workspace_bytes", "tp_shard_reduce", "tp_shard_gather",
     "tp_mlp_workspace_bytes", "tp_mlp_block", "tp_mlp_block_static", "tp_attn_workspace_bytes",
-    "tp_attn_proj", "TP_STATIC_WORKSPACE_BYTES",
+    "tp_attn_proj", "tp_attn_block", "tp_attention", "ATTN_MODES", "TP_STATIC_WORKSPACE_BYTES",
     "tp_rmsnorm", "tp_get_error", "tp_debug_set_wait_limit_ns", "tp_debug_inject",
     "tp_status_string",
 ]
@@ -35,6 +35,7 @@ TP_F32, TP_BF16 = 0, 1
 TP_COL, TP_ROW = 0, 1
 ACTS = {"none": 0, "relu": 1, "gelu": 2, "silu": 3, "swiglu": 4}
 REDUCE_OPS = {"sum": 0, "scatter": 1}
+ATTN_MODES = {"single_key": 0, "causal": 1, "full": 2}
 
 _vp, _i64, _i32, _sz, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
 
@@ -63,6 +64,8 @@ _SIGS = {
     "tp_mlp_block_static": (_i32, [_vp, _i64, _P, _P, _P, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp]),
     "tp_attn_workspace_bytes": (_sz, [_i64, _i32, _i32, _i32, _i32, _i32]),
     "tp_attn_proj": (_i32, [_vp, _i64, _P, _P, _vp, _vp, _i32, _vp, _vp, _sz, _vp, _vp]),
+    "tp_attn_block": (_i32, [_vp, _i64, _P, _P, _i32, _vp, _i32, _vp, _vp, _sz, _vp, _vp]),
+    "tp_attention": (_i32, [_vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "tp_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _f32, _i32, _vp, _i32, _vp]),
     "tp_get_error": (_i32, [_vp]),
     "tp_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
@@ -318,6 +321,35 @@ def tp_attn_proj(X, Wqkv: Shards, Wo: Shards, ctx=None, residual=None, qkv_out=N
         _ptr(X), T, Wqkv.ref(), Wo.ref(), _ptr(ctx), _ptr(residual), _dt(out), _ptr(qkv_out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _stream(X.device)))
+    return out
+
+
+def tp_attn_block(X, Wqkv: Shards, Wo: Shards, attention: str = "causal", residual=None, qkv_out=None,
+                  workspace=None, out=None, out_dtype=None):
+    """QKV by heads -> attention core ("causal", "full" or "single_key") -> O + sum."""
+    T = X.shape[0]
+    v = Wqkv.view
+    need = tp_attn_workspace_bytes(T, v.hq, v.hkv, v.hd, v.tp, _dt(X))
+    if workspace is None:
+        workspace = _workspace(need, X.device)
+    odt = _out_dtype(X.dtype, out, residual, out_dtype)
+    if out is None:
+        out = torch.empty((T, Wo.N), dtype=odt, device=X.device)
+    _check("tp_attn_block", lib.tp_attn_block(
+        _ptr(X), T, Wqkv.ref(), Wo.ref(), ATTN_MODES[attention], _ptr(residual), _dt(out), _ptr(qkv_out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _stream(X.device)))
+    return out
+
+
+def tp_attention(qkv, hq: int, hkv: int, hd: int, causal: bool = True, out=None):
+    """Attention core of every local head: qkv [tp, T, (nq + 2 nkv) * hd] ->
+    ctx [tp, T, nq * hd] (bf16, hd 128)."""
+    tp, T, _ = qkv.shape
+    if out is None:
+        out = torch.empty((tp, T, hq // tp * hd), dtype=qkv.dtype, device=qkv.device)
+    _check("tp_attention", lib.tp_attention(
+        _ptr(qkv), T, tp, hq, hkv, hd, ATTN_MODES["causal" if causal else "full"], _ptr(out),
+        _stream(qkv.device)))
     return out
 
 

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <chrono>
 #include <cstdint>
@@ -15,6 +16,7 @@
 #include <random>
 
 #include "tp.h"
+#include "tp_attention.cuh"
 #include "tp_elementwise.cuh"
 #include "tp_gemm.cuh"
 #include "tp_simt.cuh"
@@ -624,6 +626,48 @@ size_t mlp_max_tiles(int64_t H, int64_t I, int tp) {
   const size_t swap_row = cdiv(H, 128);
   return std::max<size_t>(2 * SK_MAX_CTAS, std::max(swap_col, swap_row));
 }
+// Attention core over qkv [tp][T][(nq + 2 nkv) * 128] (q | k | v per
+// shard) into ctx [tp][T][nq * 128]; mode TP_ATTN_CAUSAL or TP_ATTN_FULL.
+int attention_launch(const void* qkv, int64_t T, int tp, int hq, int hkv, int mode, void* ctx, cudaStream_t st) {
+  const int nq = hq / tp, nkv = hkv >= tp ? hkv / tp : 1;
+  const int64_t nqkv = static_cast<int64_t>(nq + 2 * nkv) * tpk::AT_HD;
+  CUtensorMap m;
+  if (!make_map_bf16(&m, qkv, nqkv, T, tp, 128)) return TP_ERR_CUDA;
+  tpk::AttnArgs a{};
+  a.ctx = static_cast<bf16*>(ctx);
+  a.T = static_cast<int>(T);
+  a.tp = tp;
+  a.hq = hq;
+  a.hkv = hkv;
+  a.nq = nq;
+  a.nkv = nkv;
+  a.group = hq / hkv;
+  a.causal = mode == TP_ATTN_CAUSAL ? 1 : 0;
+  a.q_blocks = static_cast<int>(cdiv(T, 128));
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(tpk::AT_HD)));
+  static bool attr_done[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return TP_ERR_CUDA;
+  if (!attr_done[dev]) {
+    if (cudaFuncSetAttribute(tpk::tp_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tpk::AT_SMEM) !=
+        cudaSuccess)
+      return TP_ERR_CUDA;
+    attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(tp) * nq * a.q_blocks));
+  cfg.blockDim = dim3(tpk::AT_THREADS);
+  cfg.dynamicSmemBytes = tpk::AT_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, tpk::tp_attn_kernel, m, a) != cudaSuccess) return TP_ERR_CUDA;
+  return launch_status();
+}
+
 size_t attn_max_tiles(int64_t H, int hq, int hkv, int hd, int tp) {
   const int64_t nkv = hkv >= tp ? hkv / tp : 1;
   const size_t swap_col = static_cast<size_t>(tp) * cdiv((hq / tp + 2 * nkv) * hd, 128);
@@ -948,9 +992,14 @@ size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int d
   return b;
 }
 
-int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
-                 const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
-                 size_t ws_bytes, void* Y, void* stream) {
+}  // extern "C"
+
+namespace {
+// QKV by heads -> attention core (caller context, single-key stand-in or the
+// causal / full core) -> O and the shard sum.
+int attn_block_impl(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, const void* ctx,
+                    int mode, const void* residual, int out_dtype, void* qkv_out, void* workspace,
+                    size_t ws_bytes, void* Y, void* stream) {
   if (!Wo || !Wqkv || (!workspace && T != 0)) return TP_ERR_NULL;
   int r = check_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, Y);
   if (r) return r;
@@ -967,6 +1016,8 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
     return TP_ERR_ALIGN;
   if (dt == TP_BF16 && hd % 8) return TP_ERR_ALIGN;
   if (Wqkv->K > static_cast<int64_t>(hq) * hd * 4) return TP_ERR_UNSUPPORTED;  // scratch sizing bound
+  if (mode != TP_ATTN_SINGLE_KEY && mode != TP_ATTN_CAUSAL && mode != TP_ATTN_FULL) return TP_ERR_MODE;
+  if (mode != TP_ATTN_SINGLE_KEY && (dt != TP_BF16 || hd != tpk::AT_HD)) return TP_ERR_UNSUPPORTED;
   if (ws_bytes < tp_attn_workspace_bytes(T, hq, hkv, hd, tp, dt)) return TP_ERR_WORKSPACE;
   if (T == 0) return TP_OK;
   const cudaStream_t st = as_stream(stream);
@@ -981,6 +1032,11 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
     sc = carve_scratch(workspace, qkv_bytes + ctx_bytes,
                        attn_max_tiles(static_cast<int64_t>(hq) * hd * 4, hq, hkv, hd, tp));
     scp = &sc;
+  }
+  if (mode != TP_ATTN_SINGLE_KEY) {
+    if ((r = run_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, qkv, st, scp))) return r;
+    if ((r = attention_launch(qkv, T, tp, hq, hkv, mode, ctx_ws, st))) return r;
+    return run_row(ctx_ws, T, Wo, nullptr, residual, Y, out_dtype, nullptr, st, scp);
   }
   // Without a caller context the single-key stand-in is used: on the bf16
   // path the QKV epilogue writes it from the V columns it has just computed;
@@ -998,6 +1054,35 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
   }
   if (!ctx) ctx = ctx_ws;
   return run_row(ctx, T, Wo, nullptr, residual, Y, out_dtype, nullptr, st, scp);
+}
+
+}  // namespace
+
+extern "C" {
+
+int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
+                 const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
+                 size_t ws_bytes, void* Y, void* stream) {
+  return attn_block_impl(X, T, Wqkv, Wo, ctx, TP_ATTN_SINGLE_KEY, residual, out_dtype, qkv_out, workspace,
+                         ws_bytes, Y, stream);
+}
+
+int tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, int mode,
+                  const void* residual, int out_dtype, void* qkv_out, void* workspace, size_t ws_bytes, void* Y,
+                  void* stream) {
+  return attn_block_impl(X, T, Wqkv, Wo, nullptr, mode, residual, out_dtype, qkv_out, workspace, ws_bytes, Y,
+                         stream);
+}
+
+int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, int mode, void* ctx, void* stream) {
+  if ((!qkv || !ctx) && T != 0) return TP_ERR_NULL;
+  if (mode != TP_ATTN_CAUSAL && mode != TP_ATTN_FULL) return TP_ERR_MODE;
+  if (T < 0 || tp < 1 || hq < 1 || hkv < 1 || hd < 1 || tp_qkv_shard_elems(1, hq, hkv, hd, tp) == 0)
+    return TP_ERR_SHAPE;
+  if (hd != tpk::AT_HD || T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  if (!ptr_ok(qkv, TP_BF16) || !ptr_ok(ctx, TP_BF16)) return TP_ERR_ALIGN;
+  if (T == 0) return TP_OK;
+  return attention_launch(qkv, T, tp, hq, hkv, mode, ctx, as_stream(stream));
 }
 
 int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,

@@ -1,0 +1,323 @@
+// Attention core of each local head, between the QKV and O projections:
+// ctx_h = softmax(q_h k_g^T / sqrt(hd)) v_g for every q head h of a shard,
+// g = h / (hq / hkv) its kv head ("CUDA tensor parallel computations" page,
+// attention heads; tutorial page, self-attention block sharding), causal
+// (query t sees keys 0..t) or unmasked.
+//
+// One CTA per (shard, q head, block of 128 queries), head size 128, 192
+// threads:
+//   warp 0      TMA producer: the Q tile once, then K and V tiles of each
+//               block of 128 keys, double-buffered;
+//   warp 1      TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
+//               score buffers (one key block ahead of the softmax), then
+//               O += P V into the TMEM output accumulator, with V read as an
+//               MN-major operand straight from its TMA tile;
+//   warps 2..5  softmax, one query row per thread: scores from TMEM, online
+//               maximum and sum in fp32 (exp2 with the log2(e)/sqrt(hd)
+//               scale folded in), O rescaled in TMEM when the maximum grows,
+//               P written as bf16 into a 128-byte-swizzled shared-memory tile
+//               (the next MMA's A operand); at the end O / l is stored.
+// Every wait is bounded as in the GEMM kernel.
+#pragma once
+
+#include "tp_gemm.cuh"  // epi_any, store_bf16x8_f
+#include "tp_ptx.cuh"
+
+namespace tpk {
+
+struct AttnArgs {
+  __nv_bfloat16* ctx;  // [tp][T][nq * hd]
+  int T, tp, hq, hkv, nq, nkv, group;
+  int causal;
+  int q_blocks;        // ceil(T / 128)
+  float scale_log2;    // log2(e) / sqrt(hd)
+};
+
+constexpr int AT_ROWS = 128;                   // queries per CTA, keys per block
+constexpr int AT_HD = 128;                     // head size
+constexpr int AT_PANEL = AT_ROWS * 128;        // 128 rows x 128 bytes (64 bf16 columns)
+constexpr int AT_TILE = 2 * AT_PANEL;          // 128 x 128 bf16 as two 64-column panels
+constexpr int AT_THREADS = 192;
+constexpr int AT_SMEM = 6 * AT_TILE + 1024 + 512;  // Q, K x2, V x2, P; alignment; barriers
+
+__global__ void __launch_bounds__(AT_THREADS, 1)
+    tp_attn_kernel(const __grid_constant__ CUtensorMap mapQKV, const AttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + AT_TILE;      // [2]
+  uint8_t* sV = smem + 3 * AT_TILE;  // [2]
+  uint8_t* sP = smem + 5 * AT_TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * AT_TILE);
+  uint64_t* q_full = bars;           // TMA -> MMA
+  uint64_t* k_full = bars + 1;       // [2]
+  uint64_t* v_full = bars + 3;       // [2]
+  uint64_t* kv_empty = bars + 5;     // [2] MMA -> TMA
+  uint64_t* s_full = bars + 7;       // [2] MMA -> softmax
+  uint64_t* s_empty = bars + 9;      // [2] softmax -> MMA
+  uint64_t* p_full = bars + 11;      // softmax -> MMA (P written, O rescaled)
+  uint64_t* o_done = bars + 12;      // MMA -> softmax (P V of a block complete)
+  uint64_t* drain = bars + 13;       // abort path only
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // work unit; the longest (latest, under the causal mask) query blocks first
+  const int heads = a.tp * a.nq;
+  const int qb = a.q_blocks - 1 - static_cast<int>(blockIdx.x) / heads;
+  const int hh = static_cast<int>(blockIdx.x) % heads;
+  const int s = hh / a.nq, j = hh % a.nq;
+  const int kv0 = a.hkv >= a.tp ? s * a.nkv : (s * a.hkv) / a.tp;
+  const int kvi = (s * a.nq + j) / a.group - kv0;  // the kv head within the shard's block
+  const int qcol = j * AT_HD, kcol = (a.nq + kvi) * AT_HD, vcol = (a.nq + a.nkv + kvi) * AT_HD;
+  const int q0 = qb * AT_ROWS;
+  const int nkb = a.causal ? qb + 1 : (a.T + AT_ROWS - 1) / AT_ROWS;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&mapQKV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------ TMA producer ------------------------------
+      int issued_k[2] = {-1, -1}, issued_v[2] = {-1, -1};
+      bool ok = true;
+      mbar_arrive_expect_tx(q_full, AT_TILE);
+      tma_load_3d(sQ, &mapQKV, q_full, qcol, q0, s);
+      tma_load_3d(sQ + AT_PANEL, &mapQKV, q_full, qcol + 64, q0, s);
+      for (int jb = 0; jb < nkb; ++jb) {
+        const int st = jb & 1;
+        const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
+        if (!mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int k0 = jb * AT_ROWS;
+        uint8_t* k_t = sK + st * AT_TILE;
+        uint8_t* v_t = sV + st * AT_TILE;
+        mbar_arrive_expect_tx(&k_full[st], AT_TILE);
+        tma_load_3d(k_t, &mapQKV, &k_full[st], kcol, k0, s);
+        tma_load_3d(k_t + AT_PANEL, &mapQKV, &k_full[st], kcol + 64, k0, s);
+        issued_k[st] = static_cast<int>(ph);
+        mbar_arrive_expect_tx(&v_full[st], AT_TILE);
+        tma_load_3d(v_t, &mapQKV, &v_full[st], vcol, k0, s);
+        tma_load_3d(v_t + AT_PANEL, &mapQKV, &v_full[st], vcol + 64, k0, s);
+        issued_v[st] = static_cast<int>(ph);
+      }
+      if (!ok) {  // let every copy this block started land before it exits
+        mbar_wait_drain(q_full, 0);
+        for (int i = 0; i < 2; ++i) {
+          if (issued_k[i] >= 0) mbar_wait_drain(&k_full[i], static_cast<uint32_t>(issued_k[i]));
+          if (issued_v[i] >= 0) mbar_wait_drain(&v_full[i], static_cast<uint32_t>(issued_v[i]));
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------ MMA issuer ------------------------------
+      const uint32_t idesc_s = idesc_bf16_f32(128, 128);
+      const uint32_t idesc_o = idesc_bf16_f32_bmn(128, 128);
+      const uint32_t tO = tmem_base + 256;
+      bool ok = mbar_wait(q_full, 0, abort_flag), issued_any = false;
+      // S(jb) = Q K(jb)^T: M = 128 queries, N = 128 keys, K = hd in 8 steps
+      // of 16 (two 64-wide panels, +32 bytes per step inside a panel)
+      auto issue_s = [&](int jb) -> bool {
+        const int st = jb & 1;
+        const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
+        if (!mbar_wait(&k_full[st], ph, abort_flag)) return false;
+        if (!mbar_wait(&s_empty[st], ph ^ 1u, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t q_a = smem_u32(sQ), k_a = smem_u32(sK + st * AT_TILE);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = static_cast<uint32_t>((k >> 2) * AT_PANEL + (k & 3) * 32);
+          tc_mma_bf16(tmem_base + static_cast<uint32_t>(st * 128), smem_desc_k_sw128(q_a + off),
+                      smem_desc_k_sw128(k_a + off), idesc_s, k > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[st]);
+        issued_any = true;
+        return true;
+      };
+      // O += P(jb) V(jb): M = 128 queries, N = hd, K = 128 keys in 8 steps;
+      // P is K-major (two 64-key panels), V MN-major (rows = keys, each row
+      // 64 hd values; the second 64 hd values one panel further)
+      auto issue_pv = [&](int jb) -> bool {
+        const int st = jb & 1;
+        const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
+        if (!mbar_wait(p_full, static_cast<uint32_t>(jb) & 1u, abort_flag)) return false;
+        if (!mbar_wait(&v_full[st], ph, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t p_a = smem_u32(sP), v_a = smem_u32(sV + st * AT_TILE);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t poff = static_cast<uint32_t>((k >> 2) * AT_PANEL + (k & 3) * 32);
+          tc_mma_bf16(tO, smem_desc_k_sw128(p_a + poff),
+                      smem_desc_mn_sw128(v_a + static_cast<uint32_t>(k * 16 * 128), AT_PANEL, 1024), idesc_o,
+                      (jb > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(o_done);
+        tc_commit(&kv_empty[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int jb = 0; ok && jb < nkb; ++jb) {
+        if (jb + 1 < nkb && !issue_s(jb + 1)) {
+          ok = false;
+          break;
+        }
+        ok = issue_pv(jb);
+      }
+      if (!ok && issued_any) {  // wait for MMAs in flight before TMEM is freed
+        tc_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------ softmax ------------------------------
+    const int q = warp & 3;            // TMEM lane quadrant
+    const int r = q * 32 + lane;       // query row within the block
+    const int t = q0 + r;              // query index
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t tO = tmem_base + 256 + lane_off;
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int jb = 0; jb < nkb; ++jb) {
+      const int st = jb & 1;
+      const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
+      const bool waited = mbar_wait(&s_full[st], ph, abort_flag);
+      if (epi_any(!waited || *abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[128];
+      const uint32_t tS = tmem_base + static_cast<uint32_t>(st * 128) + lane_off;
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tS + static_cast<uint32_t>(c), rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[c + i] = __uint_as_float(rr[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[st]);  // S(jb + 2) may overwrite this buffer
+      const int kbase = jb * AT_ROWS;
+      const int kmax = a.causal ? min(t, a.T - 1) : a.T - 1;  // last key this query sees
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        sv[i] = (kbase + i <= kmax) ? sv[i] * a.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sv[i]);
+      }
+      const float m_new = fmaxf(m, mx);
+      const float m_use = m_new == -INFINITY ? 0.0f : m_new;  // rows past T see no key
+      const float alpha = exp2f(m - m_use);
+      float sum = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        sv[i] = exp2f(sv[i] - m_use);
+        sum += sv[i];
+      }
+      l = l * alpha + sum;
+      m = m_new;
+      if (jb > 0) {
+        // P V of the previous block has finished: O is stable and P is free
+        const bool done = mbar_wait(o_done, static_cast<uint32_t>(jb - 1) & 1u, abort_flag);
+        if (epi_any(!done || *abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t rr[32];
+            tmem_ld32(tO + static_cast<uint32_t>(c), rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(tO + static_cast<uint32_t>(c), rr);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P row in bf16: keys 0..63 in panel 0, 64..127 in panel 1, 16-byte
+      // chunks at the 128-byte swizzle position of this row
+#pragma unroll
+      for (int c8 = 0; c8 < 16; ++c8) {
+        const int panel = c8 >> 3, ch = c8 & 7;
+        uint4 v;
+        v.x = pack_bf16x2(sv[c8 * 8 + 0], sv[c8 * 8 + 1]);
+        v.y = pack_bf16x2(sv[c8 * 8 + 2], sv[c8 * 8 + 3]);
+        v.z = pack_bf16x2(sv[c8 * 8 + 4], sv[c8 * 8 + 5]);
+        v.w = pack_bf16x2(sv[c8 * 8 + 6], sv[c8 * 8 + 7]);
+        *reinterpret_cast<uint4*>(sP + panel * AT_PANEL + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();  // the tensor core reads P through the async proxy
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (ok) {
+      const bool done = mbar_wait(o_done, static_cast<uint32_t>(nkb - 1) & 1u, abort_flag);
+      if (!epi_any(!done || *abort_flag)) {
+        tc_fence_after();
+        const float inv = 1.0f / l;
+        const int nc = a.nq * AT_HD;
+        __nv_bfloat16* out = a.ctx + (static_cast<size_t>(s) * a.T + t) * nc + j * AT_HD;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t rr[32];
+          tmem_ld32(tO + static_cast<uint32_t>(c), rr);
+          tmem_ld_wait();
+          if (t < a.T) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(rr[i + e]) * inv;
+              store_bf16x8_f(out + c + i, v);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace tpk

@@ -685,3 +685,12 @@ def test_planted_missing_scale_is_caught(monkeypatch):
     monkeypatch.setattr(O, "attention_head", bad)
     with pytest.raises(AssertionError):
         test_attention_two_keys_closed_form()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_query_offset_selects_rows(causal):
+    """Queries given from position a onwards reproduce rows a.. of the full call."""
+    rng = np.random.default_rng(209)
+    q, k, v = (rng.standard_normal((10, 4)) for _ in range(3))
+    np.testing.assert_array_equal(O.attention_head(q[6:], k, v, causal, q_offset=6),
+                                  O.attention_head(q, k, v, causal)[6:])
