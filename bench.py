@@ -61,6 +61,18 @@ def workload_spec(name: str, tp: int | None, tokens: int | None):
         return dict(name="gqa_attn_proj", T=T, H=H, hq=hq, hkv=hkv, hd=hd, tp=tp, flops=flops,
                     dominant="qkv_col_gemm (QKV by heads, replicas computed once)",
                     dominant_flops=2.0 * T * H * (hq + 2 * hkv) * hd, bound="tensor")
+    if name == "gqa_attn":
+        # the GQA projections with the causal attention core between them;
+        # the core's algorithmic FLOPs count only the visible (t' <= t) scores
+        T, H, hq, hkv, hd = tokens or 4096, 4096, 32, 8, 128
+        tp = tp or 16
+        core = 2.0 * 2.0 * hd * hq * T * (T + 1) / 2.0
+        flops = 2.0 * T * H * (hq + 2 * hkv) * hd + core + 2.0 * T * hq * hd * H
+        return dict(name="gqa_attn_block_causal", T=T, H=H, hq=hq, hkv=hkv, hd=hd, tp=tp, flops=flops,
+                    dominant="attention_core (causal, every local head)", dominant_flops=core,
+                    bound="tensor",
+                    flops_of_rows=lambda r: (2.0 * r * H * (hq + 2 * hkv) * hd + 2.0 * 2.0 * hd * hq * r * (r + 1) / 2.0
+                                             + 2.0 * r * hq * hd * H))
     if name == "decode":
         T, H, I = tokens or 1, 8192, 28672
         tp = tp or 8
@@ -115,7 +127,10 @@ class OracleLeg:
             d = S.gqa_proj(min(T, 512), H, hq, hkv, hd)
             A = {k: d[k].astype(np.float64) for k in d}
             X = A["X"]
-            self.fn = lambda r: O.attn_proj(X[:r], A["Wq"], A["Wk"], A["Wv"], A["Wo"], hq, hkv, hd, tp)
+            core = "causal" if name.startswith("gqa_attn_block") else None
+            # the first r tokens: a complete causal problem of its own
+            self.fn = lambda r: O.attn_proj(X[:r], A["Wq"], A["Wk"], A["Wv"], A["Wo"], hq, hkv, hd, tp,
+                                            attention=core)
         else:
             d = S.stack(min(T, 128))
             Ls = [{k: v.astype(np.float64) for k, v in L.items()} for L in d["layers"]]
@@ -140,6 +155,8 @@ class OracleLeg:
         if sp["bound"] == "hbm":  # algorithmic bytes of a rows-token problem, bf16 storage
             per_tok = (sp["bytes"] - 3.0 * sp["H"] * sp["I"] * 2) / sp["T"]
             return (3.0 * sp["H"] * sp["I"] * 2 + rows * per_tok) / elapsed / 1e9
+        if "flops_of_rows" in sp:
+            return sp["flops_of_rows"](rows) / elapsed / 1e12
         return sp["flops"] / sp["T"] * rows / elapsed / 1e12
 
     def timed(self, rows):
@@ -302,6 +319,26 @@ def setup_workload(spec, torch, tpl):
             tpl.tp_column_linear(X, Sg, W_up=Su, act="swiglu", out=Hs, workspace=gws)
         st.update(parts=[lambda: api_call(X, Y)], X=X, Y=Y, api=api_call, launches_per_step=2,
                   keep=[Sg, Su, Sd, Hs, ws, gws], dominant_part=part_a)
+    elif name.startswith("gqa_attn_block"):
+        H, hq, hkv, hd = spec["H"], spec["hq"], spec["hkv"], spec["hd"]
+        d = S.gqa_proj(T, H, hq, hkv, hd)
+        Sqkv = tpl.tp_shard_qkv(up(d["Wq"]), up(d["Wk"]), up(d["Wv"]), hq, hkv, hd, tp)
+        So = tpl.tp_shard_weights(up(d["Wo"]), tp, "row")
+        X = up(d["X"])
+        del d
+        qkv = torch.empty((tp, T, Sqkv.shard_width), dtype=B, device="cuda")
+        ctx = torch.empty((tp, T, hq // tp * hd), dtype=B, device="cuda")
+        Y = torch.empty((T, H), dtype=B, device="cuda")
+        ws = torch.empty(max(tpl.tp_attn_workspace_bytes(T, hq, hkv, hd, tp, B), 256), dtype=torch.uint8,
+                         device="cuda")
+
+        def api_call(Xin, Yout):  # QKV GEMM, attention core, O GEMM + sum: three launches
+            tpl.tp_attn_block(Xin, Sqkv, So, attention="causal", qkv_out=qkv, workspace=ws, out=Yout)
+
+        def part_a():  # the attention core alone, on the step's qkv
+            tpl.tp_attention(qkv, hq, hkv, hd, causal=True, out=ctx)
+        st.update(parts=[lambda: api_call(X, Y)], X=X, Y=Y, api=api_call, launches_per_step=3,
+                  keep=[Sqkv, So, qkv, ctx, ws], dominant_part=part_a)
     elif name.startswith("gqa"):
         H, hq, hkv, hd = spec["H"], spec["hq"], spec["hkv"], spec["hd"]
         d = S.gqa_proj(T, H, hq, hkv, hd)
@@ -611,7 +648,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mlp", choices=["mlp", "gqa", "decode", "stack"])
+    ap.add_argument("--workload", default="mlp", choices=["mlp", "gqa", "gqa_attn", "decode", "stack"])
     ap.add_argument("--tp", type=int, default=None)
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -14,9 +14,13 @@
 //               MN-major operand straight from its TMA tile;
 //   warps 2..5  softmax, one query row per thread: scores from TMEM, online
 //               maximum and sum in fp32 (exp2 with the log2(e)/sqrt(hd)
-//               scale folded in), O rescaled in TMEM when the maximum grows,
-//               P written as bf16 into a 128-byte-swizzled shared-memory tile
-//               (the next MMA's A operand); at the end O / l is stored.
+//               scale folded into one FFMA), P written as bf16 into one of
+//               two 128-byte-swizzled shared-memory tiles (the next MMA's A
+//               operand); at the end O / l is stored.
+// The exponent base m only moves when a row's maximum exceeds it by more
+// than 2^8 (P then stays below 256, exact enough in bf16), so O and l are
+// rescaled in TMEM only on such jumps and the softmax of block j+1 normally
+// runs without waiting for P V of block j.
 // Every wait is bounded as in the GEMM kernel.
 #pragma once
 
@@ -24,6 +28,13 @@
 #include "tp_ptx.cuh"
 
 namespace tpk {
+
+// 2^x with the MUFU approximation (flushes subnormals; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 struct AttnArgs {
   __nv_bfloat16* ctx;  // [tp][T][nq * hd]
@@ -38,7 +49,8 @@ constexpr int AT_HD = 128;                     // head size
 constexpr int AT_PANEL = AT_ROWS * 128;        // 128 rows x 128 bytes (64 bf16 columns)
 constexpr int AT_TILE = 2 * AT_PANEL;          // 128 x 128 bf16 as two 64-column panels
 constexpr int AT_THREADS = 192;
-constexpr int AT_SMEM = 6 * AT_TILE + 1024 + 512;  // Q, K x2, V x2, P; alignment; barriers
+constexpr int AT_SMEM = 7 * AT_TILE + 1024 + 512;  // Q, K x2, V x2, P x2; alignment; barriers
+constexpr float AT_RESCALE_LOG2 = 8.0f;            // move the exponent base only on a jump above 2^8
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
     tp_attn_kernel(const __grid_constant__ CUtensorMap mapQKV, const AttnArgs a) {
@@ -48,18 +60,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = smem + AT_TILE;      // [2]
   uint8_t* sV = smem + 3 * AT_TILE;  // [2]
-  uint8_t* sP = smem + 5 * AT_TILE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * AT_TILE);
+  uint8_t* sP = smem + 5 * AT_TILE;  // [2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 7 * AT_TILE);
   uint64_t* q_full = bars;           // TMA -> MMA
   uint64_t* k_full = bars + 1;       // [2]
   uint64_t* v_full = bars + 3;       // [2]
   uint64_t* kv_empty = bars + 5;     // [2] MMA -> TMA
   uint64_t* s_full = bars + 7;       // [2] MMA -> softmax
   uint64_t* s_empty = bars + 9;      // [2] softmax -> MMA
-  uint64_t* p_full = bars + 11;      // softmax -> MMA (P written, O rescaled)
-  uint64_t* o_done = bars + 12;      // MMA -> softmax (P V of a block complete)
-  uint64_t* drain = bars + 13;       // abort path only
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* p_full = bars + 11;      // [2] softmax -> MMA (P written, O rescaled)
+  uint64_t* o_done = bars + 13;      // [2] MMA -> softmax (P V of a block complete)
+  uint64_t* drain = bars + 15;       // abort path only
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -85,8 +97,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 4);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_done[i], 1);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -168,12 +182,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // P is K-major (two 64-key panels), V MN-major (rows = keys, each row
       // 64 hd values; the second 64 hd values one panel further)
       auto issue_pv = [&](int jb) -> bool {
-        const int st = jb & 1;
+        const int st = jb & 1;  // K/V stage and P buffer
         const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
-        if (!mbar_wait(p_full, static_cast<uint32_t>(jb) & 1u, abort_flag)) return false;
+        if (!mbar_wait(&p_full[st], ph, abort_flag)) return false;
         if (!mbar_wait(&v_full[st], ph, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t p_a = smem_u32(sP), v_a = smem_u32(sV + st * AT_TILE);
+        const uint32_t p_a = smem_u32(sP + st * AT_TILE), v_a = smem_u32(sV + st * AT_TILE);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t poff = static_cast<uint32_t>((k >> 2) * AT_PANEL + (k & 3) * 32);
@@ -181,7 +195,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                       smem_desc_mn_sw128(v_a + static_cast<uint32_t>(k * 16 * 128), AT_PANEL, 1024), idesc_o,
                       (jb > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit(o_done);
+        tc_commit(&o_done[st]);
         tc_commit(&kv_empty[st]);
         return true;
       };
@@ -205,7 +219,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int t = q0 + r;              // query index
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t tO = tmem_base + 256 + lane_off;
-    float m = -INFINITY, l = 0.0f;
+    const int kmax = a.causal ? min(t, a.T - 1) : a.T - 1;  // last key this query sees
+    float m = -INFINITY;  // exponent base, in log2 units of the scaled scores
+    float l = 0.0f;
     bool ok = true;
     for (int jb = 0; jb < nkb; ++jb) {
       const int st = jb & 1;
@@ -222,41 +238,59 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       for (int c = 0; c < 128; c += 32) {
         uint32_t rr[32];
         tmem_ld32(tS + static_cast<uint32_t>(c), rr);
-        tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[c + i] = __uint_as_float(rr[i]);
       }
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_empty[st]);  // S(jb + 2) may overwrite this buffer
       const int kbase = jb * AT_ROWS;
-      const int kmax = a.causal ? min(t, a.T - 1) : a.T - 1;  // last key this query sees
-      float mx = -INFINITY;
+      // only the diagonal block (causal) and a ragged last block need a mask
+      if ((a.causal && jb == qb) || kbase + AT_ROWS > a.T) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (kbase + i > kmax) sv[i] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_cand = mx * a.scale_log2;  // the scale is positive: same order
+      bool rescale = false;
+      float alpha = 1.0f;
+      if (m_cand > m + AT_RESCALE_LOG2) {  // also the first visible block (m = -inf)
+        alpha = ex2_approx(m - m_cand);    // 0 on the first block
+        rescale = jb > 0;
+        m = m_cand;
+        l *= alpha;
+      }
+      float sum8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
-        sv[i] = (kbase + i <= kmax) ? sv[i] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[i]);
+        sv[i] = ex2_approx(fmaf(sv[i], a.scale_log2, -m));
+        sum8[i & 7] += sv[i];
       }
-      const float m_new = fmaxf(m, mx);
-      const float m_use = m_new == -INFINITY ? 0.0f : m_new;  // rows past T see no key
-      const float alpha = exp2f(m - m_use);
-      float sum = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        sv[i] = exp2f(sv[i] - m_use);
-        sum += sv[i];
-      }
-      l = l * alpha + sum;
-      m = m_new;
-      if (jb > 0) {
-        // P V of the previous block has finished: O is stable and P is free
-        const bool done = mbar_wait(o_done, static_cast<uint32_t>(jb - 1) & 1u, abort_flag);
-        if (epi_any(!done || *abort_flag)) {
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      // the P buffer of this block was last read by P V of block jb - 2
+      if (jb >= 2) {
+        const bool freed = mbar_wait(&o_done[st], ph ^ 1u, abort_flag);
+        if (epi_any(!freed || *abort_flag)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // the base moved: O (all P V up to block jb - 1) is rescaled first
+        const bool done = mbar_wait(&o_done[st ^ 1], static_cast<uint32_t>((jb - 1) >> 1) & 1u, abort_flag);
+        if (!done) *abort_flag = 1;
+        if (done) {
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < 128; c += 32) {
             uint32_t rr[32];
@@ -271,6 +305,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       }
       // P row in bf16: keys 0..63 in panel 0, 64..127 in panel 1, 16-byte
       // chunks at the 128-byte swizzle position of this row
+      uint8_t* pb = sP + st * AT_TILE;
 #pragma unroll
       for (int c8 = 0; c8 < 16; ++c8) {
         const int panel = c8 >> 3, ch = c8 & 7;
@@ -279,15 +314,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         v.y = pack_bf16x2(sv[c8 * 8 + 2], sv[c8 * 8 + 3]);
         v.z = pack_bf16x2(sv[c8 * 8 + 4], sv[c8 * 8 + 5]);
         v.w = pack_bf16x2(sv[c8 * 8 + 6], sv[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(sP + panel * AT_PANEL + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
+        *reinterpret_cast<uint4*>(pb + panel * AT_PANEL + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
       }
       fence_proxy_async_smem();  // the tensor core reads P through the async proxy
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[st]);
     }
-    if (ok) {
-      const bool done = mbar_wait(o_done, static_cast<uint32_t>(nkb - 1) & 1u, abort_flag);
+    if (ok && !*abort_flag) {
+      const int last = nkb - 1;
+      const bool done = mbar_wait(&o_done[last & 1], static_cast<uint32_t>(last >> 1) & 1u, abort_flag);
       if (!epi_any(!done || *abort_flag)) {
         tc_fence_after();
         const float inv = 1.0f / l;
