@@ -6,21 +6,23 @@
 //
 // One CTA per (shard, q head, block of 128 queries), head size 128, 192
 // threads:
-//   warp 0      TMA producer: the Q tile once, then K and V tiles of each
-//               block of 128 keys, double-buffered;
+//   warp 0      TMA producer: the Q tile once, then the K and V tiles of
+//               each block of 128 keys through a ring of five 32 KB slots (a
+//               K slot is released as soon as Q K^T has read it, a V slot
+//               after P V), 2.5 key blocks of lookahead;
 //   warp 1      TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
 //               score buffers (one key block ahead of the softmax), then
 //               O += P V into the TMEM output accumulator, with V read as an
 //               MN-major operand straight from its TMA tile;
 //   warps 2..5  softmax, one query row per thread: scores from TMEM, online
 //               maximum and sum in fp32 (exp2 with the log2(e)/sqrt(hd)
-//               scale folded into one FFMA), P written as bf16 into one of
-//               two 128-byte-swizzled shared-memory tiles (the next MMA's A
-//               operand); at the end O / l is stored.
+//               scale folded into one FFMA), P written as bf16 into a
+//               128-byte-swizzled shared-memory tile (the next MMA's A
+//               operand) once P V of the previous block has read it; at the
+//               end O / l is stored.
 // The exponent base m only moves when a row's maximum exceeds it by more
 // than 2^8 (P then stays below 256, exact enough in bf16), so O and l are
-// rescaled in TMEM only on such jumps and the softmax of block j+1 normally
-// runs without waiting for P V of block j.
+// rescaled in TMEM only on such jumps.
 // Every wait is bounded as in the GEMM kernel.
 #pragma once
 
@@ -49,7 +51,8 @@ constexpr int AT_HD = 128;                     // head size
 constexpr int AT_PANEL = AT_ROWS * 128;        // 128 rows x 128 bytes (64 bf16 columns)
 constexpr int AT_TILE = 2 * AT_PANEL;          // 128 x 128 bf16 as two 64-column panels
 constexpr int AT_THREADS = 192;
-constexpr int AT_SMEM = 7 * AT_TILE + 1024 + 512;  // Q, K x2, V x2, P x2; alignment; barriers
+constexpr int AT_SLOTS = 5;                        // K/V ring slots
+constexpr int AT_SMEM = (2 + AT_SLOTS) * AT_TILE + 1024 + 512;  // Q, P, ring; alignment; barriers
 constexpr float AT_RESCALE_LOG2 = 8.0f;            // move the exponent base only on a jump above 2^8
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
@@ -58,20 +61,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = smem + AT_TILE;      // [2]
-  uint8_t* sV = smem + 3 * AT_TILE;  // [2]
-  uint8_t* sP = smem + 5 * AT_TILE;  // [2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 7 * AT_TILE);
-  uint64_t* q_full = bars;           // TMA -> MMA
-  uint64_t* k_full = bars + 1;       // [2]
-  uint64_t* v_full = bars + 3;       // [2]
-  uint64_t* kv_empty = bars + 5;     // [2] MMA -> TMA
-  uint64_t* s_full = bars + 7;       // [2] MMA -> softmax
-  uint64_t* s_empty = bars + 9;      // [2] softmax -> MMA
-  uint64_t* p_full = bars + 11;      // [2] softmax -> MMA (P written, O rescaled)
-  uint64_t* o_done = bars + 13;      // [2] MMA -> softmax (P V of a block complete)
-  uint64_t* drain = bars + 15;       // abort path only
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint8_t* sP = smem + AT_TILE;
+  uint8_t* ring = smem + 2 * AT_TILE;  // [AT_SLOTS]: K(j) is item 2j, V(j) item 2j+1
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + AT_SLOTS) * AT_TILE);
+  uint64_t* q_full = bars;              // TMA -> MMA
+  uint64_t* r_full = bars + 1;          // [AT_SLOTS] TMA -> MMA
+  uint64_t* r_empty = r_full + AT_SLOTS;  // [AT_SLOTS] MMA -> TMA
+  uint64_t* s_full = r_empty + AT_SLOTS;  // [2] MMA -> softmax
+  uint64_t* s_empty = s_full + 2;       // [2] softmax -> MMA
+  uint64_t* p_full = s_empty + 2;       // softmax -> MMA (P written, O rescaled)
+  uint64_t* o_done = p_full + 1;        // MMA -> softmax (P V of a block complete)
+  uint64_t* drain = o_done + 1;         // abort path only
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -90,17 +91,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    for (int i = 0; i < AT_SLOTS; ++i) {
+      mbar_init(&r_full[i], 1);
+      mbar_init(&r_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&k_full[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 4);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&p_full[i], 4);
-      mbar_init(&o_done[i], 1);
-    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -120,36 +120,31 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------ TMA producer ------------------------------
-      int issued_k[2] = {-1, -1}, issued_v[2] = {-1, -1};
+      int issued[AT_SLOTS];
+#pragma unroll
+      for (int i = 0; i < AT_SLOTS; ++i) issued[i] = -1;
       bool ok = true;
       mbar_arrive_expect_tx(q_full, AT_TILE);
       tma_load_3d(sQ, &mapQKV, q_full, qcol, q0, s);
       tma_load_3d(sQ + AT_PANEL, &mapQKV, q_full, qcol + 64, q0, s);
-      for (int jb = 0; jb < nkb; ++jb) {
-        const int st = jb & 1;
-        const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
-        if (!mbar_wait(&kv_empty[st], ph ^ 1u, abort_flag)) {
+      for (int it = 0; it < 2 * nkb; ++it) {  // K(j), V(j), K(j+1), ...
+        const int slot = it % AT_SLOTS;
+        const uint32_t ph = static_cast<uint32_t>(it / AT_SLOTS) & 1u;
+        if (!mbar_wait(&r_empty[slot], ph ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        const int k0 = jb * AT_ROWS;
-        uint8_t* k_t = sK + st * AT_TILE;
-        uint8_t* v_t = sV + st * AT_TILE;
-        mbar_arrive_expect_tx(&k_full[st], AT_TILE);
-        tma_load_3d(k_t, &mapQKV, &k_full[st], kcol, k0, s);
-        tma_load_3d(k_t + AT_PANEL, &mapQKV, &k_full[st], kcol + 64, k0, s);
-        issued_k[st] = static_cast<int>(ph);
-        mbar_arrive_expect_tx(&v_full[st], AT_TILE);
-        tma_load_3d(v_t, &mapQKV, &v_full[st], vcol, k0, s);
-        tma_load_3d(v_t + AT_PANEL, &mapQKV, &v_full[st], vcol + 64, k0, s);
-        issued_v[st] = static_cast<int>(ph);
+        const int col = (it & 1) ? vcol : kcol;
+        uint8_t* dst = ring + slot * AT_TILE;
+        mbar_arrive_expect_tx(&r_full[slot], AT_TILE);
+        tma_load_3d(dst, &mapQKV, &r_full[slot], col, (it >> 1) * AT_ROWS, s);
+        tma_load_3d(dst + AT_PANEL, &mapQKV, &r_full[slot], col + 64, (it >> 1) * AT_ROWS, s);
+        issued[slot] = static_cast<int>(ph);
       }
       if (!ok) {  // let every copy this block started land before it exits
         mbar_wait_drain(q_full, 0);
-        for (int i = 0; i < 2; ++i) {
-          if (issued_k[i] >= 0) mbar_wait_drain(&k_full[i], static_cast<uint32_t>(issued_k[i]));
-          if (issued_v[i] >= 0) mbar_wait_drain(&v_full[i], static_cast<uint32_t>(issued_v[i]));
-        }
+        for (int i = 0; i < AT_SLOTS; ++i)
+          if (issued[i] >= 0) mbar_wait_drain(&r_full[i], static_cast<uint32_t>(issued[i]));
       }
     }
   } else if (warp == 1) {
@@ -164,10 +159,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       auto issue_s = [&](int jb) -> bool {
         const int st = jb & 1;
         const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
-        if (!mbar_wait(&k_full[st], ph, abort_flag)) return false;
+        const int slot = (2 * jb) % AT_SLOTS;
+        if (!mbar_wait(&r_full[slot], static_cast<uint32_t>(2 * jb / AT_SLOTS) & 1u, abort_flag)) return false;
         if (!mbar_wait(&s_empty[st], ph ^ 1u, abort_flag)) return false;
         tc_fence_after();
-        const uint32_t q_a = smem_u32(sQ), k_a = smem_u32(sK + st * AT_TILE);
+        const uint32_t q_a = smem_u32(sQ), k_a = smem_u32(ring + slot * AT_TILE);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = static_cast<uint32_t>((k >> 2) * AT_PANEL + (k & 3) * 32);
@@ -175,6 +171,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                       smem_desc_k_sw128(k_a + off), idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[st]);
+        tc_commit(&r_empty[slot]);  // K(jb) read
         issued_any = true;
         return true;
       };
@@ -182,12 +179,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // P is K-major (two 64-key panels), V MN-major (rows = keys, each row
       // 64 hd values; the second 64 hd values one panel further)
       auto issue_pv = [&](int jb) -> bool {
-        const int st = jb & 1;  // K/V stage and P buffer
-        const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
-        if (!mbar_wait(&p_full[st], ph, abort_flag)) return false;
-        if (!mbar_wait(&v_full[st], ph, abort_flag)) return false;
+        const int slot = (2 * jb + 1) % AT_SLOTS;
+        if (!mbar_wait(p_full, static_cast<uint32_t>(jb) & 1u, abort_flag)) return false;
+        if (!mbar_wait(&r_full[slot], static_cast<uint32_t>((2 * jb + 1) / AT_SLOTS) & 1u, abort_flag))
+          return false;
         tc_fence_after();
-        const uint32_t p_a = smem_u32(sP + st * AT_TILE), v_a = smem_u32(sV + st * AT_TILE);
+        const uint32_t p_a = smem_u32(sP), v_a = smem_u32(ring + slot * AT_TILE);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t poff = static_cast<uint32_t>((k >> 2) * AT_PANEL + (k & 3) * 32);
@@ -195,8 +192,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                       smem_desc_mn_sw128(v_a + static_cast<uint32_t>(k * 16 * 128), AT_PANEL, 1024), idesc_o,
                       (jb > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit(&o_done[st]);
-        tc_commit(&kv_empty[st]);
+        tc_commit(o_done);
+        tc_commit(&r_empty[slot]);  // V(jb) read
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -277,20 +274,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         sum8[i & 7] += sv[i];
       }
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      // the P buffer of this block was last read by P V of block jb - 2
-      if (jb >= 2) {
-        const bool freed = mbar_wait(&o_done[st], ph ^ 1u, abort_flag);
+      // P V of the previous block has read P and finished with O
+      if (jb >= 1) {
+        const bool freed = mbar_wait(o_done, static_cast<uint32_t>(jb - 1) & 1u, abort_flag);
         if (epi_any(!freed || *abort_flag)) {
           ok = false;
           break;
         }
+        tc_fence_after();
       }
       if (__any_sync(0xffffffffu, rescale)) {
         // the base moved: O (all P V up to block jb - 1) is rescaled first
-        const bool done = mbar_wait(&o_done[st ^ 1], static_cast<uint32_t>((jb - 1) >> 1) & 1u, abort_flag);
-        if (!done) *abort_flag = 1;
-        if (done) {
-          tc_fence_after();
+        {
 #pragma unroll 1
           for (int c = 0; c < 128; c += 32) {
             uint32_t rr[32];
@@ -305,7 +300,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       }
       // P row in bf16: keys 0..63 in panel 0, 64..127 in panel 1, 16-byte
       // chunks at the 128-byte swizzle position of this row
-      uint8_t* pb = sP + st * AT_TILE;
+      uint8_t* pb = sP;
 #pragma unroll
       for (int c8 = 0; c8 < 16; ++c8) {
         const int panel = c8 >> 3, ch = c8 & 7;
@@ -319,11 +314,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       fence_proxy_async_smem();  // the tensor core reads P through the async proxy
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[st]);
+      if (lane == 0) mbar_arrive(p_full);
     }
     if (ok && !*abort_flag) {
-      const int last = nkb - 1;
-      const bool done = mbar_wait(&o_done[last & 1], static_cast<uint32_t>(last >> 1) & 1u, abort_flag);
+      const bool done = mbar_wait(o_done, static_cast<uint32_t>(nkb - 1) & 1u, abort_flag);
       if (!epi_any(!done || *abort_flag)) {
         tc_fence_after();
         const float inv = 1.0f / l;
