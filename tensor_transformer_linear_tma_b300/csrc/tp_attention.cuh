@@ -4,25 +4,37 @@
 // attention heads; tutorial page, self-attention block sharding), causal
 // (query t sees keys 0..t) or unmasked.
 //
-// One CTA per (shard, q head, block of 128 queries), head size 128, 192
+// One CTA per (shard, q head, block of 128 queries), head size 128, 320
 // threads:
 //   warp 0      TMA producer: the Q tile once, then the K and V tiles of
-//               each block of 128 keys through a ring of five 32 KB slots (a
+//               each block of 128 keys through a ring of six 32 KB slots (a
 //               K slot is released as soon as Q K^T has read it, a V slot
-//               after P V), 2.5 key blocks of lookahead;
-//   warp 1      TMEM owner and MMA issuer: S = Q K^T into one of two TMEM
-//               score buffers (one key block ahead of the softmax), then
-//               O += P V into the TMEM output accumulator, with V read as an
-//               MN-major operand straight from its TMA tile;
-//   warps 2..5  softmax, one query row per thread: scores from TMEM, online
-//               maximum and sum in fp32 (exp2 with the log2(e)/sqrt(hd)
-//               scale folded into one FFMA), P written as bf16 into a
-//               128-byte-swizzled shared-memory tile (the next MMA's A
-//               operand) once P V of the previous block has read it; at the
-//               end O / l is stored.
+//               after P V), three key blocks of lookahead;
+//   warp 1      TMEM owner and MMA issuer (one elected lane issues):
+//               S = Q K^T into one of two TMEM score buffers (one key
+//               block ahead of the softmax), then
+//               O += P V into the TMEM output accumulator. Q and P are the
+//               A operands and sit in TMEM; only K and V are read from
+//               shared memory (V as an MN-major operand straight from its
+//               TMA tile), which halves the tensor core's shared-memory
+//               traffic against staging Q and P there;
+//   warps 2..9  softmax, two threads per query row (warps w and w+4 share
+//               a TMEM lane quadrant; each takes 64 of the block's 128
+//               keys and the matching 64 output columns). They first copy
+//               Q from its TMA tile into TMEM. Per key block: scores from
+//               TMEM, online maximum (exchanged between the two halves of a
+//               row through shared memory) and sum in fp32, exp2 with the
+//               log2(e)/sqrt(hd) scale folded into one FFMA, P packed to
+//               bf16 and stored over the first half of its own scores; at
+//               the end O / l.
 // The exponent base m only moves when a row's maximum exceeds it by more
 // than 2^8 (P then stays below 256, exact enough in bf16), so O and l are
 // rescaled in TMEM only on such jumps.
+// The tensor core runs tcgen05 operations in issue order, so S(j + 2) may be
+// issued into the buffer that holds P(j) as soon as P(j) V has been issued.
+// P V of block j commits to the barrier of buffer j & 1: a softmax thread
+// waits on it only to rescale O or to read the result, and since S(j) was
+// issued after P(j - 2) V, each wait's barrier is at most one phase behind.
 // Every wait is bounded as in the GEMM kernel.
 #pragma once
 
@@ -38,6 +50,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Barrier over the two softmax warps of TMEM lane quadrant q (named barriers
+// 2..5) that ORs a predicate, so that both take the same branch.
+__device__ __forceinline__ bool pair_any(int q, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %2, 0;\n\t"
+      "bar.red.or.pred po, %1, 64, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}\n"
+      : "=r"(r)
+      : "r"(2 + q), "r"(static_cast<uint32_t>(v))
+      : "memory");
+  return r != 0;
+}
+
 struct AttnArgs {
   __nv_bfloat16* ctx;  // [tp][T][nq * hd]
   int T, tp, hq, hkv, nq, nkv, group;
@@ -50,10 +77,14 @@ constexpr int AT_ROWS = 128;                   // queries per CTA, keys per bloc
 constexpr int AT_HD = 128;                     // head size
 constexpr int AT_PANEL = AT_ROWS * 128;        // 128 rows x 128 bytes (64 bf16 columns)
 constexpr int AT_TILE = 2 * AT_PANEL;          // 128 x 128 bf16 as two 64-column panels
-constexpr int AT_THREADS = 192;
-constexpr int AT_SLOTS = 5;                        // K/V ring slots
-constexpr int AT_SMEM = (2 + AT_SLOTS) * AT_TILE + 1024 + 512;  // Q, P, ring; alignment; barriers
+constexpr int AT_THREADS = 320;
+constexpr int AT_SOFTMAX_THREADS = 256;
+constexpr int AT_SLOTS = 6;                        // K/V ring slots
+constexpr int AT_SMEM = (1 + AT_SLOTS) * AT_TILE + 1024 + 2048;  // Q, ring; alignment; barriers, row exchange
+constexpr int AT_AUX = 512 + 2048;  // barriers, then the row exchange [2 blocks][2 halves][128] floats
 constexpr float AT_RESCALE_LOG2 = 8.0f;            // move the exponent base only on a jump above 2^8
+// TMEM columns (512 allocated): two score buffers, O, Q as packed bf16
+constexpr uint32_t AT_TM_S = 0, AT_TM_O = 256, AT_TM_Q = 384;
 
 __global__ void __launch_bounds__(AT_THREADS, 1)
     tp_attn_kernel(const __grid_constant__ CUtensorMap mapQKV, const AttnArgs a) {
@@ -61,22 +92,29 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sP = smem + AT_TILE;
-  uint8_t* ring = smem + 2 * AT_TILE;  // [AT_SLOTS]: K(j) is item 2j, V(j) item 2j+1
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + AT_SLOTS) * AT_TILE);
-  uint64_t* q_full = bars;              // TMA -> MMA
-  uint64_t* r_full = bars + 1;          // [AT_SLOTS] TMA -> MMA
+  uint8_t* ring = smem + AT_TILE;  // [AT_SLOTS]: K(j) is item 2j, V(j) item 2j+1
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (1 + AT_SLOTS) * AT_TILE);
+  uint64_t* q_full = bars;                // TMA -> softmax (Q tile landed)
+  uint64_t* q_tm = bars + 1;              // softmax -> MMA (Q copied into TMEM)
+  uint64_t* r_full = bars + 2;            // [AT_SLOTS] TMA -> MMA
   uint64_t* r_empty = r_full + AT_SLOTS;  // [AT_SLOTS] MMA -> TMA
   uint64_t* s_full = r_empty + AT_SLOTS;  // [2] MMA -> softmax
-  uint64_t* s_empty = s_full + 2;       // [2] softmax -> MMA
-  uint64_t* p_full = s_empty + 2;       // softmax -> MMA (P written, O rescaled)
-  uint64_t* o_done = p_full + 1;        // MMA -> softmax (P V of a block complete)
-  uint64_t* drain = o_done + 1;         // abort path only
+  uint64_t* p_full = s_full + 2;          // [2] softmax -> MMA (P stored, O rescaled)
+  uint64_t* o_done = p_full + 2;          // [2] MMA -> softmax (P V of block j complete, buffer j & 1)
+  uint64_t* drain = o_done + 2;           // abort path only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  float* xrow = reinterpret_cast<float*>(smem + (1 + AT_SLOTS) * AT_TILE + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // the 1024-byte alignment of the tiles must leave room for the barriers
+  // and the row exchange (a dynamic shared-memory base is 1024-aligned in
+  // practice; otherwise the block reports an error instead of overrunning)
+  if ((smem - smem_raw) + (1 + AT_SLOTS) * AT_TILE + AT_AUX > AT_SMEM) {
+    if (threadIdx.x == 0) atomicCAS(&g_tp_error, TP_DEVERR_NONE, TP_DEVERR_LAYOUT);
+    return;
+  }
 
   // work unit; the longest (latest, under the causal mask) query blocks first
   const int heads = a.tp * a.nq;
@@ -91,16 +129,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_tm, 8);
     for (int i = 0; i < AT_SLOTS; ++i) {
       mbar_init(&r_full[i], 1);
       mbar_init(&r_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 8);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -120,9 +158,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------ TMA producer ------------------------------
-      int issued[AT_SLOTS];
-#pragma unroll
-      for (int i = 0; i < AT_SLOTS; ++i) issued[i] = -1;
+      uint32_t issued = 0, issued_ph = 0;  // per slot: a copy was started, its phase
       bool ok = true;
       mbar_arrive_expect_tx(q_full, AT_TILE);
       tma_load_3d(sQ, &mapQKV, q_full, qcol, q0, s);
@@ -139,123 +175,167 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_arrive_expect_tx(&r_full[slot], AT_TILE);
         tma_load_3d(dst, &mapQKV, &r_full[slot], col, (it >> 1) * AT_ROWS, s);
         tma_load_3d(dst + AT_PANEL, &mapQKV, &r_full[slot], col + 64, (it >> 1) * AT_ROWS, s);
-        issued[slot] = static_cast<int>(ph);
+        issued |= 1u << slot;
+        issued_ph = (issued_ph & ~(1u << slot)) | (ph << slot);
       }
       if (!ok) {  // let every copy this block started land before it exits
         mbar_wait_drain(q_full, 0);
         for (int i = 0; i < AT_SLOTS; ++i)
-          if (issued[i] >= 0) mbar_wait_drain(&r_full[i], static_cast<uint32_t>(issued[i]));
+          if ((issued >> i) & 1u) mbar_wait_drain(&r_full[i], (issued_ph >> i) & 1u);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------ MMA issuer ------------------------------
-      const uint32_t idesc_s = idesc_bf16_f32(128, 128);
-      const uint32_t idesc_o = idesc_bf16_f32_bmn(128, 128);
-      const uint32_t tO = tmem_base + 256;
-      bool ok = mbar_wait(q_full, 0, abort_flag), issued_any = false;
-      // S(jb) = Q K(jb)^T: M = 128 queries, N = 128 keys, K = hd in 8 steps
-      // of 16 (two 64-wide panels, +32 bytes per step inside a panel)
-      auto issue_s = [&](int jb) -> bool {
-        const int st = jb & 1;
-        const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
-        const int slot = (2 * jb) % AT_SLOTS;
-        if (!mbar_wait(&r_full[slot], static_cast<uint32_t>(2 * jb / AT_SLOTS) & 1u, abort_flag)) return false;
-        if (!mbar_wait(&s_empty[st], ph ^ 1u, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t q_a = smem_u32(sQ), k_a = smem_u32(ring + slot * AT_TILE);
+    // ------------------------------ MMA issuer ------------------------------
+    // The whole warp runs the loop (waits and descriptors are warp-uniform);
+    // one elected lane issues each MMA and commit.
+    const uint32_t idesc_s = idesc_bf16_f32(128, 128);
+    const uint32_t idesc_o = idesc_bf16_f32_bmn(128, 128);
+    const uint32_t tO = tmem_base + AT_TM_O, tQ = tmem_base + AT_TM_Q;
+    const uint64_t ring_k = smem_desc_k_sw128(smem_u32(ring));
+    const uint64_t ring_mn = smem_desc_mn_sw128(smem_u32(ring), AT_PANEL, 1024);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+    };
+    bool ok = wait_all(q_tm, 0), issued_any = false;
+    if (ok) tc_fence_after();
+    // S(jb) = Q K(jb)^T: M = 128 queries, N = 128 keys, K = hd in 8 steps
+    // of 16 (Q: 8 TMEM columns a step; K: two 64-wide panels, +32 bytes a
+    // step inside a panel; descriptor start addresses count 16-byte units).
+    // The caller has waited for K(jb).
+    auto issue_s = [&](int jb) {
+      const int st = jb & 1;
+      const int slot = (2 * jb) % AT_SLOTS;
+      const uint64_t kd = ring_k + static_cast<uint64_t>((slot * AT_TILE) >> 4);
+      const uint32_t tS = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = static_cast<uint32_t>((k >> 2) * AT_PANEL + (k & 3) * 32);
-          tc_mma_bf16(tmem_base + static_cast<uint32_t>(st * 128), smem_desc_k_sw128(q_a + off),
-                      smem_desc_k_sw128(k_a + off), idesc_s, k > 0 ? 1u : 0u);
-        }
-        tc_commit(&s_full[st]);
-        tc_commit(&r_empty[slot]);  // K(jb) read
-        issued_any = true;
-        return true;
-      };
-      // O += P(jb) V(jb): M = 128 queries, N = hd, K = 128 keys in 8 steps;
-      // P is K-major (two 64-key panels), V MN-major (rows = keys, each row
-      // 64 hd values; the second 64 hd values one panel further)
-      auto issue_pv = [&](int jb) -> bool {
-        const int slot = (2 * jb + 1) % AT_SLOTS;
-        if (!mbar_wait(p_full, static_cast<uint32_t>(jb) & 1u, abort_flag)) return false;
-        if (!mbar_wait(&r_full[slot], static_cast<uint32_t>((2 * jb + 1) / AT_SLOTS) & 1u, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t p_a = smem_u32(sP), v_a = smem_u32(ring + slot * AT_TILE);
+      for (int k = 0; k < 8; ++k)
+        tc_mma_bf16_ts_warp(tS, tQ + static_cast<uint32_t>(k * 8),
+                            kd + static_cast<uint64_t>(((k >> 2) * AT_PANEL + (k & 3) * 32) >> 4), idesc_s,
+                            k > 0 ? 1u : 0u);
+      tc_commit_warp(&s_full[st]);
+      tc_commit_warp(&r_empty[slot]);  // K(jb) read
+      issued_any = true;
+    };
+    // O += P(jb) V(jb): M = 128 queries, N = hd, K = 128 keys in 8 steps;
+    // P sits in TMEM (keys 0..63 at score columns 0..31 of its buffer,
+    // keys 64..127 at 64..95), V is MN-major (rows = keys, each row 64 hd
+    // values; the second 64 hd values one panel further). The caller has
+    // waited for V(jb) and P(jb).
+    auto issue_pv = [&](int jb) {
+      const int st = jb & 1;
+      const int slot = (2 * jb + 1) % AT_SLOTS;
+      const uint32_t tP = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128);
+      const uint64_t vd = ring_mn + static_cast<uint64_t>((slot * AT_TILE) >> 4);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t poff = static_cast<uint32_t>((k >> 2) * AT_PANEL + (k & 3) * 32);
-          tc_mma_bf16(tO, smem_desc_k_sw128(p_a + poff),
-                      smem_desc_mn_sw128(v_a + static_cast<uint32_t>(k * 16 * 128), AT_PANEL, 1024), idesc_o,
-                      (jb > 0 || k > 0) ? 1u : 0u);
-        }
-        tc_commit(o_done);
-        tc_commit(&r_empty[slot]);  // V(jb) read
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int jb = 0; ok && jb < nkb; ++jb) {
-        if (jb + 1 < nkb && !issue_s(jb + 1)) {
-          ok = false;
-          break;
-        }
-        ok = issue_pv(jb);
+      for (int k = 0; k < 8; ++k)
+        tc_mma_bf16_ts_warp(tO, tP + static_cast<uint32_t>((k >> 2) * 64 + (k & 3) * 8),
+                            vd + static_cast<uint64_t>((k * 16 * 128) >> 4), idesc_o, (jb > 0 || k > 0) ? 1u : 0u);
+      tc_commit_warp(&o_done[st]);
+      tc_commit_warp(&r_empty[slot]);  // V(jb) read
+    };
+    auto wait_item = [&](int it) {  // ring item it (K(j) = 2j, V(j) = 2j + 1) landed
+      return wait_all(&r_full[it % AT_SLOTS], static_cast<uint32_t>(it / AT_SLOTS) & 1u);
+    };
+    // S(0) and S(1) fill both score buffers; then, per block, P(jb) V and
+    // S(jb + 2) are issued back to back as soon as the softmax hands over
+    // P(jb): S(jb + 2) reuses P(jb)'s buffer, and the tensor core runs them in
+    // issue order. The ring waits come before the wait for P, off the path
+    // from the softmax to the tensor core.
+    for (int jb = 0; ok && jb < 2 && jb < nkb; ++jb) {
+      ok = wait_item(2 * jb);
+      if (ok) {
+        tc_fence_after();
+        issue_s(jb);
       }
-      if (!ok && issued_any) {  // wait for MMAs in flight before TMEM is freed
-        tc_commit(drain);
-        mbar_wait_drain(drain, 0);
-      }
+    }
+    for (int jb = 0; ok && jb < nkb; ++jb) {
+      const bool next = jb + 2 < nkb;
+      ok = wait_item(2 * jb + 1) && (!next || wait_item(2 * jb + 4)) &&
+           wait_all(&p_full[jb & 1], static_cast<uint32_t>(jb >> 1) & 1u);
+      if (!ok) break;
+      tc_fence_after();
+      issue_pv(jb);
+      if (next) issue_s(jb + 2);
+    }
+    if (!ok && issued_any) {  // wait for MMAs in flight before TMEM is freed
+      tc_commit_warp(drain);
+      mbar_wait_drain(drain, 0);
     }
   } else {
     // ------------------------------ softmax ------------------------------
     const int q = warp & 3;            // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;  // which 64 keys / output columns of the row
     const int r = q * 32 + lane;       // query row within the block
     const int t = q0 + r;              // query index
+    const int c0 = half * 64;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t tO = tmem_base + 256 + lane_off;
+    const uint32_t tO = tmem_base + AT_TM_O + lane_off + static_cast<uint32_t>(c0);
     const int kmax = a.causal ? min(t, a.T - 1) : a.T - 1;  // last key this query sees
     float m = -INFINITY;  // exponent base, in log2 units of the scaled scores
-    float l = 0.0f;
-    bool ok = true;
-    for (int jb = 0; jb < nkb; ++jb) {
+    float l = 0.0f;       // this half's share of the row sum
+    // Q into TMEM: this thread's row, hd values 64 * half .. + 63, read from
+    // the 128-byte-swizzled TMA tile
+    const bool q_ok = mbar_wait(q_full, 0, abort_flag);
+    bool ok = !pair_any(q, !q_ok || *abort_flag);
+    if (ok) {
+      const uint8_t* qrow = sQ + half * AT_PANEL + r * 128;
+      uint32_t rr[32];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) << 4));
+        rr[ch * 4 + 0] = v.x;
+        rr[ch * 4 + 1] = v.y;
+        rr[ch * 4 + 2] = v.z;
+        rr[ch * 4 + 3] = v.w;
+      }
+      tmem_st32(tmem_base + AT_TM_Q + lane_off + static_cast<uint32_t>(half * 32), rr);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_tm);
+    }
+    for (int jb = 0; ok && jb < nkb; ++jb) {
       const int st = jb & 1;
       const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
+      // (a wait that gave up leaves garbage in the scores, which the vote at
+      // the exchange below discards)
       const bool waited = mbar_wait(&s_full[st], ph, abort_flag);
-      if (epi_any(!waited || *abort_flag)) {
-        ok = false;
-        break;
-      }
       tc_fence_after();
-      float sv[128];
-      const uint32_t tS = tmem_base + static_cast<uint32_t>(st * 128) + lane_off;
+      float sv[64];
+      const uint32_t tS = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128 + c0) + lane_off;
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
+      for (int c = 0; c < 64; c += 32) {
         uint32_t rr[32];
         tmem_ld32(tS + static_cast<uint32_t>(c), rr);
 #pragma unroll
         for (int i = 0; i < 32; ++i) sv[c + i] = __uint_as_float(rr[i]);
       }
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[st]);  // S(jb + 2) may overwrite this buffer
-      const int kbase = jb * AT_ROWS;
+      const int kbase = jb * AT_ROWS + c0;
       // only the diagonal block (causal) and a ragged last block need a mask
-      if ((a.causal && jb == qb) || kbase + AT_ROWS > a.T) {
+      if ((a.causal && jb == qb) || jb * AT_ROWS + AT_ROWS > a.T) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           if (kbase + i > kmax) sv[i] = -INFINITY;
       }
       float mx8[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // the row's other half: exchange the maxima, in one of two slots by
+      // block parity (the partner's write two blocks on comes after the next
+      // exchange, which this thread reaches only after this read); the
+      // barrier also takes both halves out together if a wait gave up
+      float* xr = xrow + (jb & 1) * 256;
+      xr[half * 128 + r] = mx;
+      if (pair_any(q, !waited || *abort_flag)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, xr[(half ^ 1) * 128 + r]);
       const float m_cand = mx * a.scale_log2;  // the scale is positive: same order
       bool rescale = false;
       float alpha = 1.0f;
@@ -269,25 +349,21 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
+      for (int i = 0; i < 64; ++i) {
         sv[i] = ex2_approx(fmaf(sv[i], a.scale_log2, -m));
         sum8[i & 7] += sv[i];
       }
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      // P V of the previous block has read P and finished with O
-      if (jb >= 1) {
-        const bool freed = mbar_wait(o_done, static_cast<uint32_t>(jb - 1) & 1u, abort_flag);
-        if (epi_any(!freed || *abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
       if (__any_sync(0xffffffffu, rescale)) {
-        // the base moved: O (all P V up to block jb - 1) is rescaled first
-        {
+        // the base moved: once P V of block jb - 1 is done, this half's 64
+        // columns of O are rescaled. A wait that gives up (the abort flag is
+        // then set) skips the rescale; the next exchange takes both halves
+        // of the row out of the loop together.
+        const bool done = mbar_wait(&o_done[st ^ 1], static_cast<uint32_t>((jb - 1) >> 1) & 1u, abort_flag);
+        if (__all_sync(0xffffffffu, done)) {
+          tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 128; c += 32) {
+          for (int c = 0; c < 64; c += 32) {
             uint32_t rr[32];
             tmem_ld32(tO + static_cast<uint32_t>(c), rr);
             tmem_ld_wait();
@@ -295,36 +371,38 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
             tmem_st32(tO + static_cast<uint32_t>(c), rr);
           }
-          tmem_st_wait();
         }
       }
-      // P row in bf16: keys 0..63 in panel 0, 64..127 in panel 1, 16-byte
-      // chunks at the 128-byte swizzle position of this row
-      uint8_t* pb = sP;
+      // this half's 64 P values as bf16 pairs over its first 32 score columns
+      // (already read into registers)
+      {
+        uint32_t pk[32];
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        const int panel = c8 >> 3, ch = c8 & 7;
-        uint4 v;
-        v.x = pack_bf16x2(sv[c8 * 8 + 0], sv[c8 * 8 + 1]);
-        v.y = pack_bf16x2(sv[c8 * 8 + 2], sv[c8 * 8 + 3]);
-        v.z = pack_bf16x2(sv[c8 * 8 + 4], sv[c8 * 8 + 5]);
-        v.w = pack_bf16x2(sv[c8 * 8 + 6], sv[c8 * 8 + 7]);
-        *reinterpret_cast<uint4*>(pb + panel * AT_PANEL + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
+        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+        tmem_st32(tS, pk);
       }
-      fence_proxy_async_smem();  // the tensor core reads P through the async proxy
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[st]);
     }
-    if (ok && !*abort_flag) {
-      const bool done = mbar_wait(o_done, static_cast<uint32_t>(nkb - 1) & 1u, abort_flag);
-      if (!epi_any(!done || *abort_flag)) {
+    // ok is uniform over the two warps of a quadrant
+    if (ok) {
+      // (S(nkb - 1) was issued after P V of block nkb - 3, so the barrier of
+      // block nkb - 1 is at most one phase behind: its parity is unambiguous)
+      const int last = nkb - 1;
+      const bool done = mbar_wait(&o_done[last & 1], static_cast<uint32_t>(last >> 1) & 1u, abort_flag);
+      // the row sum is the two halves' shares (same exponent base)
+      float* xr = xrow + (nkb & 1) * 256;
+      xr[half * 128 + r] = l;
+      if (!pair_any(q, !done || *abort_flag)) {
+        l += xr[(half ^ 1) * 128 + r];
         tc_fence_after();
         const float inv = 1.0f / l;
         const int nc = a.nq * AT_HD;
-        __nv_bfloat16* out = a.ctx + (static_cast<size_t>(s) * a.T + t) * nc + j * AT_HD;
+        __nv_bfloat16* out = a.ctx + (static_cast<size_t>(s) * a.T + t) * nc + j * AT_HD + c0;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
+        for (int c = 0; c < 64; c += 32) {
           uint32_t rr[32];
           tmem_ld32(tO + static_cast<uint32_t>(c), rr);
           tmem_ld_wait();
