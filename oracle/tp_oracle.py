@@ -50,6 +50,18 @@ reason in the design notes of the repository):
     full (replicated) hidden.
   * Block wiring: x += O(ctx(QKV(norm(x)))); x += MLP(norm(x)); after the
     last block a final norm and the column-split LM head, gathered.
+  * Backward of the column/row pair ([TUT] column-wise sharding, MLP block
+    sharding and "forward and backward communication symmetry"): the
+    pages state the pattern loosely and in part contradict each other
+    (identity versus reduce-scatter for the row layer). The reading here
+    is the chain rule of the forward as written: the all-reduce after the
+    row layer hands the same dY to every shard (identity); each shard's
+    row and activation gradients are local; each shard's column layer
+    produces a partial input gradient dY_s W_s^T and the input gradient
+    is their sum in shard order (an all-reduce, or a reduce-scatter when
+    the caller wants it split along tokens). Weight gradients are local:
+    dW_s = (layer input)^T (output gradient). The ReLU derivative at 0 is
+    taken as 0.
 
 Parity pins: every function here is checked, without the GPU, against the
 worked example's printed values, brute force on tiny integer inputs, closed
@@ -71,6 +83,8 @@ __all__ = [
     "mlp_block", "qkv_head_layout", "qkv_shards", "context_standin",
     "attention_head", "context_attention", "attn_proj", "rmsnorm",
     "transformer_block", "stack_forward",
+    "activation_backward", "column_linear_backward", "row_linear_backward",
+    "mlp_backward",
 ]
 
 
@@ -394,3 +408,96 @@ def stack_forward(X, layers, W_lm, tp, hq, hkv, hd, eps=1e-5):
         x = transformer_block(x, L, tp, hq, hkv, hd, eps)
     h = rmsnorm(x, None, eps)
     return all_gather(column_parallel(h, W_lm, tp))
+
+
+# ---------------------------------------------------------------------------
+# Backward of the column/row pair
+# ---------------------------------------------------------------------------
+
+def activation_backward(act, G, dH, U=None):
+    """Gradient through the local activation ([CTP] local elementwise
+    computation; [TUT] MLP block sharding, step 2): given dL/dH for
+    H = act(G), or H = silu(G) * U for SwiGLU, return (dL/dG, dL/dU), the
+    second None except for SwiGLU. Derivatives written out:
+    relu'(g) = [g > 0]; gelu'(g) = Phi(g) + g phi(g) with Phi the normal CDF
+    and phi its density; silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + e^-g)."""
+    G = np.asarray(G)
+    if act == "none":
+        return dH, None
+    if act == "relu":
+        return dH * (G > 0), None
+    if act == "gelu":
+        erf = np.vectorize(math.erf, otypes=[np.float64])
+        g = np.asarray(G, np.float64)
+        Phi = 0.5 * (1.0 + erf(g / math.sqrt(2.0)))
+        phi = np.exp(-0.5 * g * g) / math.sqrt(2.0 * math.pi)
+        return dH * (Phi + g * phi), None
+    g = np.asarray(G, np.float64)
+    sg = 1.0 / (1.0 + np.exp(-g))
+    dsilu = sg * (1.0 + g * (1.0 - sg))
+    if act == "silu":
+        return dH * dsilu, None
+    if act == "swiglu":
+        if U is None:
+            raise ValueError("swiglu needs the up projection U")
+        return dH * U * dsilu, dH * g * sg
+    raise ValueError(f"unknown activation {act}")
+
+
+def column_linear_backward(X, W, tp, dYs, dR=None):
+    """Backward of the column-parallel layer Y_s = X @ W_s (X replicated on
+    every shard). [TUT] column-wise sharding: X is a copy on each device,
+    so each shard's input gradient dY_s @ W_s^T is only its share; the input
+    gradient is their sum in shard order (all_reduce), plus the gradient
+    dR reaching X by any other path (a residual branch). The weight
+    gradient of shard s is local: X^T @ dY_s.
+    Returns (dX, [dW_s])."""
+    Ws = column_shards(W, tp)
+    if len(dYs) != tp:
+        raise ValueError("need one output gradient per shard")
+    dX = all_reduce([dYs[s] @ Ws[s].T for s in range(tp)])
+    if dR is not None:
+        dX = dX + dR
+    return dX, [X.T @ dYs[s] for s in range(tp)]
+
+
+def row_linear_backward(Xs, W, tp, dY):
+    """Backward of the row-parallel layer Y = sum_s X_s @ W_s. [TUT]
+    communication symmetry: the forward all-reduce is an identity in the
+    backward, so every shard receives the same dY; then dX_s = dY @ W_s^T
+    and dW_s = X_s^T @ dY, both local. Returns ([dX_s], [dW_s])."""
+    Ws = row_shards(W, tp)
+    if len(Xs) != tp:
+        raise ValueError("need one input block per shard")
+    return [dY @ Ws[s].T for s in range(tp)], [Xs[s].T @ dY for s in range(tp)]
+
+
+def mlp_backward(X, W1, W2, tp, dY, act="relu", W_up=None, dR=None):
+    """Backward of mlp_block (no biases) for the output gradient dY: the
+    forward steps in reverse ([TUT] MLP block sharding, steps 4 to 1).
+    Returns a dict:
+      dX            [T, H]: sum over shards of the column layers' input
+                    gradients, plus dR
+      dW1, dW_up    lists over shards of [H, I/tp] (W_up only for SwiGLU)
+      dW2           list over shards of [I/tp, H]
+      G, U, Hs, dHs, dG, dU   per-shard forward values and gradients."""
+    gated = act == "swiglu"
+    G = column_parallel(X, W1, tp)
+    U = column_parallel(X, W_up, tp) if gated else [None] * tp
+    if gated:
+        Hs = [swiglu(G[s], U[s]) for s in range(tp)]
+    else:
+        f = ACTIVATIONS[act]
+        Hs = [G[s] if f is None else f(G[s]) for s in range(tp)]
+    dHs, dW2 = row_linear_backward(Hs, W2, tp, dY)
+    grads = [activation_backward(act, G[s], dHs[s], U[s]) for s in range(tp)]
+    dG = [g for g, _ in grads]
+    dU = [u for _, u in grads]
+    dX, dW1 = column_linear_backward(X, W1, tp, dG, dR)
+    dWu = None
+    if gated:
+        dX2, dWu = column_linear_backward(X, W_up, tp, dU)
+        dX = dX + dX2
+    return {"dX": dX, "dW1": dW1, "dW_up": dWu, "dW2": dW2,
+            "G": G, "U": U, "Hs": Hs, "dHs": dHs, "dG": dG, "dU": dU}
+
