@@ -54,6 +54,16 @@ def workload_spec(name: str, tp: int | None, tokens: int | None):
         return dict(name="llama7b_swiglu_mlp", T=T, H=H, I=I, tp=tp, flops=flops,
                     dominant="col_swiglu_gemm (gate/up + SwiGLU epilogue)",
                     dominant_flops=4.0 * T * H * I, bound="tensor")
+    if name == "mlp_bwd":
+        # backward of the same MLP: 6 GEMMs of 2*T*H*I each (dHs, dW2, and the
+        # input and weight gradients of gate and up)
+        T, H, I = tokens or 2048, 4096, 11008
+        tp = tp or 8
+        return dict(name="llama7b_swiglu_mlp_backward", T=T, H=H, I=I, tp=tp, flops=12.0 * T * H * I,
+                    dominant="weight-gradient GEMM of the gate shards (dW1, both operands MN-major)",
+                    dominant_flops=2.0 * T * H * I, bound="tensor",
+                    sample_note="the first {r} of {T} tokens, a complete backward problem of its own "
+                                "(weight gradients sum over tokens)")
     if name == "gqa":
         T, H, hq, hkv, hd = tokens or 4096, 4096, 32, 8, 128
         tp = tp or 16
@@ -71,6 +81,7 @@ def workload_spec(name: str, tp: int | None, tokens: int | None):
         return dict(name="gqa_attn_block_causal", T=T, H=H, hq=hq, hkv=hkv, hd=hd, tp=tp, flops=flops,
                     dominant="attention_core (causal, every local head)", dominant_flops=core,
                     bound="tensor",
+                    sample_note="the first {r} of {T} tokens, a complete causal problem of its own",
                     flops_of_rows=lambda r: (2.0 * r * H * (hq + 2 * hkv) * hd + 2.0 * 2.0 * hd * hq * r * (r + 1) / 2.0
                                              + 2.0 * r * hq * hd * H))
     if name == "decode":
@@ -115,7 +126,14 @@ class OracleLeg:
         import synth_inputs as S
         from oracle import tp_oracle as O
         self.spec, name, tp, T = spec, spec["name"], spec["tp"], spec["T"]
-        if name.startswith("llama7b_swiglu") or name.startswith("decode"):
+        if name.startswith("llama7b_swiglu_mlp_backward"):
+            H, I = spec["H"], spec["I"]
+            d = S.mlp_backward(min(T, 512), H, I)
+            Wg, Wu, Wd = (d[k].astype(np.float64) for k in ("Wg", "Wu", "Wd"))
+            X, dY = d["X"].astype(np.float64), d["dY"].astype(np.float64)
+            # the first r tokens: a complete backward problem of its own
+            self.fn = lambda r: O.mlp_backward(X[:r], Wg, Wd, tp, dY[:r], "swiglu", W_up=Wu)
+        elif name.startswith("llama7b_swiglu") or name.startswith("decode"):
             H, I = spec["H"], spec["I"]
             d = (S.swiglu_mlp(min(T, 512), H, I) if name.startswith("llama7b")
                  else S.decode_mlp(min(T, 512), H, I))
@@ -298,7 +316,35 @@ def setup_workload(spec, torch, tpl):
     up = lambda a: torch.from_numpy(a).to("cuda").to(B)
     name, tp, T = spec["name"], spec["tp"], spec["T"]
     st = {}
-    if name.startswith("llama7b_swiglu") or name.startswith("decode"):
+    if name.startswith("llama7b_swiglu_mlp_backward"):
+        H, I = spec["H"], spec["I"]
+        d = S.mlp_backward(T, H, I)
+        Sg = tpl.tp_shard_weights(up(d["Wg"]), tp, "col")
+        Su = tpl.tp_shard_weights(up(d["Wu"]), tp, "col")
+        Sd = tpl.tp_shard_weights(up(d["Wd"]), tp, "row")
+        X, dY = up(d["X"]), up(d["dY"])
+        del d
+        # the forward's saved values, computed once outside the timed region
+        G = tpl.tp_column_linear(X, Sg, act="none")
+        U = tpl.tp_column_linear(X, Su, act="none")
+        Hs = tpl.tp_column_linear(X, Sg, W_up=Su, act="swiglu")
+        Is = I // tp
+        grads = {"dX": torch.empty((T, H), dtype=B, device="cuda"),
+                 "dW1": torch.empty((tp, Is, H), dtype=B, device="cuda"),
+                 "dW_up": torch.empty((tp, Is, H), dtype=B, device="cuda"),
+                 "dW2": torch.empty((tp, H, Is), dtype=B, device="cuda")}
+        ws = torch.empty(tpl.tp_mlp_backward_workspace_bytes(T, H, I, tp, "swiglu"), dtype=torch.uint8,
+                         device="cuda")
+
+        def api_call(dYin, dXout):  # the whole backward: 5 GEMM launches and the activation gradient
+            tpl.tp_mlp_backward(X, Sg, Sd, G, Hs, dYin, W_up=Su, U=U, act="swiglu", workspace=ws,
+                                out=dict(grads, dX=dXout))
+
+        def part_a():  # the gate shards' weight-gradient GEMM alone
+            tpl.tp_column_linear_backward(X, Sg, G, want_dX=False, want_dW=True)
+        st.update(parts=[lambda: api_call(dY, grads["dX"])], X=dY, Y=grads["dX"], api=api_call,
+                  launches_per_step=6, keep=[Sg, Su, Sd, X, G, U, Hs, grads, ws], dominant_part=part_a)
+    elif name.startswith("llama7b_swiglu") or name.startswith("decode"):
         H, I = spec["H"], spec["I"]
         d = S.swiglu_mlp(T, H, I) if name.startswith("llama7b") else S.decode_mlp(T, H, I)
         Sg = tpl.tp_shard_weights(up(d["Wg"]), tp, "col")
@@ -637,10 +683,9 @@ def cpu_baseline_obj(spec, unit, target_s):
     leg = OracleLeg(spec)
     rows = leg.calibrate(target_s)
     elapsed = leg.timed(rows)
+    what = spec.get("sample_note", "{r} of {T} token rows (rows are independent)").format(r=rows, T=spec["T"])
     return {"value": round(leg.value(rows, elapsed), 6), "unit": unit, "cores": _blas_threads(),
-            "kind": "oracle",
-            "sample": f"{rows} of {spec['T']} token rows (rows are independent), float64 numpy "
-                      f"oracle, {elapsed:.2f} s"}
+            "kind": "oracle", "sample": f"{what}, float64 numpy oracle, {elapsed:.2f} s"}
 
 
 def main():
@@ -648,7 +693,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mlp", choices=["mlp", "gqa", "gqa_attn", "decode", "stack"])
+    ap.add_argument("--workload", default="mlp", choices=["mlp", "mlp_bwd", "gqa", "gqa_attn", "decode", "stack"])
     ap.add_argument("--tp", type=int, default=None)
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -674,8 +719,8 @@ def main():
         times = [leg.timed(rows) for _ in range(args.steps)]
         wall = time.perf_counter() - t0
         v = leg.value(rows, float(np.mean(times)))
-        sample = (f"{rows} of {spec['T']} token rows per step (rows are independent), float64 "
-                  f"numpy oracle, {np.mean(times):.3f} s per step")
+        what = spec.get("sample_note", "{r} of {T} token rows (rows are independent)").format(r=rows, T=spec["T"])
+        sample = f"{what} per step, float64 numpy oracle, {np.mean(times):.3f} s per step"
         line = {"metric": METRIC, "value": round(v, 6), "unit": unit, "n_gpus": 1, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(wall * 1e3 / args.steps, 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

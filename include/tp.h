@@ -292,6 +292,82 @@ int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_
                         const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
                         const void* residual, int act, int out_dtype, void* Y, void* stream);
 
+/*
+ * Backward of the column/row pair ("Tensor parallelism: splitting
+ * Transformer layers" tutorial page: column-wise sharding, MLP block
+ * sharding, and forward/backward communication symmetry). The forward
+ * all-reduce after a row layer is an identity in the backward: every shard
+ * receives the same dY. A column layer's shards each hold a share
+ * dY_s @ W_s^T of its input gradient, and the input gradient is their sum
+ * (all-reduce), taken in fp32 inside the accumulator in shard order.
+ * Weight gradients are local. Every GEMM reads the forward's shard storage
+ * as it is (MN-major operands on the tensor cores): nothing is transposed
+ * in memory, and each weight gradient comes out in the layout of the shards
+ * it belongs to, so an optimizer can update them in place.
+ * bf16 only (TP_ERR_DTYPE otherwise); all pointers are device pointers,
+ * 16-byte aligned; T >= 1 (T == 0 returns TP_OK and launches nothing).
+ */
+
+/*
+ * tp_row_linear_backward - backward of Y = sum_s Xs[s] @ W_s.
+ *   W: TP_ROW view (shards [tp][N][K/tp]); Xs [tp][T][K/tp] (the forward
+ *   input, needed for dW); dY [T][N].
+ *   dXs [tp][T][K/tp] = dY @ W_s^T for every shard, or NULL to skip;
+ *   dW  [tp][N][K/tp] (the view's layout) = (Xs[s]^T @ dY)^T, or NULL.
+ * Errors: TP_ERR_NULL, TP_ERR_MODE, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_ALIGN,
+ * TP_ERR_CUDA.
+ */
+int tp_row_linear_backward(const void* Xs, int64_t T, const tp_shards* W, const void* dY, void* dXs,
+                           void* dW, void* stream);
+
+/*
+ * tp_column_linear_backward - backward of Y_s = X @ W_s (X replicated).
+ *   W: TP_COL view (shards [tp][N/tp][K]); X [T][K] (the forward input,
+ *   needed for dW); dYs [tp][T][N/tp].
+ *   dX [T][K] = sum_s dYs[s] @ W_s^T (+ dR), or NULL to skip. dR [T][K]
+ *   (the gradient reaching X by another path, e.g. a residual branch) may
+ *   be NULL. Token rows [s*T/tp, (s+1)*T/tp) of dX are shard s's slice of
+ *   the reduce-scatter form.
+ *   dW [tp][N/tp][K] (the view's layout) = (X^T @ dYs[s])^T, or NULL.
+ *   workspace (optional, 256-byte aligned, >= tp_gemm_workspace_bytes(T,
+ *   W)): scratch that lets the dX GEMM split its last round; NULL runs
+ *   whole tiles only.
+ * Errors: as tp_row_linear_backward, plus TP_ERR_WORKSPACE.
+ */
+int tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W, const void* dYs,
+                              const void* dR, void* dX, void* dW, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/* Workspace bytes tp_mlp_backward needs (act decides whether dU is kept). */
+size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int act);
+
+/*
+ * tp_mlp_backward - backward of tp_mlp_block without biases (the tutorial
+ * page's MLP block steps 4 to 1 in reverse):
+ *   dHs[s] = dY @ W2_s^T                         (row layer, dY on every shard)
+ *   dW2_s  = Hs[s]^T @ dY                        -> dW2 [tp][H][I/tp]
+ *   dG, dU = activation gradients of dHs         (dU for SwiGLU only)
+ *   dW1_s  = X^T @ dG[s], dWu_s = X^T @ dU[s]    -> dW1, dW_up [tp][I/tp][H]
+ *   dX     = sum_s dG[s] @ W1_s^T (+ sum_s dU[s] @ Wu_s^T) (+ dR)
+ *   Five to six launches: five GEMMs (for SwiGLU the gate and up sums of dX
+ *   share one accumulator) and the activation gradient, an HBM-bound
+ *   elementwise pass over dHs.
+ *   X [T][H]; W1 (gate for SwiGLU), W_up: TP_COL views (K=H, N=I); W2:
+ *   TP_ROW view (K=I, N=H). Saved forward values, [tp][T][I/tp] each: G =
+ *   X @ W1_s (the pre-activation), U = X @ Wu_s (SwiGLU only, else NULL),
+ *   Hs = the activation output that fed W2. dY, dR, dX [T][H]; dR may be
+ *   NULL. Any of dX, dW1, dW_up, dW2 may be NULL to skip it (dW_up must be
+ *   NULL unless SwiGLU).
+ *   workspace: >= tp_mlp_backward_workspace_bytes(T, H, I, tp, act) bytes,
+ *   256-byte aligned: dHs, dG and dU (bf16 [tp][T][I/tp]) plus the
+ *   split-tile scratch. Contents on return are unspecified.
+ * Errors: as tp_column_linear_backward, plus TP_ERR_MODE for an unknown act.
+ */
+int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                    const tp_shards* W2, int act, const void* G, const void* U, const void* Hs,
+                    const void* dY, const void* dR, void* workspace, size_t ws_bytes, void* dX,
+                    void* dW1, void* dW_up, void* dW2, void* stream);
+
 /* Workspace bytes tp_attn_proj needs. */
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype);
 

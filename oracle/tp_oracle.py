@@ -84,7 +84,7 @@ __all__ = [
     "attention_head", "context_attention", "attn_proj", "rmsnorm",
     "transformer_block", "stack_forward",
     "activation_backward", "column_linear_backward", "row_linear_backward",
-    "mlp_backward",
+    "mlp_backward_saved", "mlp_backward",
 ]
 
 
@@ -472,23 +472,20 @@ def row_linear_backward(Xs, W, tp, dY):
     return [dY @ Ws[s].T for s in range(tp)], [Xs[s].T @ dY for s in range(tp)]
 
 
-def mlp_backward(X, W1, W2, tp, dY, act="relu", W_up=None, dR=None):
-    """Backward of mlp_block (no biases) for the output gradient dY: the
-    forward steps in reverse ([TUT] MLP block sharding, steps 4 to 1).
-    Returns a dict:
-      dX            [T, H]: sum over shards of the column layers' input
-                    gradients, plus dR
-      dW1, dW_up    lists over shards of [H, I/tp] (W_up only for SwiGLU)
-      dW2           list over shards of [I/tp, H]
-      G, U, Hs, dHs, dG, dU   per-shard forward values and gradients."""
+def mlp_backward_saved(X, W1, W2, tp, dY, G, Hs, act="relu", W_up=None, U=None, dR=None):
+    """Backward of mlp_block (no biases) given the forward's saved per-shard
+    values, as a training step runs it: G[s] the pre-activation X @ W1_s,
+    U[s] the up projection X @ Wu_s (SwiGLU only), Hs[s] the activation
+    output that fed W2. The forward steps in reverse ([TUT] MLP block
+    sharding, steps 4 to 1):
+      row layer:   dHs_s = dY @ W2_s^T, dW2_s = Hs_s^T @ dY (dY on every shard)
+      activation:  dG_s, dU_s from dHs_s, G_s, U_s
+      column layer(s): dX = sum_s dG_s @ W1_s^T (+ sum_s dU_s @ Wu_s^T) (+ dR),
+                   dW1_s = X^T @ dG_s, dWu_s = X^T @ dU_s
+    Returns a dict: dX [T, H]; dW1, dW_up (SwiGLU) lists over shards of
+    [H, I/tp]; dW2 a list of [I/tp, H]; dHs, dG, dU per shard."""
     gated = act == "swiglu"
-    G = column_parallel(X, W1, tp)
-    U = column_parallel(X, W_up, tp) if gated else [None] * tp
-    if gated:
-        Hs = [swiglu(G[s], U[s]) for s in range(tp)]
-    else:
-        f = ACTIVATIONS[act]
-        Hs = [G[s] if f is None else f(G[s]) for s in range(tp)]
+    U = U if gated else [None] * tp
     dHs, dW2 = row_linear_backward(Hs, W2, tp, dY)
     grads = [activation_backward(act, G[s], dHs[s], U[s]) for s in range(tp)]
     dG = [g for g, _ in grads]
@@ -498,6 +495,21 @@ def mlp_backward(X, W1, W2, tp, dY, act="relu", W_up=None, dR=None):
     if gated:
         dX2, dWu = column_linear_backward(X, W_up, tp, dU)
         dX = dX + dX2
-    return {"dX": dX, "dW1": dW1, "dW_up": dWu, "dW2": dW2,
-            "G": G, "U": U, "Hs": Hs, "dHs": dHs, "dG": dG, "dU": dU}
+    return {"dX": dX, "dW1": dW1, "dW_up": dWu, "dW2": dW2, "dHs": dHs, "dG": dG, "dU": dU}
 
+
+def mlp_backward(X, W1, W2, tp, dY, act="relu", W_up=None, dR=None):
+    """Backward of mlp_block (no biases) for the output gradient dY: the
+    forward recomputed in full precision (G, U, Hs per shard), then
+    mlp_backward_saved. Returns its dict plus G, U and Hs."""
+    gated = act == "swiglu"
+    G = column_parallel(X, W1, tp)
+    U = column_parallel(X, W_up, tp) if gated else [None] * tp
+    if gated:
+        Hs = [swiglu(G[s], U[s]) for s in range(tp)]
+    else:
+        f = ACTIVATIONS[act]
+        Hs = [G[s] if f is None else f(G[s]) for s in range(tp)]
+    out = mlp_backward_saved(X, W1, W2, tp, dY, G, Hs, act, W_up=W_up, U=U, dR=dR)
+    out.update(G=G, U=U, Hs=Hs)
+    return out

@@ -120,6 +120,13 @@ def swiglu_mlp(T: int, H: int, I: int, seeds=(1, 2, 3, 4), std: float = 0.02):
     )
 
 
+def mlp_backward(T: int, H: int, I: int, seeds=(1, 2, 3, 4, 40), std: float = 0.02):
+    """The SwiGLU MLP's inputs plus an output gradient dY ~ N(0,1) [T,H]."""
+    d = swiglu_mlp(T, H, I, seeds[:4], std)
+    d["dY"] = normal(seeds[4], (T, H))
+    return d
+
+
 def gqa_proj(T: int, H: int, hq: int, hkv: int, hd: int, seeds=(5, 6, 7, 8, 9),
              std: float = 0.02):
     """Attention projections: X~N(0,1); Wq [H, hq*hd], Wk, Wv [H, hkv*hd],

@@ -22,7 +22,8 @@ __all__ = [
     "tp_mlp_workspace_bytes", "tp_mlp_block", "tp_mlp_block_static", "tp_attn_workspace_bytes",
     "tp_attn_proj", "tp_attn_block", "tp_attention", "ATTN_MODES", "TP_STATIC_WORKSPACE_BYTES",
     "tp_rmsnorm", "tp_get_error", "tp_debug_set_wait_limit_ns", "tp_debug_inject",
-    "tp_status_string",
+    "tp_status_string", "tp_row_linear_backward", "tp_column_linear_backward",
+    "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp_b300.so")
@@ -68,6 +69,11 @@ _SIGS = {
     "tp_attention": (_i32, [_vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "tp_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _f32, _i32, _vp, _i32, _vp]),
     "tp_get_error": (_i32, [_vp]),
+    "tp_row_linear_backward": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp]),
+    "tp_column_linear_backward": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tp_mlp_backward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
+    "tp_mlp_backward": (_i32, [_vp, _i64, _P, _P, _P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                               _vp, _vp, _vp, _vp, _vp]),
     "tp_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "tp_debug_inject": (_i32, [_i32]),
 }
@@ -280,6 +286,62 @@ def tp_mlp_block(X, W1: Shards, W2: Shards, W_up: Shards | None = None, b1=None,
         _ptr(X), T, W1.ref(), W_up.ref() if W_up is not None else None, W2.ref(), _ptr(b1),
         _ptr(b1_up), _ptr(b2), _ptr(residual), ACTS[act], _dt(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _stream(X.device)))
+    return out
+
+
+def tp_row_linear_backward(Xs, W: Shards, dY, want_dX: bool = True, want_dW: bool = True):
+    """Backward of Y = sum_s Xs[s] @ W_s: returns (dXs [tp][T][K/tp], dW
+    [tp][N][K/tp] in W's storage layout); an output not wanted is None."""
+    T = dY.shape[0]
+    tp, Ks = W.tp, W.K // W.tp
+    dXs = torch.empty((tp, T, Ks), dtype=dY.dtype, device=dY.device) if want_dX else None
+    dW = torch.empty((tp, W.N, Ks), dtype=dY.dtype, device=dY.device) if want_dW else None
+    _check("tp_row_linear_backward", lib.tp_row_linear_backward(
+        _ptr(Xs), T, W.ref(), _ptr(dY), _ptr(dXs), _ptr(dW), _stream(dY.device)))
+    return dXs, dW
+
+
+def tp_column_linear_backward(X, W: Shards, dYs, dR=None, want_dX: bool = True, want_dW: bool = True,
+                              workspace=None):
+    """Backward of Y_s = X @ W_s: returns (dX [T][K] = sum_s dYs[s] @ W_s^T (+ dR),
+    dW [tp][N/tp][K] in W's storage layout); an output not wanted is None."""
+    T = dYs.shape[1]
+    dX = torch.empty((T, W.K), dtype=dYs.dtype, device=dYs.device) if want_dX else None
+    dW = torch.empty((W.tp, W.N // W.tp, W.K), dtype=dYs.dtype, device=dYs.device) if want_dW else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("tp_column_linear_backward", lib.tp_column_linear_backward(
+        _ptr(X), T, W.ref(), _ptr(dYs), _ptr(dR), _ptr(dX), _ptr(dW), _ptr(workspace), ws_bytes,
+        _stream(dYs.device)))
+    return dX, dW
+
+
+def tp_mlp_backward_workspace_bytes(T: int, H: int, I: int, tp: int, act: str = "swiglu") -> int:
+    return lib.tp_mlp_backward_workspace_bytes(T, H, I, tp, ACTS[act])
+
+
+def tp_mlp_backward(X, W1: Shards, W2: Shards, G, Hs, dY, W_up: Shards | None = None, U=None, dR=None,
+                    act: str = "relu", workspace=None, want=("dX", "dW1", "dW_up", "dW2"), out=None):
+    """Backward of tp_mlp_block (no biases) given the saved forward values G
+    (pre-activation), U (up projection, SwiGLU) and Hs (activation output),
+    each [tp][T][I/tp]. Returns a dict with dX [T][H], dW1 and dW_up
+    [tp][I/tp][H], dW2 [tp][H][I/tp] (the shards' storage layouts); `out`
+    may supply those tensors (a missing key is skipped)."""
+    T, H = X.shape
+    tp, Is = W1.tp, W1.N // W1.tp
+    gated = act == "swiglu"
+    need = tp_mlp_backward_workspace_bytes(T, H, W1.N, tp, act)
+    if workspace is None:
+        workspace = _workspace(need, X.device)
+    if out is None:
+        mk = lambda name, shape: torch.empty(shape, dtype=X.dtype, device=X.device) if name in want else None
+        out = {"dX": mk("dX", (T, H)), "dW1": mk("dW1", (tp, Is, H)),
+               "dW_up": mk("dW_up", (tp, Is, H)) if gated else None, "dW2": mk("dW2", (tp, H, Is))}
+    else:
+        out = {k: out.get(k) for k in ("dX", "dW1", "dW_up", "dW2")}
+    _check("tp_mlp_backward", lib.tp_mlp_backward(
+        _ptr(X), T, W1.ref(), W_up.ref() if W_up is not None else None, W2.ref(), ACTS[act], _ptr(G),
+        _ptr(U), _ptr(Hs), _ptr(dY), _ptr(dR), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(out["dX"]), _ptr(out["dW1"]), _ptr(out["dW_up"]), _ptr(out["dW2"]), _stream(X.device)))
     return out
 
 

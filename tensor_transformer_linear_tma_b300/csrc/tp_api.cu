@@ -201,14 +201,14 @@ int plan_schedule(tpk::GemmArgs& a, bool swap, const Scratch* sc) {
 
 // The kernel's dynamic shared memory limit, raised once per device (not on
 // every launch, so that launches can also be recorded into CUDA graphs).
-template <int KIND, bool SWAP, bool PAIR>
+template <int KIND, bool SWAP, bool PAIR, int MN = 0>
 bool smem_attr_set() {
   using Cfg = tpk::GemmCfg<KIND, SWAP, PAIR>;
   static bool done[128] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, PAIR, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES) != cudaSuccess)
       return false;
     done[dev] = true;
@@ -217,8 +217,9 @@ bool smem_attr_set() {
 }
 
 // CTA pairs of the 2-SM kernel that fit on the device at once (the
-// persistent grid of a paired launch), looked up once per device.
-template <int KIND>
+// persistent grid of a paired launch), looked up once per device; the
+// kernel's shared-memory limit must have been raised first.
+template <int KIND, int MN = 0>
 int max_cluster_pairs() {
   using Cfg = tpk::GemmCfg<KIND, false, true>;
   static int cache[128] = {0};
@@ -237,7 +238,8 @@ int max_cluster_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tpk::tp_gemm_kernel<KIND, false, true>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, tpk::tp_gemm_kernel<KIND, false, true, MN>, &cfg) != cudaSuccess ||
+        n < 1) {
       cudaGetLastError();
       n = -1;
     }
@@ -263,12 +265,12 @@ int split_ways_for(int rem_units, int pairs, int kpt) {
 // Paired launch: clusters of two CTAs, one pair per two SMs, each pair
 // walking the 256-token tile units round-robin. With scratch, a partial last
 // round is split along K (see the kernel's header).
-template <int KIND>
+template <int KIND, int MN = 0>
 int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
                 const OutMaps& om, tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
   using Cfg = tpk::GemmCfg<KIND, false, true>;
-  if (!smem_attr_set<KIND, false, true>()) return TP_ERR_CUDA;
-  const int pairs = max_cluster_pairs<KIND>();
+  if (!smem_attr_set<KIND, false, true, MN>()) return TP_ERR_CUDA;
+  const int pairs = max_cluster_pairs<KIND, MN>();
   if (pairs < 1) return TP_ERR_UNSUPPORTED;
   args.dp_tiles = args.num_tiles;
   args.sk_iters = 0;
@@ -300,17 +302,21 @@ int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, false, true>, a0, a1, b0, b1, om.y, om.c, args) !=
+  if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, false, true, MN>, a0, a1, b0, b1, om.y, om.c, args) !=
       cudaSuccess)
     return TP_ERR_CUDA;
   return launch_status();
 }
 
-template <int KIND, bool SWAP>
+template <int KIND, bool SWAP, int MN = 0>
 int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
                 const OutMaps& om, tpk::GemmArgs args, const Scratch* sc, cudaStream_t st) {
   using Cfg = tpk::GemmCfg<KIND, SWAP>;
   if (args.num_tiles <= 0) return TP_OK;
+  if constexpr (MN != 0) {
+    static_assert(!SWAP, "MN-major operands run as CTA pairs");
+    return args.cluster == 2 ? pair_launch<KIND, MN>(a0, a1, b0, b1, om, args, sc, st) : TP_ERR_UNSUPPORTED;
+  }
   if constexpr (!SWAP) {
     if (args.cluster > 1) return pair_launch<KIND>(a0, a1, b0, b1, om, args, sc, st);
   }
@@ -480,6 +486,41 @@ int row_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* bias, co
   const uint64_t oes = a.out_f32 ? 4 : 2;
   a.tma_store = make_store_map(&om.y, Y, a.out_f32 != 0, N, T, 1, N * oes, T * N * oes) ? 1 : 0;
   return gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, om, a, sc, st);
+}
+
+// GEMMs of the backward (bf16, CTA pairs, operands in either order):
+//   COL:     out[s][m][n] = sum_k A_s[m][k] B_s[n][k]  -> [tp][M][Ns]
+//   ROW_SUM: out[m][n]    = sum_s sum_k A_s[m][k] B_s[n][k] (+ residual) -> [M][Ns]
+// ma / mb are the operands' maps (K-major: box {64, 128}; MN-major: box
+// {64, 64}); k_ext is the K extent of one shard. With a_sharded (COL) A is
+// per shard and B shared. ma1 / mb1 (ROW_SUM) add a second (A, B) pair
+// whose sum goes into the same accumulator.
+
+template <int KIND, int MN>
+int gemm_bwd(const CUtensorMap& ma, const CUtensorMap& mb, int64_t M, int64_t Ns, int tp, int64_t k_ext,
+             int a_sharded, const void* residual, void* out, const Scratch* sc, cudaStream_t st,
+             const CUtensorMap* ma1 = nullptr, const CUtensorMap* mb1 = nullptr) {
+  tpk::GemmArgs a{};
+  a.M = static_cast<int>(M);
+  a.Ns = static_cast<int>(Ns);
+  a.tp = tp;
+  a.rep = 1;
+  a.cluster = 2;
+  a.act = TP_ACT_NONE;
+  a.two_src = ma1 != nullptr ? 1 : 0;
+  a.a_sharded = a_sharded;
+  a.residual = residual;
+  a.out = out;
+  a.kb_per_shard = static_cast<int>(cdiv(k_ext, 64));
+  a.kpt = KIND == tpk::GK_ROW_SUM ? a.kb_per_shard * tp * (a.two_src ? 2 : 1) : a.kb_per_shard;
+  a.m_tiles = static_cast<int>(cdiv(cdiv(M, 128), 2));
+  a.n_tiles = static_cast<int>(cdiv(Ns, 256));
+  a.num_tiles = a.m_tiles * a.n_tiles * (KIND == tpk::GK_ROW_SUM ? 1 : tp);
+  a.r1_tiles = a.num_tiles;
+  OutMaps om{};
+  const int d2 = KIND == tpk::GK_ROW_SUM ? 1 : tp;
+  a.tma_store = make_store_map(&om.y, out, false, Ns, M, d2, Ns * 2, M * Ns * 2) ? 1 : 0;
+  return gemm_launch<KIND, false, MN>(ma, ma1 ? *ma1 : ma, mb, mb1 ? *mb1 : mb, om, a, sc, st);
 }
 
 template <int KIND>
@@ -1132,6 +1173,167 @@ int tp_debug_set_wait_limit_ns(uint64_t ns) {
 int tp_debug_inject(int kind) {
   if (kind < 0 || kind > 1) return TP_ERR_MODE;
   return cudaMemcpyToSymbol(tpk::g_tp_inject, &kind, sizeof(int)) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward of the column/row pair (bf16, tensor cores, CTA pairs)
+// ---------------------------------------------------------------------------
+namespace {
+
+int check_bwd_view(const tp_shards* W, int mode) {
+  int r = check_view(W, mode);
+  if (r) return r;
+  return W->dtype == TP_BF16 ? TP_OK : TP_ERR_DTYPE;
+}
+
+bool ptrs16(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p && !aligned(p, 16)) return false;
+  return true;
+}
+
+// dXs[s] = dY @ W_s^T and dW_s = (Xs[s]^T @ dY)^T for a row view W
+// (shards [tp][N][Ks]). Both read W's storage, or Xs and dY, MN-major.
+int row_bwd_bf16(const void* Xs, int64_t T, const tp_shards* W, const void* dY, void* dXs, void* dW,
+                 const Scratch* sc, cudaStream_t st) {
+  const int tp = W->tp;
+  const int64_t Ks = W->K / tp, N = W->N;
+  CUtensorMap ma, mb;
+  int r = TP_OK;
+  if (dXs) {  // COL over shards: A = dY [T][N] (K = N), B_s[k][n] = W storage [tp][N][Ks] (MN-major)
+    if (!make_map_bf16(&ma, dY, N, T, 1, 128) || !make_map_bf16(&mb, W->data, Ks, N, tp, 64)) return TP_ERR_CUDA;
+    if ((r = gemm_bwd<tpk::GK_COL, 2>(ma, mb, T, Ks, tp, N, 0, nullptr, dXs, sc, st))) return r;
+  }
+  if (dW) {  // COL over shards, K = T: A = dY^T (M = N), B_s = Xs[s]^T (N = Ks), both MN-major
+    if (!make_map_bf16(&ma, dY, N, T, 1, 64) || !make_map_bf16(&mb, Xs, Ks, T, tp, 64)) return TP_ERR_CUDA;
+    if ((r = gemm_bwd<tpk::GK_COL, 3>(ma, mb, N, Ks, tp, T, 0, nullptr, dW, sc, st))) return r;
+  }
+  return r;
+}
+
+// dX = sum_s dYs[s] @ W_s^T (+ dR) and dW_s = (X^T @ dYs[s])^T for a column
+// view W (shards [tp][Ns][K]).
+int col_bwd_bf16(const void* X, int64_t T, const tp_shards* W, const void* dYs, const void* dR, void* dX,
+                 void* dW, const Scratch* sc, cudaStream_t st) {
+  const int tp = W->tp;
+  const int64_t K = W->K, Ns = W->N / tp;
+  CUtensorMap ma, mb;
+  int r = TP_OK;
+  if (dX) {  // ROW_SUM: A_s = dYs[s] [T][Ns] (K = Ns), B_s[k][n] = W storage [tp][Ns][K] (MN-major)
+    if (!make_map_bf16(&ma, dYs, Ns, T, tp, 128) || !make_map_bf16(&mb, W->data, K, Ns, tp, 64)) return TP_ERR_CUDA;
+    if ((r = gemm_bwd<tpk::GK_ROW_SUM, 2>(ma, mb, T, K, tp, Ns, 0, dR, dX, sc, st))) return r;
+  }
+  if (dW) {  // COL with A per shard, K = T: A_s = dYs[s]^T (M = Ns), B = X^T (N = K), both MN-major
+    if (!make_map_bf16(&ma, dYs, Ns, T, tp, 64) || !make_map_bf16(&mb, X, K, T, 1, 64)) return TP_ERR_CUDA;
+    if ((r = gemm_bwd<tpk::GK_COL, 3>(ma, mb, Ns, K, tp, T, 1, nullptr, dW, sc, st))) return r;
+  }
+  return r;
+}
+
+int act_bwd_launch(const void* dH, const void* G, const void* U, int64_t n, int act, void* dG, void* dU,
+                   cudaStream_t st) {
+  const int64_t n8 = n / 8;
+  if (n8 == 0) return TP_OK;
+  tpk::act_backward_kernel<<<grid_for(n8, 256), 256, 0, st>>>(
+      static_cast<const bf16*>(dH), static_cast<const bf16*>(G), static_cast<const bf16*>(U), n8, act,
+      static_cast<bf16*>(dG), static_cast<bf16*>(dU));
+  return launch_status();
+}
+
+size_t bwd_max_tiles(int64_t H, int64_t I, int tp) {
+  return std::max<size_t>(mlp_max_tiles(H, I, tp), 2 * SK_MAX_CTAS);
+}
+
+}  // namespace
+
+extern "C" {
+
+int tp_row_linear_backward(const void* Xs, int64_t T, const tp_shards* W, const void* dY, void* dXs,
+                           void* dW, void* stream) {
+  int r = check_bwd_view(W, TP_ROW);
+  if (r) return r;
+  if (T < 0) return TP_ERR_SHAPE;
+  if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  if (T > 0 && (!dY || (dW && !Xs))) return TP_ERR_NULL;
+  if (!ptrs16({Xs, dY, dXs, dW})) return TP_ERR_ALIGN;
+  if (T == 0) return TP_OK;
+  return row_bwd_bf16(Xs, T, W, dY, dXs, dW, nullptr, as_stream(stream));
+}
+
+int tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W, const void* dYs,
+                              const void* dR, void* dX, void* dW, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  int r = check_bwd_view(W, TP_COL);
+  if (r) return r;
+  if (T < 0) return TP_ERR_SHAPE;
+  if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  if (T > 0 && (!dYs || (dW && !X))) return TP_ERR_NULL;
+  if (!ptrs16({X, dYs, dR, dX, dW})) return TP_ERR_ALIGN;
+  if (W->K % 8 != 0) return TP_ERR_ALIGN;
+  Scratch sc{};
+  const Scratch* scp = nullptr;
+  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return r;
+  if (T == 0) return TP_OK;
+  return col_bwd_bf16(X, T, W, dYs, dR, dX, dW, scp, as_stream(stream));
+}
+
+size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int act) {
+  if (T < 0 || H < 1 || I < 1 || tp < 1) return 0;
+  const size_t inter = align256(static_cast<size_t>(T) * I * 2);
+  const bool gated = act == TP_ACT_SWIGLU;
+  return (gated ? 3 : 2) * inter + scratch_bytes(T, bwd_max_tiles(H, I, tp));  // dHs, dG (, dU), scratch
+}
+
+int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                    const tp_shards* W2, int act, const void* G, const void* U, const void* Hs,
+                    const void* dY, const void* dR, void* workspace, size_t ws_bytes, void* dX,
+                    void* dW1, void* dW_up, void* dW2, void* stream) {
+  if (!W1 || !W2) return TP_ERR_NULL;
+  if (act < TP_ACT_NONE || act > TP_ACT_SWIGLU) return TP_ERR_MODE;
+  const bool gated = act == TP_ACT_SWIGLU;
+  int r;
+  if ((r = check_bwd_view(W1, TP_COL)) || (r = check_bwd_view(W2, TP_ROW))) return r;
+  if (gated) {
+    if (!W_up) return TP_ERR_NULL;
+    if ((r = check_bwd_view(W_up, TP_COL))) return r;
+    if (!same_shape(W1, W_up)) return TP_ERR_SHAPE;
+  } else if (W_up || U || dW_up) {
+    return TP_ERR_MODE;
+  }
+  if (W2->tp != W1->tp || W2->K != W1->N || W2->N != W1->K) return TP_ERR_SHAPE;
+  if (T < 0) return TP_ERR_SHAPE;
+  if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  if (T > 0 && (!X || !G || !Hs || !dY || (gated && !U) || !workspace)) return TP_ERR_NULL;
+  if (!ptrs16({X, G, U, Hs, dY, dR, dX, dW1, dW_up, dW2}) || !aligned(workspace, 256)) return TP_ERR_ALIGN;
+  const int64_t H = W1->K, I = W1->N;
+  const int tp = W1->tp;
+  if (ws_bytes < tp_mlp_backward_workspace_bytes(T, H, I, tp, act)) return TP_ERR_WORKSPACE;
+  if (T == 0) return TP_OK;
+  const cudaStream_t st = as_stream(stream);
+  char* ws = static_cast<char*>(workspace);
+  const size_t inter = align256(static_cast<size_t>(T) * I * 2);
+  void* dHs = ws;
+  void* dG = ws + inter;
+  void* dU = gated ? ws + 2 * inter : nullptr;
+  const Scratch sc = carve_scratch(workspace, (gated ? 3 : 2) * inter, bwd_max_tiles(H, I, tp));
+  // row layer (every shard gets dY): dHs and dW2; then the local activation
+  if ((r = row_bwd_bf16(Hs, T, W2, dY, dHs, dW2, &sc, st))) return r;
+  if ((r = act_bwd_launch(dHs, G, U, static_cast<int64_t>(T) * I, act, dG, dU, st))) return r;
+  // column layer(s): the input gradient is the sum over shards, and over
+  // gate and up for SwiGLU (one accumulator), plus dR
+  if (!gated) return col_bwd_bf16(X, T, W1, dG, dR, dX, dW1, &sc, st);
+  const int64_t Is = I / tp;
+  if (dX) {
+    CUtensorMap ma0, mb0, ma1, mb1;
+    if (!make_map_bf16(&ma0, dG, Is, T, tp, 128) || !make_map_bf16(&mb0, W1->data, H, Is, tp, 64) ||
+        !make_map_bf16(&ma1, dU, Is, T, tp, 128) || !make_map_bf16(&mb1, W_up->data, H, Is, tp, 64))
+      return TP_ERR_CUDA;
+    if ((r = gemm_bwd<tpk::GK_ROW_SUM, 2>(ma0, mb0, T, H, tp, Is, 0, dR, dX, &sc, st, &ma1, &mb1))) return r;
+  }
+  if ((r = col_bwd_bf16(X, T, W1, dG, nullptr, nullptr, dW1, &sc, st))) return r;
+  return col_bwd_bf16(X, T, W_up, dU, nullptr, nullptr, dW_up, &sc, st);
 }
 
 }  // extern "C"

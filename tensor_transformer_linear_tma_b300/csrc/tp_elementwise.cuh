@@ -222,4 +222,40 @@ __global__ void ctx_standin_kernel(const T* __restrict__ qkv, int tp, int64_t Tn
   }
 }
 
+// ---------------------------------------------------------------------------
+// Gradient through the MLP's local activation (the backward of the tutorial
+// page's MLP block step 2), per element of the shards' intermediate
+// [tp][T][I/tp]: dG = dH * act'(G), and for SwiGLU dG = dH * U * silu'(G),
+// dU = dH * silu(G) (act_grad). bf16 in and out, fp32 arithmetic, eight
+// elements (16 bytes) per step; n8 = elements / 8. HBM-bound: per element 2
+// (SwiGLU 3) bf16 reads and 1 (2) bf16 writes.
+// ---------------------------------------------------------------------------
+__global__ void act_backward_kernel(const __nv_bfloat16* __restrict__ dH, const __nv_bfloat16* __restrict__ G,
+                                    const __nv_bfloat16* __restrict__ U, int64_t n8, int act,
+                                    __nv_bfloat16* __restrict__ dG, __nv_bfloat16* __restrict__ dU) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint4 h4 = reinterpret_cast<const uint4*>(dH)[i];
+    const uint4 g4 = reinterpret_cast<const uint4*>(G)[i];
+    const uint4 u4 = act == ACT_SWIGLU ? reinterpret_cast<const uint4*>(U)[i] : make_uint4(0, 0, 0, 0);
+    const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w},
+                   uw[4] = {u4.x, u4.y, u4.z, u4.w};
+    uint32_t og[4], ou[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float dg0, du0, dg1, du1;
+      // element 2w is the low half of a 32-bit word, 2w + 1 the high half
+      act_grad(act, __uint_as_float(hw[w] << 16), __uint_as_float(gw[w] << 16), __uint_as_float(uw[w] << 16),
+               dg0, du0);
+      act_grad(act, __uint_as_float(hw[w] & 0xFFFF0000u), __uint_as_float(gw[w] & 0xFFFF0000u),
+               __uint_as_float(uw[w] & 0xFFFF0000u), dg1, du1);
+      __nv_bfloat162 a = __floats2bfloat162_rn(dg0, dg1), b = __floats2bfloat162_rn(du0, du1);
+      og[w] = *reinterpret_cast<uint32_t*>(&a);
+      ou[w] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    reinterpret_cast<uint4*>(dG)[i] = make_uint4(og[0], og[1], og[2], og[3]);
+    if (act == ACT_SWIGLU) reinterpret_cast<uint4*>(dU)[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+  }
+}
+
 }  // namespace tpk

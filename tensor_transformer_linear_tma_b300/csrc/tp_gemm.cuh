@@ -66,6 +66,17 @@
 // consecutive shards, the tiles holding only replicated K|V columns are
 // computed once, on the first shard of each group, and stored to all rep
 // shards.
+//
+// Operand order (CTA pairs, COL and ROW_SUM; the template argument MN):
+// bit 0 set means A is given MN-major ([K][M] in memory, M contiguous),
+// bit 1 the same for B. An MN-major tile is loaded as two 64-wide panels
+// (64 K rows x 128 bytes each) and described to the tensor core with the
+// MN-major shared-memory descriptor and the instruction's transpose bit, so
+// no operand is ever transposed in memory. This serves the backward of the
+// column/row pair: data gradients read the forward's K-major weight shards
+// as MN-major B, and weight gradients contract over tokens with both
+// operands MN-major. With GemmArgs::a_sharded a COL launch takes A per shard
+// and B replicated (the weight gradient of a column layer).
 #pragma once
 
 #include "tp_epilogue.cuh"
@@ -139,6 +150,10 @@ struct GemmArgs {
   // ctx [tp][M][hq/tp * hd] from the V columns (null: no context)
   __nv_bfloat16* ctx;
   int hq, hkv, hd;   // the view's heads (global) and head size
+  int a_sharded;     // COL with MN != 0: A is [tp][..] (per shard) and B is shared
+  // ROW_SUM: the K loop also runs over a second (A, B) pair (mapA1, mapB1),
+  // so that out = sum_s A_s B_s^T + sum_s A'_s B'_s^T in one accumulator
+  int two_src;
 };
 
 // ---------------------------------------------------------------------------
@@ -727,7 +742,7 @@ __device__ __forceinline__ void epilogue_swap(const GemmArgs& a, const Src& src,
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int KIND, bool SWAP, bool PAIR>
+template <int KIND, bool SWAP, bool PAIR, int MN = 0>
 __global__ void __launch_bounds__(192, 1)
     tp_gemm_kernel(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
                    const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
@@ -735,6 +750,8 @@ __global__ void __launch_bounds__(192, 1)
                    const GemmArgs args) {
   using Cfg = GemmCfg<KIND, SWAP, PAIR>;
   static_assert(!(PAIR && SWAP), "CTA pairs are a token-major arrangement");
+  static_assert(MN == 0 || (PAIR && (KIND == GK_COL || KIND == GK_ROW_SUM)),
+                "MN-major operands: CTA pairs, COL or ROW_SUM");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -823,9 +840,14 @@ __global__ void __launch_bounds__(192, 1)
             skip_one = false;
           } else {
             int ks, kb;
+            bool src1 = false;  // ROW_SUM with two sources: the second (A, B) pair
             if constexpr (KIND == GK_ROW_SUM) {
               ks = kb_i / args.kb_per_shard;
               kb = kb_i - ks * args.kb_per_shard;
+              if (ks >= args.tp) {
+                src1 = true;
+                ks -= args.tp;
+              }
             } else {
               ks = s;
               kb = kb_i;
@@ -835,11 +857,25 @@ __global__ void __launch_bounds__(192, 1)
             if constexpr (PAIR) {
               if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
               const uint32_t fb = mapa_shared(&full[stage], 0);
-              tma_load_3d_pair(sa, &mapA0, fb, kb * 64, m * 128, Cfg::IS_COL ? 0 : ks);
-              if constexpr (Cfg::SWIGLU)
+              const int a_s = Cfg::IS_COL ? (args.a_sharded ? s : 0) : ks;
+              const int b_s = args.a_sharded ? 0 : ks;
+              const CUtensorMap* ma = src1 ? &mapA1 : &mapA0;
+              if constexpr (MN & 1) {  // [K][M]: M columns m*128 .. +127 as two panels
+                tma_load_3d_pair(sa, ma, fb, m * 128, kb * 64, a_s);
+                tma_load_3d_pair(sa + Cfg::A_TILE / 2, ma, fb, m * 128 + 64, kb * 64, a_s);
+              } else {
+                tma_load_3d_pair(sa, ma, fb, kb * 64, m * 128, a_s);
+              }
+              if constexpr (Cfg::SWIGLU) {
                 tma_load_3d_pair(sb, rank ? &mapB1 : &mapB0, fb, kb * 64, n * 128, ks);
-              else
-                tma_load_3d_pair(sb, &mapB0, fb, kb * 64, n * 256 + rank * 128, ks);
+              } else if constexpr ((MN & 2) != 0) {  // [K][N]: this CTA's 128 of the 256 N columns
+                const CUtensorMap* mb = src1 ? &mapB1 : &mapB0;
+                const int n0 = n * 256 + rank * 128;
+                tma_load_3d_pair(sb, mb, fb, n0, kb * 64, b_s);
+                tma_load_3d_pair(sb + Cfg::B_BYTES / 2, mb, fb, n0 + 64, kb * 64, b_s);
+              } else {
+                tma_load_3d_pair(sb, src1 ? &mapB1 : &mapB0, fb, kb * 64, n * 256 + rank * 128, b_s);
+              }
             } else {
               mbar_arrive_expect_tx(&full[stage], stage_tx);
               if constexpr (SWAP) {
@@ -897,7 +933,12 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ------------------------------ MMA issuer ------------------------------
-      const uint32_t idesc = SWAP ? idesc_bf16_f32(128, args.Tpad) : idesc_bf16_f32(PAIR ? 256 : 128, 256);
+      // MN-major operands set the instruction's transpose bits (15: A, 16: B)
+      const uint32_t idesc = (SWAP ? idesc_bf16_f32(128, args.Tpad) : idesc_bf16_f32(PAIR ? 256 : 128, 256)) |
+                             ((MN & 1) ? (1u << 15) : 0u) | ((MN & 2) ? (1u << 16) : 0u);
+      // a K step of 16: +32 bytes inside a K-major row, +16 rows (2048 bytes)
+      // of an MN-major panel; descriptor addresses count 16-byte units
+      constexpr uint32_t a_step = (MN & 1) ? 128u : 2u, b_step = (MN & 2) ? 128u : 2u;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -919,16 +960,17 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * Cfg::STAGE_BYTES);
-          const uint64_t bdesc = smem_desc_k_sw128(sa + Cfg::A_BYTES);
+          const uint64_t bdesc = (MN & 2) ? smem_desc_mn_sw128(sa + Cfg::A_BYTES, Cfg::B_BYTES / 2, 1024)
+                                          : smem_desc_k_sw128(sa + Cfg::A_BYTES);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t accumulate = (kb_i > sg.kb0 || k > 0) ? 1u : 0u;
 #pragma unroll
             for (int q = 0; q < Cfg::NACC; ++q) {
-              const uint64_t adesc = smem_desc_k_sw128(sa + q * Cfg::A_TILE);
-              // +32 bytes along K per step: +2 in the descriptor's 16-byte address units
+              const uint64_t adesc = (MN & 1) ? smem_desc_mn_sw128(sa, Cfg::A_TILE / 2, 1024)
+                                              : smem_desc_k_sw128(sa + q * Cfg::A_TILE);
               if constexpr (PAIR)
-                tc_mma_bf16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, idesc, accumulate);
+                tc_mma_bf16_pair(d_tmem, adesc + a_step * k, bdesc + b_step * k, idesc, accumulate);
               else
                 tc_mma_bf16(d_tmem + static_cast<uint32_t>(q * args.Tpad), adesc + 2 * k, bdesc + 2 * k,
                             idesc, accumulate);

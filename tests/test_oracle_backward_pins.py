@@ -140,6 +140,36 @@ def test_column_backward_input_gradient_is_the_shard_sum():
         np.testing.assert_allclose(dW[s], X.T @ dYs[s], rtol=1e-12)
 
 
+@pytest.mark.parametrize("act", ["relu", "swiglu"])
+def test_backward_from_saved_values_int_bruteforce(act):
+    """Saved values that need not come from this X (a training step hands
+    over whatever the forward stored): the formulas as explicit index sums
+    on small integers."""
+    r = np.random.default_rng(51)
+    T, H, I, tp = 3, 4, 6, 3
+    X, W1, Wu, W2, dY = (r.integers(-3, 4, size=sh).astype(np.int64)
+                         for sh in ((T, H), (H, I), (H, I), (I, H), (T, H)))
+    G = r.integers(-3, 4, size=(T, I)).astype(np.int64)
+    U = r.integers(-3, 4, size=(T, I)).astype(np.int64)
+    Hs = r.integers(-3, 4, size=(T, I)).astype(np.int64)
+    parts = lambda M: [M[:, s * 2:(s + 1) * 2] for s in range(tp)]
+    g = O.mlp_backward_saved(X, W1, W2, tp, dY, parts(G), parts(Hs), act, W_up=Wu if act == "swiglu" else None,
+                             U=parts(U) if act == "swiglu" else None)
+    dH = [[sum(dY[t][h] * W2[i][h] for h in range(H)) for i in range(I)] for t in range(T)]
+    if act == "relu":
+        dG = [[dH[t][i] * (1 if G[t][i] > 0 else 0) for i in range(I)] for t in range(T)]
+        dX = [[sum(dG[t][i] * W1[h][i] for i in range(I)) for h in range(H)] for t in range(T)]
+        np.testing.assert_array_equal(g["dX"], np.array(dX))
+    else:
+        sg = 1.0 / (1.0 + np.exp(-G.astype(np.float64)))
+        dG = np.array(dH) * U * sg * (1 + G * (1 - sg))
+        dU = np.array(dH) * G * sg
+        np.testing.assert_allclose(g["dX"], dG @ W1.T + dU @ Wu.T, rtol=1e-12)
+        np.testing.assert_allclose(np.concatenate(g["dW_up"], 1), X.T @ dU, rtol=1e-12)
+    dW2 = [[sum(Hs[t][i] * dY[t][h] for t in range(T)) for h in range(H)] for i in range(I)]
+    np.testing.assert_array_equal(np.concatenate(g["dW2"], 0), np.array(dW2))
+
+
 def test_activation_backward_special_values():
     g = np.array([-2.0, 0.0, 3.0])
     dh = np.ones(3)
