@@ -62,6 +62,16 @@ reason in the design notes of the repository):
     the caller wants it split along tokens). Weight gradients are local:
     dW_s = (layer input)^T (output gradient). The ReLU derivative at 0 is
     taken as 0.
+  * Vocabulary-parallel input and output layers ([TUT] input and output
+    layers; [WIT] loss computed sharded over the class dimension): the
+    embedding table [V, H] is split by vocabulary rows, shard s holding
+    rows [s*V/tp, (s+1)*V/tp); a lookup is each shard's masked lookup (a
+    zero row for ids it does not own) summed over shards (all-reduce). The
+    LM head is column-split over the vocabulary (column_parallel). The
+    cross-entropy of vocabulary-sharded logits is the plain cross-entropy of
+    the gathered logits, loss[t] = log sum_v exp(z[t, v]) - z[t, y[t]]: the
+    pages name the sharded computation without its steps, and any correct
+    sharded method reaches that value up to rounding.
 
 Parity pins: every function here is checked, without the GPU, against the
 worked example's printed values, brute force on tiny integer inputs, closed
@@ -84,7 +94,8 @@ __all__ = [
     "attention_head", "context_attention", "attn_proj", "rmsnorm",
     "transformer_block", "stack_forward",
     "activation_backward", "column_linear_backward", "row_linear_backward",
-    "mlp_backward_saved", "mlp_backward",
+    "mlp_backward_saved", "mlp_backward", "vocab_shards", "vocab_embedding", "log_softmax_normaliser",
+    "cross_entropy", "cross_entropy_grad", "vocab_parallel_cross_entropy",
 ]
 
 
@@ -513,3 +524,67 @@ def mlp_backward(X, W1, W2, tp, dY, act="relu", W_up=None, dR=None):
     out = mlp_backward_saved(X, W1, W2, tp, dY, G, Hs, act, W_up=W_up, U=U, dR=dR)
     out.update(G=G, U=U, Hs=Hs)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Vocabulary-parallel input and output layers
+# ---------------------------------------------------------------------------
+
+def vocab_shards(E: np.ndarray, tp: int) -> list[np.ndarray]:
+    """Row blocks of the embedding table E [V, H]: shard s holds the vectors
+    of ids s*V/tp .. (s+1)*V/tp - 1. [TUT] input and output layers: the
+    embedding is split along the vocabulary dimension."""
+    v = _block(E.shape[0], tp, "V")
+    return [E[s * v:(s + 1) * v] for s in range(tp)]
+
+
+def vocab_embedding(ids, E, tp):
+    """Embedding lookup from vocabulary shards: each shard returns the rows
+    of the ids it holds and zero rows for the others; the shard results are
+    summed (all_reduce). [TUT] input and output layers (each device keeps
+    part of the embedding vectors, then all-reduce)."""
+    ids = np.asarray(ids)
+    shards = vocab_shards(E, tp)
+    v = shards[0].shape[0]
+    parts = []
+    for s in range(tp):
+        local = ids - s * v
+        own = (local >= 0) & (local < v)
+        p = np.zeros((len(ids), E.shape[1]), dtype=E.dtype)
+        p[own] = shards[s][local[own]]
+        parts.append(p)
+    return all_reduce(parts)
+
+
+def log_softmax_normaliser(z):
+    """log sum_v exp(z[t, v]) per row, computed as m + log sum exp(z - m)
+    with m the row maximum (the shift changes nothing mathematically and
+    keeps exp in range)."""
+    z = np.asarray(z, np.float64)
+    m = z.max(axis=1)
+    return m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+
+
+def cross_entropy(z, labels):
+    """loss[t] = log sum_v exp(z[t, v]) - z[t, labels[t]]: the negative log
+    of the softmax probability of the label."""
+    z = np.asarray(z, np.float64)
+    labels = np.asarray(labels)
+    return log_softmax_normaliser(z) - z[np.arange(z.shape[0]), labels]
+
+
+def cross_entropy_grad(z, labels, scale=1.0):
+    """Gradient of scale * sum_t loss[t] with respect to the logits:
+    scale * (softmax(z[t]) - onehot(labels[t]))."""
+    z = np.asarray(z, np.float64)
+    p = np.exp(z - log_softmax_normaliser(z)[:, None])
+    p[np.arange(z.shape[0]), np.asarray(labels)] -= 1.0
+    return scale * p
+
+
+def vocab_parallel_cross_entropy(logit_shards, labels):
+    """Cross-entropy of logits split by vocabulary columns into shards
+    [T, V/tp] ([TUT] output layer split by columns; [WIT] loss sharded on
+    the class dimension): by definition, the cross-entropy of the gathered
+    logits."""
+    return cross_entropy(all_gather(logit_shards), labels)
