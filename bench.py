@@ -64,6 +64,16 @@ def workload_spec(name: str, tp: int | None, tokens: int | None):
                     dominant_flops=2.0 * T * H * I, bound="tensor",
                     sample_note="the first {r} of {T} tokens, a complete backward problem of its own "
                                 "(weight gradients sum over tokens)")
+    if name == "lm_ce":
+        # the vocabulary-parallel ends of a language model: embedding lookup,
+        # column-parallel LM head, vocabulary-parallel cross-entropy with its
+        # gradient (the LM head of the 7B stack: V = 32000, tp = 4)
+        T, H, V = tokens or 4096, 4096, 32000
+        tp = tp or 4
+        return dict(name="vocab_embedding_lm_head_cross_entropy", T=T, H=H, V=V, tp=tp, flops=2.0 * T * H * V,
+                    dominant="lm_head_col_gemm (logits [tp][T][V/tp])", dominant_flops=2.0 * T * H * V,
+                    bound="tensor",
+                    sample_note="{r} of {T} tokens (losses of different tokens are independent)")
     if name == "gqa":
         T, H, hq, hkv, hd = tokens or 4096, 4096, 32, 8, 128
         tp = tp or 16
@@ -126,7 +136,15 @@ class OracleLeg:
         import synth_inputs as S
         from oracle import tp_oracle as O
         self.spec, name, tp, T = spec, spec["name"], spec["tp"], spec["T"]
-        if name.startswith("llama7b_swiglu_mlp_backward"):
+        if name.startswith("vocab_embedding_lm_head"):
+            H, V = spec["H"], spec["V"]
+            d = S.vocab_lm(min(T, 256), H, V)
+            E, W = d["E"].astype(np.float64), d["W_lm"].astype(np.float64)
+            ids, labels = d["ids"], d["labels"]
+            self.fn = lambda r: O.vocab_parallel_cross_entropy(
+                O.column_parallel(O.vocab_embedding(ids[:r], E, tp), W, tp), labels[:r])
+            X = ids
+        elif name.startswith("llama7b_swiglu_mlp_backward"):
             H, I = spec["H"], spec["I"]
             d = S.mlp_backward(min(T, 512), H, I)
             Wg, Wu, Wd = (d[k].astype(np.float64) for k in ("Wg", "Wu", "Wd"))
@@ -316,7 +334,37 @@ def setup_workload(spec, torch, tpl):
     up = lambda a: torch.from_numpy(a).to("cuda").to(B)
     name, tp, T = spec["name"], spec["tp"], spec["T"]
     st = {}
-    if name.startswith("llama7b_swiglu_mlp_backward"):
+    if name.startswith("vocab_embedding_lm_head"):
+        H, V = spec["H"], spec["V"]
+        d = S.vocab_lm(T, H, V)
+        E = up(d["E"])
+        Slm = tpl.tp_shard_weights(up(d["W_lm"]), tp, "col")
+        ids = torch.from_numpy(d["ids"]).to("cuda")
+        labels = torch.from_numpy(d["labels"]).to("cuda")
+        del d
+        X0 = torch.empty((T, H), dtype=B, device="cuda")
+        logits = torch.empty((tp, T, V // tp), dtype=B, device="cuda")
+        loss = torch.empty(T, dtype=torch.float32, device="cuda")
+        mean = torch.empty(1, dtype=torch.float32, device="cuda")
+        cws = torch.empty(tpl.tp_cross_entropy_workspace_bytes(T, tp), dtype=torch.uint8, device="cuda")
+        gws = torch.empty(max(tpl.tp_gemm_workspace_bytes(T, Slm), 256), dtype=torch.uint8, device="cuda")
+
+        def p_embed(ids_in=ids):
+            tpl.tp_vocab_embedding(ids_in, E, tp, out=X0)
+
+        def p_head():
+            tpl.tp_column_linear(X0, Slm, out=logits, workspace=gws)
+
+        def p_ce(mean_out=mean):  # loss, mean and the gradient of the mean loss, in place
+            tpl.tp_vocab_cross_entropy(logits, labels, dlogits=logits, workspace=cws, loss=loss, mean_loss=mean_out)
+
+        def api_call(ids_in, mean_out):  # ids in, mean loss out: 1 + 1 + 4 launches
+            p_embed(ids_in)
+            p_head()
+            p_ce(mean_out)
+        st.update(parts=[p_embed, p_head, p_ce], X=ids, Y=mean, api=api_call, launches_per_step=6,
+                  keep=[E, Slm, labels, X0, logits, loss, cws, gws], dominant_part=p_head)
+    elif name.startswith("llama7b_swiglu_mlp_backward"):
         H, I = spec["H"], spec["I"]
         d = S.mlp_backward(T, H, I)
         Sg = tpl.tp_shard_weights(up(d["Wg"]), tp, "col")
@@ -693,7 +741,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="mlp", choices=["mlp", "mlp_bwd", "gqa", "gqa_attn", "decode", "stack"])
+    ap.add_argument("--workload", default="mlp",
+                    choices=["mlp", "mlp_bwd", "gqa", "gqa_attn", "decode", "stack", "lm_ce"])
     ap.add_argument("--tp", type=int, default=None)
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

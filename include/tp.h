@@ -63,7 +63,8 @@ enum {
   TP_ERR_WORKSPACE = 6,   /* workspace or output buffer too small */
   TP_ERR_CUDA = 7,        /* a CUDA runtime/driver call failed */
   TP_ERR_TIMEOUT = 8,     /* a bounded device-side wait expired */
-  TP_ERR_UNSUPPORTED = 9  /* valid request outside this build's limits */
+  TP_ERR_UNSUPPORTED = 9, /* valid request outside this build's limits */
+  TP_ERR_INDEX = 10       /* (from tp_get_error) a token id or label outside [0, V) */
 };
 
 /* Storage types. */
@@ -367,6 +368,57 @@ int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shar
                     const tp_shards* W2, int act, const void* G, const void* U, const void* Hs,
                     const void* dY, const void* dR, void* workspace, size_t ws_bytes, void* dX,
                     void* dW1, void* dW_up, void* dW2, void* stream);
+
+/*
+ * Vocabulary-parallel input and output layers ("Tensor parallelism:
+ * splitting Transformer layers" tutorial page, input and output layers;
+ * "What is tensor parallelism" page, loss sharded over the class dimension).
+ * The embedding table is split by vocabulary rows and the LM head by
+ * vocabulary columns (tp_shard_weights in TP_COL mode, then
+ * tp_column_linear with concat = 0 gives the logits [tp][T][V/tp]).
+ */
+
+/*
+ * tp_vocab_embedding - Y[t] = E[ids[t]] from a table split by vocabulary
+ * rows: shard s holds ids [s*V/tp, (s+1)*V/tp) as rows s*V/tp.. of E, so
+ * the shards stored one after another are E [V][H] itself. A lookup is each
+ * shard's masked lookup summed over shards (all-reduce); one shard owns
+ * each id, so the kernel copies the owner's row.
+ *   ids [T] int32 (device); E [V][H] and Y [T][H] of dtype `dtype`.
+ *   An id outside [0, V) gives a zero row and makes the next tp_get_error
+ *   return TP_ERR_INDEX.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE (V % tp != 0, sizes < 1), TP_ERR_DTYPE,
+ * TP_ERR_ALIGN (4-byte ids and element-aligned tables), TP_ERR_CUDA.
+ */
+int tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, int64_t H, int tp,
+                       int dtype, void* Y, void* stream);
+
+/* Workspace bytes tp_vocab_cross_entropy needs. */
+size_t tp_cross_entropy_workspace_bytes(int64_t T, int tp);
+
+/*
+ * tp_vocab_cross_entropy - loss[t] = log sum_v exp(z[t][v]) - z[t][labels[t]]
+ * over logits split by vocabulary columns, z_s = logits[s] [T][V/tp].
+ * Each shard reduces its own columns to (max, sum of exp(z - max), the
+ * label's logit if it holds the label); the per-token combine of those
+ * statistics over shards (max, rescaled sum, the owner's label logit) is
+ * the all-reduce of a vocabulary-parallel loss. fp32 arithmetic.
+ *   logits [tp][T][V/tp], dtype `dtype`; labels [T] int32 (device).
+ *   loss [T] fp32 per-token losses, or NULL; mean_loss [1] fp32 (their mean,
+ *   summed in a fixed order), or NULL.
+ *   dlogits [tp][T][V/tp] (dtype), or NULL: the gradient of
+ *   grad_scale * sum_t loss[t], grad_scale * (softmax(z[t]) - onehot(label));
+ *   it may be the logits buffer itself (written in place). grad_scale =
+ *   1/T gives the gradient of the mean loss.
+ *   workspace >= tp_cross_entropy_workspace_bytes(T, tp), 256-byte aligned.
+ *   A label outside [0, V) gives a NaN loss and makes the next
+ *   tp_get_error return TP_ERR_INDEX.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_ALIGN,
+ * TP_ERR_WORKSPACE, TP_ERR_CUDA.
+ */
+int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T, int64_t V, int tp,
+                           int dtype, float* loss, float* mean_loss, void* dlogits, float grad_scale,
+                           void* workspace, size_t ws_bytes, void* stream);
 
 /* Workspace bytes tp_attn_proj needs. */
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype);

@@ -127,6 +127,19 @@ def mlp_backward(T: int, H: int, I: int, seeds=(1, 2, 3, 4, 40), std: float = 0.
     return d
 
 
+def token_ids(seed: int, T: int, V: int) -> np.ndarray:
+    """Token ids (or labels) uniform on {0, ..., V-1}, int32."""
+    return uniform_ints(seed, (T,), 0, V - 1).astype(np.int32)
+
+
+def vocab_lm(T: int, H: int, V: int, seeds=(50, 51, 52, 53), std: float = 0.02):
+    """A zero-block language model's ends: embedding table E [V,H] ~ N(0,1),
+    LM head W [H,V] ~ N(0, std^2), input ids and next-token labels [T]."""
+    se, sw, si, sl = seeds
+    return dict(E=normal(se, (V, H)), W_lm=normal(sw, (H, V), std), ids=token_ids(si, T, V),
+                labels=token_ids(sl, T, V))
+
+
 def gqa_proj(T: int, H: int, hq: int, hkv: int, hd: int, seeds=(5, 6, 7, 8, 9),
              std: float = 0.02):
     """Attention projections: X~N(0,1); Wq [H, hq*hd], Wk, Wv [H, hkv*hd],

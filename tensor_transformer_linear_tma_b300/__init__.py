@@ -23,7 +23,8 @@ __all__ = [
     "tp_attn_proj", "tp_attn_block", "tp_attention", "ATTN_MODES", "TP_STATIC_WORKSPACE_BYTES",
     "tp_rmsnorm", "tp_get_error", "tp_debug_set_wait_limit_ns", "tp_debug_inject",
     "tp_status_string", "tp_row_linear_backward", "tp_column_linear_backward",
-    "tp_mlp_backward_workspace_bytes", "tp_mlp_backward",
+    "tp_mlp_backward_workspace_bytes", "tp_mlp_backward", "tp_vocab_embedding",
+    "tp_cross_entropy_workspace_bytes", "tp_vocab_cross_entropy",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp_b300.so")
@@ -74,6 +75,9 @@ _SIGS = {
     "tp_mlp_backward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
     "tp_mlp_backward": (_i32, [_vp, _i64, _P, _P, _P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                _vp, _vp, _vp, _vp, _vp]),
+    "tp_vocab_embedding": (_i32, [_vp, _i64, _vp, _i64, _i64, _i32, _i32, _vp, _vp]),
+    "tp_cross_entropy_workspace_bytes": (_sz, [_i64, _i32]),
+    "tp_vocab_cross_entropy": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _f32, _vp, _sz, _vp]),
     "tp_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "tp_debug_inject": (_i32, [_i32]),
 }
@@ -343,6 +347,46 @@ def tp_mlp_backward(X, W1: Shards, W2: Shards, G, Hs, dY, W_up: Shards | None = 
         _ptr(U), _ptr(Hs), _ptr(dY), _ptr(dR), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(out["dX"]), _ptr(out["dW1"]), _ptr(out["dW_up"]), _ptr(out["dW2"]), _stream(X.device)))
     return out
+
+
+def tp_vocab_embedding(ids, E, tp: int, out=None):
+    """Y[t] = E[ids[t]] from the vocabulary-row shards of E [V][H] (ids int32)."""
+    if ids.dtype != torch.int32:
+        raise TypeError("ids must be int32")
+    V, H = E.shape
+    T = ids.numel()
+    if out is None:
+        out = torch.empty((T, H), dtype=E.dtype, device=E.device)
+    _check("tp_vocab_embedding", lib.tp_vocab_embedding(
+        _ptr(ids), T, _ptr(E), V, H, tp, _dt(E), _ptr(out), _stream(E.device)))
+    return out
+
+
+def tp_cross_entropy_workspace_bytes(T: int, tp: int) -> int:
+    return lib.tp_cross_entropy_workspace_bytes(T, tp)
+
+
+def tp_vocab_cross_entropy(logits, labels, want_loss: bool = True, want_mean: bool = True, dlogits=None,
+                           grad_scale: float | None = None, workspace=None, loss=None, mean_loss=None):
+    """Cross-entropy of vocabulary-sharded logits [tp][T][V/tp] with int32
+    labels [T]. Returns (loss [T] fp32 or None, mean [1] fp32 or None); if
+    `dlogits` is a tensor (it may be `logits` itself) it receives the
+    gradient of grad_scale * sum(loss) (grad_scale defaults to 1/T)."""
+    if labels.dtype != torch.int32:
+        raise TypeError("labels must be int32")
+    tp, T, v = logits.shape
+    dev = logits.device
+    if workspace is None:
+        workspace = _workspace(tp_cross_entropy_workspace_bytes(T, tp), dev)
+    if loss is None and want_loss:
+        loss = torch.empty(T, dtype=torch.float32, device=dev)
+    if mean_loss is None and want_mean:
+        mean_loss = torch.empty(1, dtype=torch.float32, device=dev)
+    scale = (1.0 / max(T, 1)) if grad_scale is None else grad_scale
+    _check("tp_vocab_cross_entropy", lib.tp_vocab_cross_entropy(
+        _ptr(logits), _ptr(labels), T, tp * v, tp, _dt(logits), _ptr(loss), _ptr(mean_loss), _ptr(dlogits),
+        scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
+    return loss, mean_loss
 
 
 TP_STATIC_WORKSPACE_BYTES = 32 << 20

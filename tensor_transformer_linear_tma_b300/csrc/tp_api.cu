@@ -20,6 +20,7 @@
 #include "tp_elementwise.cuh"
 #include "tp_gemm.cuh"
 #include "tp_simt.cuh"
+#include "tp_vocab.cuh"
 
 namespace {
 
@@ -734,6 +735,7 @@ const char* tp_status_string(int s) {
     case TP_ERR_CUDA: return "CUDA error";
     case TP_ERR_TIMEOUT: return "bounded device wait expired";
     case TP_ERR_UNSUPPORTED: return "unsupported size";
+    case TP_ERR_INDEX: return "token id or label outside [0, V)";
     default: return "unknown status";
   }
 }
@@ -1160,7 +1162,9 @@ int tp_get_error(void* stream) {
   if (err != 0) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(tpk::g_tp_error, &zero, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
-    return err == tpk::TP_DEVERR_WAIT_TIMEOUT ? TP_ERR_TIMEOUT : TP_ERR_CUDA;
+    return err == tpk::TP_DEVERR_WAIT_TIMEOUT ? TP_ERR_TIMEOUT
+           : err == tpk::TP_DEVERR_INDEX      ? TP_ERR_INDEX
+                                              : TP_ERR_CUDA;
   }
   return TP_OK;
 }
@@ -1334,6 +1338,91 @@ int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shar
   }
   if ((r = col_bwd_bf16(X, T, W1, dG, nullptr, nullptr, dW1, &sc, st))) return r;
   return col_bwd_bf16(X, T, W_up, dU, nullptr, nullptr, dW_up, &sc, st);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Vocabulary-parallel embedding and cross-entropy
+// ---------------------------------------------------------------------------
+extern "C" {
+
+int tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, int64_t H, int tp,
+                       int dtype, void* Y, void* stream) {
+  if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
+  if (T < 0 || V < 1 || H < 1 || tp < 1 || V % tp != 0) return TP_ERR_SHAPE;
+  if (T == 0) return TP_OK;
+  if (!ids || !E || !Y) return TP_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  if (!aligned(ids, 4) || !aligned(E, es) || !aligned(Y, es)) return TP_ERR_ALIGN;
+  const int vec = (H * static_cast<int64_t>(es)) % 16 == 0 && aligned(E, 16) && aligned(Y, 16);
+  const int grid = static_cast<int>(std::min<int64_t>(cdiv(T, 8), static_cast<int64_t>(std::max(1, num_sms())) * 16));
+  const cudaStream_t st = as_stream(stream);
+  if (dtype == TP_BF16)
+    tpk::vocab_embed_kernel<bf16><<<grid, 256, 0, st>>>(ids, T, static_cast<const bf16*>(E), V, H, V / tp, vec,
+                                                          static_cast<bf16*>(Y));
+  else
+    tpk::vocab_embed_kernel<float><<<grid, 256, 0, st>>>(ids, T, static_cast<const float*>(E), V, H, V / tp, vec,
+                                                           static_cast<float*>(Y));
+  return launch_status();
+}
+
+size_t tp_cross_entropy_workspace_bytes(int64_t T, int tp) {
+  if (T < 0 || tp < 1) return 0;
+  return align256(static_cast<size_t>(T) * tp * 3 * sizeof(float)) + 2 * align256(static_cast<size_t>(T) * sizeof(float));
+}
+
+int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T, int64_t V, int tp,
+                           int dtype, float* loss, float* mean_loss, void* dlogits, float grad_scale,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
+  if (T < 0 || V < 1 || tp < 1 || V % tp != 0) return TP_ERR_SHAPE;
+  if (ws_bytes < tp_cross_entropy_workspace_bytes(T, tp)) return TP_ERR_WORKSPACE;
+  if (T == 0) {
+    if (mean_loss && cudaMemsetAsync(mean_loss, 0, sizeof(float), as_stream(stream)) != cudaSuccess)
+      return TP_ERR_CUDA;
+    return TP_OK;
+  }
+  if (!logits || !labels || !workspace) return TP_ERR_NULL;
+  const size_t es = elem_size(dtype);
+  if (!aligned(labels, 4) || !aligned(logits, es) || !aligned(workspace, 256) || (loss && !aligned(loss, 4)) ||
+      (mean_loss && !aligned(mean_loss, 4)) || (dlogits && !aligned(dlogits, es)))
+    return TP_ERR_ALIGN;
+  const int64_t v = V / tp;
+  const int vec = (v % 8 == 0) && aligned(logits, 16) && (!dlogits || aligned(dlogits, 16));
+  const cudaStream_t st = as_stream(stream);
+  char* ws = static_cast<char*>(workspace);
+  float* stats = reinterpret_cast<float*>(ws);
+  float* lse = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(T) * tp * 3 * sizeof(float)));
+  float* loss_ws = lse + align256(static_cast<size_t>(T) * sizeof(float)) / sizeof(float);
+  float* per_tok = loss ? loss : loss_ws;
+  const int sms = std::max(1, num_sms());
+  const int grid_rows = static_cast<int>(std::min<int64_t>(cdiv(T * tp, 8), static_cast<int64_t>(sms) * 16));
+  if (dtype == TP_BF16)
+    tpk::ce_stats_kernel<bf16><<<grid_rows, 256, 0, st>>>(static_cast<const bf16*>(logits), labels, T, tp, v, vec,
+                                                            stats);
+  else
+    tpk::ce_stats_kernel<float><<<grid_rows, 256, 0, st>>>(static_cast<const float*>(logits), labels, T, tp, v,
+                                                             vec, stats);
+  int r = launch_status();
+  if (r) return r;
+  tpk::ce_combine_kernel<<<grid_for(T, 256), 256, 0, st>>>(stats, labels, T, tp, V, lse, per_tok);
+  if ((r = launch_status())) return r;
+  if (mean_loss) {
+    tpk::ce_mean_kernel<<<1, 1024, 0, st>>>(per_tok, T, mean_loss);
+    if ((r = launch_status())) return r;
+  }
+  if (dlogits) {
+    const int64_t work = vec ? T * V / 8 : T * V;
+    if (dtype == TP_BF16)
+      tpk::ce_grad_kernel<bf16><<<grid_for(work, 256), 256, 0, st>>>(
+          static_cast<const bf16*>(logits), labels, lse, T, tp, v, grad_scale, vec, static_cast<bf16*>(dlogits));
+    else
+      tpk::ce_grad_kernel<float><<<grid_for(work, 256), 256, 0, st>>>(
+          static_cast<const float*>(logits), labels, lse, T, tp, v, grad_scale, vec, static_cast<float*>(dlogits));
+    r = launch_status();
+  }
+  return r;
 }
 
 }  // extern "C"

@@ -17,7 +17,7 @@ namespace tpk {
 // ---------------------------------------------------------------------------
 // Device error word and wait limit
 // ---------------------------------------------------------------------------
-enum : int { TP_DEVERR_NONE = 0, TP_DEVERR_WAIT_TIMEOUT = 1, TP_DEVERR_LAYOUT = 2 };
+enum : int { TP_DEVERR_NONE = 0, TP_DEVERR_WAIT_TIMEOUT = 1, TP_DEVERR_LAYOUT = 2, TP_DEVERR_INDEX = 3 };
 
 __device__ int g_tp_error;                                  // first error seen
 __device__ unsigned long long g_tp_wait_limit_ns = 2000000000ull;
