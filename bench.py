@@ -346,7 +346,7 @@ def setup_workload(spec, torch, tpl):
         logits = torch.empty((tp, T, V // tp), dtype=B, device="cuda")
         loss = torch.empty(T, dtype=torch.float32, device="cuda")
         mean = torch.empty(1, dtype=torch.float32, device="cuda")
-        cws = torch.empty(tpl.tp_cross_entropy_workspace_bytes(T, tp), dtype=torch.uint8, device="cuda")
+        cws = torch.empty(tpl.tp_cross_entropy_workspace_bytes(T, V, tp), dtype=torch.uint8, device="cuda")
         gws = torch.empty(max(tpl.tp_gemm_workspace_bytes(T, Slm), 256), dtype=torch.uint8, device="cuda")
 
         def p_embed(ids_in=ids):

@@ -393,16 +393,17 @@ int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shar
 int tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, int64_t H, int tp,
                        int dtype, void* Y, void* stream);
 
-/* Workspace bytes tp_vocab_cross_entropy needs. */
-size_t tp_cross_entropy_workspace_bytes(int64_t T, int tp);
+/* Workspace bytes tp_vocab_cross_entropy needs (T tokens, vocabulary V). */
+size_t tp_cross_entropy_workspace_bytes(int64_t T, int64_t V, int tp);
 
 /*
  * tp_vocab_cross_entropy - loss[t] = log sum_v exp(z[t][v]) - z[t][labels[t]]
  * over logits split by vocabulary columns, z_s = logits[s] [T][V/tp].
- * Each shard reduces its own columns to (max, sum of exp(z - max), the
- * label's logit if it holds the label); the per-token combine of those
- * statistics over shards (max, rescaled sum, the owner's label logit) is
- * the all-reduce of a vocabulary-parallel loss. fp32 arithmetic.
+ * Each shard reduces its own columns, in chunks of 2048, to (max, sum of
+ * exp(z - max), the label's logit where it holds the label, else 0); the
+ * per-token combine of those statistics in shard and chunk order (max,
+ * rescaled sum, the sum of the masked label logits) is the all-reduce of a
+ * vocabulary-parallel loss. fp32 arithmetic.
  *   logits [tp][T][V/tp], dtype `dtype`; labels [T] int32 (device).
  *   loss [T] fp32 per-token losses, or NULL; mean_loss [1] fp32 (their mean,
  *   summed in a fixed order), or NULL.
@@ -410,7 +411,8 @@ size_t tp_cross_entropy_workspace_bytes(int64_t T, int tp);
  *   grad_scale * sum_t loss[t], grad_scale * (softmax(z[t]) - onehot(label));
  *   it may be the logits buffer itself (written in place). grad_scale =
  *   1/T gives the gradient of the mean loss.
- *   workspace >= tp_cross_entropy_workspace_bytes(T, tp), 256-byte aligned.
+ *   workspace >= tp_cross_entropy_workspace_bytes(T, V, tp), 256-byte
+ *   aligned.
  *   A label outside [0, V) gives a NaN loss and makes the next
  *   tp_get_error return TP_ERR_INDEX.
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_ALIGN,

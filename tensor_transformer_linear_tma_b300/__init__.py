@@ -76,7 +76,7 @@ _SIGS = {
     "tp_mlp_backward": (_i32, [_vp, _i64, _P, _P, _P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                _vp, _vp, _vp, _vp, _vp]),
     "tp_vocab_embedding": (_i32, [_vp, _i64, _vp, _i64, _i64, _i32, _i32, _vp, _vp]),
-    "tp_cross_entropy_workspace_bytes": (_sz, [_i64, _i32]),
+    "tp_cross_entropy_workspace_bytes": (_sz, [_i64, _i64, _i32]),
     "tp_vocab_cross_entropy": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _f32, _vp, _sz, _vp]),
     "tp_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "tp_debug_inject": (_i32, [_i32]),
@@ -362,8 +362,8 @@ def tp_vocab_embedding(ids, E, tp: int, out=None):
     return out
 
 
-def tp_cross_entropy_workspace_bytes(T: int, tp: int) -> int:
-    return lib.tp_cross_entropy_workspace_bytes(T, tp)
+def tp_cross_entropy_workspace_bytes(T: int, V: int, tp: int) -> int:
+    return lib.tp_cross_entropy_workspace_bytes(T, V, tp)
 
 
 def tp_vocab_cross_entropy(logits, labels, want_loss: bool = True, want_mean: bool = True, dlogits=None,
@@ -377,7 +377,7 @@ def tp_vocab_cross_entropy(logits, labels, want_loss: bool = True, want_mean: bo
     tp, T, v = logits.shape
     dev = logits.device
     if workspace is None:
-        workspace = _workspace(tp_cross_entropy_workspace_bytes(T, tp), dev)
+        workspace = _workspace(tp_cross_entropy_workspace_bytes(T, tp * v, tp), dev)
     if loss is None and want_loss:
         loss = torch.empty(T, dtype=torch.float32, device=dev)
     if mean_loss is None and want_mean:

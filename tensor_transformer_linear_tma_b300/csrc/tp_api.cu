@@ -1367,9 +1367,16 @@ int tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, 
   return launch_status();
 }
 
-size_t tp_cross_entropy_workspace_bytes(int64_t T, int tp) {
-  if (T < 0 || tp < 1) return 0;
-  return align256(static_cast<size_t>(T) * tp * 3 * sizeof(float)) + 2 * align256(static_cast<size_t>(T) * sizeof(float));
+// Partial statistics of the cross-entropy's first pass: 3 floats per
+// (shard, token, chunk of CE_CHUNK logits) unit.
+size_t ce_stats_bytes(int64_t T, int64_t V, int tp) {
+  const int64_t v = V / std::max(tp, 1), nchunk = cdiv(std::max<int64_t>(v, 1), tpk::CE_CHUNK);
+  return align256(static_cast<size_t>(T) * tp * nchunk * 3 * sizeof(float));
+}
+
+size_t tp_cross_entropy_workspace_bytes(int64_t T, int64_t V, int tp) {
+  if (T < 0 || V < 1 || tp < 1) return 0;
+  return ce_stats_bytes(T, V, tp) + 2 * align256(static_cast<size_t>(T) * sizeof(float));
 }
 
 int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T, int64_t V, int tp,
@@ -1377,7 +1384,7 @@ int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T,
                            void* workspace, size_t ws_bytes, void* stream) {
   if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
   if (T < 0 || V < 1 || tp < 1 || V % tp != 0) return TP_ERR_SHAPE;
-  if (ws_bytes < tp_cross_entropy_workspace_bytes(T, tp)) return TP_ERR_WORKSPACE;
+  if (ws_bytes < tp_cross_entropy_workspace_bytes(T, V, tp)) return TP_ERR_WORKSPACE;
   if (T == 0) {
     if (mean_loss && cudaMemsetAsync(mean_loss, 0, sizeof(float), as_stream(stream)) != cudaSuccess)
       return TP_ERR_CUDA;
@@ -1393,11 +1400,13 @@ int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T,
   const cudaStream_t st = as_stream(stream);
   char* ws = static_cast<char*>(workspace);
   float* stats = reinterpret_cast<float*>(ws);
-  float* lse = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(T) * tp * 3 * sizeof(float)));
+  float* lse = reinterpret_cast<float*>(ws + ce_stats_bytes(T, V, tp));
   float* loss_ws = lse + align256(static_cast<size_t>(T) * sizeof(float)) / sizeof(float);
   float* per_tok = loss ? loss : loss_ws;
   const int sms = std::max(1, num_sms());
-  const int grid_rows = static_cast<int>(std::min<int64_t>(cdiv(T * tp, 8), static_cast<int64_t>(sms) * 16));
+  const int64_t nchunk = cdiv(v, tpk::CE_CHUNK);  // units of pass 1: (shard, token, chunk)
+  const int64_t units = T * tp * nchunk;            // one warp per unit, 8 per CTA
+  const int grid_rows = static_cast<int>(std::min<int64_t>(cdiv(units, 8), static_cast<int64_t>(sms) * 16));
   if (dtype == TP_BF16)
     tpk::ce_stats_kernel<bf16><<<grid_rows, 256, 0, st>>>(static_cast<const bf16*>(logits), labels, T, tp, v, vec,
                                                             stats);
@@ -1406,19 +1415,20 @@ int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T,
                                                              vec, stats);
   int r = launch_status();
   if (r) return r;
-  tpk::ce_combine_kernel<<<grid_for(T, 256), 256, 0, st>>>(stats, labels, T, tp, V, lse, per_tok);
+  tpk::ce_combine_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(T, 8), static_cast<int64_t>(sms) * 16)), 256, 0,
+                           st>>>(stats, labels, T, tp, V, nchunk, lse, per_tok);
   if ((r = launch_status())) return r;
   if (mean_loss) {
     tpk::ce_mean_kernel<<<1, 1024, 0, st>>>(per_tok, T, mean_loss);
     if ((r = launch_status())) return r;
   }
   if (dlogits) {
-    const int64_t work = vec ? T * V / 8 : T * V;
+    const int grid_g = vec ? grid_rows : grid_for(T * V, 256);
     if (dtype == TP_BF16)
-      tpk::ce_grad_kernel<bf16><<<grid_for(work, 256), 256, 0, st>>>(
+      tpk::ce_grad_kernel<bf16><<<grid_g, 256, 0, st>>>(
           static_cast<const bf16*>(logits), labels, lse, T, tp, v, grad_scale, vec, static_cast<bf16*>(dlogits));
     else
-      tpk::ce_grad_kernel<float><<<grid_for(work, 256), 256, 0, st>>>(
+      tpk::ce_grad_kernel<float><<<grid_g, 256, 0, st>>>(
           static_cast<const float*>(logits), labels, lse, T, tp, v, grad_scale, vec, static_cast<float*>(dlogits));
     r = launch_status();
   }

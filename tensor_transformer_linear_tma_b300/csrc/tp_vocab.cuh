@@ -11,10 +11,12 @@
 //                 is x): one warp per token, 16-byte vectors.
 //   cross-entropy logits [tp][T][V/tp] split by vocabulary columns (the
 //                 column-parallel LM head's per-shard output). Pass 1: per
-//                 (shard, token) row the maximum m_s, the sum of exp(z - m_s)
-//                 and, on the shard that owns the label, its logit. Pass 2:
-//                 per token, the all-reduce of those statistics
-//                 (m = max m_s, S = sum_s S_s exp(m_s - m)) and
+//                 (shard, token) row, in chunks of 2048 logits, the maximum,
+//                 the sum of exp(z - max) and the label's logit where the
+//                 chunk holds it (else 0). Pass 2: per token, the all-reduce
+//                 of those statistics over shards and chunks
+//                 (m = max m_i, S = sum_i S_i exp(m_i - m), z_label = the
+//                 sum of the masked label logits) and
 //                 loss = m + log S - z_label; then the mean over tokens in a
 //                 fixed order. Pass 3 (optional): the gradient of
 //                 scale * sum_t loss[t], scale * (exp(z - lse) - [v == label]),
@@ -74,51 +76,75 @@ __device__ __forceinline__ void lse_merge(float& m, float& S, float m2, float S2
   m = mn;
 }
 
+// Units of work: a row (shard s, token t) of v logits in chunks of CE_CHUNK;
+// one warp per (row, chunk). On the vector path each lane keeps CE_NV
+// packed 16-byte vectors in flight (bf16: 8 x 8 logits, the whole 2048-logit
+// chunk in one step; fp32: two steps of 8 x 4), all loads issued before the
+// arithmetic. Partial statistics per unit:
+// stats[((s * T + t) * nchunk + c) * 3 + {0, 1, 2}] = {max, sum exp(z - max),
+// label logit if this chunk holds the label, else 0}.
+constexpr int CE_CHUNK = 2048;
+constexpr int CE_NV = 8;
+
+// Element j of a 16-byte vector of T.
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&x)[8]);
+__device__ __forceinline__ float vec_elem(const uint4& q, int j);
 template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
-  const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = bf16_lo(w[i]);
-    x[2 * i + 1] = bf16_hi(w[i]);
-  }
+__device__ __forceinline__ float vec_elem<__nv_bfloat16>(const uint4& q, int j) {
+  const uint32_t w = j < 2 ? q.x : j < 4 ? q.y : j < 6 ? q.z : q.w;
+  return (j & 1) ? bf16_hi(w) : bf16_lo(w);
 }
 template <>
-__device__ __forceinline__ void load8<float>(const float* p, float (&x)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+__device__ __forceinline__ float vec_elem<float>(const uint4& q, int j) {
+  return __uint_as_float(j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w);
 }
 
 template <typename T>
 __global__ void ce_stats_kernel(const T* __restrict__ logits, const int32_t* __restrict__ labels, int64_t n_tok,
                                 int tp, int64_t v, int vec, float* __restrict__ stats) {
   const int lane = threadIdx.x & 31;
-  const int64_t rows = n_tok * tp;
+  const int64_t nchunk = (v + CE_CHUNK - 1) / CE_CHUNK;
+  const int64_t units = n_tok * tp * nchunk;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
+  for (int64_t un = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); un < units;
+       un += warps) {
+    const int64_t r = un / nchunk, c0 = (un - r * nchunk) * CE_CHUNK;
+    const int64_t c1 = min(v, c0 + CE_CHUNK);
     const int64_t s = r / n_tok, t = r - s * n_tok;
     const T* z = logits + r * v;
+    // the label and, where this chunk holds it, its logit: loaded with the
+    // data rather than after the reduction
+    const int64_t loc = static_cast<int64_t>(labels[t]) - s * v;
+    const bool has_label = loc >= c0 && loc < c1;
+    const float zy = (has_label && lane == 0) ? to_f32<T>(z[loc]) : 0.0f;
     float m = -INFINITY, S = 0.0f;
-    if (vec) {  // 8 logits per step, v % 8 == 0
-      for (int64_t i = static_cast<int64_t>(lane) * 8; i < v; i += 32 * 8) {
-        float x[8];
-        load8<T>(z + i, x);
-        float mx = x[0];
+    if (vec) {  // v % 8 == 0, so every 16-byte vector is whole and aligned
+      constexpr int EPV = 16 / sizeof(T);
+      for (int64_t base = c0; base < c1; base += CE_NV * 32 * EPV) {
+        uint4 q[CE_NV];
 #pragma unroll
-        for (int j = 1; j < 8; ++j) mx = fmaxf(mx, x[j]);
-        float acc = 0.0f;
-        const float mn = fmaxf(m, mx);
+        for (int u = 0; u < CE_NV; ++u) {
+          const int64_t i = base + (u * 32 + lane) * EPV;
+          q[u] = i < c1 ? __ldg(reinterpret_cast<const uint4*>(z + i)) : make_uint4(0, 0, 0, 0);
+        }
+        float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc += __expf(x[j] - mn);
-        S = (m == -INFINITY ? 0.0f : S * __expf(m - mn)) + acc;
-        m = mn;
+        for (int u = 0; u < CE_NV; ++u)
+          if (base + (u * 32 + lane) * EPV < c1)
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) mx = fmaxf(mx, vec_elem<T>(q[u], j));
+        if (mx != -INFINITY) {
+          float acc = 0.0f;
+#pragma unroll
+          for (int u = 0; u < CE_NV; ++u)
+            if (base + (u * 32 + lane) * EPV < c1)
+#pragma unroll
+              for (int j = 0; j < EPV; ++j) acc += __expf(vec_elem<T>(q[u], j) - mx);
+          lse_merge(m, S, mx, acc);
+        }
       }
     } else {
-      for (int64_t i = lane; i < v; i += 32) {
+      for (int64_t i = c0 + lane; i < c1; i += 32) {
         const float x = to_f32<T>(z[i]);
         const float mn = fmaxf(m, x);
         S = (m == -INFINITY ? 0.0f : S * __expf(m - mn)) + __expf(x - mn);
@@ -131,10 +157,7 @@ __global__ void ce_stats_kernel(const T* __restrict__ logits, const int32_t* __r
       lse_merge(m, S, m2, S2);
     }
     if (lane == 0) {
-      const int64_t y = labels[t];
-      const int64_t loc = y - s * v;
-      const float zy = (loc >= 0 && loc < v) ? to_f32<T>(z[loc]) : 0.0f;
-      float* o = stats + r * 3;
+      float* o = stats + un * 3;
       o[0] = m;
       o[1] = S;
       o[2] = zy;
@@ -147,24 +170,38 @@ __global__ void ce_stats_kernel(const T* __restrict__ logits, const int32_t* __r
 // lse[t] = m + log S (kept for the gradient); loss[t] = lse[t] - z_label.
 // ---------------------------------------------------------------------------
 __global__ void ce_combine_kernel(const float* __restrict__ stats, const int32_t* __restrict__ labels,
-                                  int64_t n_tok, int tp, int64_t V, float* __restrict__ lse,
+                                  int64_t n_tok, int tp, int64_t V, int64_t nchunk, float* __restrict__ lse,
                                   float* __restrict__ loss) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n_tok; t += stride) {
-    const int64_t y = labels[t];
-    const bool ok = y >= 0 && y < V;
-    if (!ok) atomicCAS(&g_tp_error, TP_DEVERR_NONE, TP_DEVERR_INDEX);
-    const int64_t v = V / tp;
-    const int owner = ok ? static_cast<int>(y / v) : 0;
+  // one warp per token: lane i merges units i, i + 32, ... (shard-major,
+  // then chunk), then the lanes merge in a fixed butterfly; the label logit
+  // is the sum of the units' entries, all zero but the owner's (a masked
+  // value summed)
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t nu = tp * nchunk;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_tok;
+       t += warps) {
     float m = -INFINITY, S = 0.0f, zy = 0.0f;
-    for (int s = 0; s < tp; ++s) {
-      const float* st = stats + (static_cast<int64_t>(s) * n_tok + t) * 3;
+    for (int64_t i = lane; i < nu; i += 32) {
+      const int64_t s = i / nchunk, c = i - s * nchunk;
+      const float* st = stats + ((s * n_tok + t) * nchunk + c) * 3;
       lse_merge(m, S, st[0], st[1]);
-      if (s == owner) zy = st[2];
+      zy += st[2];
     }
-    const float l = m + __logf(S);
-    lse[t] = l;
-    loss[t] = ok ? l - zy : __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
+      lse_merge(m, S, m2, S2);
+      zy += __shfl_xor_sync(0xffffffffu, zy, o);
+    }
+    if (lane == 0) {
+      const int64_t y = labels[t];
+      const bool ok = y >= 0 && y < V;
+      if (!ok) atomicCAS(&g_tp_error, TP_DEVERR_NONE, TP_DEVERR_INDEX);
+      const float l = m + __logf(S);
+      lse[t] = l;
+      loss[t] = ok ? l - zy : __int_as_float(0x7fc00000);
+    }
   }
 }
 
@@ -188,48 +225,48 @@ __global__ void ce_mean_kernel(const float* __restrict__ loss, int64_t n, float*
 // [tp][T][v] logits; out may alias logits (each element is read, then
 // written, by the same thread). 8 elements per step when vec.
 // ---------------------------------------------------------------------------
-// Plain (coherent) loads for the gradient pass, whose output may be the
-// logits themselves.
-template <typename T>
-__device__ __forceinline__ void load8_rw(const T* p, float (&x)[8]);
-template <>
-__device__ __forceinline__ void load8_rw<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
-  const uint4 q = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = bf16_lo(w[i]);
-    x[2 * i + 1] = bf16_hi(w[i]);
-  }
-}
-template <>
-__device__ __forceinline__ void load8_rw<float>(const float* p, float (&x)[8]) {
-  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-
 template <typename T>
 __global__ void ce_grad_kernel(const T* logits, const int32_t* __restrict__ labels, const float* __restrict__ lse,
                                int64_t n_tok, int tp, int64_t v, float scale, int vec, T* out) {
   const int64_t total = n_tok * tp * v;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  if (vec) {
-    const int64_t n8 = total / 8;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
-      const int64_t e = i * 8, r = e / v, c = e - r * v;  // r = s * T + t; 8 | v, so the 8 share a row
+  if (vec) {  // one warp per (row, chunk) unit as in pass 1; v % 8 == 0
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunk = (v + CE_CHUNK - 1) / CE_CHUNK;
+    const int64_t units = n_tok * tp * nchunk;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t un = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); un < units;
+         un += warps) {
+      const int64_t r = un / nchunk, c0 = (un - r * nchunk) * CE_CHUNK;
+      const int64_t c1 = min(v, c0 + CE_CHUNK);
       const int64_t s = r / n_tok, t = r - s * n_tok;
       const float l = lse[t];
       const int64_t loc = static_cast<int64_t>(labels[t]) - s * v;
-      float x[8], g[8];
-      load8_rw<T>(logits + e, x);
+      const T* z = logits + r * v;
+      T* o = out + r * v;
+      constexpr int EPV = 16 / sizeof(T);
+      for (int64_t base = c0; base < c1; base += CE_NV * 32 * EPV) {
+        uint4 q[CE_NV];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) g[j] = scale * (__expf(x[j] - l) - (c + j == loc ? 1.0f : 0.0f));
-      if constexpr (sizeof(T) == 2) {
-        *reinterpret_cast<uint4*>(out + e) = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
-                                                        pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
-      } else {
-        reinterpret_cast<float4*>(out + e)[0] = make_float4(g[0], g[1], g[2], g[3]);
-        reinterpret_cast<float4*>(out + e)[1] = make_float4(g[4], g[5], g[6], g[7]);
+        for (int u = 0; u < CE_NV; ++u) {
+          const int64_t i = base + (u * 32 + lane) * EPV;
+          if (i < c1) q[u] = *reinterpret_cast<const uint4*>(z + i);  // coherent: o may be z
+        }
+#pragma unroll
+        for (int u = 0; u < CE_NV; ++u) {
+          const int64_t i = base + (u * 32 + lane) * EPV;
+          if (i >= c1) break;
+          float g[EPV];
+#pragma unroll
+          for (int j = 0; j < EPV; ++j)
+            g[j] = scale * (__expf(vec_elem<T>(q[u], j) - l) - (i + j == loc ? 1.0f : 0.0f));
+          if constexpr (sizeof(T) == 2) {
+            *reinterpret_cast<uint4*>(o + i) = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
+                                                          pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]));
+          } else {
+            *reinterpret_cast<float4*>(o + i) = make_float4(g[0], g[1], g[2], g[3]);
+          }
+        }
       }
     }
   } else {

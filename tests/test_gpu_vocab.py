@@ -54,7 +54,7 @@ def test_embedding_id_out_of_range_reports_index_error():
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("tp,T,V", [(4, 300, 32000), (8, 37, 1000), (1, 1, 4096), (2, 129, 520)])
+@pytest.mark.parametrize("tp,T,V", [(4, 300, 32000), (8, 37, 1000), (1, 1, 4096), (2, 129, 520), (2, 33, 4100)])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_cross_entropy(dtype, tp, T, V, in_place):
     z = S.normal(511, (tp, T, V // tp), 2.0)
