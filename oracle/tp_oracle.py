@@ -72,6 +72,13 @@ reason in the design notes of the repository):
     the gathered logits, loss[t] = log sum_v exp(z[t, v]) - z[t, y[t]]: the
     pages name the sharded computation without its steps, and any correct
     sharded method reaches that value up to rounding.
+  * Mixture of experts under TP ([TRT] FFN module, mixture of experts: the
+    TP mode splits every expert's weights across all shards and every shard
+    sees all tokens): each expert is an MLP block sharded as above (gate and
+    up by columns, down by rows, shard sum); token t's output is
+    sum_k w[t, k] * MLP_{e[t, k]}(x_t) for its top-k experts e[t, :] with
+    weights w[t, :]. The router's choice is an input (synthetic routing):
+    the pages describe the selection but not the router.
 
 Parity pins: every function here is checked, without the GPU, against the
 worked example's printed values, brute force on tiny integer inputs, closed
@@ -95,7 +102,7 @@ __all__ = [
     "transformer_block", "stack_forward",
     "activation_backward", "column_linear_backward", "row_linear_backward",
     "mlp_backward_saved", "mlp_backward", "vocab_shards", "vocab_embedding", "log_softmax_normaliser",
-    "cross_entropy", "cross_entropy_grad", "vocab_parallel_cross_entropy",
+    "cross_entropy", "cross_entropy_grad", "vocab_parallel_cross_entropy", "moe_tp",
 ]
 
 
@@ -588,3 +595,31 @@ def vocab_parallel_cross_entropy(logit_shards, labels):
     the class dimension): by definition, the cross-entropy of the gathered
     logits."""
     return cross_entropy(all_gather(logit_shards), labels)
+
+
+# ---------------------------------------------------------------------------
+# Mixture of experts with tensor-parallel experts
+# ---------------------------------------------------------------------------
+
+def moe_tp(X, experts, ids, weights, tp, act="swiglu", residual=None):
+    """[TRT] FFN module, mixture of experts, TP mode: the router has chosen
+    top-k experts ids[t, :] with weights weights[t, :] for token t; every
+    expert's MLP is column/row sharded over tp shards (mlp_block) and sees
+    the tokens routed to it; token t's output is the weighted sum of its
+    experts' outputs, in k order (+ residual).
+    experts: list of dicts with W1 (gate, [H, I]), W_up ([H, I], SwiGLU) and
+    W2 ([I, H])."""
+    X = np.asarray(X)
+    ids = np.asarray(ids)
+    T, k = ids.shape
+    Y = np.zeros((T, experts[0]["W2"].shape[1]), dtype=np.result_type(X, experts[0]["W2"], np.asarray(weights)))
+    for j in range(k):
+        for e, ex in enumerate(experts):
+            rows = np.nonzero(ids[:, j] == e)[0]
+            if rows.size == 0:
+                continue
+            _, ye = mlp_block(X[rows], ex["W1"], ex["W2"], tp, act, W_up=ex.get("W_up"))
+            Y[rows] = Y[rows] + np.asarray(weights)[rows, j][:, None] * ye
+    if residual is not None:
+        Y = Y + residual
+    return Y
