@@ -64,6 +64,17 @@ def workload_spec(name: str, tp: int | None, tokens: int | None):
                     dominant_flops=2.0 * T * H * I, bound="tensor",
                     sample_note="the first {r} of {T} tokens, a complete backward problem of its own "
                                 "(weight gradients sum over tokens)")
+    if name == "moe":
+        # a Mixtral-shaped MoE FFN: 8 SwiGLU experts (H=4096, I=14336), top-2
+        # synthetic routing, every expert split over tp=8 shards; the work
+        # counts the routed tokens only (not the units' padding rows)
+        T, H, I, E, k = tokens or 4096, 4096, 14336, 8, 2
+        tp = tp or 8
+        fl = 6.0 * T * k * H * I
+        return dict(name="moe_8x_swiglu_top2_tp", T=T, H=H, I=I, E=E, k=k, tp=tp, flops=fl,
+                    dominant="moe block (dispatch, grouped gate/up + SwiGLU, grouped down + shard sum, combine)",
+                    dominant_flops=fl, bound="tensor",
+                    sample_note="{r} of {T} tokens (tokens are independent)")
     if name == "lm_ce":
         # the vocabulary-parallel ends of a language model: embedding lookup,
         # column-parallel LM head, vocabulary-parallel cross-entropy with its
@@ -136,7 +147,13 @@ class OracleLeg:
         import synth_inputs as S
         from oracle import tp_oracle as O
         self.spec, name, tp, T = spec, spec["name"], spec["tp"], spec["T"]
-        if name.startswith("vocab_embedding_lm_head"):
+        if name.startswith("moe_"):
+            H, I, E, k = spec["H"], spec["I"], spec["E"], spec["k"]
+            X = S.normal(70, (T, H))[:min(T, 64)].astype(np.float64)
+            ex = [{kk: v.astype(np.float64) for kk, v in e.items()} for e in S.moe_experts(E, H, I)]
+            ids, w = S.moe_routing(71, T, E, k)
+            self.fn = lambda r: O.moe_tp(X[:r], ex, ids[:r], w[:r].astype(np.float64), tp)
+        elif name.startswith("vocab_embedding_lm_head"):
             H, V = spec["H"], spec["V"]
             d = S.vocab_lm(min(T, 256), H, V)
             E, W = d["E"].astype(np.float64), d["W_lm"].astype(np.float64)
@@ -334,7 +351,25 @@ def setup_workload(spec, torch, tpl):
     up = lambda a: torch.from_numpy(a).to("cuda").to(B)
     name, tp, T = spec["name"], spec["tp"], spec["T"]
     st = {}
-    if name.startswith("vocab_embedding_lm_head"):
+    if name.startswith("moe_"):
+        H, I, E, k = spec["H"], spec["I"], spec["E"], spec["k"]
+        ex = S.moe_experts(E, H, I)
+        Wg = tpl.tp_shard_experts([up(e["W1"]) for e in ex], tp, "col")
+        Wu = tpl.tp_shard_experts([up(e["W_up"]) for e in ex], tp, "col")
+        Wd = tpl.tp_shard_experts([up(e["W2"]) for e in ex], tp, "row")
+        del ex
+        X = up(S.normal(70, (T, H)))
+        ids_h, w_h = S.moe_routing(71, T, E, k)
+        ids = torch.from_numpy(ids_h).to("cuda")
+        wts = torch.from_numpy(w_h).to("cuda")
+        Y = torch.empty((T, H), dtype=B, device="cuda")
+        ws = torch.empty(tpl.tp_moe_workspace_bytes(T, H, I, k, E, tp), dtype=torch.uint8, device="cuda")
+
+        def api_call(Xin, Yout):  # dispatch (3), grouped gate/up, grouped down, combine: 6 launches
+            tpl.tp_moe_block(Xin, ids, wts, Wg, Wu, Wd, E, workspace=ws, out=Yout)
+        st.update(parts=[lambda: api_call(X, Y)], X=X, Y=Y, api=api_call, launches_per_step=6,
+                  keep=[Wg, Wu, Wd, ids, wts, ws])
+    elif name.startswith("vocab_embedding_lm_head"):
         H, V = spec["H"], spec["V"]
         d = S.vocab_lm(T, H, V)
         E = up(d["E"])
@@ -682,7 +717,7 @@ def run_gpu(args, spec):
             peak = peaks["bf16_tflops_sustained" if capped else "bf16_tflops"]
             achieved = spec["dominant_flops"] / (dom_ms * 1e-3) / 1e12 if dom_ms else None
         clocks = clk.summary()
-        cfg = {k: v for k, v in spec.items() if k in ("T", "H", "I", "hq", "hkv", "hd", "V", "L", "tp")}
+        cfg = {k: v for k, v in spec.items() if k in ("T", "H", "I", "hq", "hkv", "hd", "V", "L", "E", "k", "tp")}
         cfg.update(workload=spec["name"], tokens_per_step=spec["T"], launches=launch_mode,
                    l2="flushed before every timed step (256 MB write, then 256 MB read to evict it)",
                    layout=f"tp={spec['tp']} shards in one device's memory")
@@ -742,7 +777,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mlp",
-                    choices=["mlp", "mlp_bwd", "gqa", "gqa_attn", "decode", "stack", "lm_ce"])
+                    choices=["mlp", "mlp_bwd", "gqa", "gqa_attn", "decode", "stack", "lm_ce", "moe"])
     ap.add_argument("--tp", type=int, default=None)
     ap.add_argument("--tokens", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -422,6 +422,38 @@ int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T,
                            int dtype, float* loss, float* mean_loss, void* dlogits, float grad_scale,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * Mixture of experts with tensor-parallel experts ("Parallel strategies in
+ * TensorRT LLM" page, FFN module, mixture of experts, TP mode: each expert's
+ * weights are split across all shards; every shard sees all tokens).
+ */
+
+/* Workspace bytes tp_moe_block needs (T tokens, top-k of E experts). */
+size_t tp_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int k, int E, int tp);
+
+/*
+ * tp_moe_block - Y[t] = sum_j weights[t][j] * MLP_{ids[t][j]}(X[t]) (+ residual)
+ * with SwiGLU experts, each an MLP block under TP (gate and up column-split,
+ * down row-split, shard sum). The router's choice is an input.
+ *   X [T][H] bf16; ids [T][k] int32 in [0, E); weights [T][k] fp32.
+ *   Wg, Wu: TP_COL views of ONE expert's shape (K = H, N = I) whose data
+ *   holds the E experts' shard sets one after another ([E][tp][I/tp][H]);
+ *   Wd: TP_ROW view (K = I, N = H), data [E][tp][H][I/tp]. bf16. E <= 1024.
+ *   residual [T][H] or NULL; Y [T][H] bf16.
+ *   The tokens of each expert are gathered, in token order, into a segment
+ *   padded to 256 rows; the gate/up and down GEMMs each run as one grouped
+ *   launch over all segments (the expert rows kept in fp32); Y sums a
+ *   token's k slots in order in fp32.
+ *   workspace >= tp_moe_workspace_bytes(...), 256-byte aligned.
+ *   An id outside [0, E) drops that slot and makes the next tp_get_error
+ *   return TP_ERR_INDEX.
+ * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN,
+ * TP_ERR_WORKSPACE, TP_ERR_UNSUPPORTED, TP_ERR_CUDA.
+ */
+int tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weights, int k, int E,
+                 const tp_shards* Wg, const tp_shards* Wu, const tp_shards* Wd, const void* residual,
+                 void* workspace, size_t ws_bytes, void* Y, void* stream);
+
 /* Workspace bytes tp_attn_proj needs. */
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype);
 

@@ -42,6 +42,10 @@ def _fill(seed: int, n: int, kind: str, a: float, b: float) -> np.ndarray:
             to_bf16_inplace(o)
         elif kind == "int":
             o[:] = r.integers(int(a), int(b) + 1, size=hi - lo, dtype=np.int32)
+        elif kind == "uniform":
+            r.random(hi - lo, dtype=np.float32, out=o)
+            o *= np.float32(b - a)
+            o += np.float32(a)
         else:  # pragma: no cover - internal misuse
             raise ValueError(kind)
 
@@ -138,6 +142,39 @@ def vocab_lm(T: int, H: int, V: int, seeds=(50, 51, 52, 53), std: float = 0.02):
     se, sw, si, sl = seeds
     return dict(E=normal(se, (V, H)), W_lm=normal(sw, (H, V), std), ids=token_ids(si, T, V),
                 labels=token_ids(sl, T, V))
+
+
+def moe_routing(seed: int, T: int, E: int, k: int):
+    """Synthetic top-k routing: for each token k distinct experts (the first
+    uniform on {0..E-1}, each next one a uniform nonzero step further,
+    modulo E, moved on past experts the token already has) and k weights
+    uniform on [0.05, 1), fp32."""
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    first = uniform_ints(seed, (T,), 0, E - 1).astype(np.int64)
+    ids = np.empty((T, k), dtype=np.int64)
+    ids[:, 0] = first
+    taken = [first]
+    for j in range(1, k):
+        step = uniform_ints(seed + 1000 * j, (T,), 1, max(E - 1, 1)).astype(np.int64)
+        cand = (ids[:, j - 1] + step) % E
+        for _ in range(E):
+            clash = np.zeros(T, dtype=bool)
+            for prev in taken:
+                clash |= cand == prev
+            if not clash.any():
+                break
+            cand = np.where(clash, (cand + 1) % E, cand)
+        ids[:, j] = cand
+        taken.append(cand)
+    w = _fill(seed + 7, T * k, "uniform", 0.05, 1.0).reshape(T, k).astype(np.float32)
+    return ids.astype(np.int32), w
+
+
+def moe_experts(E: int, H: int, I: int, seed: int = 60, std: float = 0.02):
+    """E SwiGLU experts: Wg, Wu [H,I], Wd [I,H] ~ N(0, std^2)."""
+    return [dict(W1=normal(seed + 3 * e, (H, I), std), W_up=normal(seed + 3 * e + 1, (H, I), std),
+                 W2=normal(seed + 3 * e + 2, (I, H), std)) for e in range(E)]
 
 
 def gqa_proj(T: int, H: int, hq: int, hkv: int, hd: int, seeds=(5, 6, 7, 8, 9),

@@ -24,7 +24,8 @@ __all__ = [
     "tp_rmsnorm", "tp_get_error", "tp_debug_set_wait_limit_ns", "tp_debug_inject",
     "tp_status_string", "tp_row_linear_backward", "tp_column_linear_backward",
     "tp_mlp_backward_workspace_bytes", "tp_mlp_backward", "tp_vocab_embedding",
-    "tp_cross_entropy_workspace_bytes", "tp_vocab_cross_entropy",
+    "tp_cross_entropy_workspace_bytes", "tp_vocab_cross_entropy", "tp_shard_experts",
+    "tp_moe_workspace_bytes", "tp_moe_block",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp_b300.so")
@@ -78,6 +79,8 @@ _SIGS = {
     "tp_vocab_embedding": (_i32, [_vp, _i64, _vp, _i64, _i64, _i32, _i32, _vp, _vp]),
     "tp_cross_entropy_workspace_bytes": (_sz, [_i64, _i64, _i32]),
     "tp_vocab_cross_entropy": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _f32, _vp, _sz, _vp]),
+    "tp_moe_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32, _i32]),
+    "tp_moe_block": (_i32, [_vp, _i64, _vp, _vp, _i32, _i32, _P, _P, _P, _vp, _vp, _sz, _vp, _vp]),
     "tp_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "tp_debug_inject": (_i32, [_i32]),
 }
@@ -387,6 +390,46 @@ def tp_vocab_cross_entropy(logits, labels, want_loss: bool = True, want_mean: bo
         _ptr(logits), _ptr(labels), T, tp * v, tp, _dt(logits), _ptr(loss), _ptr(mean_loss), _ptr(dlogits),
         scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
     return loss, mean_loss
+
+
+def tp_shard_experts(Ws, tp: int, mode: str) -> Shards:
+    """Shard each expert's W [K, N] like tp_shard_weights and store the E
+    shard sets one after another; the view describes one expert."""
+    K, N = Ws[0].shape
+    m = TP_COL if mode == "col" else TP_ROW
+    out = torch.empty(len(Ws) * K * N, dtype=Ws[0].dtype, device=Ws[0].device)
+    view = TpShardsC()
+    per = K * N * out.element_size()
+    for e, W in enumerate(Ws):
+        if tuple(W.shape) != (K, N):
+            raise ValueError("experts must share one shape")
+        _check("tp_shard_weights", lib.tp_shard_weights(
+            _ptr(W), K, N, _dt(W), tp, m, out.data_ptr() + e * per, per, ctypes.byref(view), _stream(W.device)))
+    view.data = out.data_ptr()
+    return Shards(out, view)
+
+
+def tp_moe_workspace_bytes(T: int, H: int, I: int, k: int, E: int, tp: int) -> int:
+    return lib.tp_moe_workspace_bytes(T, H, I, k, E, tp)
+
+
+def tp_moe_block(X, ids, weights, Wg: Shards, Wu: Shards, Wd: Shards, E: int, residual=None, workspace=None,
+                 out=None):
+    """Mixture of TP-sharded SwiGLU experts: ids [T, k] int32, weights [T, k]
+    fp32; returns Y [T, H] (bf16)."""
+    if ids.dtype != torch.int32 or weights.dtype != torch.float32:
+        raise TypeError("ids must be int32 and weights fp32")
+    T, H = X.shape
+    k = ids.shape[1]
+    need = tp_moe_workspace_bytes(T, H, Wg.N, k, E, Wg.tp)
+    if workspace is None:
+        workspace = _workspace(need, X.device)
+    if out is None:
+        out = torch.empty((T, H), dtype=X.dtype, device=X.device)
+    _check("tp_moe_block", lib.tp_moe_block(
+        _ptr(X), T, _ptr(ids), _ptr(weights), k, E, Wg.ref(), Wu.ref(), Wd.ref(), _ptr(residual),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _stream(X.device)))
+    return out
 
 
 TP_STATIC_WORKSPACE_BYTES = 32 << 20

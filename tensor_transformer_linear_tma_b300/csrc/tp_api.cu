@@ -20,6 +20,7 @@
 #include "tp_elementwise.cuh"
 #include "tp_gemm.cuh"
 #include "tp_simt.cuh"
+#include "tp_moe.cuh"
 #include "tp_vocab.cuh"
 
 namespace {
@@ -1433,6 +1434,145 @@ int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T,
     r = launch_status();
   }
   return r;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Mixture of experts with tensor-parallel experts (grouped GEMMs)
+// ---------------------------------------------------------------------------
+namespace {
+
+struct MoeLayout {
+  int64_t units, rows;  // 256-row units of the permuted buffers, and their rows
+  size_t xp, hs, yp, pos, inv, counts, off, unit_expert, total;
+};
+
+MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int k, int E) {
+  MoeLayout L{};
+  L.units = cdiv(T * k, tpk::MOE_UNIT) + E;  // each expert's padding adds at most one unit
+  L.rows = L.units * tpk::MOE_UNIT;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  L.xp = take(static_cast<size_t>(L.rows) * H * 2);   // bf16
+  L.hs = take(static_cast<size_t>(L.rows) * I * 2);   // bf16 [tp][rows][I/tp]
+  L.yp = take(static_cast<size_t>(L.rows) * H * 4);   // fp32
+  L.pos = take(static_cast<size_t>(T) * k * 4);
+  L.inv = take(static_cast<size_t>(T) * k * 4);
+  L.counts = take(static_cast<size_t>(E) * 4);
+  L.off = take(static_cast<size_t>(E) * 4);
+  L.unit_expert = take(static_cast<size_t>(L.units) * 4);
+  L.total = o;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tp_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int k, int E, int tp) {
+  if (T < 0 || H < 1 || I < 1 || k < 1 || E < 1 || tp < 1) return 0;
+  return moe_layout(T, H, I, k, E).total;
+}
+
+int tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weights, int k, int E,
+                 const tp_shards* Wg, const tp_shards* Wu, const tp_shards* Wd, const void* residual,
+                 void* workspace, size_t ws_bytes, void* Y, void* stream) {
+  if (!Wg || !Wu || !Wd) return TP_ERR_NULL;
+  int r;
+  if ((r = check_view(Wg, TP_COL)) || (r = check_view(Wu, TP_COL)) || (r = check_view(Wd, TP_ROW))) return r;
+  if (Wg->dtype != TP_BF16 || !same_shape(Wg, Wu) || Wd->dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (Wd->tp != Wg->tp || Wd->K != Wg->N || Wd->N != Wg->K) return TP_ERR_SHAPE;
+  if (T < 0 || k < 1 || E < 1 || E > 1024) return TP_ERR_SHAPE;
+  if (T * k > INT32_MAX / 2) return TP_ERR_UNSUPPORTED;
+  const int64_t H = Wg->K, I = Wg->N;
+  const int tp = Wg->tp;
+  const MoeLayout L = moe_layout(T, H, I, k, E);
+  if (ws_bytes < L.total) return TP_ERR_WORKSPACE;
+  if (T == 0) return TP_OK;
+  if (!X || !ids || !weights || !workspace || !Y) return TP_ERR_NULL;
+  if (!ptrs16({X, residual, Y}) || !aligned(workspace, 256) || !aligned(ids, 4) || !aligned(weights, 4))
+    return TP_ERR_ALIGN;
+  const cudaStream_t st = as_stream(stream);
+  char* ws = static_cast<char*>(workspace);
+  bf16* Xp = reinterpret_cast<bf16*>(ws + L.xp);
+  bf16* Hs = reinterpret_cast<bf16*>(ws + L.hs);
+  float* Yp = reinterpret_cast<float*>(ws + L.yp);
+  int32_t* pos = reinterpret_cast<int32_t*>(ws + L.pos);
+  int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+  int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+  int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
+  int32_t* unit_expert = reinterpret_cast<int32_t*>(ws + L.unit_expert);
+  const int64_t n = T * k;
+  const int64_t grid_cap = static_cast<int64_t>(std::max(1, num_sms())) * 16;
+  // 1. dispatch
+  tpk::moe_route_kernel<<<E, 1024, 0, st>>>(ids, n, E, pos, counts);
+  if ((r = launch_status())) return r;
+  tpk::moe_units_kernel<<<1, 256, 0, st>>>(counts, E, static_cast<int>(L.units), off, unit_expert);
+  if ((r = launch_status())) return r;
+  tpk::moe_gather_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(n, 8), grid_cap)), 256, 0, st>>>(
+      static_cast<const bf16*>(X), ids, pos, off, n, k, E, H, Xp, inv);
+  if ((r = launch_status())) return r;
+  // 2. the experts' MLP blocks over all units: gate/up + SwiGLU per shard,
+  // then down + the shard sum; each tile takes its expert's shard set
+  const int64_t Is = I / tp;
+  {
+    CUtensorMap mx, mg, mu;
+    if (!make_map_bf16(&mx, Xp, H, L.rows, 1, 128) ||
+        !make_map_bf16(&mg, Wg->data, H, Is, static_cast<uint64_t>(E) * tp, 128) ||
+        !make_map_bf16(&mu, Wu->data, H, Is, static_cast<uint64_t>(E) * tp, 128))
+      return TP_ERR_CUDA;
+    tpk::GemmArgs a{};
+    a.M = static_cast<int>(L.rows);
+    a.Ns = static_cast<int>(Is);
+    a.tp = tp;
+    a.rep = 1;
+    a.cluster = 2;
+    a.kb_per_shard = static_cast<int>(cdiv(H, 64));
+    a.kpt = a.kb_per_shard;
+    a.act = TP_ACT_SWIGLU;
+    a.out = Hs;
+    a.m_tiles = static_cast<int>(L.units);
+    a.n_tiles = static_cast<int>(cdiv(Is, 128));
+    a.num_tiles = a.m_tiles * a.n_tiles * tp;
+    a.r1_tiles = a.num_tiles;
+    a.unit_expert = unit_expert;
+    OutMaps om{};
+    a.tma_store = make_store_map(&om.y, Hs, false, Is, L.rows, tp, Is * 2, L.rows * Is * 2) ? 1 : 0;
+    if ((r = gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mg, mu, om, a, nullptr, st))) return r;
+  }
+  {
+    CUtensorMap mx, mw;
+    if (!make_map_bf16(&mx, Hs, Is, L.rows, tp, 128) ||
+        !make_map_bf16(&mw, Wd->data, Is, H, static_cast<uint64_t>(E) * tp, 128))
+      return TP_ERR_CUDA;
+    tpk::GemmArgs a{};
+    a.M = static_cast<int>(L.rows);
+    a.Ns = static_cast<int>(H);
+    a.tp = tp;
+    a.rep = 1;
+    a.cluster = 2;
+    a.kb_per_shard = static_cast<int>(cdiv(Is, 64));
+    a.kpt = a.kb_per_shard * tp;
+    a.out = Yp;
+    a.out_f32 = 1;  // the expert rows stay fp32 until the weighted combine
+    a.m_tiles = static_cast<int>(L.units);
+    a.n_tiles = static_cast<int>(cdiv(H, 256));
+    a.num_tiles = a.m_tiles * a.n_tiles;
+    a.r1_tiles = a.num_tiles;
+    a.unit_expert = unit_expert;
+    OutMaps om{};
+    a.tma_store = make_store_map(&om.y, Yp, true, H, L.rows, 1, H * 4, L.rows * H * 4) ? 1 : 0;
+    if ((r = gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, om, a, nullptr, st))) return r;
+  }
+  // 3. combine
+  tpk::moe_combine_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(T, 8), grid_cap)), 256, 0, st>>>(
+      Yp, inv, weights, T, k, H, static_cast<const bf16*>(residual), static_cast<bf16*>(Y));
+  return launch_status();
 }
 
 }  // extern "C"

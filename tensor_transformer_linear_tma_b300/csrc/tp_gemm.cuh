@@ -154,6 +154,12 @@ struct GemmArgs {
   // ROW_SUM: the K loop also runs over a second (A, B) pair (mapA1, mapB1),
   // so that out = sum_s A_s B_s^T + sum_s A'_s B'_s^T in one accumulator
   int two_src;
+  // Grouped experts (CTA pairs, whole tiles only): the token rows are the
+  // experts' routed tokens, each expert's segment padded to 256-row units;
+  // unit_expert[u] is the expert of unit u (tile % m_tiles), or -1 for an
+  // unused unit, which every warp role skips. The weight maps hold the
+  // experts' shard sets one after another: shard coordinate e * tp + s.
+  const int* unit_expert;
 };
 
 // ---------------------------------------------------------------------------
@@ -182,11 +188,13 @@ struct SegIter {
     i_end = sk_begin(a, blockIdx.x + 1);
   }
   __device__ bool next(const GemmArgs& a, Seg& s) {
-    if (dp_next < a.dp_tiles) {
-      s.tile = dp_next;
+    while (dp_next < a.dp_tiles) {
+      const int t = dp_next;
+      dp_next += gridDim.x / a.cluster;
+      if (a.unit_expert && __ldg(a.unit_expert + t % a.m_tiles) < 0) continue;  // an unused expert unit
+      s.tile = t;
       s.kb0 = 0;
       s.kb1 = a.kpt;
-      dp_next += gridDim.x / a.cluster;
       return true;
     }
     if (piece_left) {  // this pair's piece of the split last round
@@ -858,7 +866,9 @@ __global__ void __launch_bounds__(192, 1)
               if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
               const uint32_t fb = mapa_shared(&full[stage], 0);
               const int a_s = Cfg::IS_COL ? (args.a_sharded ? s : 0) : ks;
-              const int b_s = args.a_sharded ? 0 : ks;
+              // grouped experts: the tile's expert selects its shard set
+              const int wks = args.unit_expert ? __ldg(args.unit_expert + sg.tile % args.m_tiles) * args.tp : 0;
+              const int b_s = (args.a_sharded ? 0 : ks) + wks;
               const CUtensorMap* ma = src1 ? &mapA1 : &mapA0;
               if constexpr (MN & 1) {  // [K][M]: M columns m*128 .. +127 as two panels
                 tma_load_3d_pair(sa, ma, fb, m * 128, kb * 64, a_s);
@@ -867,7 +877,7 @@ __global__ void __launch_bounds__(192, 1)
                 tma_load_3d_pair(sa, ma, fb, kb * 64, m * 128, a_s);
               }
               if constexpr (Cfg::SWIGLU) {
-                tma_load_3d_pair(sb, rank ? &mapB1 : &mapB0, fb, kb * 64, n * 128, ks);
+                tma_load_3d_pair(sb, rank ? &mapB1 : &mapB0, fb, kb * 64, n * 128, ks + wks);
               } else if constexpr ((MN & 2) != 0) {  // [K][N]: this CTA's 128 of the 256 N columns
                 const CUtensorMap* mb = src1 ? &mapB1 : &mapB0;
                 const int n0 = n * 256 + rank * 128;

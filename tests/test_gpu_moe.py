@@ -1,0 +1,100 @@
+"""Mixture of TP-sharded SwiGLU experts on the GPU against the oracle.
+
+The GPU rounds the experts' intermediate (Hs) to bf16, keeps each expert's
+output row in fp32 until the weighted combine, and rounds Y once; the
+oracle rounds nothing. Outputs are held to the bf16 bound, 2e-2 * RMS.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as S
+from oracle import tp_oracle as O
+from tests._util import TOL_BF16, assert_close, assert_close_stored, dev, f64, host
+
+pytestmark = pytest.mark.gpu
+
+tpl = pytest.importorskip("tensor_transformer_linear_tma_b300")
+TP_ERR_INDEX = 10
+
+
+def gpu_experts(ex, tp):
+    Wg = tpl.tp_shard_experts([dev(e["W1"]) for e in ex], tp, "col")
+    Wu = tpl.tp_shard_experts([dev(e["W_up"]) for e in ex], tp, "col")
+    Wd = tpl.tp_shard_experts([dev(e["W2"]) for e in ex], tp, "row")
+    return Wg, Wu, Wd
+
+
+def i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def f32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def oracle(X, ex, ids, w, tp, R=None):
+    exf = [{k: f64(v) for k, v in e.items()} for e in ex]
+    return O.moe_tp(f64(X), exf, ids, f64(w), tp, residual=None if R is None else f64(R))
+
+
+@pytest.mark.parametrize("tp,T,H,I,E,k", [(2, 300, 256, 512, 4, 2), (8, 129, 384, 1408, 8, 2),
+                                          (4, 64, 256, 1024, 3, 1), (1, 1, 256, 512, 2, 2), (2, 200, 256, 768, 6, 3)])
+def test_moe_block(tp, T, H, I, E, k):
+    """Ragged tails: H = 384 (a 128-column last block of the down GEMM),
+    I/tp = 176; a single token; top-1 and top-3."""
+    X = S.normal(601, (T, H))
+    ex = S.moe_experts(E, H, I, seed=602, std=0.05)
+    ids, w = S.moe_routing(603, T, E, k)
+    R = S.normal(604, (T, H))
+    Wg, Wu, Wd = gpu_experts(ex, tp)
+    Y = tpl.tp_moe_block(dev(X), i32(ids), f32(w), Wg, Wu, Wd, E, residual=dev(R))
+    assert tpl.tp_get_error() == 0
+    assert_close(Y, oracle(X, ex, ids, w, tp, R), TOL_BF16, "Y")
+
+
+def test_moe_skewed_routing_and_unused_experts():
+    """All first slots to expert 0, all second slots to expert 3 (experts 1
+    and 2 unused): segments of 300 rows span two units each."""
+    T, H, I, E, tp = 300, 256, 512, 4, 2
+    X = S.normal(611, (T, H))
+    ex = S.moe_experts(E, H, I, seed=612, std=0.05)
+    ids = np.stack([np.zeros(T), np.full(T, 3)], 1).astype(np.int32)
+    _, w = S.moe_routing(613, T, E, 2)
+    Wg, Wu, Wd = gpu_experts(ex, tp)
+    Y = tpl.tp_moe_block(dev(X), i32(ids), f32(w), Wg, Wu, Wd, E)
+    assert tpl.tp_get_error() == 0
+    assert_close(Y, oracle(X, ex, ids, w, tp), TOL_BF16, "Y")
+
+
+def test_moe_bad_id_is_dropped_and_reported():
+    T, H, I, E, tp = 8, 256, 512, 2, 2
+    X = S.normal(621, (T, H))
+    ex = S.moe_experts(E, H, I, seed=622, std=0.05)
+    ids = np.array([[0, 1]] * T, dtype=np.int32)
+    ids[3, 1] = 7
+    w = np.full((T, 2), 0.5, dtype=np.float32)
+    Wg, Wu, Wd = gpu_experts(ex, tp)
+    Y = tpl.tp_moe_block(dev(X), i32(ids), f32(w), Wg, Wu, Wd, E)
+    assert tpl.tp_get_error() == TP_ERR_INDEX
+    ids_ok, w_ok = ids.copy(), w.copy()
+    ids_ok[3, 1], w_ok[3, 1] = 0, 0.0  # a zero-weight slot stands for the dropped one
+    assert_close(Y, oracle(X, ex, ids_ok, w_ok, tp), TOL_BF16, "Y")
+
+
+def test_moe_full_size_sampled():
+    """The bench workload (T = 4096, H = 4096, I = 14336, 8 experts, top-2,
+    tp = 8): sampled tokens against the oracle, each computed on its own.
+    A token's output mixes two experts' outputs with weights in [0.05, 1),
+    so the values are heavy-tailed: the largest sit 5-6x above the RMS, where
+    the bf16 storage of one element alone (2^-9 of it) is about 1.2% of the
+    RMS. The bound adds each element's storage rounding (2^-8 of it)."""
+    T, H, I, E, k, tp = 4096, 4096, 14336, 8, 2, 8
+    X = S.normal(70, (T, H))
+    ex = S.moe_experts(E, H, I)
+    ids, w = S.moe_routing(71, T, E, k)
+    Wg, Wu, Wd = gpu_experts(ex, tp)
+    Y = host(tpl.tp_moe_block(dev(X), i32(ids), f32(w), Wg, Wu, Wd, E))
+    assert tpl.tp_get_error() == 0
+    rows = np.sort(np.random.default_rng(3).choice(T, 16, replace=False))
+    assert_close_stored(Y[rows], oracle(X[rows], ex, ids[rows], w[rows], tp), TOL_BF16, "sampled tokens")
