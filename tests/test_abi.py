@@ -14,7 +14,7 @@ import tensor_transformer_linear_tma_b300 as tpl  # noqa: E402
 HEADER = os.path.join(ROOT, "include", "tp.h")
 
 # constants from tp.h
-OK, NULL, SHAPE, DTYPE, MODE, ALIGN, WORKSPACE, CUDA, TIMEOUT, UNSUP = range(10)
+OK, NULL, SHAPE, DTYPE, MODE, ALIGN, WORKSPACE, CUDA, TIMEOUT, UNSUP, INDEX = range(11)
 F32, BF16 = 0, 1
 COL, ROW = 0, 1
 
@@ -42,8 +42,8 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
-    for s in range(10):
-        assert tpl.tp_status_string(s)
+    for s in range(11):
+        assert tpl.tp_status_string(s) != "unknown status"
     assert tpl.tp_status_string(1234) == "unknown status"
     assert tpl.lib.tp_abi_version() == 1
 
@@ -194,3 +194,68 @@ def test_binding_raises_on_error_status():
     with pytest.raises(tpl.TpError) as e:
         tpl._check("tp_column_linear", SHAPE)
     assert e.value.status == SHAPE and "shape" in str(e.value)
+
+
+def test_backward_validation():
+    L = tpl.lib
+    rowv, colv = view(K=256, N=128, mode=ROW, dtype=BF16), view(K=128, N=256, mode=COL, dtype=BF16)
+    # row layer
+    assert L.tp_row_linear_backward(FAKE, 8, ctypes.byref(view(mode=ROW)), FAKE, FAKE, FAKE, None) == DTYPE
+    assert L.tp_row_linear_backward(FAKE, 8, ctypes.byref(colv), FAKE, FAKE, FAKE, None) == MODE
+    assert L.tp_row_linear_backward(FAKE, -1, ctypes.byref(rowv), FAKE, FAKE, FAKE, None) == SHAPE
+    assert L.tp_row_linear_backward(FAKE, 8, ctypes.byref(rowv), None, FAKE, FAKE, None) == NULL
+    assert L.tp_row_linear_backward(None, 8, ctypes.byref(rowv), FAKE, FAKE, FAKE, None) == NULL  # dW needs Xs
+    assert L.tp_row_linear_backward(FAKE + 2, 8, ctypes.byref(rowv), FAKE, FAKE, FAKE, None) == ALIGN
+    assert L.tp_row_linear_backward(FAKE, 0, ctypes.byref(rowv), FAKE, FAKE, FAKE, None) == OK
+    # column layer
+    assert L.tp_column_linear_backward(FAKE, 8, ctypes.byref(rowv), FAKE, None, FAKE, FAKE, None, 0, None) == MODE
+    assert L.tp_column_linear_backward(FAKE, 8, ctypes.byref(colv), None, None, FAKE, FAKE, None, 0, None) == NULL
+    assert L.tp_column_linear_backward(FAKE, 8, ctypes.byref(colv), FAKE, None, FAKE, FAKE, FAKE, 16, None) == WORKSPACE
+    assert L.tp_column_linear_backward(FAKE, 0, ctypes.byref(colv), FAKE, None, FAKE, FAKE, None, 0, None) == OK
+    # MLP block
+    W1, W2 = view(K=128, N=256, mode=COL, dtype=BF16), view(K=256, N=128, mode=ROW, dtype=BF16)
+    need = L.tp_mlp_backward_workspace_bytes(8, 128, 256, 2, 4)
+    assert need > L.tp_mlp_backward_workspace_bytes(8, 128, 256, 2, 1) > 0
+    args = lambda act, Wu, U, ws_bytes, T=8: (FAKE, T, ctypes.byref(W1), Wu, ctypes.byref(W2), act, FAKE, U, FAKE,
+                                              FAKE, None, FAKE, ws_bytes, FAKE, FAKE, None, FAKE, None)
+    assert L.tp_mlp_backward(*args(9, None, None, need)) == MODE
+    assert L.tp_mlp_backward(*args(1, ctypes.byref(W1), None, need)) == MODE  # W_up without SwiGLU
+    assert L.tp_mlp_backward(*args(4, None, FAKE, need)) == NULL               # SwiGLU needs W_up
+    assert L.tp_mlp_backward(*args(4, ctypes.byref(W1), None, need)) == NULL  # and U
+    assert L.tp_mlp_backward(*args(4, ctypes.byref(W1), FAKE, need - 1)) == WORKSPACE
+    assert L.tp_mlp_backward(*args(4, ctypes.byref(W1), FAKE, need, T=0)) == OK
+
+
+def test_vocab_validation():
+    L = tpl.lib
+    assert L.tp_vocab_embedding(FAKE, 8, FAKE, 1000, 64, 3, BF16, FAKE, None) == SHAPE  # V % tp
+    assert L.tp_vocab_embedding(FAKE, 8, FAKE, 1024, 64, 4, 7, FAKE, None) == DTYPE
+    assert L.tp_vocab_embedding(None, 8, FAKE, 1024, 64, 4, BF16, FAKE, None) == NULL
+    assert L.tp_vocab_embedding(FAKE + 1, 8, FAKE, 1024, 64, 4, BF16, FAKE, None) == ALIGN
+    assert L.tp_vocab_embedding(FAKE, 0, FAKE, 1024, 64, 4, BF16, FAKE, None) == OK
+    need = L.tp_cross_entropy_workspace_bytes(16, 32000, 4)
+    assert need > 0
+    ce = lambda T, V, tp, dt, ws_bytes, labels=FAKE: L.tp_vocab_cross_entropy(
+        FAKE, labels, T, V, tp, dt, FAKE, None, None, ctypes.c_float(1.0), FAKE, ws_bytes, None)
+    assert ce(16, 32001, 4, BF16, need) == SHAPE
+    assert ce(16, 32000, 4, 9, need) == DTYPE
+    assert ce(16, 32000, 4, BF16, need - 1) == WORKSPACE
+    assert ce(16, 32000, 4, BF16, need, labels=None) == NULL
+    assert ce(0, 32000, 4, BF16, need) == OK
+
+
+def test_moe_validation():
+    L = tpl.lib
+    Wg, Wd = view(K=128, N=256, mode=COL, dtype=BF16), view(K=256, N=128, mode=ROW, dtype=BF16)
+    need = L.tp_moe_workspace_bytes(64, 128, 256, 2, 4, 2)
+    assert need > L.tp_moe_workspace_bytes(64, 128, 256, 1, 4, 2) > 0
+    moe = lambda T=64, k=2, E=4, g=Wg, d=Wd, ws=need, ids=FAKE: L.tp_moe_block(
+        FAKE, T, ids, FAKE, k, E, ctypes.byref(g), ctypes.byref(g), ctypes.byref(d), None, FAKE, ws, FAKE, None)
+    assert moe(g=view(K=128, N=256, mode=COL, dtype=F32), d=view(K=256, N=128, mode=ROW, dtype=F32)) == DTYPE
+    assert moe(d=view(K=256, N=256, mode=ROW, dtype=BF16)) == SHAPE  # down does not match gate/up
+    assert moe(E=0) == SHAPE
+    assert moe(k=0) == SHAPE
+    assert moe(E=2000) == SHAPE
+    assert moe(ws=need - 1) == WORKSPACE
+    assert moe(ids=None) == NULL
+    assert moe(T=0) == OK
