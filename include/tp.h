@@ -63,7 +63,7 @@ enum {
   TP_ERR_WORKSPACE = 6,   /* workspace or output buffer too small */
   TP_ERR_CUDA = 7,        /* a CUDA runtime/driver call failed */
   TP_ERR_TIMEOUT = 8,     /* a bounded device-side wait expired */
-  TP_ERR_UNSUPPORTED = 9, /* valid request outside this build's limits */
+  TP_ERR_UNSUPPORTED = 9, /* valid request outside the library's limits */
   TP_ERR_INDEX = 10       /* (from tp_get_error) a token id or label outside [0, V) */
 };
 

@@ -499,7 +499,7 @@ def test_planted_transposed_operand_is_caught(monkeypatch):
 
 
 # ---------------------------------------------------------------------------
-# 11. Property tests over random shapes (Hypothesis), brute force as the judge
+# 11. Property tests over random shapes (Hypothesis), checked by brute force
 # ---------------------------------------------------------------------------
 from hypothesis import given, settings, strategies as st  # noqa: E402
 
