@@ -320,10 +320,12 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(files=None) -> str:
+    """sha256 prefix over the named csrc files (all of them by default), so
+    that a change to one kernel's sources leaves the others' records valid."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_transformer_linear_tma_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files is not None else os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -331,14 +333,15 @@ def kernel_source_sha() -> str:
 
 def ncu_traffic(kernel: str, workload: str, T: int):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources and at this token count (null otherwise)."""
+    the current sources of that kernel (the files its record lists) and at
+    this token count (null otherwise)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(f"{workload}:{kernel}")
-    if not e or e.get("source_sha") != kernel_source_sha() or e.get("T") != T:
+    if not e or e.get("source_sha") != kernel_source_sha(e.get("source_files")) or e.get("T") != T:
         return None
     return e.get("dram_bytes_per_launch")
 
