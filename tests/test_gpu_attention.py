@@ -66,6 +66,22 @@ def test_attention_core(tp, T, hq, hkv, causal):
                         f"attention tp={tp} T={T} causal={causal}")
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_growing_keys_move_the_exponent_base(causal):
+    """Key rows scaled by 1 + t/40, so that the scores of later key blocks
+    exceed the running base by more than 2^8 and O is rescaled in TMEM after
+    the first block of each key-block parity (T = 700: six blocks, the last
+    ragged)."""
+    tp, T, hq, hkv, hd = 1, 700, 2, 1, 128
+    qkv = qkv_input(341, tp, T, hq, hkv)
+    k0 = hq * hd
+    qkv[:, :, k0:k0 + hd] *= (1.0 + np.arange(T) / 40.0)[None, :, None]
+    S.to_bf16_inplace(qkv)  # the kernel's inputs, exactly
+    ctx = tpl.tp_attention(dev(qkv), hq, hkv, hd, causal=causal)
+    assert tpl.tp_get_error() == 0
+    assert_close_stored(ctx, oracle_ctx(qkv, hq, hkv, hd, causal), TOL_BF16, f"growing keys causal={causal}")
+
+
 def test_attention_single_token_is_v():
     """One token: the softmax weight is exactly 1, so the context is V."""
     qkv = qkv_input(311, 2, 1, 4, 2)
