@@ -687,6 +687,7 @@ int attention_launch(const void* qkv, int64_t T, int tp, int hq, int hkv, int mo
   a.group = hq / hkv;
   a.causal = mode == TP_ATTN_CAUSAL ? 1 : 0;
   a.q_blocks = static_cast<int>(cdiv(T, 128));
+  a.units = tp * nq * a.q_blocks;
   a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(tpk::AT_HD)));
   static bool attr_done[128] = {};
   int dev = 0;
@@ -698,7 +699,8 @@ int attention_launch(const void* qkv, int64_t T, int tp, int hq, int hkv, int mo
     attr_done[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(tp) * nq * a.q_blocks));
+  // persistent: one CTA per SM (each holds all of its SM's TMEM), none idle
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min(a.units, std::max(1, num_sms()))));
   cfg.blockDim = dim3(tpk::AT_THREADS);
   cfg.dynamicSmemBytes = tpk::AT_SMEM;
   cfg.stream = st;
@@ -1062,6 +1064,8 @@ int attn_block_impl(const void* X, int64_t T, const tp_shards* Wqkv, const tp_sh
   if (Wqkv->K > static_cast<int64_t>(hq) * hd * 4) return TP_ERR_UNSUPPORTED;  // scratch sizing bound
   if (mode != TP_ATTN_SINGLE_KEY && mode != TP_ATTN_CAUSAL && mode != TP_ATTN_FULL) return TP_ERR_MODE;
   if (mode != TP_ATTN_SINGLE_KEY && (dt != TP_BF16 || hd != tpk::AT_HD)) return TP_ERR_UNSUPPORTED;
+  if (mode != TP_ATTN_SINGLE_KEY && static_cast<int64_t>(hq) * cdiv(T, 128) > INT32_MAX / 2)
+    return TP_ERR_UNSUPPORTED;  // the core counts its work units in int
   if (ws_bytes < tp_attn_workspace_bytes(T, hq, hkv, hd, tp, dt)) return TP_ERR_WORKSPACE;
   if (T == 0) return TP_OK;
   const cudaStream_t st = as_stream(stream);
@@ -1123,7 +1127,9 @@ int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, in
   if (mode != TP_ATTN_CAUSAL && mode != TP_ATTN_FULL) return TP_ERR_MODE;
   if (T < 0 || tp < 1 || hq < 1 || hkv < 1 || hd < 1 || tp_qkv_shard_elems(1, hq, hkv, hd, tp) == 0)
     return TP_ERR_SHAPE;
-  if (hd != tpk::AT_HD || T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  // (work units, one per shard, q head and 128 queries, are counted in int)
+  if (hd != tpk::AT_HD || T > INT32_MAX || static_cast<int64_t>(hq) * cdiv(T, 128) > INT32_MAX / 2)
+    return TP_ERR_UNSUPPORTED;
   if (!ptr_ok(qkv, TP_BF16) || !ptr_ok(ctx, TP_BF16)) return TP_ERR_ALIGN;
   if (T == 0) return TP_OK;
   return attention_launch(qkv, T, tp, hq, hkv, mode, ctx, as_stream(stream));

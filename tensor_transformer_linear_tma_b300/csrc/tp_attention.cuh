@@ -4,8 +4,13 @@
 // attention heads; tutorial page, self-attention block sharding), causal
 // (query t sees keys 0..t) or unmasked.
 //
-// One CTA per (shard, q head, block of 128 queries), head size 128, 320
-// threads:
+// Work units are (shard, q head, block of 128 queries), head size 128. The
+// kernel is persistent: one CTA per SM (all of TMEM is allocated) walks its
+// units, the longest (latest, under the causal mask) first, in alternating
+// directions from wave to wave. Within a CTA the ring, the score buffers and
+// their barriers run on across units, so the next unit's Q, K and V tiles
+// are loaded, and its first scores computed, while the softmax warps write
+// the last unit's output. 320 threads:
 //   warp 0      TMA producer: the Q tile once, then the K and V tiles of
 //               each block of 128 keys through a ring of six 32 KB slots (a
 //               K slot is released as soon as Q K^T has read it, a V slot
@@ -20,8 +25,11 @@
 //               traffic against staging Q and P there;
 //   warps 2..9  softmax, two threads per query row (warps w and w+4 share
 //               a TMEM lane quadrant; each takes 64 of the block's 128
-//               keys and the matching 64 output columns). They first copy
-//               Q from its TMA tile into TMEM. Per key block: scores from
+//               keys and the matching 64 output columns). They copy each
+//               unit's Q from its TMA tile into TMEM, the next unit's as
+//               soon as the last scores of the current one are in (every
+//               S MMA that read the old Q is then complete), before they
+//               write the current unit's output. Per key block: scores from
 //               TMEM, online maximum (exchanged between the two halves of a
 //               row through shared memory) and sum in fp32, exp2 with the
 //               log2(e)/sqrt(hd) scale folded into one FFMA, P packed to
@@ -70,6 +78,7 @@ struct AttnArgs {
   int T, tp, hq, hkv, nq, nkv, group;
   int causal;
   int q_blocks;        // ceil(T / 128)
+  int units;           // tp * nq * q_blocks work units; the grid has at most this many CTAs
   float scale_log2;    // log2(e) / sqrt(hd)
 };
 
@@ -86,6 +95,37 @@ constexpr float AT_RESCALE_LOG2 = 8.0f;            // move the exponent base onl
 // TMEM columns (512 allocated): two score buffers, O, Q as packed bf16
 constexpr uint32_t AT_TM_S = 0, AT_TM_O = 256, AT_TM_Q = 384;
 
+// The w-th unit of CTA c in a grid of g CTAs, or -1 past its last one.
+// Units are numbered longest first; wave w covers units w*g .. w*g + g - 1,
+// taken in reverse on odd waves, which keeps every CTA's total within a
+// unit's length of the mean.
+__device__ __forceinline__ int at_unit(int c, int g, int w, int units) {
+  const int u = w * g + ((w & 1) ? g - 1 - c : c);
+  return u < units ? u : -1;
+}
+
+struct AtUnit {
+  int qb, s, j;          // query block, shard, q head within the shard
+  int qcol, kcol, vcol;  // columns of its q, k and v head in the shard's qkv rows
+  int nkb;               // key blocks its queries see
+};
+
+__device__ __forceinline__ AtUnit at_decode(const AttnArgs& a, int u) {
+  AtUnit w;
+  const int heads = a.tp * a.nq;
+  w.qb = a.q_blocks - 1 - u / heads;
+  const int hh = u % heads;
+  w.s = hh / a.nq;
+  w.j = hh % a.nq;
+  const int kv0 = a.hkv >= a.tp ? w.s * a.nkv : (w.s * a.hkv) / a.tp;
+  const int kvi = (w.s * a.nq + w.j) / a.group - kv0;  // the kv head within the shard's block
+  w.qcol = w.j * AT_HD;
+  w.kcol = (a.nq + kvi) * AT_HD;
+  w.vcol = (a.nq + a.nkv + kvi) * AT_HD;
+  w.nkb = a.causal ? w.qb + 1 : a.q_blocks;
+  return w;
+}
+
 __global__ void __launch_bounds__(AT_THREADS, 1)
     tp_attn_kernel(const __grid_constant__ CUtensorMap mapQKV, const AttnArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -94,13 +134,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* ring = smem + AT_TILE;  // [AT_SLOTS]: K(j) is item 2j, V(j) item 2j+1
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (1 + AT_SLOTS) * AT_TILE);
-  uint64_t* q_full = bars;                // TMA -> softmax (Q tile landed)
-  uint64_t* q_tm = bars + 1;              // softmax -> MMA (Q copied into TMEM)
-  uint64_t* r_full = bars + 2;            // [AT_SLOTS] TMA -> MMA
+  uint64_t* q_full = bars;                // TMA -> softmax (a unit's Q tile landed)
+  uint64_t* q_tm = bars + 1;              // softmax -> MMA, TMA (that Q copied into TMEM; its tile free)
+  uint64_t* o_free = bars + 2;            // softmax -> MMA (a unit's O read out)
+  uint64_t* r_full = bars + 3;            // [AT_SLOTS] TMA -> MMA
   uint64_t* r_empty = r_full + AT_SLOTS;  // [AT_SLOTS] MMA -> TMA
-  uint64_t* s_full = r_empty + AT_SLOTS;  // [2] MMA -> softmax
+  uint64_t* s_full = r_empty + AT_SLOTS;  // [2] MMA -> softmax (S of block gb in buffer gb & 1)
   uint64_t* p_full = s_full + 2;          // [2] softmax -> MMA (P stored, O rescaled)
-  uint64_t* o_done = p_full + 2;          // [2] MMA -> softmax (P V of block j complete, buffer j & 1)
+  uint64_t* o_done = p_full + 2;          // [2] MMA -> softmax (P V of block gb complete, barrier gb & 1)
   uint64_t* drain = o_done + 2;           // abort path only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   float* xrow = reinterpret_cast<float*>(smem + (1 + AT_SLOTS) * AT_TILE + 512);
@@ -116,20 +157,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     return;
   }
 
-  // work unit; the longest (latest, under the causal mask) query blocks first
-  const int heads = a.tp * a.nq;
-  const int qb = a.q_blocks - 1 - static_cast<int>(blockIdx.x) / heads;
-  const int hh = static_cast<int>(blockIdx.x) % heads;
-  const int s = hh / a.nq, j = hh % a.nq;
-  const int kv0 = a.hkv >= a.tp ? s * a.nkv : (s * a.hkv) / a.tp;
-  const int kvi = (s * a.nq + j) / a.group - kv0;  // the kv head within the shard's block
-  const int qcol = j * AT_HD, kcol = (a.nq + kvi) * AT_HD, vcol = (a.nq + a.nkv + kvi) * AT_HD;
-  const int q0 = qb * AT_ROWS;
-  const int nkb = a.causal ? qb + 1 : (a.T + AT_ROWS - 1) / AT_ROWS;
+  const int cta = static_cast<int>(blockIdx.x), grid = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_tm, 8);
+    mbar_init(o_free, 8);
     for (int i = 0; i < AT_SLOTS; ++i) {
       mbar_init(&r_full[i], 1);
       mbar_init(&r_empty[i], 1);
@@ -158,28 +191,42 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------ TMA producer ------------------------------
+      // Per unit: its Q tile (once the last unit's Q has been copied out of
+      // the tile), then its K and V tiles through the ring.
       uint32_t issued = 0, issued_ph = 0;  // per slot: a copy was started, its phase
+      int it = 0;                          // ring items of all units so far
+      int q_loads = 0;
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, AT_TILE);
-      tma_load_3d(sQ, &mapQKV, q_full, qcol, q0, s);
-      tma_load_3d(sQ + AT_PANEL, &mapQKV, q_full, qcol + 64, q0, s);
-      for (int it = 0; it < 2 * nkb; ++it) {  // K(j), V(j), K(j+1), ...
-        const int slot = it % AT_SLOTS;
-        const uint32_t ph = static_cast<uint32_t>(it / AT_SLOTS) & 1u;
-        if (!mbar_wait(&r_empty[slot], ph ^ 1u, abort_flag)) {
+      for (int w = 0; ok; ++w) {
+        const int u = at_unit(cta, grid, w, a.units);
+        if (u < 0) break;
+        const AtUnit wu = at_decode(a, u);
+        if (w > 0 && !mbar_wait(q_tm, static_cast<uint32_t>(w - 1) & 1u, abort_flag)) {
           ok = false;
           break;
         }
-        const int col = (it & 1) ? vcol : kcol;
-        uint8_t* dst = ring + slot * AT_TILE;
-        mbar_arrive_expect_tx(&r_full[slot], AT_TILE);
-        tma_load_3d(dst, &mapQKV, &r_full[slot], col, (it >> 1) * AT_ROWS, s);
-        tma_load_3d(dst + AT_PANEL, &mapQKV, &r_full[slot], col + 64, (it >> 1) * AT_ROWS, s);
-        issued |= 1u << slot;
-        issued_ph = (issued_ph & ~(1u << slot)) | (ph << slot);
+        mbar_arrive_expect_tx(q_full, AT_TILE);
+        tma_load_3d(sQ, &mapQKV, q_full, wu.qcol, wu.qb * AT_ROWS, wu.s);
+        tma_load_3d(sQ + AT_PANEL, &mapQKV, q_full, wu.qcol + 64, wu.qb * AT_ROWS, wu.s);
+        ++q_loads;
+        for (int i = 0; i < 2 * wu.nkb; ++i, ++it) {  // K(j), V(j), K(j+1), ...
+          const int slot = it % AT_SLOTS;
+          const uint32_t ph = static_cast<uint32_t>(it / AT_SLOTS) & 1u;
+          if (!mbar_wait(&r_empty[slot], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int col = (i & 1) ? wu.vcol : wu.kcol;
+          uint8_t* dst = ring + slot * AT_TILE;
+          mbar_arrive_expect_tx(&r_full[slot], AT_TILE);
+          tma_load_3d(dst, &mapQKV, &r_full[slot], col, (i >> 1) * AT_ROWS, wu.s);
+          tma_load_3d(dst + AT_PANEL, &mapQKV, &r_full[slot], col + 64, (i >> 1) * AT_ROWS, wu.s);
+          issued |= 1u << slot;
+          issued_ph = (issued_ph & ~(1u << slot)) | (ph << slot);
+        }
       }
       if (!ok) {  // let every copy this block started land before it exits
-        mbar_wait_drain(q_full, 0);
+        if (q_loads > 0) mbar_wait_drain(q_full, static_cast<uint32_t>(q_loads - 1) & 1u);
         for (int i = 0; i < AT_SLOTS; ++i)
           if ((issued >> i) & 1u) mbar_wait_drain(&r_full[i], (issued_ph >> i) & 1u);
       }
@@ -196,15 +243,18 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
     };
-    bool ok = wait_all(q_tm, 0), issued_any = false;
-    if (ok) tc_fence_after();
-    // S(jb) = Q K(jb)^T: M = 128 queries, N = 128 keys, K = hd in 8 steps
-    // of 16 (Q: 8 TMEM columns a step; K: two 64-wide panels, +32 bytes a
-    // step inside a panel; descriptor start addresses count 16-byte units).
-    // The caller has waited for K(jb).
-    auto issue_s = [&](int jb) {
-      const int st = jb & 1;
-      const int slot = (2 * jb) % AT_SLOTS;
+    bool ok = true, issued_any = false;
+    // Block gb counts the key blocks of all this CTA's units so far: it
+    // picks the score buffer (gb & 1) and the phases of its barriers. Ring
+    // item `item` holds a K tile (S) or a V tile (P V).
+    //
+    // S(gb) = Q K^T: M = 128 queries, N = 128 keys, K = hd in 8 steps of 16
+    // (Q: 8 TMEM columns a step; K: two 64-wide panels, +32 bytes a step
+    // inside a panel; descriptor start addresses count 16-byte units). The
+    // caller has waited for the K tile.
+    auto issue_s = [&](int gb, int item) {
+      const int st = gb & 1;
+      const int slot = item % AT_SLOTS;
       const uint64_t kd = ring_k + static_cast<uint64_t>((slot * AT_TILE) >> 4);
       const uint32_t tS = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128);
 #pragma unroll
@@ -213,49 +263,63 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                             kd + static_cast<uint64_t>(((k >> 2) * AT_PANEL + (k & 3) * 32) >> 4), idesc_s,
                             k > 0 ? 1u : 0u);
       tc_commit_warp(&s_full[st]);
-      tc_commit_warp(&r_empty[slot]);  // K(jb) read
+      tc_commit_warp(&r_empty[slot]);  // K read
       issued_any = true;
     };
-    // O += P(jb) V(jb): M = 128 queries, N = hd, K = 128 keys in 8 steps;
-    // P sits in TMEM (keys 0..63 at score columns 0..31 of its buffer,
-    // keys 64..127 at 64..95), V is MN-major (rows = keys, each row 64 hd
-    // values; the second 64 hd values one panel further). The caller has
-    // waited for V(jb) and P(jb).
-    auto issue_pv = [&](int jb) {
-      const int st = jb & 1;
-      const int slot = (2 * jb + 1) % AT_SLOTS;
+    // O (+)= P(gb) V: M = 128 queries, N = hd, K = 128 keys in 8 steps; P
+    // sits in TMEM (keys 0..63 at score columns 0..31 of its buffer, keys
+    // 64..127 at 64..95), V is MN-major (rows = keys, each row 64 hd values;
+    // the second 64 hd values one panel further). A unit's first block
+    // overwrites O. The caller has waited for the V tile and P.
+    auto issue_pv = [&](int gb, int item, bool first) {
+      const int st = gb & 1;
+      const int slot = item % AT_SLOTS;
       const uint32_t tP = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128);
       const uint64_t vd = ring_mn + static_cast<uint64_t>((slot * AT_TILE) >> 4);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
         tc_mma_bf16_ts_warp(tO, tP + static_cast<uint32_t>((k >> 2) * 64 + (k & 3) * 8),
-                            vd + static_cast<uint64_t>((k * 16 * 128) >> 4), idesc_o, (jb > 0 || k > 0) ? 1u : 0u);
+                            vd + static_cast<uint64_t>((k * 16 * 128) >> 4), idesc_o, (!first || k > 0) ? 1u : 0u);
       tc_commit_warp(&o_done[st]);
-      tc_commit_warp(&r_empty[slot]);  // V(jb) read
+      tc_commit_warp(&r_empty[slot]);  // V read
     };
-    auto wait_item = [&](int it) {  // ring item it (K(j) = 2j, V(j) = 2j + 1) landed
-      return wait_all(&r_full[it % AT_SLOTS], static_cast<uint32_t>(it / AT_SLOTS) & 1u);
+    auto wait_item = [&](int item) {
+      return wait_all(&r_full[item % AT_SLOTS], static_cast<uint32_t>(item / AT_SLOTS) & 1u);
     };
-    // S(0) and S(1) fill both score buffers; then, per block, P(jb) V and
-    // S(jb + 2) are issued back to back as soon as the softmax hands over
-    // P(jb): S(jb + 2) reuses P(jb)'s buffer, and the tensor core runs them in
-    // issue order. The ring waits come before the wait for P, off the path
-    // from the softmax to the tensor core.
-    for (int jb = 0; ok && jb < 2 && jb < nkb; ++jb) {
-      ok = wait_item(2 * jb);
-      if (ok) {
-        tc_fence_after();
-        issue_s(jb);
+    // Per unit: once its Q is in TMEM, S(0) and S(1) fill both score
+    // buffers (right behind the last unit's final P V, which the tensor
+    // core runs first); then, per block, P(jb) V and S(jb + 2) are issued
+    // back to back as soon as the softmax hands over P(jb): S(jb + 2) reuses
+    // P(jb)'s buffer, and the tensor core runs them in issue order. The
+    // ring waits come before the wait for P, off the path from the softmax
+    // to the tensor core. The unit's first P V also waits until the softmax
+    // has read the last unit's O out of TMEM.
+    int it0 = 0, g0 = 0;  // ring items and key blocks of the earlier units
+    for (int w = 0; ok; ++w) {
+      const int u = at_unit(cta, grid, w, a.units);
+      if (u < 0) break;
+      const int nkb = at_decode(a, u).nkb;
+      ok = wait_all(q_tm, static_cast<uint32_t>(w) & 1u);
+      for (int jb = 0; ok && jb < 2 && jb < nkb; ++jb) {
+        ok = wait_item(it0 + 2 * jb);
+        if (ok) {
+          tc_fence_after();
+          issue_s(g0 + jb, it0 + 2 * jb);
+        }
       }
-    }
-    for (int jb = 0; ok && jb < nkb; ++jb) {
-      const bool next = jb + 2 < nkb;
-      ok = wait_item(2 * jb + 1) && (!next || wait_item(2 * jb + 4)) &&
-           wait_all(&p_full[jb & 1], static_cast<uint32_t>(jb >> 1) & 1u);
-      if (!ok) break;
-      tc_fence_after();
-      issue_pv(jb);
-      if (next) issue_s(jb + 2);
+      for (int jb = 0; ok && jb < nkb; ++jb) {
+        const bool next = jb + 2 < nkb;
+        const int gb = g0 + jb;
+        ok = wait_item(it0 + 2 * jb + 1) && (!next || wait_item(it0 + 2 * jb + 4)) &&
+             wait_all(&p_full[gb & 1], static_cast<uint32_t>(gb >> 1) & 1u) &&
+             (jb > 0 || w == 0 || wait_all(o_free, static_cast<uint32_t>(w - 1) & 1u));
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(gb, it0 + 2 * jb + 1, jb == 0);
+        if (next) issue_s(gb + 2, it0 + 2 * jb + 4);
+      }
+      it0 += 2 * nkb;
+      g0 += nkb;
     }
     if (!ok && issued_any) {  // wait for MMAs in flight before TMEM is freed
       tc_commit_warp(drain);
@@ -266,18 +330,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int q = warp & 3;            // TMEM lane quadrant
     const int half = (warp - 2) >> 2;  // which 64 keys / output columns of the row
     const int r = q * 32 + lane;       // query row within the block
-    const int t = q0 + r;              // query index
     const int c0 = half * 64;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t tO = tmem_base + AT_TM_O + lane_off + static_cast<uint32_t>(c0);
-    const int kmax = a.causal ? min(t, a.T - 1) : a.T - 1;  // last key this query sees
-    float m = -INFINITY;  // exponent base, in log2 units of the scaled scores
-    float l = 0.0f;       // this half's share of the row sum
-    // Q into TMEM: this thread's row, hd values 64 * half .. + 63, read from
-    // the 128-byte-swizzled TMA tile
-    const bool q_ok = mbar_wait(q_full, 0, abort_flag);
-    bool ok = !pair_any(q, !q_ok || *abort_flag);
-    if (ok) {
+    // Q of unit w into TMEM: this thread's row, hd values 64 * half .. + 63,
+    // read from the 128-byte-swizzled TMA tile. Returns false (for both
+    // warps of the quadrant) if the wait gave up.
+    auto copy_q = [&](int w) -> bool {
+      const bool q_ok = mbar_wait(q_full, static_cast<uint32_t>(w) & 1u, abort_flag);
+      if (pair_any(q, !q_ok || *abort_flag)) return false;
       const uint8_t* qrow = sQ + half * AT_PANEL + r * 128;
       uint32_t rr[32];
 #pragma unroll
@@ -293,130 +354,162 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_tm);
-    }
-    for (int jb = 0; ok && jb < nkb; ++jb) {
-      const int st = jb & 1;
-      const uint32_t ph = static_cast<uint32_t>(jb >> 1) & 1u;
-      // (a wait that gave up leaves garbage in the scores, which the vote at
-      // the exchange below discards)
-      const bool waited = mbar_wait(&s_full[st], ph, abort_flag);
-      tc_fence_after();
-      float sv[64];
-      const uint32_t tS = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128 + c0) + lane_off;
-#pragma unroll
-      for (int c = 0; c < 64; c += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tS + static_cast<uint32_t>(c), rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[c + i] = __uint_as_float(rr[i]);
-      }
-      tmem_ld_wait();
-      const int kbase = jb * AT_ROWS + c0;
-      // only the diagonal block (causal) and a ragged last block need a mask
-      if ((a.causal && jb == qb) || jb * AT_ROWS + AT_ROWS > a.T) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (kbase + i > kmax) sv[i] = -INFINITY;
-      }
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
-#pragma unroll
-      for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      // the row's other half: exchange the maxima, in one of two slots by
-      // block parity (the partner's write two blocks on comes after the next
-      // exchange, which this thread reaches only after this read); the
-      // barrier also takes both halves out together if a wait gave up
-      float* xr = xrow + (jb & 1) * 256;
-      xr[half * 128 + r] = mx;
-      if (pair_any(q, !waited || *abort_flag)) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, xr[(half ^ 1) * 128 + r]);
-      const float m_cand = mx * a.scale_log2;  // the scale is positive: same order
-      bool rescale = false;
-      float alpha = 1.0f;
-      if (m_cand > m + AT_RESCALE_LOG2) {  // also the first visible block (m = -inf)
-        alpha = ex2_approx(m - m_cand);    // 0 on the first block
-        rescale = jb > 0;
-        m = m_cand;
-        l *= alpha;
-      }
-      float sum8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        sv[i] = ex2_approx(fmaf(sv[i], a.scale_log2, -m));
-        sum8[i & 7] += sv[i];
-      }
-      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      if (__any_sync(0xffffffffu, rescale)) {
-        // the base moved: once P V of block jb - 1 is done, this half's 64
-        // columns of O are rescaled. A wait that gives up (the abort flag is
-        // then set) skips the rescale; the next exchange takes both halves
-        // of the row out of the loop together.
-        const bool done = mbar_wait(&o_done[st ^ 1], static_cast<uint32_t>((jb - 1) >> 1) & 1u, abort_flag);
-        if (__all_sync(0xffffffffu, done)) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 64; c += 32) {
-            uint32_t rr[32];
-            tmem_ld32(tO + static_cast<uint32_t>(c), rr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            tmem_st32(tO + static_cast<uint32_t>(c), rr);
-          }
-        }
-      }
-      // this half's 64 P values as bf16 pairs over its first 32 score columns
-      // (already read into registers)
-      {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
-        tmem_st32(tS, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[st]);
-    }
-    // ok is uniform over the two warps of a quadrant
-    if (ok) {
-      // (S(nkb - 1) was issued after P V of block nkb - 3, so the barrier of
-      // block nkb - 1 is at most one phase behind: its parity is unambiguous)
-      const int last = nkb - 1;
-      const bool done = mbar_wait(&o_done[last & 1], static_cast<uint32_t>(last >> 1) & 1u, abort_flag);
-      // the row sum is the two halves' shares (same exponent base)
-      float* xr = xrow + (nkb & 1) * 256;
-      xr[half * 128 + r] = l;
-      if (!pair_any(q, !done || *abort_flag)) {
-        l += xr[(half ^ 1) * 128 + r];
+      return true;
+    };
+    // (the grid has no more CTAs than units, so every CTA has a first one)
+    bool ok = copy_q(0);
+    int g0 = 0;  // key blocks of the earlier units
+    for (int w = 0; ok; ++w) {
+      const int u = at_unit(cta, grid, w, a.units);
+      if (u < 0) break;
+      const AtUnit wu = at_decode(a, u);
+      const int nkb = wu.nkb, qb = wu.qb;
+      const int t = qb * AT_ROWS + r;                         // query index
+      const int kmax = a.causal ? min(t, a.T - 1) : a.T - 1;  // last key this query sees
+      float m = -INFINITY;  // exponent base, in log2 units of the scaled scores
+      float l = 0.0f;       // this half's share of the row sum
+      for (int jb = 0; ok && jb < nkb; ++jb) {
+        const int gb = g0 + jb;  // block count over this CTA's units: buffer and phases
+        const int st = gb & 1;
+        const uint32_t ph = static_cast<uint32_t>(gb >> 1) & 1u;
+        // (a wait that gave up leaves garbage in the scores, which the vote at
+        // the exchange below discards)
+        const bool waited = mbar_wait(&s_full[st], ph, abort_flag);
         tc_fence_after();
-        const float inv = 1.0f / l;
-        const int nc = a.nq * AT_HD;
-        __nv_bfloat16* out = a.ctx + (static_cast<size_t>(s) * a.T + t) * nc + j * AT_HD + c0;
-#pragma unroll 1
+        float sv[64];
+        const uint32_t tS = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128 + c0) + lane_off;
+#pragma unroll
         for (int c = 0; c < 64; c += 32) {
           uint32_t rr[32];
-          tmem_ld32(tO + static_cast<uint32_t>(c), rr);
-          tmem_ld_wait();
-          if (t < a.T) {
+          tmem_ld32(tS + static_cast<uint32_t>(c), rr);
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              float v[8];
+          for (int i = 0; i < 32; ++i) sv[c + i] = __uint_as_float(rr[i]);
+        }
+        tmem_ld_wait();
+        const int kbase = jb * AT_ROWS + c0;
+        // only the diagonal block (causal) and a ragged last block need a mask
+        if ((a.causal && jb == qb) || jb * AT_ROWS + AT_ROWS > a.T) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(rr[i + e]) * inv;
-              store_bf16x8_f(out + c + i, v);
+          for (int i = 0; i < 64; ++i)
+            if (kbase + i > kmax) sv[i] = -INFINITY;
+        }
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+        for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
+        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        // the row's other half: exchange the maxima, in one of two slots by
+        // block parity (the partner's write two blocks on comes after the next
+        // exchange, which this thread reaches only after this read); the
+        // barrier also takes both halves out together if a wait gave up
+        float* xr = xrow + st * 256;
+        xr[half * 128 + r] = mx;
+        if (pair_any(q, !waited || *abort_flag)) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, xr[(half ^ 1) * 128 + r]);
+        const float m_cand = mx * a.scale_log2;  // the scale is positive: same order
+        bool rescale = false;
+        float alpha = 1.0f;
+        if (m_cand > m + AT_RESCALE_LOG2) {  // also the first visible block (m = -inf)
+          alpha = ex2_approx(m - m_cand);    // 0 on the first block
+          rescale = jb > 0;
+          m = m_cand;
+          l *= alpha;
+        }
+        float sum8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          sv[i] = ex2_approx(fmaf(sv[i], a.scale_log2, -m));
+          sum8[i & 7] += sv[i];
+        }
+        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        if (__any_sync(0xffffffffu, rescale)) {
+          // the base moved: once P V of block jb - 1 is done, this half's 64
+          // columns of O are rescaled. A wait that gives up (the abort flag is
+          // then set) skips the rescale; the next exchange takes both halves
+          // of the row out of the loop together.
+          const bool done = mbar_wait(&o_done[st ^ 1], static_cast<uint32_t>((gb - 1) >> 1) & 1u, abort_flag);
+          if (__all_sync(0xffffffffu, done)) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 64; c += 32) {
+              uint32_t rr[32];
+              tmem_ld32(tO + static_cast<uint32_t>(c), rr);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+              tmem_st32(tO + static_cast<uint32_t>(c), rr);
             }
           }
         }
+        // this half's 64 P values as bf16 pairs over its first 32 score columns
+        // (already read into registers)
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
+          tmem_st32(tS, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[st]);
       }
+      // ok is uniform over the two warps of a quadrant
+      const int gl = g0 + nkb - 1;  // the unit's last block
+      g0 += nkb;
+      if (!ok) break;
+      // The next unit's Q into TMEM now: every S MMA of this unit is complete
+      // (its last scores are in), so the next unit's first scores are computed
+      // while this unit's output is written.
+      if (at_unit(cta, grid, w + 1, a.units) >= 0 && !copy_q(w + 1)) {
+        ok = false;
+        break;
+      }
+      // (S(gl) was issued after P V of block gl - 2, so the barrier of block
+      // gl is at most one phase behind: its parity is unambiguous)
+      const bool done = mbar_wait(&o_done[gl & 1], static_cast<uint32_t>(gl >> 1) & 1u, abort_flag);
+      // The row sum is the two halves' shares (same exponent base), exchanged
+      // in the slot that the next block's maxima use; the second barrier keeps
+      // those out until both halves have read.
+      float* xr = xrow + ((gl + 1) & 1) * 256;
+      xr[half * 128 + r] = l;
+      if (pair_any(q, !done || *abort_flag)) {
+        ok = false;
+        break;
+      }
+      l += xr[(half ^ 1) * 128 + r];
+      pair_any(q, false);
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      const int nc = a.nq * AT_HD;
+      __nv_bfloat16* out = a.ctx + (static_cast<size_t>(wu.s) * a.T + t) * nc + wu.j * AT_HD + c0;
+#pragma unroll 1
+      for (int c = 0; c < 64; c += 32) {
+        uint32_t rr[32];
+        tmem_ld32(tO + static_cast<uint32_t>(c), rr);
+        tmem_ld_wait();
+        if (t < a.T) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(rr[i + e]) * inv;
+            store_bf16x8_f(out + c + i, v);
+          }
+        }
+      }
+      // O is read out (each load waited for): the next unit's first P V may
+      // overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
     }
   }
 

@@ -55,10 +55,12 @@ def oracle_ctx(qkv, hq, hkv, hd, causal, rows=None):
 
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("tp,T,hq,hkv", [(1, 128, 1, 1), (2, 200, 4, 2), (4, 384, 8, 2), (2, 1, 2, 2),
-                                         (2, 300, 4, 4)])
+                                         (2, 300, 4, 4), (16, 1100, 32, 8)])
 def test_attention_core(tp, T, hq, hkv, causal):
-    """Several key blocks, a ragged last block (200, 300), replicated kv heads
-    (tp 4 with 2 kv heads), a single token."""
+    """Several key blocks, a ragged last block (200, 300, 1100), replicated kv
+    heads (tp 4 with 2 kv heads), a single token, and more work units
+    (shard, q head, query block) than SMs (16 x 2 x 9 = 288), so that each
+    CTA of the persistent kernel runs several units of different lengths."""
     qkv = qkv_input(301 + T, tp, T, hq, hkv)
     ctx = tpl.tp_attention(dev(qkv), hq, hkv, 128, causal=causal)
     assert tpl.tp_get_error() == 0
