@@ -128,8 +128,17 @@ def _out_dtype(default, out=None, residual=None, out_dtype=None):
 
 
 def _ptr(t):
+    """Device address of a tensor. The library takes pointers into the
+    current CUDA device's memory and launches on that device, so a host
+    tensor, or one on another device, is refused here rather than handed to
+    a kernel."""
     if t is None:
         return None
+    if t.device.type != "cuda":
+        raise ValueError(f"tensors must be in CUDA device memory (got one on {t.device})")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensors must be on the current CUDA device "
+                         f"(cuda:{torch.cuda.current_device()}), got one on {t.device}")
     if not t.is_contiguous():
         raise ValueError("tensors must be contiguous")
     return t.data_ptr()

@@ -259,3 +259,37 @@ def test_moe_validation():
     assert moe(ws=need - 1) == WORKSPACE
     assert moe(ids=None) == NULL
     assert moe(T=0) == OK
+
+
+def test_attention_validation():
+    """The attention core's checks, in the order the entry point runs them,
+    none of which reaches a launch."""
+    L = tpl.lib
+    att = lambda qkv=FAKE, T=8, tp=2, hq=4, hkv=2, hd=128, mode=1, ctx=FAKE: L.tp_attention(
+        qkv, T, tp, hq, hkv, hd, mode, ctx, None)
+    assert att(qkv=None) == NULL
+    assert att(ctx=None) == NULL
+    assert att(mode=0) == MODE        # the single-key stand-in is not a core mode
+    assert att(mode=3) == MODE
+    assert att(hq=3) == SHAPE         # 3 q heads over 2 shards
+    assert att(T=-1) == SHAPE
+    assert att(hd=64, hq=4, hkv=2) == UNSUP
+    assert att(T=2 ** 31) == UNSUP
+    # work units (shard, q head, block of 128 queries) past the kernel's int range
+    assert att(T=2 ** 31 - 1, tp=64, hq=64, hkv=64) == UNSUP
+    assert att(qkv=FAKE + 1) == ALIGN
+    assert att(T=0) == OK
+    assert att(T=0, qkv=None, ctx=None) == OK
+
+
+def test_binding_refuses_host_tensors():
+    """The binding hands the library device pointers only: a host tensor is
+    refused before any call into it."""
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        tpl._ptr(torch.zeros(4))
+    assert tpl._ptr(None) is None
+    with pytest.raises(ValueError):
+        tpl.tp_attention(torch.zeros((2, 8, 512), dtype=torch.bfloat16), 4, 2, 128)
+    with pytest.raises(ValueError):
+        tpl.tp_rmsnorm(torch.zeros((4, 64), dtype=torch.bfloat16))
