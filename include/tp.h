@@ -495,7 +495,13 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
  *   ctx   [tp][T][nq * hd] bf16, written.
  *   hd must be 128 (TP_ERR_UNSUPPORTED otherwise). Scores, the softmax and
  *   the P V accumulation are fp32; P is rounded to bf16 before P V.
- * Errors: TP_ERR_NULL, TP_ERR_MODE, TP_ERR_SHAPE (head counts that
+ *   T = 0 is a no-op (null pointers allowed). The launch is persistent, one
+ *   CTA per SM over the hq * ceil(T / 128) work units; more than 2^30 - 1
+ *   units is TP_ERR_UNSUPPORTED.
+ * Ownership: both buffers belong to the caller; nothing is allocated. The
+ * call is asynchronous on `stream`; a bounded device wait that expired shows
+ * as TP_ERR_TIMEOUT from tp_get_error.
+ * Errors: TP_ERR_NULL, TP_ERR_MODE, TP_ERR_SHAPE (T < 0, or head counts that
  * tp_shard_qkv rejects), TP_ERR_UNSUPPORTED, TP_ERR_ALIGN, TP_ERR_CUDA.
  */
 int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, int mode, void* ctx, void* stream);
@@ -508,8 +514,8 @@ int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, in
  * qkv_out is given), the context and the split-tile scratch
  * (tp_attn_workspace_bytes).
  * Errors: as tp_attn_proj, plus TP_ERR_MODE for an unknown mode and
- * TP_ERR_UNSUPPORTED for a core other than the single-key one on fp32 views
- * or hd != 128.
+ * TP_ERR_UNSUPPORTED for a core other than the single-key one on fp32 views,
+ * hd != 128 or more than 2^30 - 1 work units (as tp_attention).
  */
 int tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, int mode,
                   const void* residual, int out_dtype, void* qkv_out, void* workspace, size_t ws_bytes, void* Y,
