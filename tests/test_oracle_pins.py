@@ -573,6 +573,25 @@ def test_property_qkv_dedup_every_layout(heads, seed):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("q_offset", [0, 5])
+def test_attention_against_library_softmax_per_row(causal, q_offset):
+    """Each query row on its own: scipy's softmax over the scaled scores of
+    exactly the keys it sees (a slice, not a mask), then the weighted sum of
+    their values, in pure Python."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(211)
+    T, Tq, hd = 11, 6, 16
+    k, v = rng.standard_normal((T, hd)), rng.standard_normal((T, hd))
+    q = rng.standard_normal((Tq, hd)) * 2.0
+    got = O.attention_head(q, k, v, causal, q_offset=q_offset)
+    for i in range(Tq):
+        seen = range(q_offset + i + 1) if causal else range(T)
+        w = softmax([float(np.dot(q[i], k[j])) / hd ** 0.5 for j in seen])
+        want = [sum(w[n] * v[j][c] for n, j in enumerate(seen)) for c in range(hd)]
+        np.testing.assert_allclose(got[i], want, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("causal", [True, False])
 def test_attention_single_key_is_v(causal):
     """One token: the softmax over one score is 1, so the context is V exactly."""
     rng = np.random.default_rng(201)
