@@ -52,8 +52,8 @@
 extern "C" {
 #endif
 
-/* Status codes. */
-enum {
+/* Status codes: every entry point that can fail returns one. */
+typedef enum tp_status {
   TP_OK = 0,
   TP_ERR_NULL = 1,        /* a required pointer is NULL */
   TP_ERR_SHAPE = 2,       /* bad size: < 1, not divisible by tp, or mismatched */
@@ -65,7 +65,7 @@ enum {
   TP_ERR_TIMEOUT = 8,     /* a bounded device-side wait expired */
   TP_ERR_UNSUPPORTED = 9, /* valid request outside the library's limits */
   TP_ERR_INDEX = 10       /* (from tp_get_error) a token id or label outside [0, V) */
-};
+} tp_status;
 
 /* Storage types. */
 enum { TP_F32 = 0, TP_BF16 = 1 };
@@ -108,7 +108,7 @@ typedef struct tp_shards {
 } tp_shards;
 
 /* Human-readable name of a status code. Never NULL. */
-const char* tp_status_string(int status);
+const char* tp_status_string(tp_status status);
 
 /* ABI version of this header (increments on incompatible change). */
 int tp_abi_version(void);
@@ -126,8 +126,8 @@ int tp_abi_version(void);
  * TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_WORKSPACE (out_bytes < K*N*elem),
  * TP_ERR_ALIGN (bf16: K/tp, N/tp must be multiples of 8; 16-byte pointers).
  */
-int tp_shard_weights(const void* W, int64_t K, int64_t N, int dtype, int tp, int mode, void* out,
-                     size_t out_bytes, tp_shards* view, void* stream);
+tp_status tp_shard_weights(const void* W, int64_t K, int64_t N, int dtype, int tp, int mode, void* out,
+                           size_t out_bytes, tp_shards* view, void* stream);
 
 /*
  * tp_shard_qkv - shard the Q, K, V projections by whole heads.
@@ -144,8 +144,8 @@ int tp_shard_weights(const void* W, int64_t K, int64_t N, int dtype, int tp, int
  *   tp % hkv == 0 (hkv < tp).
  * Errors as tp_shard_weights.
  */
-int tp_shard_qkv(const void* Wq, const void* Wk, const void* Wv, int64_t H, int hq, int hkv, int hd,
-                 int tp, int dtype, void* out, size_t out_bytes, tp_shards* view, void* stream);
+tp_status tp_shard_qkv(const void* Wq, const void* Wk, const void* Wv, int64_t H, int hq, int hkv, int hd,
+                       int tp, int dtype, void* out, size_t out_bytes, tp_shards* view, void* stream);
 
 /* Elements of tp_shard_qkv's output, or 0 if the head counts are invalid. */
 size_t tp_qkv_shard_elems(int64_t H, int hq, int hkv, int hd, int tp);
@@ -176,9 +176,9 @@ size_t tp_qkv_shard_elems(int64_t H, int hq, int hkv, int hd, int tp);
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN,
  * TP_ERR_WORKSPACE, TP_ERR_CUDA.
  */
-int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shards* W_up,
-                     const void* bias, const void* bias_up, int act, int concat, void* Y,
-                     void* workspace, size_t ws_bytes, void* stream);
+tp_status tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shards* W_up,
+                           const void* bias, const void* bias_up, int act, int concat, void* Y,
+                           void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * tp_row_linear - row-parallel linear with the combine fused:
@@ -197,9 +197,9 @@ int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shar
  *   workspace, ws_bytes: as tp_column_linear.
  * Errors as tp_column_linear.
  */
-int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
-                  const void* residual, void* Y, int out_dtype, void* workspace, size_t ws_bytes,
-                  void* stream);
+tp_status tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
+                        const void* residual, void* Y, int out_dtype, void* workspace, size_t ws_bytes,
+                        void* stream);
 
 /* Scratch bytes that let tp_column_linear / tp_row_linear over W at T
  * tokens split tiles (the weight-streaming arrangement at T <= 64, the split
@@ -212,8 +212,8 @@ size_t tp_gemm_workspace_bytes(int64_t T, const tp_shards* W);
  *   partials  [tp][T][N] fp32 (always fp32, whatever W->dtype).
  * Errors as tp_column_linear.
  */
-int tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float* partials,
-                           void* stream);
+tp_status tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float* partials,
+                                 void* stream);
 
 /*
  * tp_shard_reduce - combine row-parallel partials.
@@ -229,8 +229,8 @@ int tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float*
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN
  * (16-byte pointers when N % 4 == 0), TP_ERR_CUDA.
  */
-int tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op, const void* bias,
-                    const void* residual, int out_dtype, void* out, void* stream);
+tp_status tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op, const void* bias,
+                          const void* residual, int out_dtype, void* out, void* stream);
 
 /*
  * tp_shard_gather - all-gather by concatenation:
@@ -238,8 +238,8 @@ int tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op,
  * not add). shards [tp][T][N/tp], out [T][N], dtype `dtype`.
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_CUDA.
  */
-int tp_shard_gather(const void* shards, int tp, int64_t T, int64_t N, int dtype, void* out,
-                    void* stream);
+tp_status tp_shard_gather(const void* shards, int tp, int64_t T, int64_t N, int dtype, void* out,
+                          void* stream);
 
 /* Workspace bytes tp_mlp_block needs for T tokens, hidden H, intermediate I. */
 size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype);
@@ -258,10 +258,10 @@ size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype
  *   scratch (see tp_column_linear). Its contents on return are unspecified.
  * Errors: as tp_column_linear, plus TP_ERR_WORKSPACE.
  */
-int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
-                 const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
-                 const void* residual, int act, int out_dtype, void* workspace, size_t ws_bytes,
-                 void* Y, void* stream);
+tp_status tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                       const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
+                       const void* residual, int act, int out_dtype, void* workspace, size_t ws_bytes,
+                       void* Y, void* stream);
 
 /*
  * tp_mlp_block_static - tp_mlp_block without a caller workspace.
@@ -278,20 +278,29 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
  *   launched. For bf16 that covers T * I up to about 6.2M, whatever T
  *   (Hs plus about 21 MB of scratch; e.g. the 70B-shaped decode block at
  *   T = 64).
- *   The first call on each device looks up the array's device address
- *   (with that device current) and caches it; make that first call before
- *   any stream capture. The call allocates nothing: no cudaMalloc/cudaFree
- *   and no allocating library routine.
+ *   The array belongs to the library's device code. CUDA loads that code,
+ *   and reserves the array with it, on a device the first time anything of
+ *   the library runs there: a kernel launch from any entry point, or the
+ *   first tp_mlp_block_static call, which also looks up the array's device
+ *   address (with that device current) and caches it. Make one call of any
+ *   entry point on each device before the point where allocation is
+ *   forbidden, and make that first tp_mlp_block_static call before any
+ *   stream capture. Every later call allocates nothing: no
+ *   cudaMalloc/cudaFree and no allocating library routine.
  *   Every call shares the one array and the array keeps the last call's
- *   contents (each call clears what must start at zero). Calls that overlap
- *   on the GPU -- on different streams, or from different host threads
- *   without ordering -- race on the array; serialise them.
+ *   contents. Leftover contents are harmless: Hs is rewritten before it is
+ *   read, and the split-tile synchronisation words are tagged with each
+ *   launch's own epoch (a word left by an earlier call reads as "not
+ *   arrived") and returned to zero by the kernel that used them; this is
+ *   also why calls in a row can share the array. Calls that overlap on the
+ *   GPU -- on different streams, or from different host threads without
+ *   ordering -- race on the array; serialise them.
  * Errors: as tp_mlp_block.
  */
 #define TP_STATIC_WORKSPACE_BYTES ((size_t)32 << 20)
-int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
-                        const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
-                        const void* residual, int act, int out_dtype, void* Y, void* stream);
+tp_status tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                              const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
+                              const void* residual, int act, int out_dtype, void* Y, void* stream);
 
 /*
  * Backward of the column/row pair ("Tensor parallelism: splitting
@@ -318,8 +327,8 @@ int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_
  * Errors: TP_ERR_NULL, TP_ERR_MODE, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_ALIGN,
  * TP_ERR_CUDA.
  */
-int tp_row_linear_backward(const void* Xs, int64_t T, const tp_shards* W, const void* dY, void* dXs,
-                           void* dW, void* stream);
+tp_status tp_row_linear_backward(const void* Xs, int64_t T, const tp_shards* W, const void* dY, void* dXs,
+                                 void* dW, void* stream);
 
 /*
  * tp_column_linear_backward - backward of Y_s = X @ W_s (X replicated).
@@ -335,9 +344,9 @@ int tp_row_linear_backward(const void* Xs, int64_t T, const tp_shards* W, const 
  *   whole tiles only.
  * Errors: as tp_row_linear_backward, plus TP_ERR_WORKSPACE.
  */
-int tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W, const void* dYs,
-                              const void* dR, void* dX, void* dW, void* workspace, size_t ws_bytes,
-                              void* stream);
+tp_status tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W, const void* dYs,
+                                    const void* dR, void* dX, void* dW, void* workspace, size_t ws_bytes,
+                                    void* stream);
 
 /* Workspace bytes tp_mlp_backward needs (act decides whether dU is kept). */
 size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int act);
@@ -364,10 +373,10 @@ size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, 
  *   split-tile scratch. Contents on return are unspecified.
  * Errors: as tp_column_linear_backward, plus TP_ERR_MODE for an unknown act.
  */
-int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
-                    const tp_shards* W2, int act, const void* G, const void* U, const void* Hs,
-                    const void* dY, const void* dR, void* workspace, size_t ws_bytes, void* dX,
-                    void* dW1, void* dW_up, void* dW2, void* stream);
+tp_status tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                          const tp_shards* W2, int act, const void* G, const void* U, const void* Hs,
+                          const void* dY, const void* dR, void* workspace, size_t ws_bytes, void* dX,
+                          void* dW1, void* dW_up, void* dW2, void* stream);
 
 /*
  * Vocabulary-parallel input and output layers ("Tensor parallelism:
@@ -390,8 +399,8 @@ int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shar
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE (V % tp != 0, sizes < 1), TP_ERR_DTYPE,
  * TP_ERR_ALIGN (4-byte ids and element-aligned tables), TP_ERR_CUDA.
  */
-int tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, int64_t H, int tp,
-                       int dtype, void* Y, void* stream);
+tp_status tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, int64_t H, int tp,
+                             int dtype, void* Y, void* stream);
 
 /* Workspace bytes tp_vocab_cross_entropy needs (T tokens, vocabulary V). */
 size_t tp_cross_entropy_workspace_bytes(int64_t T, int64_t V, int tp);
@@ -418,9 +427,9 @@ size_t tp_cross_entropy_workspace_bytes(int64_t T, int64_t V, int tp);
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_ALIGN,
  * TP_ERR_WORKSPACE, TP_ERR_CUDA.
  */
-int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T, int64_t V, int tp,
-                           int dtype, float* loss, float* mean_loss, void* dlogits, float grad_scale,
-                           void* workspace, size_t ws_bytes, void* stream);
+tp_status tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T, int64_t V, int tp,
+                                 int dtype, float* loss, float* mean_loss, void* dlogits, float grad_scale,
+                                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Mixture of experts with tensor-parallel experts ("Parallel strategies in
@@ -450,9 +459,9 @@ size_t tp_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int k, int E, int
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_MODE, TP_ERR_DTYPE, TP_ERR_ALIGN,
  * TP_ERR_WORKSPACE, TP_ERR_UNSUPPORTED, TP_ERR_CUDA.
  */
-int tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weights, int k, int E,
-                 const tp_shards* Wg, const tp_shards* Wu, const tp_shards* Wd, const void* residual,
-                 void* workspace, size_t ws_bytes, void* Y, void* stream);
+tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weights, int k, int E,
+                       const tp_shards* Wg, const tp_shards* Wu, const tp_shards* Wd, const void* residual,
+                       void* workspace, size_t ws_bytes, void* Y, void* stream);
 
 /* Workspace bytes tp_attn_proj needs. */
 size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int dtype);
@@ -477,9 +486,9 @@ size_t tp_attn_workspace_bytes(int64_t T, int hq, int hkv, int hd, int tp, int d
  *   Requires H <= 4 * hq * hd (TP_ERR_UNSUPPORTED otherwise).
  * Errors: as tp_mlp_block.
  */
-int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
-                 const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
-                 size_t ws_bytes, void* Y, void* stream);
+tp_status tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
+                       const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
+                       size_t ws_bytes, void* Y, void* stream);
 
 /*
  * tp_attention - the attention core of every local head of every shard
@@ -504,7 +513,7 @@ int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shard
  * Errors: TP_ERR_NULL, TP_ERR_MODE, TP_ERR_SHAPE (T < 0, or head counts that
  * tp_shard_qkv rejects), TP_ERR_UNSUPPORTED, TP_ERR_ALIGN, TP_ERR_CUDA.
  */
-int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, int mode, void* ctx, void* stream);
+tp_status tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, int mode, void* ctx, void* stream);
 
 /*
  * tp_attn_block - tp_attn_proj with the attention core chosen by `mode`:
@@ -517,9 +526,9 @@ int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, in
  * TP_ERR_UNSUPPORTED for a core other than the single-key one on fp32 views,
  * hd != 128 or more than 2^30 - 1 work units (as tp_attention).
  */
-int tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, int mode,
-                  const void* residual, int out_dtype, void* qkv_out, void* workspace, size_t ws_bytes, void* Y,
-                  void* stream);
+tp_status tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, int mode,
+                        const void* residual, int out_dtype, void* qkv_out, void* workspace, size_t ws_bytes, void* Y,
+                        void* stream);
 
 /*
  * tp_rmsnorm - RMSNorm on the replicated hidden ("CUDA tensor parallel
@@ -530,8 +539,8 @@ int tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shar
  * input).
  * Errors: TP_ERR_NULL, TP_ERR_SHAPE, TP_ERR_DTYPE, TP_ERR_ALIGN, TP_ERR_CUDA.
  */
-int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
-               int out_dtype, void* stream);
+tp_status tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
+                     int out_dtype, void* stream);
 
 /*
  * tp_get_error - synchronise `stream`, then report and clear the device
@@ -539,7 +548,7 @@ int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps
  * last call (that kernel's outputs are then undefined), TP_ERR_CUDA if the
  * stream reported an error, else TP_OK.
  */
-int tp_get_error(void* stream);
+tp_status tp_get_error(void* stream);
 
 /*
  * Test hooks (synchronous; they change device-global state used by every
@@ -550,8 +559,8 @@ int tp_get_error(void* stream);
  *     withholds one operand load, so its consumer's wait expires and the
  *     kernel takes its abort path. tp_debug_inject(0) disarms.
  */
-int tp_debug_set_wait_limit_ns(uint64_t ns);
-int tp_debug_inject(int kind);
+tp_status tp_debug_set_wait_limit_ns(uint64_t ns);
+tp_status tp_debug_inject(int kind);
 
 #ifdef __cplusplus
 }

@@ -36,6 +36,8 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+// a status computed as an int (a helper's result) as the public return type
+inline tp_status as_status(int r) { return static_cast<tp_status>(r); }
 
 // Pointer alignment each dtype path needs (bf16 feeds TMA / 16-byte vectors).
 inline bool ptr_ok(const void* p, int dtype) {
@@ -726,7 +728,7 @@ size_t attn_max_tiles(int64_t H, int hq, int hkv, int hd, int tp) {
 // ===========================================================================
 extern "C" {
 
-const char* tp_status_string(int s) {
+const char* tp_status_string(tp_status s) {
   switch (s) {
     case TP_OK: return "ok";
     case TP_ERR_NULL: return "null pointer";
@@ -745,8 +747,8 @@ const char* tp_status_string(int s) {
 
 int tp_abi_version(void) { return 1; }
 
-int tp_shard_weights(const void* W, int64_t K, int64_t N, int dtype, int tp, int mode, void* out,
-                     size_t out_bytes, tp_shards* view, void* stream) {
+tp_status tp_shard_weights(const void* W, int64_t K, int64_t N, int dtype, int tp, int mode, void* out,
+                           size_t out_bytes, tp_shards* view, void* stream) {
   if (!W || !out) return TP_ERR_NULL;
   if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
   if (mode != TP_COL && mode != TP_ROW) return TP_ERR_MODE;
@@ -779,7 +781,7 @@ int tp_shard_weights(const void* W, int64_t K, int64_t N, int dtype, int tp, int
     view->mode = mode;
     view->dtype = dtype;
   }
-  return r;
+  return as_status(r);
 }
 
 size_t tp_qkv_shard_elems(int64_t H, int hq, int hkv, int hd, int tp) {
@@ -790,8 +792,8 @@ size_t tp_qkv_shard_elems(int64_t H, int hq, int hkv, int hd, int tp) {
   return static_cast<size_t>(tp) * static_cast<size_t>((hq / tp + 2 * nkv) * hd) * static_cast<size_t>(H);
 }
 
-int tp_shard_qkv(const void* Wq, const void* Wk, const void* Wv, int64_t H, int hq, int hkv, int hd,
-                 int tp, int dtype, void* out, size_t out_bytes, tp_shards* view, void* stream) {
+tp_status tp_shard_qkv(const void* Wq, const void* Wk, const void* Wv, int64_t H, int hq, int hkv, int hd,
+                       int tp, int dtype, void* out, size_t out_bytes, tp_shards* view, void* stream) {
   if (!Wq || !Wk || !Wv || !out) return TP_ERR_NULL;
   if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
   const size_t elems = tp_qkv_shard_elems(H, hq, hkv, hd, tp);
@@ -831,7 +833,7 @@ int tp_shard_qkv(const void* Wq, const void* Wk, const void* Wv, int64_t H, int 
     view->hkv = hkv;
     view->hd = hd;
   }
-  return r;
+  return as_status(r);
 }
 
 size_t tp_gemm_workspace_bytes(int64_t T, const tp_shards* W) {
@@ -857,37 +859,37 @@ int linear_scratch(const tp_shards* W, int64_t T, void* ws, size_t ws_bytes, Scr
   return TP_OK;
 }
 
-int tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shards* W_up,
-                     const void* bias, const void* bias_up, int act, int concat, void* Y,
-                     void* workspace, size_t ws_bytes, void* stream) {
+tp_status tp_column_linear(const void* X, int64_t T, const tp_shards* W, const tp_shards* W_up,
+                           const void* bias, const void* bias_up, int act, int concat, void* Y,
+                           void* workspace, size_t ws_bytes, void* stream) {
   int r = check_col(X, T, W, W_up, bias, bias_up, act, concat, Y);
-  if (r) return r;
+  if (r) return as_status(r);
   Scratch sc{};
   const Scratch* scp;
-  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return r;
-  return run_col(X, T, W, W_up, bias, bias_up, act, concat, Y, as_stream(stream), scp);
+  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return as_status(r);
+  return as_status(run_col(X, T, W, W_up, bias, bias_up, act, concat, Y, as_stream(stream), scp));
 }
 
-int tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
-                  const void* residual, void* Y, int out_dtype, void* workspace, size_t ws_bytes,
-                  void* stream) {
+tp_status tp_row_linear(const void* Xs, int64_t T, const tp_shards* W, const void* bias,
+                        const void* residual, void* Y, int out_dtype, void* workspace, size_t ws_bytes,
+                        void* stream) {
   int r = check_row(Xs, T, W, bias, residual, Y, out_dtype);
-  if (r) return r;
+  if (r) return as_status(r);
   Scratch sc{};
   const Scratch* scp;
-  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return r;
-  return run_row(Xs, T, W, bias, residual, Y, out_dtype, nullptr, as_stream(stream), scp);
+  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return as_status(r);
+  return as_status(run_row(Xs, T, W, bias, residual, Y, out_dtype, nullptr, as_stream(stream), scp));
 }
 
-int tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float* partials,
-                           void* stream) {
+tp_status tp_row_linear_partials(const void* Xs, int64_t T, const tp_shards* W, float* partials,
+                                 void* stream) {
   const int r = check_row(Xs, T, W, nullptr, nullptr, partials, TP_F32);
-  if (r) return r;
-  return run_row(Xs, T, W, nullptr, nullptr, nullptr, TP_F32, partials, as_stream(stream));
+  if (r) return as_status(r);
+  return as_status(run_row(Xs, T, W, nullptr, nullptr, nullptr, TP_F32, partials, as_stream(stream)));
 }
 
-int tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op, const void* bias,
-                    const void* residual, int out_dtype, void* out, void* stream) {
+tp_status tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op, const void* bias,
+                          const void* residual, int out_dtype, void* out, void* stream) {
   if (!partials || !out) return TP_ERR_NULL;
   if (op != TP_REDUCE_SUM && op != TP_REDUCE_SCATTER) return TP_ERR_MODE;
   if (!dtype_ok(out_dtype)) return TP_ERR_DTYPE;
@@ -918,11 +920,11 @@ int tp_shard_reduce(const float* partials, int tp, int64_t T, int64_t N, int op,
     if (vec) tpk::reduce_kernel<float><<<grid, 256, 0, st>>>(partials, tp, T, N, b, rr, o);
     else tpk::reduce_kernel_scalar<float><<<grid, 256, 0, st>>>(partials, tp, T, N, b, rr, o);
   }
-  return launch_status();
+  return as_status(launch_status());
 }
 
-int tp_shard_gather(const void* shards, int tp, int64_t T, int64_t N, int dtype, void* out,
-                    void* stream) {
+tp_status tp_shard_gather(const void* shards, int tp, int64_t T, int64_t N, int dtype, void* out,
+                          void* stream) {
   if (!shards || !out) return TP_ERR_NULL;
   if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
   if (tp < 1 || T < 0 || N < 1 || N % tp) return TP_ERR_SHAPE;
@@ -943,7 +945,7 @@ int tp_shard_gather(const void* shards, int tp, int64_t T, int64_t N, int dtype,
     if (vec) tpk::gather_kernel<float, 4><<<grid_for(tp * T * Ns / 4, 256), 256, 0, st>>>(in, tp, T, Ns, o);
     else tpk::gather_kernel<float, 1><<<grid_for(tp * T * Ns, 256), 256, 0, st>>>(in, tp, T, Ns, o);
   }
-  return launch_status();
+  return as_status(launch_status());
 }
 
 size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype) {
@@ -953,15 +955,15 @@ size_t tp_mlp_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int dtype
   return b;
 }
 
-int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
-                 const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
-                 const void* residual, int act, int out_dtype, void* workspace, size_t ws_bytes,
-                 void* Y, void* stream) {
+tp_status tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                       const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
+                       const void* residual, int act, int out_dtype, void* workspace, size_t ws_bytes,
+                       void* Y, void* stream) {
   if (!W2 || (!workspace && T != 0)) return TP_ERR_NULL;
   int r = check_col(X, T, W1, W_up, b1, b1_up, act, 0, Y);
-  if (r) return r;
-  if ((r = check_view(W2, TP_ROW))) return r;
-  if ((r = check_out_dtype(W2, out_dtype))) return r;
+  if (r) return as_status(r);
+  if ((r = check_view(W2, TP_ROW))) return as_status(r);
+  if ((r = check_out_dtype(W2, out_dtype))) return as_status(r);
   if (W2->dtype != W1->dtype) return TP_ERR_DTYPE;
   if (W2->tp != W1->tp || W2->K != W1->N || W2->N != W1->K) return TP_ERR_SHAPE;
   const int dt = W1->dtype;
@@ -977,8 +979,8 @@ int tp_mlp_block(const void* X, int64_t T, const tp_shards* W1, const tp_shards*
     sc = carve_scratch(workspace, hs_bytes, mlp_max_tiles(W1->K, W1->N, W1->tp));
     scp = &sc;
   }
-  if ((r = run_col(X, T, W1, W_up, b1, b1_up, act, 0, Hs, st, scp))) return r;
-  return run_row(Hs, T, W2, b2, residual, Y, out_dtype, nullptr, st, scp);
+  if ((r = run_col(X, T, W1, W_up, b1, b1_up, act, 0, Hs, st, scp))) return as_status(r);
+  return as_status(run_row(Hs, T, W2, b2, residual, Y, out_dtype, nullptr, st, scp));
 }
 
 }  // extern "C"
@@ -1012,16 +1014,16 @@ int static_workspace(void** out) {
 
 extern "C" {
 
-int tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
-                        const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
-                        const void* residual, int act, int out_dtype, void* Y, void* stream) {
+tp_status tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                              const tp_shards* W2, const void* b1, const void* b1_up, const void* b2,
+                              const void* residual, int act, int out_dtype, void* Y, void* stream) {
   if (!W1 || !W2) return TP_ERR_NULL;
   // sizes beyond the static array are refused before anything else happens
   if (tp_mlp_workspace_bytes(T, W1->K, W1->N, W1->tp, W1->dtype) > TP_STATIC_WORKSPACE_BYTES)
     return TP_ERR_WORKSPACE;
   void* ws = nullptr;
   const int r = static_workspace(&ws);
-  if (r) return r;
+  if (r) return as_status(r);
   return tp_mlp_block(X, T, W1, W_up, W2, b1, b1_up, b2, residual, act, out_dtype, ws,
                       TP_STATIC_WORKSPACE_BYTES, Y, stream);
 }
@@ -1108,21 +1110,21 @@ int attn_block_impl(const void* X, int64_t T, const tp_shards* Wqkv, const tp_sh
 
 extern "C" {
 
-int tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
-                 const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
-                 size_t ws_bytes, void* Y, void* stream) {
-  return attn_block_impl(X, T, Wqkv, Wo, ctx, TP_ATTN_SINGLE_KEY, residual, out_dtype, qkv_out, workspace,
-                         ws_bytes, Y, stream);
+tp_status tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo,
+                       const void* ctx, const void* residual, int out_dtype, void* qkv_out, void* workspace,
+                       size_t ws_bytes, void* Y, void* stream) {
+  return as_status(attn_block_impl(X, T, Wqkv, Wo, ctx, TP_ATTN_SINGLE_KEY, residual, out_dtype,
+                                                qkv_out, workspace, ws_bytes, Y, stream));
 }
 
-int tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, int mode,
-                  const void* residual, int out_dtype, void* qkv_out, void* workspace, size_t ws_bytes, void* Y,
-                  void* stream) {
-  return attn_block_impl(X, T, Wqkv, Wo, nullptr, mode, residual, out_dtype, qkv_out, workspace, ws_bytes, Y,
-                         stream);
+tp_status tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, int mode,
+                        const void* residual, int out_dtype, void* qkv_out, void* workspace, size_t ws_bytes, void* Y,
+                        void* stream) {
+  return as_status(attn_block_impl(X, T, Wqkv, Wo, nullptr, mode, residual, out_dtype, qkv_out,
+                                                workspace, ws_bytes, Y, stream));
 }
 
-int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, int mode, void* ctx, void* stream) {
+tp_status tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, int mode, void* ctx, void* stream) {
   if ((!qkv || !ctx) && T != 0) return TP_ERR_NULL;
   if (mode != TP_ATTN_CAUSAL && mode != TP_ATTN_FULL) return TP_ERR_MODE;
   if (T < 0 || tp < 1 || hq < 1 || hkv < 1 || hd < 1 || tp_qkv_shard_elems(1, hq, hkv, hd, tp) == 0)
@@ -1132,11 +1134,11 @@ int tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, in
     return TP_ERR_UNSUPPORTED;
   if (!ptr_ok(qkv, TP_BF16) || !ptr_ok(ctx, TP_BF16)) return TP_ERR_ALIGN;
   if (T == 0) return TP_OK;
-  return attention_launch(qkv, T, tp, hq, hkv, mode, ctx, as_stream(stream));
+  return as_status(attention_launch(qkv, T, tp, hq, hkv, mode, ctx, as_stream(stream)));
 }
 
-int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
-               int out_dtype, void* stream) {
+tp_status tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
+                     int out_dtype, void* stream) {
   if ((!X || !Y) && T != 0) return TP_ERR_NULL;
   if (!dtype_ok(dtype) || !dtype_ok(out_dtype)) return TP_ERR_DTYPE;
   if (T < 0 || H < 1 || !(eps >= 0.0f)) return TP_ERR_SHAPE;
@@ -1159,10 +1161,10 @@ int tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps
   else
     tpk::rmsnorm_kernel<float, float><<<grid, 256, 0, st>>>(
         static_cast<const float*>(X), static_cast<const float*>(gamma), H, eps, static_cast<float*>(Y));
-  return launch_status();
+  return as_status(launch_status());
 }
 
-int tp_get_error(void* stream) {
+tp_status tp_get_error(void* stream) {
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return TP_ERR_CUDA;
   int err = 0;
   if (cudaMemcpyFromSymbol(&err, tpk::g_tp_error, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
@@ -1176,14 +1178,14 @@ int tp_get_error(void* stream) {
   return TP_OK;
 }
 
-int tp_debug_set_wait_limit_ns(uint64_t ns) {
+tp_status tp_debug_set_wait_limit_ns(uint64_t ns) {
   const unsigned long long v = ns;
-  return cudaMemcpyToSymbol(tpk::g_tp_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  return as_status(cudaMemcpyToSymbol(tpk::g_tp_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? TP_OK : TP_ERR_CUDA);
 }
 
-int tp_debug_inject(int kind) {
+tp_status tp_debug_inject(int kind) {
   if (kind < 0 || kind > 1) return TP_ERR_MODE;
-  return cudaMemcpyToSymbol(tpk::g_tp_inject, &kind, sizeof(int)) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  return as_status(cudaMemcpyToSymbol(tpk::g_tp_inject, &kind, sizeof(int)) == cudaSuccess ? TP_OK : TP_ERR_CUDA);
 }
 
 }  // extern "C"
@@ -1261,23 +1263,23 @@ size_t bwd_max_tiles(int64_t H, int64_t I, int tp) {
 
 extern "C" {
 
-int tp_row_linear_backward(const void* Xs, int64_t T, const tp_shards* W, const void* dY, void* dXs,
-                           void* dW, void* stream) {
+tp_status tp_row_linear_backward(const void* Xs, int64_t T, const tp_shards* W, const void* dY, void* dXs,
+                                 void* dW, void* stream) {
   int r = check_bwd_view(W, TP_ROW);
-  if (r) return r;
+  if (r) return as_status(r);
   if (T < 0) return TP_ERR_SHAPE;
   if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
   if (T > 0 && (!dY || (dW && !Xs))) return TP_ERR_NULL;
   if (!ptrs16({Xs, dY, dXs, dW})) return TP_ERR_ALIGN;
   if (T == 0) return TP_OK;
-  return row_bwd_bf16(Xs, T, W, dY, dXs, dW, nullptr, as_stream(stream));
+  return as_status(row_bwd_bf16(Xs, T, W, dY, dXs, dW, nullptr, as_stream(stream)));
 }
 
-int tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W, const void* dYs,
-                              const void* dR, void* dX, void* dW, void* workspace, size_t ws_bytes,
-                              void* stream) {
+tp_status tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W, const void* dYs,
+                                    const void* dR, void* dX, void* dW, void* workspace, size_t ws_bytes,
+                                    void* stream) {
   int r = check_bwd_view(W, TP_COL);
-  if (r) return r;
+  if (r) return as_status(r);
   if (T < 0) return TP_ERR_SHAPE;
   if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
   if (T > 0 && (!dYs || (dW && !X))) return TP_ERR_NULL;
@@ -1285,9 +1287,9 @@ int tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W, cons
   if (W->K % 8 != 0) return TP_ERR_ALIGN;
   Scratch sc{};
   const Scratch* scp = nullptr;
-  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return r;
+  if ((r = linear_scratch(W, T, workspace, ws_bytes, &sc, &scp))) return as_status(r);
   if (T == 0) return TP_OK;
-  return col_bwd_bf16(X, T, W, dYs, dR, dX, dW, scp, as_stream(stream));
+  return as_status(col_bwd_bf16(X, T, W, dYs, dR, dX, dW, scp, as_stream(stream)));
 }
 
 size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int act) {
@@ -1297,18 +1299,18 @@ size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, 
   return (gated ? 3 : 2) * inter + scratch_bytes(T, bwd_max_tiles(H, I, tp));  // dHs, dG (, dU), scratch
 }
 
-int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
-                    const tp_shards* W2, int act, const void* G, const void* U, const void* Hs,
-                    const void* dY, const void* dR, void* workspace, size_t ws_bytes, void* dX,
-                    void* dW1, void* dW_up, void* dW2, void* stream) {
+tp_status tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
+                          const tp_shards* W2, int act, const void* G, const void* U, const void* Hs,
+                          const void* dY, const void* dR, void* workspace, size_t ws_bytes, void* dX,
+                          void* dW1, void* dW_up, void* dW2, void* stream) {
   if (!W1 || !W2) return TP_ERR_NULL;
   if (act < TP_ACT_NONE || act > TP_ACT_SWIGLU) return TP_ERR_MODE;
   const bool gated = act == TP_ACT_SWIGLU;
   int r;
-  if ((r = check_bwd_view(W1, TP_COL)) || (r = check_bwd_view(W2, TP_ROW))) return r;
+  if ((r = check_bwd_view(W1, TP_COL)) || (r = check_bwd_view(W2, TP_ROW))) return as_status(r);
   if (gated) {
     if (!W_up) return TP_ERR_NULL;
-    if ((r = check_bwd_view(W_up, TP_COL))) return r;
+    if ((r = check_bwd_view(W_up, TP_COL))) return as_status(r);
     if (!same_shape(W1, W_up)) return TP_ERR_SHAPE;
   } else if (W_up || U || dW_up) {
     return TP_ERR_MODE;
@@ -1330,21 +1332,21 @@ int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shar
   void* dU = gated ? ws + 2 * inter : nullptr;
   const Scratch sc = carve_scratch(workspace, (gated ? 3 : 2) * inter, bwd_max_tiles(H, I, tp));
   // row layer (every shard gets dY): dHs and dW2; then the local activation
-  if ((r = row_bwd_bf16(Hs, T, W2, dY, dHs, dW2, &sc, st))) return r;
-  if ((r = act_bwd_launch(dHs, G, U, static_cast<int64_t>(T) * I, act, dG, dU, st))) return r;
+  if ((r = row_bwd_bf16(Hs, T, W2, dY, dHs, dW2, &sc, st))) return as_status(r);
+  if ((r = act_bwd_launch(dHs, G, U, static_cast<int64_t>(T) * I, act, dG, dU, st))) return as_status(r);
   // column layer(s): the input gradient is the sum over shards, and over
   // gate and up for SwiGLU (one accumulator), plus dR
-  if (!gated) return col_bwd_bf16(X, T, W1, dG, dR, dX, dW1, &sc, st);
+  if (!gated) return as_status(col_bwd_bf16(X, T, W1, dG, dR, dX, dW1, &sc, st));
   const int64_t Is = I / tp;
   if (dX) {
     CUtensorMap ma0, mb0, ma1, mb1;
     if (!make_map_bf16(&ma0, dG, Is, T, tp, 128) || !make_map_bf16(&mb0, W1->data, H, Is, tp, 64) ||
         !make_map_bf16(&ma1, dU, Is, T, tp, 128) || !make_map_bf16(&mb1, W_up->data, H, Is, tp, 64))
       return TP_ERR_CUDA;
-    if ((r = gemm_bwd<tpk::GK_ROW_SUM, 2>(ma0, mb0, T, H, tp, Is, 0, dR, dX, &sc, st, &ma1, &mb1))) return r;
+    if ((r = gemm_bwd<tpk::GK_ROW_SUM, 2>(ma0, mb0, T, H, tp, Is, 0, dR, dX, &sc, st, &ma1, &mb1))) return as_status(r);
   }
-  if ((r = col_bwd_bf16(X, T, W1, dG, nullptr, nullptr, dW1, &sc, st))) return r;
-  return col_bwd_bf16(X, T, W_up, dU, nullptr, nullptr, dW_up, &sc, st);
+  if ((r = col_bwd_bf16(X, T, W1, dG, nullptr, nullptr, dW1, &sc, st))) return as_status(r);
+  return as_status(col_bwd_bf16(X, T, W_up, dU, nullptr, nullptr, dW_up, &sc, st));
 }
 
 }  // extern "C"
@@ -1354,8 +1356,8 @@ int tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shar
 // ---------------------------------------------------------------------------
 extern "C" {
 
-int tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, int64_t H, int tp,
-                       int dtype, void* Y, void* stream) {
+tp_status tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, int64_t H, int tp,
+                             int dtype, void* Y, void* stream) {
   if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
   if (T < 0 || V < 1 || H < 1 || tp < 1 || V % tp != 0) return TP_ERR_SHAPE;
   if (T == 0) return TP_OK;
@@ -1371,7 +1373,7 @@ int tp_vocab_embedding(const int32_t* ids, int64_t T, const void* E, int64_t V, 
   else
     tpk::vocab_embed_kernel<float><<<grid, 256, 0, st>>>(ids, T, static_cast<const float*>(E), V, H, V / tp, vec,
                                                            static_cast<float*>(Y));
-  return launch_status();
+  return as_status(launch_status());
 }
 
 // Partial statistics of the cross-entropy's first pass: 3 floats per
@@ -1386,9 +1388,9 @@ size_t tp_cross_entropy_workspace_bytes(int64_t T, int64_t V, int tp) {
   return ce_stats_bytes(T, V, tp) + 2 * align256(static_cast<size_t>(T) * sizeof(float));
 }
 
-int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T, int64_t V, int tp,
-                           int dtype, float* loss, float* mean_loss, void* dlogits, float grad_scale,
-                           void* workspace, size_t ws_bytes, void* stream) {
+tp_status tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T, int64_t V, int tp,
+                                 int dtype, float* loss, float* mean_loss, void* dlogits, float grad_scale,
+                                 void* workspace, size_t ws_bytes, void* stream) {
   if (!dtype_ok(dtype)) return TP_ERR_DTYPE;
   if (T < 0 || V < 1 || tp < 1 || V % tp != 0) return TP_ERR_SHAPE;
   if (ws_bytes < tp_cross_entropy_workspace_bytes(T, V, tp)) return TP_ERR_WORKSPACE;
@@ -1421,13 +1423,13 @@ int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T,
     tpk::ce_stats_kernel<float><<<grid_rows, 256, 0, st>>>(static_cast<const float*>(logits), labels, T, tp, v,
                                                              vec, stats);
   int r = launch_status();
-  if (r) return r;
+  if (r) return as_status(r);
   tpk::ce_combine_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(T, 8), static_cast<int64_t>(sms) * 16)), 256, 0,
                            st>>>(stats, labels, T, tp, V, nchunk, lse, per_tok);
-  if ((r = launch_status())) return r;
+  if ((r = launch_status())) return as_status(r);
   if (mean_loss) {
     tpk::ce_mean_kernel<<<1, 1024, 0, st>>>(per_tok, T, mean_loss);
-    if ((r = launch_status())) return r;
+    if ((r = launch_status())) return as_status(r);
   }
   if (dlogits) {
     const int grid_g = vec ? grid_rows : grid_for(T * V, 256);
@@ -1439,7 +1441,7 @@ int tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int64_t T,
           static_cast<const float*>(logits), labels, lse, T, tp, v, grad_scale, vec, static_cast<float*>(dlogits));
     r = launch_status();
   }
-  return r;
+  return as_status(r);
 }
 
 }  // extern "C"
@@ -1485,12 +1487,12 @@ size_t tp_moe_workspace_bytes(int64_t T, int64_t H, int64_t I, int k, int E, int
   return moe_layout(T, H, I, k, E).total;
 }
 
-int tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weights, int k, int E,
-                 const tp_shards* Wg, const tp_shards* Wu, const tp_shards* Wd, const void* residual,
-                 void* workspace, size_t ws_bytes, void* Y, void* stream) {
+tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weights, int k, int E,
+                       const tp_shards* Wg, const tp_shards* Wu, const tp_shards* Wd, const void* residual,
+                       void* workspace, size_t ws_bytes, void* Y, void* stream) {
   if (!Wg || !Wu || !Wd) return TP_ERR_NULL;
   int r;
-  if ((r = check_view(Wg, TP_COL)) || (r = check_view(Wu, TP_COL)) || (r = check_view(Wd, TP_ROW))) return r;
+  if ((r = check_view(Wg, TP_COL)) || (r = check_view(Wu, TP_COL)) || (r = check_view(Wd, TP_ROW))) return as_status(r);
   if (Wg->dtype != TP_BF16 || !same_shape(Wg, Wu) || Wd->dtype != TP_BF16) return TP_ERR_DTYPE;
   if (Wd->tp != Wg->tp || Wd->K != Wg->N || Wd->N != Wg->K) return TP_ERR_SHAPE;
   if (T < 0 || k < 1 || E < 1 || E > 1024) return TP_ERR_SHAPE;
@@ -1517,12 +1519,12 @@ int tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weig
   const int64_t grid_cap = static_cast<int64_t>(std::max(1, num_sms())) * 16;
   // 1. dispatch
   tpk::moe_route_kernel<<<E, 1024, 0, st>>>(ids, n, E, pos, counts);
-  if ((r = launch_status())) return r;
+  if ((r = launch_status())) return as_status(r);
   tpk::moe_units_kernel<<<1, 256, 0, st>>>(counts, E, static_cast<int>(L.units), off, unit_expert);
-  if ((r = launch_status())) return r;
+  if ((r = launch_status())) return as_status(r);
   tpk::moe_gather_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(n, 8), grid_cap)), 256, 0, st>>>(
       static_cast<const bf16*>(X), ids, pos, off, n, k, E, H, Xp, inv);
-  if ((r = launch_status())) return r;
+  if ((r = launch_status())) return as_status(r);
   // 2. the experts' MLP blocks over all units: gate/up + SwiGLU per shard,
   // then down + the shard sum; each tile takes its expert's shard set
   const int64_t Is = I / tp;
@@ -1549,7 +1551,7 @@ int tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weig
     a.unit_expert = unit_expert;
     OutMaps om{};
     a.tma_store = make_store_map(&om.y, Hs, false, Is, L.rows, tp, Is * 2, L.rows * Is * 2) ? 1 : 0;
-    if ((r = gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mg, mu, om, a, nullptr, st))) return r;
+    if ((r = gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mg, mu, om, a, nullptr, st))) return as_status(r);
   }
   {
     CUtensorMap mx, mw;
@@ -1573,12 +1575,12 @@ int tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float* weig
     a.unit_expert = unit_expert;
     OutMaps om{};
     a.tma_store = make_store_map(&om.y, Yp, true, H, L.rows, 1, H * 4, L.rows * H * 4) ? 1 : 0;
-    if ((r = gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, om, a, nullptr, st))) return r;
+    if ((r = gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, om, a, nullptr, st))) return as_status(r);
   }
   // 3. combine
   tpk::moe_combine_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(T, 8), grid_cap)), 256, 0, st>>>(
       Yp, inv, weights, T, k, H, static_cast<const bf16*>(residual), static_cast<bf16*>(Y));
-  return launch_status();
+  return as_status(launch_status());
 }
 
 }  // extern "C"

@@ -172,9 +172,13 @@ def test_backward_validation():
 
 def test_mlp_backward_full_size_sampled():
     """The 7B SwiGLU MLP at tp = 8, T = 2048 (the bench workload), forward
-    then backward on the GPU: sampled rows of dX and sampled weight-gradient
-    rows against the oracle's float64 chain, each computed on its own from
-    the same inputs (the chain bound)."""
+    then backward on the GPU, against the oracle's float64 chain (the chain
+    bound) on a sample. Token rows are independent, so dX of sampled rows is
+    the oracle's backward of those rows alone (all eight shards). Columns of
+    the intermediate are independent too: the gradients of sampled gate / up
+    weight rows (columns of W1 and Wu) and down weight columns (rows of W2)
+    are the oracle's backward of the block restricted to those intermediate
+    columns, over all tokens, unsharded."""
     T, H, I, tp = 2048, 4096, 11008, 8
     d = S.mlp_backward(T, H, I)
     X, Sg, Su, Sd, G, U, Hs = gpu_forward(d, tp, "swiglu")
@@ -183,20 +187,15 @@ def test_mlp_backward_full_size_sampled():
     Xf, Wg, Wu, Wd, dY = (f64(d[k]) for k in ("X", "Wg", "Wu", "Wd", "dY"))
     rng = np.random.default_rng(7)
     rows = np.sort(rng.choice(T, 24, replace=False))
-    # dX rows: the chain rule for those tokens only
-    Gr, Ur = Xf[rows] @ Wg, Xf[rows] @ Wu
-    dGr, dUr = O.activation_backward("swiglu", Gr, dY[rows] @ Wd.T, Ur)
-    assert_close(host(g["dX"])[rows], dGr @ Wg.T + dUr @ Wu.T, TOL_CHAIN, "dX rows")
-    # weight-gradient rows: columns i of the intermediate need all tokens
+    ref_rows = O.mlp_backward(Xf[rows], Wg, Wd, tp, dY[rows], "swiglu", W_up=Wu)
+    assert_close(host(g["dX"])[rows], ref_rows["dX"], TOL_CHAIN, "dX rows")
     cols = np.sort(rng.choice(I, 12, replace=False))
-    Gc, Uc = Xf @ Wg[:, cols], Xf @ Wu[:, cols]
-    dGc, dUc = O.activation_backward("swiglu", Gc, dY @ Wd[cols].T, Uc)
+    ref_cols = O.mlp_backward(Xf, Wg[:, cols], Wd[cols], 1, dY, "swiglu", W_up=Wu[:, cols])
     Is = I // tp
     dW1 = host(g["dW1"]).reshape(I, H)[cols]  # storage [tp][I/tp][H] = [I][H] rows
     dWu = host(g["dW_up"]).reshape(I, H)[cols]
-    assert_close(dW1, dGc.T @ Xf, TOL_CHAIN, "dW1 rows")
-    assert_close(dWu, dUc.T @ Xf, TOL_CHAIN, "dW_up rows")
+    assert_close(dW1, ref_cols["dW1"][0].T, TOL_CHAIN, "dW1 rows")
+    assert_close(dWu, ref_cols["dW_up"][0].T, TOL_CHAIN, "dW_up rows")
     dW2 = host(g["dW2"])  # [tp][H][I/tp]
-    Hc = O.swiglu(Gc, Uc)
     got = np.stack([dW2[c // Is, :, c % Is] for c in cols])  # [len(cols)][H]
-    assert_close(got, Hc.T @ dY, TOL_CHAIN, "dW2 columns")
+    assert_close(got, ref_cols["dW2"][0], TOL_CHAIN, "dW2 columns")

@@ -9,7 +9,7 @@ import torch
 
 import synth_inputs as S
 from oracle import tp_oracle as O
-from tests._util import TOL_BF16, assert_close, dev, f64, sample_rows
+from tests._util import TOL_BF16, assert_close, dev, f64, host, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -100,23 +100,32 @@ def test_stack4_lmhead_full():
     x = torch.from_numpy(d["X"]).to("cuda")          # fp32 residual stream
     x1 = torch.empty_like(x)
     h = torch.empty(x.shape, dtype=B, device="cuda")  # bf16 GEMM input
+    rows = sample_rows(T, 48)
+    block_io = []  # the GPU's fp32 residual stream into and out of each block, sampled rows
     for Lw in layers:   # the same call sequence bench.py times
+        x_in = host(x[rows])
         tpl.tp_rmsnorm(x, out=h)
         tpl.tp_attn_proj(h, Lw["qkv"], Lw["o"], residual=x, out=x1)
         tpl.tp_rmsnorm(x1, out=h)
         tpl.tp_mlp_block(h, Lw["g"], Lw["d"], W_up=Lw["u"], residual=x1, act="swiglu", out=x1)
         x = x1
+        block_io.append((x_in, host(x[rows])))
     tpl.tp_rmsnorm(x, out=h)
     logits = tpl.tp_column_linear(h, lm, concat=True)
     assert tpl.tp_get_error() == 0
-    rows = sample_rows(T, 48)
     Ls = [{k: f64(v) for k, v in L.items()} for L in d["layers"]]
+    # Each block on its own, inside the real stack: the oracle's block fed the
+    # GPU's own fp32 input to that block holds the GPU block's output to the
+    # bf16 bound (rows are independent through a block).
+    for b, (x_in, x_out) in enumerate(block_io):
+        ref_b = O.transformer_block(x_in, Ls[b], tp, hq, hkv, hd)
+        assert_close(x_out, ref_b, TOL_BF16, f"stack block {b} on its own input")
     ref = O.stack_forward(f64(d["X"][rows]), Ls, f64(d["W_lm"]), tp, hq, hkv, hd)
     # Four blocks compound the bf16 rounding of every GEMM input (the normed
     # activations, V, Hs; logits are stored bf16). The model below rounds just
     # those tensors on the same rows, with no GPU involved: it lands above 2e-2
     # on its own, so the end-to-end bound is 5e-2 (each block alone meets 2e-2
-    # in the block tests).
+    # in the checks above).
     model_err = bf16_storage_model_error(f64(d["X"][rows]), Ls, f64(d["W_lm"]), ref, hq, hkv, hd)
     assert model_err > TOL_BF16
     assert_close(logits[rows], ref, TOL_STACK, "4-block stack + LM head")
@@ -135,11 +144,11 @@ def bf16_storage_model_error(X, Ls, Wlm, ref, hq, hkv, hd):
     group = hq // hkv
     for L in Ls:
         h = bf(O.rmsnorm(x))
-        V = bf(h @ L["Wv"])
+        V = bf(O.linear(h, L["Wv"]))
         ctx = np.concatenate([V[:, (q // group) * hd:(q // group + 1) * hd] for q in range(hq)], 1)
-        x = x + ctx @ L["Wo"]
+        x = x + O.linear(ctx, L["Wo"])
         h = bf(O.rmsnorm(x))
-        g, u = h @ L["Wg"], h @ L["Wu"]
-        x = x + bf(O.silu(g) * u) @ L["Wd"]
-    y = bf(bf(O.rmsnorm(x)) @ Wlm)
+        g, u = O.linear(h, L["Wg"]), O.linear(h, L["Wu"])
+        x = x + O.linear(bf(O.swiglu(g, u)), L["Wd"])
+    y = bf(O.linear(bf(O.rmsnorm(x)), Wlm))
     return float(np.abs(y - ref).max() / np.sqrt(np.mean(ref ** 2)))

@@ -2,9 +2,11 @@
 
 Every mbarrier wait in the GEMM kernel is bounded. A test-only switch makes
 the first CTA of the next GEMM launch withhold one operand load, so the MMA
-warp's wait on that stage runs out (after a 100 ms limit set for the test);
-in a paired launch the other CTA of the pair, which misses the withheld half
-of the shared B tile, runs out too.
+warp's wait on that stage runs out (after a 100 ms limit set for the test).
+In a paired launch (the 2-SM MMA, cta_group::2) each CTA of the pair loads
+its own half of the operands, and both halves count on one barrier of the
+even CTA, so a half withheld by either CTA starves the pair's MMA; no TMA
+multicast is involved.
 The kernel then raises its abort flag, drains the copies and MMAs it started,
 frees its tensor memory and returns; the host reads TP_ERR_TIMEOUT from
 tp_get_error(), and the next launch on the same context computes correctly.
@@ -39,7 +41,8 @@ def short_wait_limit():
 @pytest.mark.parametrize("path", ["whole_tiles", "cluster_pairs", "weight_streaming"])
 def test_expired_wait_is_reported_and_context_survives(short_wait_limit, path):
     # 300 tokens: 3 token blocks, single CTAs; 512 tokens: 4 blocks, CTA pairs
-    # sharing B tiles by multicast (the withheld load starves both CTAs of the pair)
+    # on the 2-SM MMA, each CTA loading its own operand half (the withheld load
+    # starves the pair's MMA)
     T = {"whole_tiles": 300, "cluster_pairs": 512, "weight_streaming": 8}[path]
     K, N, tp = 256, 2 * 1024, 2
     X, W = S.normal(101, (T, K)), S.normal(102, (K, N), 0.05)

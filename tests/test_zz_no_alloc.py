@@ -8,7 +8,9 @@ times in a row and compared with the existing tp_mlp_block, which takes a
 caller workspace, within the bf16 tolerance of the other tests
 (max|a - b| <= 2e-2 * RMS), and with the oracle. Requests whose workspace
 would exceed the static array are refused with TP_ERR_WORKSPACE before
-anything is launched. This file is collected last so that a failure here
+anything is launched. The second call must leave the device's free memory
+exactly as it found it (a cudaMalloc inside would take at least one 2 MiB
+page). This file is collected last so that a failure here
 cannot hide the other tests' results; it also passes on its own in a fresh
 process (the first call on the device performs the one-time address lookup).
 """
@@ -52,7 +54,12 @@ def test_static_workspace_matches_caller_workspace(T, H, I, tp):
                               residual=f64(R))
     for call in range(2):  # two calls in a row share (and reuse) the static array
         Y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         assert call_static(X, T, Sg, Su, Sd, Rd, Y) == 0
+        torch.cuda.synchronize()
+        if call == 1:  # after the first call, a call takes no device memory at all
+            assert torch.cuda.mem_get_info()[0] == free_before, "the call changed free device memory"
         assert tpl.tp_get_error() == 0
         assert_close(Y, host(Y_ref), TOL_BF16, f"static vs caller workspace, call {call}")
         assert_close(Y, oracle_Y, TOL_BF16, f"static vs oracle, call {call}")
