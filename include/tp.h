@@ -502,11 +502,14 @@ tp_status tp_attn_proj(const void* X, int64_t T, const tp_shards* Wqkv, const tp
  *   qkv   [tp][T][(nq + 2 nkv) * hd] bf16, the layout tp_column_linear writes
  *         for a tp_shard_qkv view (q heads | k heads | v heads per shard).
  *   ctx   [tp][T][nq * hd] bf16, written.
- *   hd must be 128 (TP_ERR_UNSUPPORTED otherwise). Scores, the softmax and
- *   the P V accumulation are fp32; P is rounded to bf16 before P V.
+ *   hd must be 64 or 128 (TP_ERR_UNSUPPORTED otherwise). Scores, the
+ *   softmax and the P V accumulation are fp32; P is rounded to bf16 before
+ *   P V.
  *   T = 0 is a no-op (null pointers allowed). The launch is persistent, one
- *   CTA per SM over the hq * ceil(T / 128) work units; more than 2^30 - 1
- *   units is TP_ERR_UNSUPPORTED.
+ *   CTA per SM; a work unit is two tiles of 128 queries that read the same
+ *   keys (two q heads of one kv head, or two query blocks of one head), so
+ *   there are about hq * ceil(T / 128) / 2 units; hq * ceil(T / 128) above
+ *   2^30 - 1 is TP_ERR_UNSUPPORTED.
  * Ownership: both buffers belong to the caller; nothing is allocated. The
  * call is asynchronous on `stream`; a bounded device wait that expired shows
  * as TP_ERR_TIMEOUT from tp_get_error.
@@ -518,13 +521,13 @@ tp_status tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int 
 /*
  * tp_attn_block - tp_attn_proj with the attention core chosen by `mode`:
  * TP_ATTN_SINGLE_KEY (as tp_attn_proj without ctx), TP_ATTN_CAUSAL or
- * TP_ATTN_FULL (tp_attention between the QKV and O launches; bf16, hd 128).
+ * TP_ATTN_FULL (tp_attention between the QKV and O launches; bf16, hd 64 or 128).
  * Arguments otherwise as tp_attn_proj; the workspace holds qkv (unless
  * qkv_out is given), the context and the split-tile scratch
  * (tp_attn_workspace_bytes).
  * Errors: as tp_attn_proj, plus TP_ERR_MODE for an unknown mode and
  * TP_ERR_UNSUPPORTED for a core other than the single-key one on fp32 views,
- * hd != 128 or more than 2^30 - 1 work units (as tp_attention).
+ * hd other than 64 and 128, or too many query blocks (as tp_attention).
  */
 tp_status tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const tp_shards* Wo, int mode,
                         const void* residual, int out_dtype, void* qkv_out, void* workspace, size_t ws_bytes, void* Y,
@@ -541,6 +544,18 @@ tp_status tp_attn_block(const void* X, int64_t T, const tp_shards* Wqkv, const t
  */
 tp_status tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
                      int out_dtype, void* stream);
+
+/*
+ * tp_last_cuda_error - the error code of the most recent CUDA call made by
+ * this library on the calling host thread that failed (a cudaError_t, or
+ * the CUresult of a tensor-map encoding), 0 if none has failed. A call that
+ * returned TP_ERR_CUDA has set it; it is not cleared by later successes.
+ * tp_cuda_error_name - the runtime's name for such a code (a static
+ * string). The pages have no counterpart: these say why TP_ERR_CUDA was
+ * returned.
+ */
+int tp_last_cuda_error(void);
+const char* tp_cuda_error_name(int code);
 
 /*
  * tp_get_error - synchronise `stream`, then report and clear the device

@@ -98,7 +98,7 @@ __all__ = [
     "column_parallel", "all_gather", "row_parallel_partials", "all_reduce",
     "reduce_scatter", "relu", "gelu", "silu", "swiglu", "ACTIVATIONS",
     "mlp_block", "qkv_head_layout", "qkv_shards", "context_standin",
-    "attention_head", "context_attention", "attn_proj", "rmsnorm",
+    "attention_weights", "attention_head", "context_attention", "attn_proj", "rmsnorm",
     "transformer_block", "stack_forward",
     "activation_backward", "column_linear_backward", "row_linear_backward",
     "mlp_backward_saved", "mlp_backward", "vocab_shards", "vocab_embedding", "log_softmax_normaliser",
@@ -328,13 +328,11 @@ def context_standin(qkv_s, q_heads, kv_heads, hq, hkv, hd):
     return np.concatenate(cols, axis=1)
 
 
-def attention_head(q, k, v, causal=True, q_offset=0):
-    """Scaled dot-product attention of one head: softmax(q k^T / sqrt(hd)) v,
-    the softmax over keys, with query t restricted to keys 0..t when causal.
-    q is [Tq, hd] holding the queries at positions q_offset..q_offset+Tq-1;
-    k, v are [T, hd]. [CTP] attention heads (each GPU runs the attention of
-    its own heads); [TUT] self-attention block sharding (heads are local
-    between the QKV and output projections)."""
+def attention_weights(q, k, causal=True, q_offset=0):
+    """The attention weights of one head, softmax(q k^T / sqrt(hd)) over the
+    keys, with query t restricted to keys 0..t when causal (a key it may not
+    see has weight 0). q is [Tq, hd] holding the queries at positions
+    q_offset..q_offset+Tq-1; k is [T, hd]. Returns [Tq, T]."""
     Tq, hd = q.shape
     s = (q @ k.T) / math.sqrt(hd)
     if causal:
@@ -342,8 +340,15 @@ def attention_head(q, k, v, causal=True, q_offset=0):
         s = np.where(np.arange(k.shape[0])[None, :] <= pos, s, -np.inf)
     s = s - s.max(axis=1, keepdims=True)
     p = np.exp(s)
-    p = p / p.sum(axis=1, keepdims=True)
-    return p @ v
+    return p / p.sum(axis=1, keepdims=True)
+
+
+def attention_head(q, k, v, causal=True, q_offset=0):
+    """Scaled dot-product attention of one head: the attention weights times
+    v ([T, hd]). [CTP] attention heads (each GPU runs the attention of its
+    own heads); [TUT] self-attention block sharding (heads are local between
+    the QKV and output projections)."""
+    return attention_weights(q, k, causal, q_offset) @ v
 
 
 def context_attention(qkv_s, q_heads, kv_heads, hq, hkv, hd, causal=True):

@@ -71,6 +71,8 @@ _SIGS = {
     "tp_attention": (_i32, [_vp, _i64, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "tp_rmsnorm": (_i32, [_vp, _vp, _i64, _i64, _f32, _i32, _vp, _i32, _vp]),
     "tp_get_error": (_i32, [_vp]),
+    "tp_last_cuda_error": (_i32, []),
+    "tp_cuda_error_name": (ctypes.c_char_p, [_i32]),
     "tp_row_linear_backward": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp]),
     "tp_column_linear_backward": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "tp_mlp_backward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
@@ -92,7 +94,11 @@ for _name, (_res, _args) in _SIGS.items():
 class TpError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__(f"{fn}: status {status} ({tp_status_string(status)})")
+        msg = f"{fn}: status {status} ({tp_status_string(status)})"
+        if status == 7:  # TP_ERR_CUDA: name the failing CUDA call's code
+            code = lib.tp_last_cuda_error()
+            msg += f": CUDA code {code} ({lib.tp_cuda_error_name(code).decode()})"
+        super().__init__(msg)
 
 
 def tp_status_string(status: int) -> str:
@@ -501,7 +507,7 @@ def tp_attn_block(X, Wqkv: Shards, Wo: Shards, attention: str = "causal", residu
 
 def tp_attention(qkv, hq: int, hkv: int, hd: int, causal: bool = True, out=None):
     """Attention core of every local head: qkv [tp, T, (nq + 2 nkv) * hd] ->
-    ctx [tp, T, nq * hd] (bf16, hd 128)."""
+    ctx [tp, T, nq * hd] (bf16, hd 64 or 128)."""
     tp, T, _ = qkv.shape
     if out is None:
         out = torch.empty((tp, T, hq // tp * hd), dtype=qkv.dtype, device=qkv.device)

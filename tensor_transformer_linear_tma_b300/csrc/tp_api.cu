@@ -44,19 +44,27 @@ inline bool ptr_ok(const void* p, int dtype) {
   return p == nullptr || aligned(p, dtype == TP_BF16 ? 16 : 4);
 }
 
-int launch_status() {
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+// The code of the last CUDA runtime or driver call of this library that
+// failed on the calling host thread (tp_last_cuda_error).
+thread_local int g_last_cuda_error = 0;
+
+// Records a failed call's code; true when the call succeeded.
+inline bool cuda_ok(cudaError_t e) {
+  if (e == cudaSuccess) return true;
+  g_last_cuda_error = static_cast<int>(e);
+  return false;
 }
+
+int launch_status() { return cuda_ok(cudaGetLastError()) ? TP_OK : TP_ERR_CUDA; }
 
 int num_sms() {
   static int cache[128] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (!cuda_ok(cudaGetDevice(&dev))) return 0;
   if (dev < 0 || dev >= 128) return 0;
   if (cache[dev] == 0) {
     int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (!cuda_ok(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev))) return 0;
     cache[dev] = v;
   }
   return cache[dev];
@@ -97,9 +105,11 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, u
   const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
   const cuuint32_t box[3] = {64, box1, 1};
   const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) g_last_cuda_error = static_cast<int>(r);
+  return r == CUDA_SUCCESS;
 }
 
 // 3-D map for bulk tensor stores of an output [d2][d1][d0] (d0 contiguous)
@@ -113,9 +123,11 @@ bool make_store_map(CUtensorMap* m, void* base, bool f32, uint64_t d0, uint64_t 
   const cuuint64_t strides[2] = {s1, s2};
   const cuuint32_t box[3] = {f32 ? 32u : 64u, 32, 1};
   const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides,
-            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) g_last_cuda_error = static_cast<int>(r);
+  return r == CUDA_SUCCESS;
 }
 
 // Output maps of a token-major launch (unused by the weight-streaming one).
@@ -210,10 +222,10 @@ bool smem_attr_set() {
   using Cfg = tpk::GemmCfg<KIND, SWAP, PAIR>;
   static bool done[128] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
+  if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= 128) return false;
   if (!done[dev]) {
-    if (cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, PAIR, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM_BYTES) != cudaSuccess)
+    if (!cuda_ok(cudaFuncSetAttribute(tpk::tp_gemm_kernel<KIND, SWAP, PAIR, MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM_BYTES)))
       return false;
     done[dev] = true;
   }
@@ -228,7 +240,7 @@ int max_cluster_pairs() {
   using Cfg = tpk::GemmCfg<KIND, false, true>;
   static int cache[128] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= 128) return 0;
   if (cache[dev] == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * std::max(1, num_sms() / 2));
@@ -242,7 +254,7 @@ int max_cluster_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tpk::tp_gemm_kernel<KIND, false, true, MN>, &cfg) != cudaSuccess ||
+    if (!cuda_ok(cudaOccupancyMaxActiveClusters(&n, tpk::tp_gemm_kernel<KIND, false, true, MN>, &cfg)) ||
         n < 1) {
       cudaGetLastError();
       n = -1;
@@ -306,8 +318,7 @@ int pair_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, false, true, MN>, a0, a1, b0, b1, om.y, om.c, args) !=
-      cudaSuccess)
+  if (!cuda_ok(cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, false, true, MN>, a0, a1, b0, b1, om.y, om.c, args)))
     return TP_ERR_CUDA;
   return launch_status();
 }
@@ -340,8 +351,7 @@ int gemm_launch(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap&
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, SWAP, false>, a0, a1, b0, b1, om.y, om.c, args) !=
-      cudaSuccess)
+  if (!cuda_ok(cudaLaunchKernelEx(&cfg, tpk::tp_gemm_kernel<KIND, SWAP, false>, a0, a1, b0, b1, om.y, om.c, args)))
     return TP_ERR_CUDA;
   return launch_status();
 }
@@ -671,11 +681,14 @@ size_t mlp_max_tiles(int64_t H, int64_t I, int tp) {
   const size_t swap_row = cdiv(H, 128);
   return std::max<size_t>(2 * SK_MAX_CTAS, std::max(swap_col, swap_row));
 }
-// Attention core over qkv [tp][T][(nq + 2 nkv) * 128] (q | k | v per
-// shard) into ctx [tp][T][nq * 128]; mode TP_ATTN_CAUSAL or TP_ATTN_FULL.
-int attention_launch(const void* qkv, int64_t T, int tp, int hq, int hkv, int mode, void* ctx, cudaStream_t st) {
+// Attention core over qkv [tp][T][(nq + 2 nkv) * hd] (q | k | v per
+// shard) into ctx [tp][T][nq * hd]; mode TP_ATTN_CAUSAL or TP_ATTN_FULL,
+// hd 64 or 128.
+template <int HD>
+int attention_launch_hd(const void* qkv, int64_t T, int tp, int hq, int hkv, int mode, void* ctx, cudaStream_t st) {
+  using Cfg = tpk::AttnCfg<HD>;
   const int nq = hq / tp, nkv = hkv >= tp ? hkv / tp : 1;
-  const int64_t nqkv = static_cast<int64_t>(nq + 2 * nkv) * tpk::AT_HD;
+  const int64_t nqkv = static_cast<int64_t>(nq + 2 * nkv) * HD;
   CUtensorMap m;
   if (!make_map_bf16(&m, qkv, nqkv, T, tp, 128)) return TP_ERR_CUDA;
   tpk::AttnArgs a{};
@@ -689,30 +702,41 @@ int attention_launch(const void* qkv, int64_t T, int tp, int hq, int hkv, int mo
   a.group = hq / hkv;
   a.causal = mode == TP_ATTN_CAUSAL ? 1 : 0;
   a.q_blocks = static_cast<int>(cdiv(T, 128));
-  a.units = tp * nq * a.q_blocks;
-  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(tpk::AT_HD)));
+  // two q heads of one kv head share a unit when the shard's heads pair up
+  // that way (an even group, an even count per shard); else two query blocks
+  a.pair_heads = (a.group % 2 == 0 && nq % 2 == 0) ? 1 : 0;
+  a.units = a.pair_heads ? a.q_blocks * tp * (nq / 2) : static_cast<int>((a.q_blocks + 1) / 2) * tp * nq;
+  a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(HD)));
   static bool attr_done[128] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return TP_ERR_CUDA;
+  if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= 128) return TP_ERR_CUDA;
   if (!attr_done[dev]) {
-    if (cudaFuncSetAttribute(tpk::tp_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tpk::AT_SMEM) !=
-        cudaSuccess)
+    if (!cuda_ok(cudaFuncSetAttribute(tpk::tp_attn_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM)))
       return TP_ERR_CUDA;
     attr_done[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   // persistent: one CTA per SM (each holds all of its SM's TMEM), none idle
   cfg.gridDim = dim3(static_cast<unsigned>(std::min(a.units, std::max(1, num_sms()))));
-  cfg.blockDim = dim3(tpk::AT_THREADS);
-  cfg.dynamicSmemBytes = tpk::AT_SMEM;
+  cfg.blockDim = dim3(Cfg::THREADS);
+  cfg.dynamicSmemBytes = Cfg::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, tpk::tp_attn_kernel, m, a) != cudaSuccess) return TP_ERR_CUDA;
+  if (!cuda_ok(cudaLaunchKernelEx(&cfg, tpk::tp_attn_kernel<HD>, m, a))) return TP_ERR_CUDA;
   return launch_status();
+}
+
+inline bool attention_hd_ok(int hd) { return hd == 64 || hd == 128; }
+
+int attention_launch(const void* qkv, int64_t T, int tp, int hq, int hkv, int hd, int mode, void* ctx,
+                     cudaStream_t st) {
+  if (hd == 64) return attention_launch_hd<64>(qkv, T, tp, hq, hkv, mode, ctx, st);
+  if (hd == 128) return attention_launch_hd<128>(qkv, T, tp, hq, hkv, mode, ctx, st);
+  return TP_ERR_UNSUPPORTED;
 }
 
 size_t attn_max_tiles(int64_t H, int hq, int hkv, int hd, int tp) {
@@ -999,12 +1023,12 @@ void* g_static_ptr[128] = {};
 
 int static_workspace(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TP_ERR_CUDA;
+  if (!cuda_ok(cudaGetDevice(&dev))) return TP_ERR_CUDA;
   if (dev < 0 || dev >= 128) return TP_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_static_mu);
   if (!g_static_ptr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return TP_ERR_CUDA;
+    if (!cuda_ok(cudaGetSymbolAddress(&p, g_static_workspace)) || !p) return TP_ERR_CUDA;
     g_static_ptr[dev] = p;
   }
   *out = g_static_ptr[dev];
@@ -1065,7 +1089,7 @@ int attn_block_impl(const void* X, int64_t T, const tp_shards* Wqkv, const tp_sh
   if (dt == TP_BF16 && hd % 8) return TP_ERR_ALIGN;
   if (Wqkv->K > static_cast<int64_t>(hq) * hd * 4) return TP_ERR_UNSUPPORTED;  // scratch sizing bound
   if (mode != TP_ATTN_SINGLE_KEY && mode != TP_ATTN_CAUSAL && mode != TP_ATTN_FULL) return TP_ERR_MODE;
-  if (mode != TP_ATTN_SINGLE_KEY && (dt != TP_BF16 || hd != tpk::AT_HD)) return TP_ERR_UNSUPPORTED;
+  if (mode != TP_ATTN_SINGLE_KEY && (dt != TP_BF16 || !attention_hd_ok(hd))) return TP_ERR_UNSUPPORTED;
   if (mode != TP_ATTN_SINGLE_KEY && static_cast<int64_t>(hq) * cdiv(T, 128) > INT32_MAX / 2)
     return TP_ERR_UNSUPPORTED;  // the core counts its work units in int
   if (ws_bytes < tp_attn_workspace_bytes(T, hq, hkv, hd, tp, dt)) return TP_ERR_WORKSPACE;
@@ -1085,7 +1109,7 @@ int attn_block_impl(const void* X, int64_t T, const tp_shards* Wqkv, const tp_sh
   }
   if (mode != TP_ATTN_SINGLE_KEY) {
     if ((r = run_col(X, T, Wqkv, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, qkv, st, scp))) return r;
-    if ((r = attention_launch(qkv, T, tp, hq, hkv, mode, ctx_ws, st))) return r;
+    if ((r = attention_launch(qkv, T, tp, hq, hkv, hd, mode, ctx_ws, st))) return r;
     return run_row(ctx_ws, T, Wo, nullptr, residual, Y, out_dtype, nullptr, st, scp);
   }
   // Without a caller context the single-key stand-in is used: on the bf16
@@ -1130,11 +1154,11 @@ tp_status tp_attention(const void* qkv, int64_t T, int tp, int hq, int hkv, int 
   if (T < 0 || tp < 1 || hq < 1 || hkv < 1 || hd < 1 || tp_qkv_shard_elems(1, hq, hkv, hd, tp) == 0)
     return TP_ERR_SHAPE;
   // (work units, one per shard, q head and 128 queries, are counted in int)
-  if (hd != tpk::AT_HD || T > INT32_MAX || static_cast<int64_t>(hq) * cdiv(T, 128) > INT32_MAX / 2)
+  if (!attention_hd_ok(hd) || T > INT32_MAX || static_cast<int64_t>(hq) * cdiv(T, 128) > INT32_MAX / 2)
     return TP_ERR_UNSUPPORTED;
   if (!ptr_ok(qkv, TP_BF16) || !ptr_ok(ctx, TP_BF16)) return TP_ERR_ALIGN;
   if (T == 0) return TP_OK;
-  return as_status(attention_launch(qkv, T, tp, hq, hkv, mode, ctx, as_stream(stream)));
+  return as_status(attention_launch(qkv, T, tp, hq, hkv, hd, mode, ctx, as_stream(stream)));
 }
 
 tp_status tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, float eps, int dtype, void* Y,
@@ -1164,13 +1188,20 @@ tp_status tp_rmsnorm(const void* X, const void* gamma, int64_t T, int64_t H, flo
   return as_status(launch_status());
 }
 
+int tp_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* tp_cuda_error_name(int code) {
+  const char* name = cudaGetErrorName(static_cast<cudaError_t>(code));
+  return name ? name : "unrecognised CUDA error code";
+}
+
 tp_status tp_get_error(void* stream) {
-  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return TP_ERR_CUDA;
+  if (!cuda_ok(cudaStreamSynchronize(as_stream(stream)))) return TP_ERR_CUDA;
   int err = 0;
-  if (cudaMemcpyFromSymbol(&err, tpk::g_tp_error, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
+  if (!cuda_ok(cudaMemcpyFromSymbol(&err, tpk::g_tp_error, sizeof(int)))) return TP_ERR_CUDA;
   if (err != 0) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(tpk::g_tp_error, &zero, sizeof(int)) != cudaSuccess) return TP_ERR_CUDA;
+    if (!cuda_ok(cudaMemcpyToSymbol(tpk::g_tp_error, &zero, sizeof(int)))) return TP_ERR_CUDA;
     return err == tpk::TP_DEVERR_WAIT_TIMEOUT ? TP_ERR_TIMEOUT
            : err == tpk::TP_DEVERR_INDEX      ? TP_ERR_INDEX
                                               : TP_ERR_CUDA;
@@ -1180,12 +1211,12 @@ tp_status tp_get_error(void* stream) {
 
 tp_status tp_debug_set_wait_limit_ns(uint64_t ns) {
   const unsigned long long v = ns;
-  return as_status(cudaMemcpyToSymbol(tpk::g_tp_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? TP_OK : TP_ERR_CUDA);
+  return cuda_ok(cudaMemcpyToSymbol(tpk::g_tp_wait_limit_ns, &v, sizeof(v))) ? TP_OK : TP_ERR_CUDA;
 }
 
 tp_status tp_debug_inject(int kind) {
   if (kind < 0 || kind > 1) return TP_ERR_MODE;
-  return as_status(cudaMemcpyToSymbol(tpk::g_tp_inject, &kind, sizeof(int)) == cudaSuccess ? TP_OK : TP_ERR_CUDA);
+  return cuda_ok(cudaMemcpyToSymbol(tpk::g_tp_inject, &kind, sizeof(int))) ? TP_OK : TP_ERR_CUDA;
 }
 
 }  // extern "C"
@@ -1395,7 +1426,7 @@ tp_status tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int6
   if (T < 0 || V < 1 || tp < 1 || V % tp != 0) return TP_ERR_SHAPE;
   if (ws_bytes < tp_cross_entropy_workspace_bytes(T, V, tp)) return TP_ERR_WORKSPACE;
   if (T == 0) {
-    if (mean_loss && cudaMemsetAsync(mean_loss, 0, sizeof(float), as_stream(stream)) != cudaSuccess)
+    if (mean_loss && !cuda_ok(cudaMemsetAsync(mean_loss, 0, sizeof(float), as_stream(stream))))
       return TP_ERR_CUDA;
     return TP_OK;
   }

@@ -2,51 +2,47 @@
 // ctx_h = softmax(q_h k_g^T / sqrt(hd)) v_g for every q head h of a shard,
 // g = h / (hq / hkv) its kv head ("CUDA tensor parallel computations" page,
 // attention heads; tutorial page, self-attention block sharding), causal
-// (query t sees keys 0..t) or unmasked.
+// (query t sees keys 0..t) or unmasked. Head size 64 or 128 (template HD).
 //
-// Work units are (shard, q head, block of 128 queries), head size 128. The
-// kernel is persistent: one CTA per SM (all of TMEM is allocated) walks its
-// units, the longest (latest, under the causal mask) first, in alternating
-// directions from wave to wave. Within a CTA the ring, the score buffers and
-// their barriers run on across units, so the next unit's Q, K and V tiles
-// are loaded, and its first scores computed, while the softmax warps write
-// the last unit's output. 320 threads:
-//   warp 0      TMA producer: the Q tile once, then the K and V tiles of
-//               each block of 128 keys through a ring of six 32 KB slots (a
-//               K slot is released as soon as Q K^T has read it, a V slot
-//               after P V), three key blocks of lookahead;
-//   warp 1      TMEM owner and MMA issuer (one elected lane issues):
-//               S = Q K^T into one of two TMEM score buffers (one key
-//               block ahead of the softmax), then
-//               O += P V into the TMEM output accumulator. Q and P are the
-//               A operands and sit in TMEM; only K and V are read from
-//               shared memory (V as an MN-major operand straight from its
-//               TMA tile), which halves the tensor core's shared-memory
-//               traffic against staging Q and P there;
-//   warps 2..9  softmax, two threads per query row (warps w and w+4 share
-//               a TMEM lane quadrant; each takes 64 of the block's 128
-//               keys and the matching 64 output columns). They copy each
-//               unit's Q from its TMA tile into TMEM, the next unit's as
-//               soon as the last scores of the current one are in (every
-//               S MMA that read the old Q is then complete), before they
-//               write the current unit's output. Per key block: scores from
-//               TMEM, online maximum (exchanged between the two halves of a
-//               row through shared memory) and sum in fp32, exp2 with the
-//               log2(e)/sqrt(hd) scale folded into one FFMA, P packed to
-//               bf16 and stored over the first half of its own scores; at
-//               the end O / l.
+// A work unit is two query tiles of 128 rows that read the same keys and
+// values: two q heads of one kv head over one block of queries (when the
+// heads of a shard pair up that way), else two consecutive query blocks of
+// one head. The tiles share every K and V tile the ring brings in, and the
+// tensor core alternates between them: while the softmax of one tile runs,
+// it computes the other tile's P V and next scores, so the exponentials
+// and the MMAs overlap.
+//
+// The kernel is persistent: one CTA per SM (all of TMEM is allocated)
+// walks its units, the longest (latest, under the causal mask) first, in
+// alternating directions from wave to wave. 320 threads:
+//   warp 0      TMA producer: each unit's two Q tiles (tile t once the last
+//               unit's scores of tile t are computed), then the K and V
+//               tiles of each block of 128 keys through a ring, K(j), V(j),
+//               K(j+1), ... (the ring runs on across units);
+//   warp 1      TMEM owner and MMA issuer (all lanes run the loop, one
+//               elected lane issues): S_t = Q_t K^T with both operands in
+//               shared memory, into tile t's score buffer, and
+//               O_t += P_t V with P_t in TMEM (over the first half of its
+//               scores) and V an MN-major operand straight from its TMA
+//               tile. Per key block the order is P_0 V, S_0(next),
+//               P_1 V, S_1(next);
+//   warps 2..5  softmax of tile 0, warps 6..9 of tile 1, one thread per
+//               query row: the row's 128 scores from TMEM, the row maximum,
+//               exp2 with the log2(e)/sqrt(hd) scale folded into one paired
+//               FMA, the row sum, P packed to bf16 and stored over the
+//               scores; at the end of a unit O / l to the context.
 // The exponent base m only moves when a row's maximum exceeds it by more
 // than 2^8 (P then stays below 256, exact enough in bf16), so O and l are
-// rescaled in TMEM only on such jumps.
-// The tensor core runs tcgen05 operations in issue order, so S(j + 2) may be
-// issued into the buffer that holds P(j) as soon as P(j) V has been issued.
-// P V of block j commits to the barrier of buffer j & 1: a softmax thread
-// waits on it only to rescale O or to read the result, and since S(j) was
-// issued after P(j - 2) V, each wait's barrier is at most one phase behind.
+// rescaled only on such jumps. S_t(j) is issued after P_t(j-1) V, and a
+// commit arrives once every earlier MMA of the issuer is complete, so the
+// scores of block j reaching the softmax mean that O_t holds blocks
+// 0..j-1 and no MMA writes it: the rescale needs no other wait.
+// The tensor core runs tcgen05 operations in issue order, so S_t(j+1) may be
+// issued into the buffer that holds P_t(j) right after P_t(j) V.
 // Every wait is bounded as in the GEMM kernel.
 #pragma once
 
-#include "tp_gemm.cuh"  // epi_any, store_bf16x8_f
+#include "tp_gemm.cuh"  // store_bf16x8_f
 #include "tp_ptx.cuh"
 
 namespace tpk {
@@ -58,42 +54,57 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Barrier over the two softmax warps of TMEM lane quadrant q (named barriers
-// 2..5) that ORs a predicate, so that both take the same branch.
-__device__ __forceinline__ bool pair_any(int q, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %2, 0;\n\t"
-      "bar.red.or.pred po, %1, 64, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}\n"
-      : "=r"(r)
-      : "r"(2 + q), "r"(static_cast<uint32_t>(v))
-      : "memory");
-  return r != 0;
+// Two fp32 values in one 64-bit register pair (the first in the low half),
+// for the paired fp32 instructions: one instruction, two results.
+__device__ __forceinline__ uint64_t f2_make(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max(a, b, c). (Written with two fmaxf: the three-input max.f32 of inline
+// PTX returned about 0 for all-negative inputs on this toolchain, so it is
+// not used.)
+__device__ __forceinline__ float fmax3(float a, float b, float c) { return fmaxf(fmaxf(a, b), c); }
 
 struct AttnArgs {
   __nv_bfloat16* ctx;  // [tp][T][nq * hd]
   int T, tp, hq, hkv, nq, nkv, group;
   int causal;
   int q_blocks;        // ceil(T / 128)
-  int units;           // tp * nq * q_blocks work units; the grid has at most this many CTAs
+  int pair_heads;      // 1: a unit's tiles are q heads 2i, 2i+1 (one kv head) over one query block;
+                       // 0: query blocks 2i, 2i+1 of one head
+  int units;           // work units; the grid has at most this many CTAs
   float scale_log2;    // log2(e) / sqrt(hd)
 };
 
-constexpr int AT_ROWS = 128;                   // queries per CTA, keys per block
-constexpr int AT_HD = 128;                     // head size
-constexpr int AT_PANEL = AT_ROWS * 128;        // 128 rows x 128 bytes (64 bf16 columns)
-constexpr int AT_TILE = 2 * AT_PANEL;          // 128 x 128 bf16 as two 64-column panels
-constexpr int AT_THREADS = 320;
-constexpr int AT_SOFTMAX_THREADS = 256;
-constexpr int AT_SLOTS = 6;                        // K/V ring slots
-constexpr int AT_SMEM = (1 + AT_SLOTS) * AT_TILE + 1024 + 2048;  // Q, ring; alignment; barriers, row exchange
-constexpr int AT_AUX = 512 + 2048;  // barriers, then the row exchange [2 blocks][2 halves][128] floats
-constexpr float AT_RESCALE_LOG2 = 8.0f;            // move the exponent base only on a jump above 2^8
-// TMEM columns (512 allocated): two score buffers, O, Q as packed bf16
-constexpr uint32_t AT_TM_S = 0, AT_TM_O = 256, AT_TM_Q = 384;
+template <int HD>
+struct AttnCfg {
+  static_assert(HD == 64 || HD == 128, "head size 64 or 128");
+  static constexpr int ROWS = 128;                  // queries per tile, keys per block
+  static constexpr int PANEL = ROWS * 128;          // 128 rows x 128 bytes (64 bf16 columns)
+  static constexpr int PANELS = HD / 64;
+  static constexpr int TILE = PANELS * PANEL;       // 128 x HD bf16
+  static constexpr int SLOTS = HD == 128 ? 5 : 8;   // K/V ring
+  static constexpr int THREADS = 320;
+  static constexpr int AUX = 256;                   // barriers, TMEM address, abort flag
+  static constexpr int SMEM = (2 + SLOTS) * TILE + AUX + 1024;  // Q tiles, ring, aux; alignment
+  static constexpr uint32_t TM_S = 0;               // scores / P of tile t at column 128 t
+  static constexpr uint32_t TM_O = 256;             // O of tile t at 256 + HD t
+};
+constexpr float AT_RESCALE_LOG2 = 8.0f;  // move the exponent base only on a jump above 2^8
 
 // The w-th unit of CTA c in a grid of g CTAs, or -1 past its last one.
 // Units are numbered longest first; wave w covers units w*g .. w*g + g - 1,
@@ -105,54 +116,101 @@ __device__ __forceinline__ int at_unit(int c, int g, int w, int units) {
 }
 
 struct AtUnit {
-  int qb, s, j;          // query block, shard, q head within the shard
-  int qcol, kcol, vcol;  // columns of its q, k and v head in the shard's qkv rows
-  int nkb;               // key blocks its queries see
+  int s;                     // shard
+  int qb[2], j[2];           // per tile: query block, q head within the shard
+  int nkb[2];                // key blocks the tile's queries see (0: no such tile)
+  int nkb_max;
+  int kcol, vcol;            // columns of the shared kv head in the shard's qkv rows
 };
 
-__device__ __forceinline__ AtUnit at_decode(const AttnArgs& a, int u) {
+__device__ __forceinline__ AtUnit at_decode(const AttnArgs& a, int u, int hd) {
   AtUnit w;
-  const int heads = a.tp * a.nq;
-  w.qb = a.q_blocks - 1 - u / heads;
-  const int hh = u % heads;
-  w.s = hh / a.nq;
-  w.j = hh % a.nq;
+  if (a.pair_heads) {
+    const int half = a.nq >> 1;
+    const int hp = a.tp * half;
+    const int qb = a.q_blocks - 1 - u / hp;
+    const int hh = u % hp;
+    w.s = hh / half;
+    w.j[0] = 2 * (hh % half);
+    w.j[1] = w.j[0] + 1;
+    w.qb[0] = w.qb[1] = qb;
+  } else {
+    const int heads = a.tp * a.nq;
+    const int qp = (a.q_blocks + 1) / 2 - 1 - u / heads;
+    const int hh = u % heads;
+    w.s = hh / a.nq;
+    w.j[0] = w.j[1] = hh % a.nq;
+    w.qb[0] = 2 * qp;
+    w.qb[1] = 2 * qp + 1;
+  }
   const int kv0 = a.hkv >= a.tp ? w.s * a.nkv : (w.s * a.hkv) / a.tp;
-  const int kvi = (w.s * a.nq + w.j) / a.group - kv0;  // the kv head within the shard's block
-  w.qcol = w.j * AT_HD;
-  w.kcol = (a.nq + kvi) * AT_HD;
-  w.vcol = (a.nq + a.nkv + kvi) * AT_HD;
-  w.nkb = a.causal ? w.qb + 1 : a.q_blocks;
+  const int kvi = (w.s * a.nq + w.j[0]) / a.group - kv0;  // the kv head within the shard's block
+  w.kcol = (a.nq + kvi) * hd;
+  w.vcol = (a.nq + a.nkv + kvi) * hd;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) w.nkb[t] = w.qb[t] >= a.q_blocks ? 0 : (a.causal ? w.qb[t] + 1 : a.q_blocks);
+  w.nkb_max = max(w.nkb[0], w.nkb[1]);
   return w;
 }
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
+// A moved exponent base (rare): this warp's rows of O_t (blocks 0..jb-1; no
+// MMA writes O_t until P_t(jb) is handed over, see the top of this file)
+// and, when the base moved in the block's second half, the first half's P,
+// stored with the old base, are multiplied by alpha (1 for rows whose base
+// stayed). Kept out of line: its registers are paid for only when it runs.
+template <int HD>
+__device__ __noinline__ void at_rescale(uint32_t tO, uint32_t tS, float alpha, bool o_too, bool p_too) {
+  if (o_too) {
+#pragma unroll 1
+    for (int c = 0; c < HD; c += 32) {
+      uint32_t rr[32];
+      tmem_ld32(tO + static_cast<uint32_t>(c), rr);
+      tmem_ld_wait_regs(rr);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+      tmem_st32(tO + static_cast<uint32_t>(c), rr);
+    }
+  }
+  if (p_too) {
+    uint32_t rr[32];
+    tmem_st_wait();  // the first half's P has been written
+    tmem_ld32(tS, rr);
+    tmem_ld_wait_regs(rr);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) rr[i] = pack_bf16x2(bf16_lo(rr[i]) * alpha, bf16_hi(rr[i]) * alpha);
+    tmem_st32(tS, rr);
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(320, 1)
     tp_attn_kernel(const __grid_constant__ CUtensorMap mapQKV, const AttnArgs a) {
+  using Cfg = AttnCfg<HD>;
+  constexpr int SLOTS = Cfg::SLOTS, TILE = Cfg::TILE, PANEL = Cfg::PANEL;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem;
-  uint8_t* ring = smem + AT_TILE;  // [AT_SLOTS]: K(j) is item 2j, V(j) item 2j+1
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (1 + AT_SLOTS) * AT_TILE);
-  uint64_t* q_full = bars;                // TMA -> softmax (a unit's Q tile landed)
-  uint64_t* q_tm = bars + 1;              // softmax -> MMA, TMA (that Q copied into TMEM; its tile free)
-  uint64_t* o_free = bars + 2;            // softmax -> MMA (a unit's O read out)
-  uint64_t* r_full = bars + 3;            // [AT_SLOTS] TMA -> MMA
-  uint64_t* r_empty = r_full + AT_SLOTS;  // [AT_SLOTS] MMA -> TMA
-  uint64_t* s_full = r_empty + AT_SLOTS;  // [2] MMA -> softmax (S of block gb in buffer gb & 1)
-  uint64_t* p_full = s_full + 2;          // [2] softmax -> MMA (P stored, O rescaled)
-  uint64_t* o_done = p_full + 2;          // [2] MMA -> softmax (P V of block gb complete, barrier gb & 1)
-  uint64_t* drain = o_done + 2;           // abort path only
+  uint8_t* sQ = smem;                // [2] Q tiles
+  uint8_t* ring = smem + 2 * TILE;   // [SLOTS]: K(j) is item 2j, V(j) item 2j+1
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + SLOTS) * TILE);
+  uint64_t* q_full = bars;                // [2] TMA -> MMA (a unit's Q tile t landed)
+  uint64_t* q_free = bars + 2;            // [2] MMA -> TMA (the unit's last S_t is computed: Q_t tile free)
+  uint64_t* r_full = bars + 4;            // [SLOTS] TMA -> MMA
+  uint64_t* r_empty = r_full + SLOTS;     // [SLOTS] MMA -> TMA
+  uint64_t* s_full = r_empty + SLOTS;     // [2] MMA -> softmax t (scores of tile t)
+  uint64_t* p_full = s_full + 2;          // [2] softmax t -> MMA (P_t stored, O_t rescaled)
+  uint64_t* o_done = p_full + 2;          // [2] MMA -> softmax t (the unit's last P_t V complete)
+  uint64_t* o_free = o_done + 2;          // [2] softmax t -> MMA (O_t read out)
+  uint64_t* drain = o_free + 2;           // abort path only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  float* xrow = reinterpret_cast<float*>(smem + (1 + AT_SLOTS) * AT_TILE + 512);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // the 1024-byte alignment of the tiles must leave room for the barriers
-  // and the row exchange (a dynamic shared-memory base is 1024-aligned in
-  // practice; otherwise the block reports an error instead of overrunning)
-  if ((smem - smem_raw) + (1 + AT_SLOTS) * AT_TILE + AT_AUX > AT_SMEM) {
+  // the 1024-byte alignment of the tiles must leave room for the barriers (a
+  // dynamic shared-memory base is 1024-aligned in practice; otherwise the
+  // block reports an error instead of overrunning)
+  if ((smem - smem_raw) + (2 + SLOTS) * TILE + Cfg::AUX > Cfg::SMEM) {
     if (threadIdx.x == 0) atomicCAS(&g_tp_error, TP_DEVERR_NONE, TP_DEVERR_LAYOUT);
     return;
   }
@@ -160,17 +218,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const int cta = static_cast<int>(blockIdx.x), grid = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_tm, 8);
-    mbar_init(o_free, 8);
-    for (int i = 0; i < AT_SLOTS; ++i) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&q_full[t], 1);
+      mbar_init(&q_free[t], 1);
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_done[t], 1);
+      mbar_init(&o_free[t], 4);
+    }
+    for (int i = 0; i < SLOTS; ++i) {
       mbar_init(&r_full[i], 1);
       mbar_init(&r_empty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
-      mbar_init(&o_done[i], 1);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -191,135 +249,149 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------ TMA producer ------------------------------
-      // Per unit: its Q tile (once the last unit's Q has been copied out of
-      // the tile), then its K and V tiles through the ring.
-      uint32_t issued = 0, issued_ph = 0;  // per slot: a copy was started, its phase
+      uint32_t issued = 0, issued_ph = 0;  // per ring slot: a copy was started, its phase
       int it = 0;                          // ring items of all units so far
-      int q_loads = 0;
+      int ua[2] = {0, 0};                  // units that had a tile t so far (= Q_t loads)
       bool ok = true;
       for (int w = 0; ok; ++w) {
         const int u = at_unit(cta, grid, w, a.units);
         if (u < 0) break;
-        const AtUnit wu = at_decode(a, u);
-        if (w > 0 && !mbar_wait(q_tm, static_cast<uint32_t>(w - 1) & 1u, abort_flag)) {
-          ok = false;
-          break;
+        const AtUnit wu = at_decode(a, u, HD);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || wu.nkb[t] == 0) continue;
+          if (ua[t] > 0 && !mbar_wait(&q_free[t], static_cast<uint32_t>(ua[t] - 1) & 1u, abort_flag)) {
+            ok = false;
+            continue;
+          }
+          mbar_arrive_expect_tx(&q_full[t], TILE);
+#pragma unroll
+          for (int p = 0; p < Cfg::PANELS; ++p)
+            tma_load_3d(sQ + t * TILE + p * PANEL, &mapQKV, &q_full[t], wu.j[t] * HD + 64 * p, wu.qb[t] * 128, wu.s);
+          ++ua[t];
         }
-        mbar_arrive_expect_tx(q_full, AT_TILE);
-        tma_load_3d(sQ, &mapQKV, q_full, wu.qcol, wu.qb * AT_ROWS, wu.s);
-        tma_load_3d(sQ + AT_PANEL, &mapQKV, q_full, wu.qcol + 64, wu.qb * AT_ROWS, wu.s);
-        ++q_loads;
-        for (int i = 0; i < 2 * wu.nkb; ++i, ++it) {  // K(j), V(j), K(j+1), ...
-          const int slot = it % AT_SLOTS;
-          const uint32_t ph = static_cast<uint32_t>(it / AT_SLOTS) & 1u;
+        for (int i = 0; ok && i < 2 * wu.nkb_max; ++i, ++it) {  // K(j), V(j), K(j+1), ...
+          const int slot = it % SLOTS;
+          const uint32_t ph = static_cast<uint32_t>(it / SLOTS) & 1u;
           if (!mbar_wait(&r_empty[slot], ph ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
           const int col = (i & 1) ? wu.vcol : wu.kcol;
-          uint8_t* dst = ring + slot * AT_TILE;
-          mbar_arrive_expect_tx(&r_full[slot], AT_TILE);
-          tma_load_3d(dst, &mapQKV, &r_full[slot], col, (i >> 1) * AT_ROWS, wu.s);
-          tma_load_3d(dst + AT_PANEL, &mapQKV, &r_full[slot], col + 64, (i >> 1) * AT_ROWS, wu.s);
+          uint8_t* dst = ring + slot * TILE;
+          mbar_arrive_expect_tx(&r_full[slot], TILE);
+#pragma unroll
+          for (int p = 0; p < Cfg::PANELS; ++p)
+            tma_load_3d(dst + p * PANEL, &mapQKV, &r_full[slot], col + 64 * p, (i >> 1) * 128, wu.s);
           issued |= 1u << slot;
           issued_ph = (issued_ph & ~(1u << slot)) | (ph << slot);
         }
       }
       if (!ok) {  // let every copy this block started land before it exits
-        if (q_loads > 0) mbar_wait_drain(q_full, static_cast<uint32_t>(q_loads - 1) & 1u);
-        for (int i = 0; i < AT_SLOTS; ++i)
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+          if (ua[t] > 0) mbar_wait_drain(&q_full[t], static_cast<uint32_t>(ua[t] - 1) & 1u);
+        for (int i = 0; i < SLOTS; ++i)
           if ((issued >> i) & 1u) mbar_wait_drain(&r_full[i], (issued_ph >> i) & 1u);
       }
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
-    // The whole warp runs the loop (waits and descriptors are warp-uniform);
-    // one elected lane issues each MMA and commit.
     const uint32_t idesc_s = idesc_bf16_f32(128, 128);
-    const uint32_t idesc_o = idesc_bf16_f32_bmn(128, 128);
-    const uint32_t tO = tmem_base + AT_TM_O, tQ = tmem_base + AT_TM_Q;
+    const uint32_t idesc_o = idesc_bf16_f32_bmn(128, HD);
+    const uint64_t q_desc = smem_desc_k_sw128(smem_u32(sQ));
     const uint64_t ring_k = smem_desc_k_sw128(smem_u32(ring));
-    const uint64_t ring_mn = smem_desc_mn_sw128(smem_u32(ring), AT_PANEL, 1024);
+    const uint64_t ring_mn = smem_desc_mn_sw128(smem_u32(ring), PANEL, 1024);
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
     };
+    auto wait_item = [&](int item) {
+      return wait_all(&r_full[item % SLOTS], static_cast<uint32_t>(item / SLOTS) & 1u);
+    };
     bool ok = true, issued_any = false;
-    // Block gb counts the key blocks of all this CTA's units so far: it
-    // picks the score buffer (gb & 1) and the phases of its barriers. Ring
-    // item `item` holds a K tile (S) or a V tile (P V).
-    //
-    // S(gb) = Q K^T: M = 128 queries, N = 128 keys, K = hd in 8 steps of 16
-    // (Q: 8 TMEM columns a step; K: two 64-wide panels, +32 bytes a step
-    // inside a panel; descriptor start addresses count 16-byte units). The
-    // caller has waited for the K tile.
-    auto issue_s = [&](int gb, int item) {
-      const int st = gb & 1;
-      const int slot = item % AT_SLOTS;
-      const uint64_t kd = ring_k + static_cast<uint64_t>((slot * AT_TILE) >> 4);
-      const uint32_t tS = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128);
+    // S_t = Q_t K^T: M = 128 queries, N = 128 keys, K = HD in steps of 16
+    // (both operands K-major in 64-wide panels: +32 bytes a step inside a
+    // panel; descriptor start addresses count 16-byte units). The caller has
+    // waited for Q_t and the K tile.
+    auto issue_s = [&](int t, int item) {
+      const uint64_t qd = q_desc + static_cast<uint64_t>((t * TILE) >> 4);
+      const uint64_t kd = ring_k + static_cast<uint64_t>(((item % SLOTS) * TILE) >> 4);
+      const uint32_t tS = tmem_base + Cfg::TM_S + static_cast<uint32_t>(t * 128);
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        tc_mma_bf16_ts_warp(tS, tQ + static_cast<uint32_t>(k * 8),
-                            kd + static_cast<uint64_t>(((k >> 2) * AT_PANEL + (k & 3) * 32) >> 4), idesc_s,
-                            k > 0 ? 1u : 0u);
-      tc_commit_warp(&s_full[st]);
-      tc_commit_warp(&r_empty[slot]);  // K read
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint64_t off = static_cast<uint64_t>(((k >> 2) * PANEL + (k & 3) * 32) >> 4);
+        tc_mma_bf16_warp(tS, qd + off, kd + off, idesc_s, k > 0 ? 1u : 0u);
+      }
       issued_any = true;
     };
-    // O (+)= P(gb) V: M = 128 queries, N = hd, K = 128 keys in 8 steps; P
-    // sits in TMEM (keys 0..63 at score columns 0..31 of its buffer, keys
-    // 64..127 at 64..95), V is MN-major (rows = keys, each row 64 hd values;
-    // the second 64 hd values one panel further). A unit's first block
-    // overwrites O. The caller has waited for the V tile and P.
-    auto issue_pv = [&](int gb, int item, bool first) {
-      const int st = gb & 1;
-      const int slot = item % AT_SLOTS;
-      const uint32_t tP = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128);
-      const uint64_t vd = ring_mn + static_cast<uint64_t>((slot * AT_TILE) >> 4);
+    // O_t (+)= P_t V: M = 128 queries, N = HD, K = 128 keys in 8 steps; P_t
+    // sits in TMEM (key pairs at the first 64 columns of tile t's scores), V
+    // is MN-major (rows = keys, 64 hd values a row, the next 64 hd values one
+    // panel further). A unit's first block overwrites O_t. The caller has
+    // waited for the V tile and P_t.
+    auto issue_pv = [&](int t, int item, bool first) {
+      const uint32_t tP = tmem_base + Cfg::TM_S + static_cast<uint32_t>(t * 128);
+      const uint32_t tO = tmem_base + Cfg::TM_O + static_cast<uint32_t>(t * HD);
+      const uint64_t vd = ring_mn + static_cast<uint64_t>(((item % SLOTS) * TILE) >> 4);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        tc_mma_bf16_ts_warp(tO, tP + static_cast<uint32_t>((k >> 2) * 64 + (k & 3) * 8),
-                            vd + static_cast<uint64_t>((k * 16 * 128) >> 4), idesc_o, (!first || k > 0) ? 1u : 0u);
-      tc_commit_warp(&o_done[st]);
-      tc_commit_warp(&r_empty[slot]);  // V read
+        tc_mma_bf16_ts_warp(tO, tP + static_cast<uint32_t>(k * 8), vd + static_cast<uint64_t>((k * 16 * 128) >> 4),
+                            idesc_o, (!first || k > 0) ? 1u : 0u);
+      issued_any = true;
     };
-    auto wait_item = [&](int item) {
-      return wait_all(&r_full[item % AT_SLOTS], static_cast<uint32_t>(item / AT_SLOTS) & 1u);
-    };
-    // Per unit: once its Q is in TMEM, S(0) and S(1) fill both score
-    // buffers (right behind the last unit's final P V, which the tensor
-    // core runs first); then, per block, P(jb) V and S(jb + 2) are issued
-    // back to back as soon as the softmax hands over P(jb): S(jb + 2) reuses
-    // P(jb)'s buffer, and the tensor core runs them in issue order. The
-    // ring waits come before the wait for P, off the path from the softmax
-    // to the tensor core. The unit's first P V also waits until the softmax
-    // has read the last unit's O out of TMEM.
-    int it0 = 0, g0 = 0;  // ring items and key blocks of the earlier units
+    int it0 = 0;                          // ring items of the earlier units
+    int ua[2] = {0, 0}, pg[2] = {0, 0};   // units with tile t, P_t blocks consumed
     for (int w = 0; ok; ++w) {
       const int u = at_unit(cta, grid, w, a.units);
       if (u < 0) break;
-      const int nkb = at_decode(a, u).nkb;
-      ok = wait_all(q_tm, static_cast<uint32_t>(w) & 1u);
-      for (int jb = 0; ok && jb < 2 && jb < nkb; ++jb) {
-        ok = wait_item(it0 + 2 * jb);
-        if (ok) {
-          tc_fence_after();
-          issue_s(g0 + jb, it0 + 2 * jb);
-        }
-      }
-      for (int jb = 0; ok && jb < nkb; ++jb) {
-        const bool next = jb + 2 < nkb;
-        const int gb = g0 + jb;
-        ok = wait_item(it0 + 2 * jb + 1) && (!next || wait_item(it0 + 2 * jb + 4)) &&
-             wait_all(&p_full[gb & 1], static_cast<uint32_t>(gb >> 1) & 1u) &&
-             (jb > 0 || w == 0 || wait_all(o_free, static_cast<uint32_t>(w - 1) & 1u));
-        if (!ok) break;
+      const AtUnit wu = at_decode(a, u, HD);
+      // first scores of each tile (right behind the last unit's final P V)
+      ok = wait_item(it0);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (!ok || wu.nkb[t] == 0) continue;
+        ok = wait_all(&q_full[t], static_cast<uint32_t>(ua[t]) & 1u);
+        if (!ok) continue;
         tc_fence_after();
-        issue_pv(gb, it0 + 2 * jb + 1, jb == 0);
-        if (next) issue_s(gb + 2, it0 + 2 * jb + 4);
+        issue_s(t, it0);
+        tc_commit_warp(&s_full[t]);
+        if (wu.nkb[t] == 1) tc_commit_warp(&q_free[t]);
       }
-      it0 += 2 * nkb;
-      g0 += nkb;
+      if (!ok) break;
+      tc_commit_warp(&r_empty[it0 % SLOTS]);  // K(0) read
+      // per key block: P_0 V, S_0(next), P_1 V, S_1(next). The ring waits
+      // come before the waits for P, off the path from the softmax to the
+      // tensor core; a unit's first P_t V also waits until the softmax has
+      // read the last unit's O_t out of TMEM.
+      for (int jb = 0; ok && jb < wu.nkb_max; ++jb) {
+        const bool next = jb + 1 < wu.nkb_max;
+        const int iv = it0 + 2 * jb + 1, ik = iv + 1;
+        ok = wait_item(iv) && (!next || wait_item(ik));
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || jb >= wu.nkb[t]) continue;
+          ok = wait_all(&p_full[t], static_cast<uint32_t>(pg[t]) & 1u) &&
+               (jb > 0 || ua[t] == 0 || wait_all(&o_free[t], static_cast<uint32_t>(ua[t] - 1) & 1u));
+          if (!ok) continue;
+          ++pg[t];
+          tc_fence_after();
+          issue_pv(t, iv, jb == 0);
+          if (jb + 1 < wu.nkb[t]) {
+            issue_s(t, ik);
+            tc_commit_warp(&s_full[t]);
+            if (jb + 2 == wu.nkb[t]) tc_commit_warp(&q_free[t]);  // that was the unit's last S_t
+          } else {
+            tc_commit_warp(&o_done[t]);
+          }
+        }
+        if (!ok) break;
+        tc_commit_warp(&r_empty[iv % SLOTS]);          // V(jb) read
+        if (next) tc_commit_warp(&r_empty[ik % SLOTS]);  // K(jb + 1) read
+      }
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (wu.nkb[t] > 0) ++ua[t];
+      it0 += 2 * wu.nkb_max;
     }
     if (!ok && issued_any) {  // wait for MMAs in flight before TMEM is freed
       tc_commit_warp(drain);
@@ -327,175 +399,127 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
   } else {
     // ------------------------------ softmax ------------------------------
+    const int t = (warp - 2) >> 2;     // query tile
     const int q = warp & 3;            // TMEM lane quadrant
-    const int half = (warp - 2) >> 2;  // which 64 keys / output columns of the row
-    const int r = q * 32 + lane;       // query row within the block
-    const int c0 = half * 64;
+    const int r = q * 32 + lane;       // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t tO = tmem_base + AT_TM_O + lane_off + static_cast<uint32_t>(c0);
-    // Q of unit w into TMEM: this thread's row, hd values 64 * half .. + 63,
-    // read from the 128-byte-swizzled TMA tile. Returns false (for both
-    // warps of the quadrant) if the wait gave up.
-    auto copy_q = [&](int w) -> bool {
-      const bool q_ok = mbar_wait(q_full, static_cast<uint32_t>(w) & 1u, abort_flag);
-      if (pair_any(q, !q_ok || *abort_flag)) return false;
-      const uint8_t* qrow = sQ + half * AT_PANEL + r * 128;
-      uint32_t rr[32];
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((ch ^ (r & 7)) << 4));
-        rr[ch * 4 + 0] = v.x;
-        rr[ch * 4 + 1] = v.y;
-        rr[ch * 4 + 2] = v.z;
-        rr[ch * 4 + 3] = v.w;
-      }
-      tmem_st32(tmem_base + AT_TM_Q + lane_off + static_cast<uint32_t>(half * 32), rr);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_tm);
-      return true;
-    };
-    // (the grid has no more CTAs than units, so every CTA has a first one)
-    bool ok = copy_q(0);
-    int g0 = 0;  // key blocks of the earlier units
+    const uint32_t tS = tmem_base + Cfg::TM_S + static_cast<uint32_t>(t * 128) + lane_off;
+    const uint32_t tO = tmem_base + Cfg::TM_O + static_cast<uint32_t>(t * HD) + lane_off;
+    const uint64_t scale2 = f2_make(a.scale_log2, a.scale_log2);
+    const int nc = a.nq * HD;
+    bool ok = true;
+    int ua = 0, sg = 0;  // units with this tile, score blocks consumed
     for (int w = 0; ok; ++w) {
       const int u = at_unit(cta, grid, w, a.units);
       if (u < 0) break;
-      const AtUnit wu = at_decode(a, u);
-      const int nkb = wu.nkb, qb = wu.qb;
-      const int t = qb * AT_ROWS + r;                         // query index
-      const int kmax = a.causal ? min(t, a.T - 1) : a.T - 1;  // last key this query sees
+      const AtUnit wu = at_decode(a, u, HD);
+      const int nkb = t ? wu.nkb[1] : wu.nkb[0];
+      if (nkb == 0) continue;
+      const int qb = t ? wu.qb[1] : wu.qb[0];
+      const int jq = t ? wu.j[1] : wu.j[0];
+      const int tq = qb * 128 + r;                             // query index
+      const int kmax = a.causal ? min(tq, a.T - 1) : a.T - 1;  // last key this query sees
       float m = -INFINITY;  // exponent base, in log2 units of the scaled scores
-      float l = 0.0f;       // this half's share of the row sum
-      for (int jb = 0; ok && jb < nkb; ++jb) {
-        const int gb = g0 + jb;  // block count over this CTA's units: buffer and phases
-        const int st = gb & 1;
-        const uint32_t ph = static_cast<uint32_t>(gb >> 1) & 1u;
-        // (a wait that gave up leaves garbage in the scores, which the vote at
-        // the exchange below discards)
-        const bool waited = mbar_wait(&s_full[st], ph, abort_flag);
-        tc_fence_after();
-        float sv[64];
-        const uint32_t tS = tmem_base + AT_TM_S + static_cast<uint32_t>(st * 128 + c0) + lane_off;
-#pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          uint32_t rr[32];
-          tmem_ld32(tS + static_cast<uint32_t>(c), rr);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[c + i] = __uint_as_float(rr[i]);
-        }
-        tmem_ld_wait();
-        const int kbase = jb * AT_ROWS + c0;
-        // only the diagonal block (causal) and a ragged last block need a mask
-        if ((a.causal && jb == qb) || jb * AT_ROWS + AT_ROWS > a.T) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (kbase + i > kmax) sv[i] = -INFINITY;
-        }
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
-#pragma unroll
-        for (int i = 8; i < 64; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
-        float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-        // the row's other half: exchange the maxima, in one of two slots by
-        // block parity (the partner's write two blocks on comes after the next
-        // exchange, which this thread reaches only after this read); the
-        // barrier also takes both halves out together if a wait gave up
-        float* xr = xrow + st * 256;
-        xr[half * 128 + r] = mx;
-        if (pair_any(q, !waited || *abort_flag)) {
+      float l = 0.0f;       // row sum of the exponentials
+      for (int jb = 0; jb < nkb; ++jb, ++sg) {
+        const bool waited = mbar_wait(&s_full[t], static_cast<uint32_t>(sg) & 1u, abort_flag);
+        if (__any_sync(0xffffffffu, !waited)) {
           ok = false;
           break;
         }
-        mx = fmaxf(mx, xr[(half ^ 1) * 128 + r]);
-        const float m_cand = mx * a.scale_log2;  // the scale is positive: same order
-        bool rescale = false;
-        float alpha = 1.0f;
-        if (m_cand > m + AT_RESCALE_LOG2) {  // also the first visible block (m = -inf)
-          alpha = ex2_approx(m - m_cand);    // 0 on the first block
-          rescale = jb > 0;
-          m = m_cand;
-          l *= alpha;
-        }
-        float sum8[8];
+        tc_fence_after();
+        // The block's 128 keys in two halves of 64, each a step of the online
+        // softmax: its scores from TMEM, its maximum, a move of the base if
+        // needed, its exponentials packed to bf16 over the score columns the
+        // first half has already consumed (P keys 0..63 at columns 0..31,
+        // keys 64..127 at 32..63). A base that moves in the second half
+        // (rarely: only on a jump above 2^8) rescales the first half's P as
+        // well as O and l.
+        const bool masked = (a.causal && jb == qb) || jb * 128 + 128 > a.T;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sum8[i] = 0.0f;
+        for (int h = 0; h < 2; ++h) {
+          float sv[64];
+          {
+            uint32_t ra[32], rb[32];
+            tmem_ld32(tS + static_cast<uint32_t>(h * 64), ra);
+            tmem_ld32(tS + static_cast<uint32_t>(h * 64 + 32), rb);
+            tmem_ld_wait_regs(ra);
+            reg_fence32(rb);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          sv[i] = ex2_approx(fmaf(sv[i], a.scale_log2, -m));
-          sum8[i & 7] += sv[i];
-        }
-        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        if (__any_sync(0xffffffffu, rescale)) {
-          // the base moved: once P V of block jb - 1 is done, this half's 64
-          // columns of O are rescaled. A wait that gives up (the abort flag is
-          // then set) skips the rescale; the next exchange takes both halves
-          // of the row out of the loop together.
-          const bool done = mbar_wait(&o_done[st ^ 1], static_cast<uint32_t>((gb - 1) >> 1) & 1u, abort_flag);
-          if (__all_sync(0xffffffffu, done)) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < 64; c += 32) {
-              uint32_t rr[32];
-              tmem_ld32(tO + static_cast<uint32_t>(c), rr);
-              tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-              tmem_st32(tO + static_cast<uint32_t>(c), rr);
+            for (int i = 0; i < 32; ++i) {
+              sv[i] = __uint_as_float(ra[i]);
+              sv[32 + i] = __uint_as_float(rb[i]);
             }
           }
-        }
-        // this half's 64 P values as bf16 pairs over its first 32 score columns
-        // (already read into registers)
-        {
+          // only the diagonal block (causal) and a ragged last block need a mask
+          if (masked) {
+            const int kb = jb * 128 + h * 64;
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (kb + i > kmax) sv[i] = -INFINITY;
+          }
+          float mx4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mx4[i] = sv[i];
+#pragma unroll
+          for (int i = 4; i < 64; i += 8) {
+            mx4[0] = fmax3(mx4[0], sv[i], sv[i + 1]);
+            mx4[1] = fmax3(mx4[1], sv[i + 2], sv[i + 3]);
+            mx4[2] = fmax3(mx4[2], sv[i + 4], sv[i + 5]);
+            mx4[3] = fmax3(mx4[3], sv[i + 6], sv[i + 7]);
+          }
+          const float m_cand = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * a.scale_log2;
+          // (the scale is positive: the same order; a half with no visible key
+          // gives -inf and moves nothing)
+          float alpha = 1.0f;
+          bool moved = false;
+          if (m_cand > m + AT_RESCALE_LOG2) {  // also the block's first half on a unit's first block
+            alpha = ex2_approx(m - m_cand);    // 0 while m = -inf
+            moved = true;
+            m = m_cand;
+            l *= alpha;
+          }
+          if (__any_sync(0xffffffffu, moved && (jb > 0 || h > 0)))
+            at_rescale<HD>(tO, tS, alpha, jb > 0, h > 0);
+          // P = 2^(s * scale - m), two at a time; the half's row sum in pairs
+          const uint64_t negm = f2_make(-m, -m);
+          uint64_t acc[2] = {f2_make(0.0f, 0.0f), f2_make(0.0f, 0.0f)};
           uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(sv[2 * i], sv[2 * i + 1]);
-          tmem_st32(tS, pk);
+          for (int i = 0; i < 32; ++i) {
+            float x0, x1;
+            f2_split(f2_fma(f2_make(sv[2 * i], sv[2 * i + 1]), scale2, negm), x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            acc[i & 1] = f2_add(acc[i & 1], f2_make(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + static_cast<uint32_t>(h * 32), pk);
+          float s0, s1, s2, s3;
+          f2_split(acc[0], s0, s1);
+          f2_split(acc[1], s2, s3);
+          l += (s0 + s1) + (s2 + s3);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[st]);
+        if (lane == 0) mbar_arrive(&p_full[t]);
       }
-      // ok is uniform over the two warps of a quadrant
-      const int gl = g0 + nkb - 1;  // the unit's last block
-      g0 += nkb;
       if (!ok) break;
-      // The next unit's Q into TMEM now: every S MMA of this unit is complete
-      // (its last scores are in), so the next unit's first scores are computed
-      // while this unit's output is written.
-      if (at_unit(cta, grid, w + 1, a.units) >= 0 && !copy_q(w + 1)) {
+      const bool done = mbar_wait(&o_done[t], static_cast<uint32_t>(ua) & 1u, abort_flag);
+      if (__any_sync(0xffffffffu, !done)) {
         ok = false;
         break;
       }
-      // (S(gl) was issued after P V of block gl - 2, so the barrier of block
-      // gl is at most one phase behind: its parity is unambiguous)
-      const bool done = mbar_wait(&o_done[gl & 1], static_cast<uint32_t>(gl >> 1) & 1u, abort_flag);
-      // The row sum is the two halves' shares (same exponent base), exchanged
-      // in the slot that the next block's maxima use; the second barrier keeps
-      // those out until both halves have read.
-      float* xr = xrow + ((gl + 1) & 1) * 256;
-      xr[half * 128 + r] = l;
-      if (pair_any(q, !done || *abort_flag)) {
-        ok = false;
-        break;
-      }
-      l += xr[(half ^ 1) * 128 + r];
-      pair_any(q, false);
+      ++ua;
       tc_fence_after();
       const float inv = 1.0f / l;
-      const int nc = a.nq * AT_HD;
-      __nv_bfloat16* out = a.ctx + (static_cast<size_t>(wu.s) * a.T + t) * nc + wu.j * AT_HD + c0;
+      __nv_bfloat16* out = a.ctx + (static_cast<size_t>(wu.s) * a.T + tq) * nc + jq * HD;
 #pragma unroll 1
-      for (int c = 0; c < 64; c += 32) {
+      for (int c = 0; c < HD; c += 32) {
         uint32_t rr[32];
         tmem_ld32(tO + static_cast<uint32_t>(c), rr);
-        tmem_ld_wait();
-        if (t < a.T) {
+        tmem_ld_wait_regs(rr);
+        if (tq < a.T) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             float v[8];
@@ -505,11 +529,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           }
         }
       }
-      // O is read out (each load waited for): the next unit's first P V may
-      // overwrite it
+      // O_t is read out (each load waited for): the next unit's first P_t V
+      // may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
+      if (lane == 0) mbar_arrive(&o_free[t]);
     }
   }
 

@@ -313,13 +313,13 @@ struct TmemSrc {
     if constexpr (N == 32) {
       uint32_t r[32];
       tmem_ld32(t_acc + col, r);
-      tmem_ld_wait();
+      tmem_ld_wait_regs(r);
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
     } else {
       uint32_t r[16];
       tmem_ld16(t_acc + col, r);
-      tmem_ld_wait();
+      tmem_ld_wait_regs(r);
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
     }

@@ -273,9 +273,10 @@ def test_attention_validation():
     assert att(mode=3) == MODE
     assert att(hq=3) == SHAPE         # 3 q heads over 2 shards
     assert att(T=-1) == SHAPE
-    assert att(hd=64, hq=4, hkv=2) == UNSUP
+    assert att(hd=96, hq=4, hkv=2) == UNSUP   # head sizes 64 and 128 only
+    assert att(hd=256, hq=4, hkv=2) == UNSUP
     assert att(T=2 ** 31) == UNSUP
-    # work units (shard, q head, block of 128 queries) past the kernel's int range
+    # query tiles (shard, q head, block of 128 queries) past the kernel's int range
     assert att(T=2 ** 31 - 1, tp=64, hq=64, hkv=64) == UNSUP
     assert att(qkv=FAKE + 1) == ALIGN
     assert att(T=0) == OK

@@ -592,6 +592,25 @@ def test_attention_against_library_softmax_per_row(causal, q_offset):
 
 
 @pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("q_offset", [0, 5])
+def test_attention_weights_against_library_softmax_per_row(causal, q_offset):
+    """The weights alone: each row is scipy's softmax over the scaled scores
+    of exactly the keys that query sees (a slice), and 0 at every other key."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(212)
+    T, Tq, hd = 11, 6, 16
+    k = rng.standard_normal((T, hd))
+    q = rng.standard_normal((Tq, hd)) * 2.0
+    w = O.attention_weights(q, k, causal, q_offset=q_offset)
+    assert w.shape == (Tq, T)
+    for i in range(Tq):
+        n = q_offset + i + 1 if causal else T
+        want = softmax([float(np.dot(q[i], k[j])) / hd ** 0.5 for j in range(n)])
+        np.testing.assert_allclose(w[i, :n], want, rtol=1e-12, atol=1e-15)
+        assert np.all(w[i, n:] == 0.0)
+
+
+@pytest.mark.parametrize("causal", [True, False])
 def test_attention_single_key_is_v(causal):
     """One token: the softmax over one score is 1, so the context is V exactly."""
     rng = np.random.default_rng(201)
