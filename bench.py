@@ -82,7 +82,8 @@ def workload_spec(name: str, tp: int | None, tokens: int | None):
         T, H, V = tokens or 4096, 4096, 32000
         tp = tp or 4
         return dict(name="vocab_embedding_lm_head_cross_entropy", T=T, H=H, V=V, tp=tp, flops=2.0 * T * H * V,
-                    dominant="lm_head_col_gemm (logits [tp][T][V/tp])", dominant_flops=2.0 * T * H * V,
+                    dominant="lm_head_col_gemm with loss statistics in its epilogue (logits [tp][T][V/tp])",
+                    dominant_flops=2.0 * T * H * V,
                     bound="tensor",
                     sample_note="{r} of {T} tokens (losses of different tokens are independent)")
     if name == "gqa":
@@ -384,24 +385,27 @@ def setup_workload(spec, torch, tpl):
         logits = torch.empty((tp, T, V // tp), dtype=B, device="cuda")
         loss = torch.empty(T, dtype=torch.float32, device="cuda")
         mean = torch.empty(1, dtype=torch.float32, device="cuda")
-        cws = torch.empty(tpl.tp_cross_entropy_workspace_bytes(T, V, tp), dtype=torch.uint8, device="cuda")
-        gws = torch.empty(max(tpl.tp_gemm_workspace_bytes(T, Slm), 256), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(max(tpl.lib.tp_lm_head_ce_workspace_bytes(T, Slm.ref()), 256), dtype=torch.uint8,
+                         device="cuda")
 
         def p_embed(ids_in=ids):
             tpl.tp_vocab_embedding(ids_in, E, tp, out=X0)
 
-        def p_head():
-            tpl.tp_column_linear(X0, Slm, out=logits, workspace=gws)
+        def p_head_ce(mean_out=mean):
+            # LM head with the loss statistics in its epilogue, the per-token
+            # combine, the mean and the gradient of the mean loss (in place)
+            tpl.tp_lm_head_cross_entropy(X0, Slm, labels, logits=logits, dlogits=logits, workspace=ws, loss=loss,
+                                         mean_loss=mean_out)
 
-        def p_ce(mean_out=mean):  # loss, mean and the gradient of the mean loss, in place
-            tpl.tp_vocab_cross_entropy(logits, labels, dlogits=logits, workspace=cws, loss=loss, mean_loss=mean_out)
+        def p_dominant():  # the LM head GEMM with its statistics epilogue (+ the small combine)
+            tpl.tp_lm_head_cross_entropy(X0, Slm, labels, logits=logits, workspace=ws, loss=loss,
+                                         want_mean=False)
 
-        def api_call(ids_in, mean_out):  # ids in, mean loss out: 1 + 1 + 4 launches
+        def api_call(ids_in, mean_out):  # ids in, mean loss out: 1 + 4 launches
             p_embed(ids_in)
-            p_head()
-            p_ce(mean_out)
-        st.update(parts=[p_embed, p_head, p_ce], X=ids, Y=mean, api=api_call, launches_per_step=6,
-                  keep=[E, Slm, labels, X0, logits, loss, cws, gws], dominant_part=p_head)
+            p_head_ce(mean_out)
+        st.update(parts=[p_embed, p_head_ce], X=ids, Y=mean, api=api_call, launches_per_step=5,
+                  keep=[E, Slm, labels, X0, logits, loss, ws], dominant_part=p_dominant)
     elif name.startswith("llama7b_swiglu_mlp_backward"):
         H, I = spec["H"], spec["I"]
         d = S.mlp_backward(T, H, I)

@@ -431,6 +431,38 @@ tp_status tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int6
                                  int dtype, float* loss, float* mean_loss, void* dlogits, float grad_scale,
                                  void* workspace, size_t ws_bytes, void* stream);
 
+/* Workspace bytes tp_lm_head_cross_entropy needs (T tokens, the LM head's view). */
+size_t tp_lm_head_ce_workspace_bytes(int64_t T, const tp_shards* W_lm);
+
+/*
+ * tp_lm_head_cross_entropy - the column-parallel LM head and the
+ * vocabulary-parallel loss in one call (same pages as above): logits
+ * z_s = X W_s for every vocabulary shard s, then the losses, their mean and
+ * optionally the gradient, as tp_vocab_cross_entropy defines them. On the
+ * bf16 path with T > 64 the GEMM's epilogue reduces each (shard, token,
+ * 256-column tile) of logits to (max, sum of exp(z - max), the label's
+ * logit) from its fp32 accumulator while it stores the bf16 logits, so no
+ * pass re-reads the logits for the loss; the statistics are then combined
+ * per token in shard and tile order. The loss is thus that of the fp32
+ * logits; the gradient is computed from the stored logits. With T <= 64
+ * (the weight-streaming GEMM) or fp32 views the logits are reduced by a
+ * separate pass, as in tp_vocab_cross_entropy.
+ *   X [T][K] (K = W_lm->K); W_lm a TP_COL view of the [K][V] head, V = W_lm->N;
+ *   labels [T] int32 (device).
+ *   logits [tp][T][V/tp] (the view's dtype), written.
+ *   loss, mean_loss, dlogits (may be `logits`), grad_scale: as
+ *   tp_vocab_cross_entropy.
+ *   workspace >= tp_lm_head_ce_workspace_bytes(T, W_lm), 256-byte aligned.
+ *   A label outside [0, V) gives a NaN loss and makes the next
+ *   tp_get_error return TP_ERR_INDEX.
+ * Ownership: every buffer belongs to the caller; nothing is allocated.
+ * Errors: as tp_column_linear (no activation, no bias), plus TP_ERR_NULL
+ * for missing labels or workspace and TP_ERR_WORKSPACE.
+ */
+tp_status tp_lm_head_cross_entropy(const void* X, int64_t T, const tp_shards* W_lm, const int32_t* labels,
+                                   void* logits, float* loss, float* mean_loss, void* dlogits, float grad_scale,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
 /*
  * Mixture of experts with tensor-parallel experts ("Parallel strategies in
  * TensorRT LLM" page, FFN module, mixture of experts, TP mode: each expert's

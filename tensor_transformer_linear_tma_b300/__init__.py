@@ -81,6 +81,8 @@ _SIGS = {
     "tp_vocab_embedding": (_i32, [_vp, _i64, _vp, _i64, _i64, _i32, _i32, _vp, _vp]),
     "tp_cross_entropy_workspace_bytes": (_sz, [_i64, _i64, _i32]),
     "tp_vocab_cross_entropy": (_i32, [_vp, _vp, _i64, _i64, _i32, _i32, _vp, _vp, _vp, _f32, _vp, _sz, _vp]),
+    "tp_lm_head_ce_workspace_bytes": (_sz, [_i64, _P]),
+    "tp_lm_head_cross_entropy": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _sz, _vp]),
     "tp_moe_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32, _i32]),
     "tp_moe_block": (_i32, [_vp, _i64, _vp, _vp, _i32, _i32, _P, _P, _P, _vp, _vp, _sz, _vp, _vp]),
     "tp_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
@@ -405,6 +407,34 @@ def tp_vocab_cross_entropy(logits, labels, want_loss: bool = True, want_mean: bo
         _ptr(logits), _ptr(labels), T, tp * v, tp, _dt(logits), _ptr(loss), _ptr(mean_loss), _ptr(dlogits),
         scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
     return loss, mean_loss
+
+
+def tp_lm_head_cross_entropy(X, W_lm: Shards, labels, logits=None, want_loss: bool = True,
+                             want_mean: bool = True, dlogits=None, grad_scale: float | None = None,
+                             workspace=None, loss=None, mean_loss=None):
+    """LM head and vocabulary-parallel loss in one call: logits [tp][T][V/tp]
+    (returned, or written into `logits`), losses [T] fp32, their mean [1]
+    fp32, and, if `dlogits` is a tensor (it may be the logits), the gradient
+    of grad_scale * sum(loss) (grad_scale defaults to 1/T). Returns
+    (logits, loss, mean)."""
+    if labels.dtype != torch.int32:
+        raise TypeError("labels must be int32")
+    T = X.shape[0]
+    tp, V = W_lm.tp, W_lm.N
+    dev = X.device
+    if logits is None:
+        logits = torch.empty((tp, T, V // tp), dtype=X.dtype, device=dev)
+    if workspace is None:
+        workspace = _workspace(lib.tp_lm_head_ce_workspace_bytes(T, W_lm.ref()), dev)
+    if loss is None and want_loss:
+        loss = torch.empty(T, dtype=torch.float32, device=dev)
+    if mean_loss is None and want_mean:
+        mean_loss = torch.empty(1, dtype=torch.float32, device=dev)
+    scale = (1.0 / max(T, 1)) if grad_scale is None else grad_scale
+    _check("tp_lm_head_cross_entropy", lib.tp_lm_head_cross_entropy(
+        _ptr(X), T, W_lm.ref(), _ptr(labels), _ptr(logits), _ptr(loss), _ptr(mean_loss), _ptr(dlogits), scale,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
+    return logits, loss, mean_loss
 
 
 def tp_shard_experts(Ws, tp: int, mode: str) -> Shards:

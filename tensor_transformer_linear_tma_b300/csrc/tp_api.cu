@@ -368,13 +368,17 @@ inline int tpad_of(int64_t T) { return static_cast<int>(cdiv(std::max<int64_t>(T
 // Column-parallel bf16 GEMM. `rep` > 1 computes replicated K|V column blocks
 // once per group of rep shards (QKV views with kv heads < tp). A non-null
 // `ctx` (QKV views only) also receives the single-key attention context.
+// With ce_stats, the token-major launch also writes the cross-entropy
+// statistics of every (shard, token, 256-column tile) (GemmArgs::ce_stats);
+// the caller keeps such launches out of the weight-streaming arrangement.
 int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, const void* bias,
              const void* bias_up, int act, int concat, void* Y, const Scratch* sc, int rep, int64_t kv_col0,
-             void* ctx, cudaStream_t st) {
+             void* ctx, cudaStream_t st, const int32_t* ce_labels = nullptr, float* ce_stats = nullptr) {
   const int tp = W->tp;
   const int64_t K = W->K, Ns = W->N / tp;
   const bool swiglu = act == TP_ACT_SWIGLU;
-  const bool swap = sc != nullptr && T <= SWAP_MAX_T;
+  const bool swap = sc != nullptr && T <= SWAP_MAX_T && !ce_stats;
+  if (ce_stats && (swiglu || act != TP_ACT_NONE || ctx)) return TP_ERR_MODE;
   tpk::GemmArgs a{};
   a.M = static_cast<int>(T);
   a.Ns = static_cast<int>(Ns);
@@ -388,6 +392,8 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
   a.bias = bias;
   a.bias_up = static_cast<const bf16*>(bias_up);
   a.out = Y;
+  a.ce_labels = ce_labels;
+  a.ce_stats = ce_stats;
   if (ctx) {
     a.ctx = static_cast<bf16*>(ctx);
     a.hq = W->hq;
@@ -1465,6 +1471,100 @@ tp_status tp_vocab_cross_entropy(const void* logits, const int32_t* labels, int6
   if (dlogits) {
     const int grid_g = vec ? grid_rows : grid_for(T * V, 256);
     if (dtype == TP_BF16)
+      tpk::ce_grad_kernel<bf16><<<grid_g, 256, 0, st>>>(
+          static_cast<const bf16*>(logits), labels, lse, T, tp, v, grad_scale, vec, static_cast<bf16*>(dlogits));
+    else
+      tpk::ce_grad_kernel<float><<<grid_g, 256, 0, st>>>(
+          static_cast<const float*>(logits), labels, lse, T, tp, v, grad_scale, vec, static_cast<float*>(dlogits));
+    r = launch_status();
+  }
+  return as_status(r);
+}
+
+// Statistics of the fused LM head: one (max, sum, label logit) triple per
+// (shard, token, 256-column tile of the shard's vocabulary).
+size_t lm_ce_stats_bytes(int64_t T, int64_t V, int tp) {
+  const int64_t v = V / std::max(tp, 1);
+  return align256(static_cast<size_t>(T) * tp * cdiv(std::max<int64_t>(v, 1), 256) * 3 * sizeof(float));
+}
+
+size_t tp_lm_head_ce_workspace_bytes(int64_t T, const tp_shards* W_lm) {
+  if (!W_lm || T < 0 || W_lm->tp < 1 || W_lm->N < 1 || W_lm->K < 1) return 0;
+  const int tp = W_lm->tp;
+  const int64_t V = W_lm->N;
+  const size_t head = std::max(lm_ce_stats_bytes(T, V, tp), ce_stats_bytes(T, V, tp)) +
+                      2 * align256(static_cast<size_t>(T) * sizeof(float));
+  return head + tp_gemm_workspace_bytes(T, W_lm);
+}
+
+tp_status tp_lm_head_cross_entropy(const void* X, int64_t T, const tp_shards* W_lm, const int32_t* labels,
+                                   void* logits, float* loss, float* mean_loss, void* dlogits, float grad_scale,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+  int r = check_col(X, T, W_lm, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, logits);
+  if (r) return as_status(r);
+  const int tp = W_lm->tp, dt = W_lm->dtype;
+  const int64_t V = W_lm->N, v = V / tp;
+  if (T == 0) {  // an empty call needs no labels or workspace
+    if (mean_loss && !cuda_ok(cudaMemsetAsync(mean_loss, 0, sizeof(float), as_stream(stream))))
+      return TP_ERR_CUDA;
+    return TP_OK;
+  }
+  if (!labels || !workspace) return TP_ERR_NULL;
+  if (ws_bytes < tp_lm_head_ce_workspace_bytes(T, W_lm)) return TP_ERR_WORKSPACE;
+  const size_t es = elem_size(dt);
+  if (!aligned(labels, 4) || !aligned(workspace, 256) || (loss && !aligned(loss, 4)) ||
+      (mean_loss && !aligned(mean_loss, 4)) || (dlogits && !aligned(dlogits, es)))
+    return TP_ERR_ALIGN;
+  const cudaStream_t st = as_stream(stream);
+  char* ws = static_cast<char*>(workspace);
+  const size_t stats_bytes = std::max(lm_ce_stats_bytes(T, V, tp), ce_stats_bytes(T, V, tp));
+  float* stats = reinterpret_cast<float*>(ws);
+  float* lse = reinterpret_cast<float*>(ws + stats_bytes);
+  float* loss_ws = lse + align256(static_cast<size_t>(T) * sizeof(float)) / sizeof(float);
+  float* per_tok = loss ? loss : loss_ws;
+  const size_t head = stats_bytes + 2 * align256(static_cast<size_t>(T) * sizeof(float));
+  const int sms = std::max(1, num_sms());
+  const int vec = (v % 8 == 0) && aligned(logits, 16) && (!dlogits || aligned(dlogits, 16));
+  int64_t nchunk;
+  if (dt == TP_BF16 && T > SWAP_MAX_T) {
+    // the statistics come out of the GEMM's epilogue, per 256-column tile
+    Scratch sc = carve_scratch(ws, head, std::max<size_t>(2 * SK_MAX_CTAS, static_cast<size_t>(tp) * cdiv(v, 128)));
+    if ((r = col_bf16(X, T, W_lm, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, logits, &sc, 1, 0, nullptr, st,
+                      labels, stats)))
+      return as_status(r);
+    nchunk = cdiv(v, 256);
+  } else {
+    // few tokens (weight-streaming GEMM) or fp32: the logits, then a pass over them
+    Scratch sc{};
+    const Scratch* scp = nullptr;
+    if (dt == TP_BF16) {
+      sc = carve_scratch(ws, head, std::max<size_t>(2 * SK_MAX_CTAS, static_cast<size_t>(tp) * cdiv(v, 128)));
+      scp = &sc;
+    }
+    if ((r = run_col(X, T, W_lm, nullptr, nullptr, nullptr, TP_ACT_NONE, 0, logits, st, scp))) return as_status(r);
+    nchunk = cdiv(v, tpk::CE_CHUNK);
+    const int64_t units = T * tp * nchunk;
+    const int grid_rows = static_cast<int>(std::min<int64_t>(cdiv(units, 8), static_cast<int64_t>(sms) * 16));
+    if (dt == TP_BF16)
+      tpk::ce_stats_kernel<bf16><<<grid_rows, 256, 0, st>>>(static_cast<const bf16*>(logits), labels, T, tp, v,
+                                                              vec, stats);
+    else
+      tpk::ce_stats_kernel<float><<<grid_rows, 256, 0, st>>>(static_cast<const float*>(logits), labels, T, tp, v,
+                                                               vec, stats);
+    if ((r = launch_status())) return as_status(r);
+  }
+  tpk::ce_combine_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(T, 8), static_cast<int64_t>(sms) * 16)), 256, 0,
+                           st>>>(stats, labels, T, tp, V, nchunk, lse, per_tok);
+  if ((r = launch_status())) return as_status(r);
+  if (mean_loss) {
+    tpk::ce_mean_kernel<<<1, 1024, 0, st>>>(per_tok, T, mean_loss);
+    if ((r = launch_status())) return as_status(r);
+  }
+  if (dlogits) {
+    const int64_t units = T * tp * cdiv(v, tpk::CE_CHUNK);
+    const int grid_g = vec ? static_cast<int>(std::min<int64_t>(cdiv(units, 8), static_cast<int64_t>(sms) * 16))
+                           : grid_for(T * V, 256);
+    if (dt == TP_BF16)
       tpk::ce_grad_kernel<bf16><<<grid_g, 256, 0, st>>>(
           static_cast<const bf16*>(logits), labels, lse, T, tp, v, grad_scale, vec, static_cast<bf16*>(dlogits));
     else

@@ -154,6 +154,13 @@ struct GemmArgs {
   // ROW_SUM: the K loop also runs over a second (A, B) pair (mapA1, mapB1),
   // so that out = sum_s A_s B_s^T + sum_s A'_s B'_s^T in one accumulator
   int two_src;
+  // COL without activation on a vocabulary-split LM head: the epilogue also
+  // reduces each token row of the tile to cross-entropy statistics of its
+  // logits (taken from the fp32 accumulator), ce_stats[((s * M + t) * n_tiles
+  // + n) * 3 + {0, 1, 2}] = {max, sum exp(z - max), the label's logit where
+  // the tile holds column labels[t] - s * Ns, else 0}. Null: no statistics.
+  const int32_t* ce_labels;
+  float* ce_stats;
   // Grouped experts (CTA pairs, whole tiles only): the token rows are the
   // experts' routed tokens, each expert's segment padded to 256-row units;
   // unit_expert[u] is the expert of unit u (tile % m_tiles), or -1 for an
@@ -475,6 +482,25 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
                     pack_bf16x2(v[6], v[7]));
 }
 
+// Online cross-entropy statistics of one token row over a tile's columns:
+// the running maximum m, the sum S of exp(z - m), and the label's logit.
+struct CeAcc {
+  float m, S, zy;
+};
+// Eight logits at once (all inside the shard or none: widths are multiples
+// of 8 on this path).
+__device__ __forceinline__ void ce_add8(CeAcc& c, const float* v) {
+  float mx = v[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) mx = fmaxf(mx, v[j]);
+  if (mx > c.m) {
+    c.S *= __expf(c.m - mx);  // exp(-inf) = 0 on the first group
+    c.m = mx;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) c.S += __expf(v[j] - c.m);
+}
+
 // normal mode: this thread owns token row `row`; columns are output features.
 template <class Cfg, class Src>
 __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& src, int row, int n_blk, int s,
@@ -489,6 +515,9 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
         a.bias ? static_cast<const __nv_bfloat16*>(a.bias) + static_cast<size_t>(s) * a.Ns : nullptr;
     const __nv_bfloat16* bias_up = a.bias_up ? a.bias_up + static_cast<size_t>(s) * a.Ns : nullptr;
     const bool with_ctx = !Cfg::SWIGLU && a.ctx != nullptr;
+    const bool with_ce = !Cfg::SWIGLU && a.ce_stats != nullptr;
+    CeAcc ce{-INFINITY, 0.0f, 0.0f};
+    const int ce_loc = (with_ce && row_ok) ? __ldg(a.ce_labels + row) - s * a.Ns : -1;  // the label's shard column
 #pragma unroll 1
     for (int cc = 0; cc < NOUT; cc += 64) {  // one 128-byte chunk of bf16 per row
       uint8_t* sb = os.buf ? stage_acquire(os) : nullptr;
@@ -525,6 +554,14 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = apply_act(a.act, v[j]);
+            if (with_ce && col_ok) {
+              ce_add8(ce, v);
+              if (ce_loc >= n && ce_loc < n + 8) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (ce_loc == n + j) ce.zy = v[j];
+              }
+            }
           }
           if (sb) {
             stage_put(sb, os.lane, (h + j8) >> 3, pack_bf16x8(v));
@@ -575,6 +612,12 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
         }
         os.next ^= 1;
       }
+    }
+    if (with_ce && row_ok) {
+      float* o = a.ce_stats + ((static_cast<size_t>(s) * a.M + row) * a.n_tiles + n_blk) * 3;
+      o[0] = ce.m;
+      o[1] = ce.S;
+      o[2] = ce.zy;
     }
   } else if constexpr (Cfg::KIND == GK_ROW_SUM) {
     const int n0 = n_blk * 256;

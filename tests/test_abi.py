@@ -244,6 +244,27 @@ def test_vocab_validation():
     assert ce(0, 32000, 4, BF16, need) == OK
 
 
+def test_lm_head_cross_entropy_validation():
+    """The fused LM head and loss: the column-linear checks, then labels,
+    workspace and alignment, none of which reaches a launch."""
+    L = tpl.lib
+    W = view(K=256, N=4 * 512, tp=4, mode=COL, dtype=BF16)
+    need = L.tp_lm_head_ce_workspace_bytes(300, ctypes.byref(W))
+    assert need > L.tp_lm_head_ce_workspace_bytes(100, ctypes.byref(W)) > 0
+    assert L.tp_lm_head_ce_workspace_bytes(300, None) == 0
+    f = lambda T=300, w=W, labels=FAKE, logits=FAKE, ws=need, wsp=FAKE, dl=None: L.tp_lm_head_cross_entropy(
+        FAKE, T, ctypes.byref(w), labels, logits, FAKE, None, dl, ctypes.c_float(1.0), wsp, ws, None)
+    assert f(w=view(K=256, N=4 * 512, tp=4, mode=ROW, dtype=BF16)) == MODE   # a row view
+    assert f(logits=None) == NULL
+    assert f(labels=None) == NULL
+    assert f(wsp=None) == NULL
+    assert f(ws=need - 1) == WORKSPACE
+    assert f(labels=FAKE + 2) == ALIGN
+    assert f(dl=FAKE + 1) == ALIGN
+    assert f(T=-1) == SHAPE
+    assert f(T=0, labels=None, wsp=None, ws=0, logits=None) == OK
+
+
 def test_moe_validation():
     L = tpl.lib
     Wg, Wd = view(K=128, N=256, mode=COL, dtype=BF16), view(K=256, N=128, mode=ROW, dtype=BF16)

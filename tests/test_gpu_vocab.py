@@ -104,18 +104,76 @@ def test_embedding_lm_head_cross_entropy_chain(tp, T, H, V):
     assert abs(float(host(mean)[0]) - ref.mean()) <= TOL_BF16 * np.sqrt(np.mean(ref ** 2))
 
 
+@pytest.mark.parametrize("tp,T,H,V,dtype", [
+    (4, 260, 256, 4096, torch.bfloat16),      # statistics from the GEMM epilogue, 4 tiles per shard
+    (2, 300, 512, 2000, torch.bfloat16),      # 1000 columns a shard: the last tile holds 232
+    (1, 129, 256, 520, torch.bfloat16),       # one shard, a last tile of 8 columns, a ragged token block
+    (8, 37, 128, 4096, torch.bfloat16),       # 37 tokens: weight-streaming GEMM, then a pass over the logits
+    (2, 100, 128, 1024, torch.float32),       # fp32 views: FFMA GEMM, then a pass over the logits
+])
+def test_lm_head_cross_entropy_fused(tp, T, H, V, dtype):
+    """The LM head and the loss in one call against the oracle's chain. On
+    the fused bf16 path the statistics come from the fp32 accumulator, so
+    the losses are those of unrounded logits: held to the fp32 bound. Where
+    a pass reads stored bf16 logits (37 tokens) the chain bound applies."""
+    d = S.vocab_lm(T, H, V)
+    E, W = dev(d["E"], dtype), dev(d["W_lm"], dtype)
+    Slm = tpl.tp_shard_weights(W, tp, "col")
+    X0 = tpl.tp_vocab_embedding(ids_dev(d["ids"]), E, tp)
+    dz = torch.empty((tp, T, V // tp), dtype=dtype, device="cuda")
+    logits, loss, mean = tpl.tp_lm_head_cross_entropy(X0, Slm, ids_dev(d["labels"]), dlogits=dz)
+    assert tpl.tp_get_error() == 0
+    Xr = O.vocab_embedding(d["ids"], f64(host(E)), tp)
+    z = O.column_parallel(Xr, f64(host(W)), tp)
+    ref = O.vocab_parallel_cross_entropy(z, d["labels"])
+    fused = dtype == torch.bfloat16 and T > 64
+    tol = TOL_F32 if (fused or dtype == torch.float32) else TOL_BF16
+    assert_close(logits, np.stack(z), TOL_BF16 if dtype == torch.bfloat16 else TOL_F32, "logits")
+    assert_close(loss, ref, tol, "losses")
+    assert abs(float(host(mean)[0]) - ref.mean()) <= tol * np.sqrt(np.mean(ref ** 2)), "mean loss"
+    gref = O.cross_entropy_grad(O.all_gather(z), d["labels"], 1.0 / T)
+    got = host(dz).transpose(1, 0, 2).reshape(T, V)
+    if dtype == torch.bfloat16:
+        assert_close_stored(got, gref, TOL_BF16, "dlogits")
+    else:
+        err = np.abs(got - gref) - (TOL_F32 * np.sqrt(np.mean(gref ** 2)) + 1e-6 * np.abs(gref))
+        assert (err <= 0).all(), f"dlogits fp32: worst excess {err.max():.3g}"
+
+
+def test_lm_head_cross_entropy_fused_bad_label():
+    T, H, V, tp = 130, 128, 1024, 2
+    d = S.vocab_lm(T, H, V)
+    d["labels"][[3, 77]] = [V, -5]
+    Slm = tpl.tp_shard_weights(dev(d["W_lm"]), tp, "col")
+    X0 = tpl.tp_vocab_embedding(ids_dev(d["ids"]), dev(d["E"]), tp)
+    _, loss, _ = tpl.tp_lm_head_cross_entropy(X0, Slm, ids_dev(d["labels"]))
+    assert tpl.tp_get_error() == TP_ERR_INDEX
+    l = host(loss)
+    assert np.isnan(l[[3, 77]]).all() and np.isfinite(np.delete(l, [3, 77])).all()
+
+
 def test_lm_head_cross_entropy_full_size():
     """The bench workload (T = 4096, H = 4096, V = 32000, tp = 4): every
     token's loss and the mean loss against the oracle's chain (vocabulary
     embedding, column-parallel LM head, vocabulary-parallel cross-entropy),
-    which runs over blocks of token rows (rows are independent)."""
+    which runs over blocks of token rows (rows are independent). Both ways:
+    the LM head then a loss over its stored bf16 logits (the chain bound),
+    and the fused call, whose statistics come from the fp32 accumulator (the
+    fp32 bound)."""
     T, H, V, tp = 4096, 4096, 32000, 4
     d = S.vocab_lm(T, H, V)
     loss, mean, _ = lm_chain(d, tp)
     assert tpl.tp_get_error() == 0
-    X0 = O.vocab_embedding(d["ids"], f64(d["E"]), tp)
+    Slm = tpl.tp_shard_weights(dev(d["W_lm"]), tp, "col")
+    X0 = tpl.tp_vocab_embedding(ids_dev(d["ids"]), dev(d["E"]), tp)
+    _, loss_f, mean_f = tpl.tp_lm_head_cross_entropy(X0, Slm, ids_dev(d["labels"]))
+    assert tpl.tp_get_error() == 0
+    X0r = O.vocab_embedding(d["ids"], f64(d["E"]), tp)
     W = f64(d["W_lm"])
-    ref = np.concatenate([O.vocab_parallel_cross_entropy(O.column_parallel(X0[r:r + 512], W, tp),
+    ref = np.concatenate([O.vocab_parallel_cross_entropy(O.column_parallel(X0r[r:r + 512], W, tp),
                                                          d["labels"][r:r + 512]) for r in range(0, T, 512)])
+    rms = np.sqrt(np.mean(ref ** 2))
     assert_close(loss, ref, TOL_BF16, "losses")
-    assert abs(float(host(mean)[0]) - ref.mean()) <= TOL_BF16 * np.sqrt(np.mean(ref ** 2)), "mean loss"
+    assert abs(float(host(mean)[0]) - ref.mean()) <= TOL_BF16 * rms, "mean loss"
+    assert_close(loss_f, ref, TOL_F32, "losses (fused)")
+    assert abs(float(host(mean_f)[0]) - ref.mean()) <= TOL_F32 * rms, "mean loss (fused)"
