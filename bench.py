@@ -423,7 +423,7 @@ def setup_workload(spec, torch, tpl):
                  "dW1": torch.empty((tp, Is, H), dtype=B, device="cuda"),
                  "dW_up": torch.empty((tp, Is, H), dtype=B, device="cuda"),
                  "dW2": torch.empty((tp, H, Is), dtype=B, device="cuda")}
-        ws = torch.empty(tpl.tp_mlp_backward_workspace_bytes(T, H, I, tp, "swiglu"), dtype=torch.uint8,
+        ws = torch.empty(tpl.tp_mlp_backward_workspace_bytes(T, H, I, tp, "swiglu", B), dtype=torch.uint8,
                          device="cuda")
 
         def api_call(dYin, dXout):  # the whole backward: 5 GEMM launches and the activation gradient

@@ -314,8 +314,12 @@ tp_status tp_mlp_block_static(const void* X, int64_t T, const tp_shards* W1, con
  * as it is (MN-major operands on the tensor cores): nothing is transposed
  * in memory, and each weight gradient comes out in the layout of the shards
  * it belongs to, so an optimizer can update them in place.
- * bf16 only (TP_ERR_DTYPE otherwise); all pointers are device pointers,
- * 16-byte aligned; T >= 1 (T == 0 returns TP_OK and launches nothing).
+ * bf16 views run on the tensor cores; fp32 views on an FFMA GEMM in which
+ * every element is a fixed-order chain of fmaf, so integer-valued inputs
+ * whose partial sums stay below 2^24 give exact results. All pointers are
+ * device pointers, 16-byte aligned for bf16 and 4-byte aligned for fp32;
+ * every tensor has the view's dtype. T >= 1 (T == 0 returns TP_OK and
+ * launches nothing).
  */
 
 /*
@@ -349,7 +353,7 @@ tp_status tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W
                                     void* stream);
 
 /* Workspace bytes tp_mlp_backward needs (act decides whether dU is kept). */
-size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int act);
+size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int act, int dtype);
 
 /*
  * tp_mlp_backward - backward of tp_mlp_block without biases (the tutorial
@@ -368,7 +372,7 @@ size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, 
  *   Hs = the activation output that fed W2. dY, dR, dX [T][H]; dR may be
  *   NULL. Any of dX, dW1, dW_up, dW2 may be NULL to skip it (dW_up must be
  *   NULL unless SwiGLU).
- *   workspace: >= tp_mlp_backward_workspace_bytes(T, H, I, tp, act) bytes,
+ *   workspace: >= tp_mlp_backward_workspace_bytes(T, H, I, tp, act, dtype) bytes,
  *   256-byte aligned: dHs, dG and dU (bf16 [tp][T][I/tp]) plus the
  *   split-tile scratch. Contents on return are unspecified.
  * Errors: as tp_column_linear_backward, plus TP_ERR_MODE for an unknown act.

@@ -75,7 +75,7 @@ _SIGS = {
     "tp_cuda_error_name": (ctypes.c_char_p, [_i32]),
     "tp_row_linear_backward": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp]),
     "tp_column_linear_backward": (_i32, [_vp, _i64, _P, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "tp_mlp_backward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
+    "tp_mlp_backward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32, _i32]),
     "tp_mlp_backward": (_i32, [_vp, _i64, _P, _P, _P, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
                                _vp, _vp, _vp, _vp, _vp]),
     "tp_vocab_embedding": (_i32, [_vp, _i64, _vp, _i64, _i64, _i32, _i32, _vp, _vp]),
@@ -339,8 +339,9 @@ def tp_column_linear_backward(X, W: Shards, dYs, dR=None, want_dX: bool = True, 
     return dX, dW
 
 
-def tp_mlp_backward_workspace_bytes(T: int, H: int, I: int, tp: int, act: str = "swiglu") -> int:
-    return lib.tp_mlp_backward_workspace_bytes(T, H, I, tp, ACTS[act])
+def tp_mlp_backward_workspace_bytes(T: int, H: int, I: int, tp: int, act: str = "swiglu",
+                                    dtype=torch.bfloat16) -> int:
+    return lib.tp_mlp_backward_workspace_bytes(T, H, I, tp, ACTS[act], TP_F32 if dtype == torch.float32 else TP_BF16)
 
 
 def tp_mlp_backward(X, W1: Shards, W2: Shards, G, Hs, dY, W_up: Shards | None = None, U=None, dR=None,
@@ -353,7 +354,7 @@ def tp_mlp_backward(X, W1: Shards, W2: Shards, G, Hs, dY, W_up: Shards | None = 
     T, H = X.shape
     tp, Is = W1.tp, W1.N // W1.tp
     gated = act == "swiglu"
-    need = tp_mlp_backward_workspace_bytes(T, H, W1.N, tp, act)
+    need = tp_mlp_backward_workspace_bytes(T, H, W1.N, tp, act, X.dtype)
     if workspace is None:
         workspace = _workspace(need, X.device)
     if out is None:

@@ -1232,10 +1232,73 @@ tp_status tp_debug_inject(int kind) {
 // ---------------------------------------------------------------------------
 namespace {
 
-int check_bwd_view(const tp_shards* W, int mode) {
-  int r = check_view(W, mode);
-  if (r) return r;
-  return W->dtype == TP_BF16 ? TP_OK : TP_ERR_DTYPE;
+int check_bwd_view(const tp_shards* W, int mode) { return check_view(W, mode); }
+
+// --- fp32 backward: the strided FFMA GEMM (exact on integer inputs) ---------
+int simt_g_launch(const tpk::SimtGArgs& a, int z, cudaStream_t st) {
+  if (a.M <= 0 || a.N <= 0 || z <= 0) return TP_OK;
+  const dim3 grid(static_cast<unsigned>(cdiv(a.N, tpk::SK_BN)), static_cast<unsigned>(cdiv(a.M, tpk::SK_BM)),
+                  static_cast<unsigned>(z));
+  tpk::simt_gemm_strided_kernel<<<grid, tpk::SK_THREADS, 0, st>>>(a);
+  return launch_status();
+}
+// Row layer on fp32 (view [tp][N][Ks], dY [T][N], Xs [tp][T][Ks]):
+// dXs_s = dY W_s^T, dW_s = (Xs_s^T dY)^T in the view's storage layout.
+int row_bwd_f32(const void* Xs, int64_t T, const tp_shards* W, const void* dY, void* dXs, void* dW,
+                cudaStream_t st) {
+  const int tp = W->tp;
+  const int64_t N = W->N, Ks = W->K / tp;
+  int r;
+  if (dXs) {
+    tpk::SimtGArgs a{};
+    a.M = static_cast<int>(T), a.N = static_cast<int>(Ks), a.K = static_cast<int>(N), a.Q = 1;
+    a.A = static_cast<const float*>(dY), a.a_m = N, a.a_k = 1;
+    a.B = static_cast<const float*>(W->data), a.b_k = Ks, a.b_n = 1, a.b_z = N * Ks;
+    a.C = static_cast<float*>(dXs), a.c_m = Ks, a.c_n = 1, a.c_z = T * Ks;
+    if ((r = simt_g_launch(a, tp, st))) return r;
+  }
+  if (dW) {
+    tpk::SimtGArgs a{};
+    a.M = static_cast<int>(N), a.N = static_cast<int>(Ks), a.K = static_cast<int>(T), a.Q = 1;
+    a.A = static_cast<const float*>(dY), a.a_m = 1, a.a_k = N;
+    a.B = static_cast<const float*>(Xs), a.b_k = Ks, a.b_n = 1, a.b_z = T * Ks;
+    a.C = static_cast<float*>(dW), a.c_m = Ks, a.c_n = 1, a.c_z = N * Ks;
+    if ((r = simt_g_launch(a, tp, st))) return r;
+  }
+  return TP_OK;
+}
+// Column layer on fp32 (view [tp][Ns][K], dYs [tp][T][Ns], X [T][K]):
+// dX = sum_s dYs_s W_s^T (+ add, which may be dX itself), dW_s = (X^T dYs_s)^T.
+int col_bwd_f32(const void* X, int64_t T, const tp_shards* W, const void* dYs, const void* add, void* dX,
+                void* dW, cudaStream_t st) {
+  const int tp = W->tp;
+  const int64_t K = W->K, Ns = W->N / tp;
+  int r;
+  if (dX) {
+    tpk::SimtGArgs a{};
+    a.M = static_cast<int>(T), a.N = static_cast<int>(K), a.K = static_cast<int>(Ns), a.Q = tp;
+    a.A = static_cast<const float*>(dYs), a.a_m = Ns, a.a_k = 1, a.a_q = T * Ns;
+    a.B = static_cast<const float*>(W->data), a.b_k = K, a.b_n = 1, a.b_q = Ns * K;
+    a.C = static_cast<float*>(dX), a.c_m = K, a.c_n = 1;
+    a.add = static_cast<const float*>(add);
+    if ((r = simt_g_launch(a, 1, st))) return r;
+  }
+  if (dW) {
+    tpk::SimtGArgs a{};
+    a.M = static_cast<int>(Ns), a.N = static_cast<int>(K), a.K = static_cast<int>(T), a.Q = 1;
+    a.A = static_cast<const float*>(dYs), a.a_m = 1, a.a_k = Ns, a.a_z = T * Ns;
+    a.B = static_cast<const float*>(X), a.b_k = K, a.b_n = 1;
+    a.C = static_cast<float*>(dW), a.c_m = K, a.c_n = 1, a.c_z = Ns * K;
+    if ((r = simt_g_launch(a, tp, st))) return r;
+  }
+  return TP_OK;
+}
+// Pointer alignment of the backward's buffers: 16 bytes on the bf16
+// (tensor-map) path, the element on the fp32 one.
+bool bwd_ptrs_ok(std::initializer_list<const void*> ps, int dtype) {
+  for (const void* p : ps)
+    if (!ptr_ok(p, dtype)) return false;
+  return true;
 }
 
 bool ptrs16(std::initializer_list<const void*> ps) {
@@ -1283,7 +1346,14 @@ int col_bwd_bf16(const void* X, int64_t T, const tp_shards* W, const void* dYs, 
 }
 
 int act_bwd_launch(const void* dH, const void* G, const void* U, int64_t n, int act, void* dG, void* dU,
-                   cudaStream_t st) {
+                   cudaStream_t st, int dtype = TP_BF16) {
+  if (dtype == TP_F32) {
+    if (n == 0) return TP_OK;
+    tpk::act_backward_f32_kernel<<<grid_for(n, 256), 256, 0, st>>>(
+        static_cast<const float*>(dH), static_cast<const float*>(G), static_cast<const float*>(U), n, act,
+        static_cast<float*>(dG), static_cast<float*>(dU));
+    return launch_status();
+  }
   const int64_t n8 = n / 8;
   if (n8 == 0) return TP_OK;
   tpk::act_backward_kernel<<<grid_for(n8, 256), 256, 0, st>>>(
@@ -1307,8 +1377,9 @@ tp_status tp_row_linear_backward(const void* Xs, int64_t T, const tp_shards* W, 
   if (T < 0) return TP_ERR_SHAPE;
   if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
   if (T > 0 && (!dY || (dW && !Xs))) return TP_ERR_NULL;
-  if (!ptrs16({Xs, dY, dXs, dW})) return TP_ERR_ALIGN;
+  if (!bwd_ptrs_ok({Xs, dY, dXs, dW}, W->dtype)) return TP_ERR_ALIGN;
   if (T == 0) return TP_OK;
+  if (W->dtype == TP_F32) return as_status(row_bwd_f32(Xs, T, W, dY, dXs, dW, as_stream(stream)));
   return as_status(row_bwd_bf16(Xs, T, W, dY, dXs, dW, nullptr, as_stream(stream)));
 }
 
@@ -1320,7 +1391,11 @@ tp_status tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W
   if (T < 0) return TP_ERR_SHAPE;
   if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
   if (T > 0 && (!dYs || (dW && !X))) return TP_ERR_NULL;
-  if (!ptrs16({X, dYs, dR, dX, dW})) return TP_ERR_ALIGN;
+  if (!bwd_ptrs_ok({X, dYs, dR, dX, dW}, W->dtype)) return TP_ERR_ALIGN;
+  if (W->dtype == TP_F32) {
+    if (T == 0) return TP_OK;
+    return as_status(col_bwd_f32(X, T, W, dYs, dR, dX, dW, as_stream(stream)));
+  }
   if (W->K % 8 != 0) return TP_ERR_ALIGN;
   Scratch sc{};
   const Scratch* scp = nullptr;
@@ -1329,11 +1404,12 @@ tp_status tp_column_linear_backward(const void* X, int64_t T, const tp_shards* W
   return as_status(col_bwd_bf16(X, T, W, dYs, dR, dX, dW, scp, as_stream(stream)));
 }
 
-size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int act) {
-  if (T < 0 || H < 1 || I < 1 || tp < 1) return 0;
-  const size_t inter = align256(static_cast<size_t>(T) * I * 2);
+size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, int act, int dtype) {
+  if (T < 0 || H < 1 || I < 1 || tp < 1 || !dtype_ok(dtype)) return 0;
+  const size_t inter = align256(static_cast<size_t>(T) * I * elem_size(dtype));
   const bool gated = act == TP_ACT_SWIGLU;
-  return (gated ? 3 : 2) * inter + scratch_bytes(T, bwd_max_tiles(H, I, tp));  // dHs, dG (, dU), scratch
+  // dHs, dG (, dU); the bf16 (tcgen05) path also takes the split-tile scratch
+  return (gated ? 3 : 2) * inter + (dtype == TP_BF16 ? scratch_bytes(T, bwd_max_tiles(H, I, tp)) : 0);
 }
 
 tp_status tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
@@ -1355,14 +1431,29 @@ tp_status tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const t
   if (W2->tp != W1->tp || W2->K != W1->N || W2->N != W1->K) return TP_ERR_SHAPE;
   if (T < 0) return TP_ERR_SHAPE;
   if (T > INT32_MAX) return TP_ERR_UNSUPPORTED;
+  if (W2->dtype != W1->dtype || (gated && W_up->dtype != W1->dtype)) return TP_ERR_DTYPE;
   if (T > 0 && (!X || !G || !Hs || !dY || (gated && !U) || !workspace)) return TP_ERR_NULL;
-  if (!ptrs16({X, G, U, Hs, dY, dR, dX, dW1, dW_up, dW2}) || !aligned(workspace, 256)) return TP_ERR_ALIGN;
+  const int dt = W1->dtype;
+  if (!bwd_ptrs_ok({X, G, U, Hs, dY, dR, dX, dW1, dW_up, dW2}, dt) || !aligned(workspace, 256)) return TP_ERR_ALIGN;
   const int64_t H = W1->K, I = W1->N;
   const int tp = W1->tp;
-  if (ws_bytes < tp_mlp_backward_workspace_bytes(T, H, I, tp, act)) return TP_ERR_WORKSPACE;
+  if (ws_bytes < tp_mlp_backward_workspace_bytes(T, H, I, tp, act, dt)) return TP_ERR_WORKSPACE;
   if (T == 0) return TP_OK;
   const cudaStream_t st = as_stream(stream);
   char* ws = static_cast<char*>(workspace);
+  if (dt == TP_F32) {
+    // the same steps on the FFMA GEMM: row layer, activation, column layer(s)
+    // with the input gradient accumulated over gate and up, plus dR
+    const size_t inter = align256(static_cast<size_t>(T) * I * sizeof(float));
+    void* dHs = ws;
+    void* dG = ws + inter;
+    void* dU = gated ? ws + 2 * inter : nullptr;
+    if ((r = row_bwd_f32(Hs, T, W2, dY, dHs, dW2, st))) return as_status(r);
+    if ((r = act_bwd_launch(dHs, G, U, static_cast<int64_t>(T) * I, act, dG, dU, st, TP_F32))) return as_status(r);
+    if ((r = col_bwd_f32(X, T, W1, dG, dR, dX, dW1, st))) return as_status(r);
+    if (gated) r = col_bwd_f32(X, T, W_up, dU, dX, dX, dW_up, st);
+    return as_status(r);
+  }
   const size_t inter = align256(static_cast<size_t>(T) * I * 2);
   void* dHs = ws;
   void* dG = ws + inter;

@@ -258,4 +258,17 @@ __global__ void act_backward_kernel(const __nv_bfloat16* __restrict__ dH, const 
   }
 }
 
+// fp32 form of act_backward_kernel: one element per step, any count.
+__global__ void act_backward_f32_kernel(const float* __restrict__ dH, const float* __restrict__ G,
+                                        const float* __restrict__ U, int64_t n, int act, float* __restrict__ dG,
+                                        float* __restrict__ dU) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    float dg, du;
+    act_grad(act, dH[i], G[i], act == ACT_SWIGLU ? U[i] : 0.0f, dg, du);
+    dG[i] = dg;
+    if (act == ACT_SWIGLU) dU[i] = du;
+  }
+}
+
 }  // namespace tpk

@@ -112,4 +112,76 @@ __global__ void __launch_bounds__(SK_THREADS) simt_gemm_kernel(const SimtArgs a)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Strided fp32 GEMM for the backward of the column/row pair on fp32 tensors:
+//   C_z(m, n) = sum_{q < Q} sum_{k < K} A_{q,z}(m, k) * B_{q,z}(k, n)  (+ add_z(m, n))
+// with every operand given by strides, so that the data and weight
+// gradients read the forward's tensors and shard layouts as they are
+// (A_{q,z}(m, k) = A[q * a_q + z * a_z + m * a_m + k * a_k], likewise B, C).
+// Each element is a fixed-order chain of fmaf (q ascending, then k
+// ascending), so integer-valued inputs whose partial sums stay below 2^24
+// give exact results. `add` has C's strides and may be C itself (each
+// element is read, then written, by one thread).
+// grid: (ceil(N / 64), ceil(M / 64), Z)
+// ---------------------------------------------------------------------------
+struct SimtGArgs {
+  int M, N, K, Q;
+  const float* A;
+  int64_t a_m, a_k, a_q, a_z;
+  const float* B;
+  int64_t b_k, b_n, b_q, b_z;
+  float* C;
+  int64_t c_m, c_n, c_z;
+  const float* add;
+};
+
+__global__ void __launch_bounds__(SK_THREADS) simt_gemm_strided_kernel(const SimtGArgs a) {
+  __shared__ float As[SK_BK][SK_BM + 4];
+  __shared__ float Bs[SK_BK][SK_BN + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * SK_BM, n0 = blockIdx.x * SK_BN;
+  const int64_t z = blockIdx.z;
+  float acc[4][4] = {};
+  for (int q = 0; q < a.Q; ++q) {
+    const float* A = a.A + q * a.a_q + z * a.a_z;
+    const float* B = a.B + q * a.b_q + z * a.b_z;
+    for (int k0 = 0; k0 < a.K; k0 += SK_BK) {
+      for (int i = threadIdx.x; i < SK_BK * SK_BM; i += SK_THREADS) {
+        const int kk = i % SK_BK, r = i / SK_BK;
+        const int gk = k0 + kk, gm = m0 + r, gn = n0 + r;
+        As[kk][r] = (gm < a.M && gk < a.K) ? A[gm * a.a_m + gk * a.a_k] : 0.0f;
+        Bs[kk][r] = (gn < a.N && gk < a.K) ? B[gk * a.b_k + gn * a.b_n] : 0.0f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < SK_BK; ++kk) {
+        float av[4], bv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      }
+      __syncthreads();
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= a.M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= a.N) continue;
+      const int64_t off = z * a.c_z + m * a.c_m + n * a.c_n;
+      float v = acc[i][j];
+      if (a.add) v += a.add[off];
+      a.C[off] = v;
+    }
+  }
+}
+
 }  // namespace tpk

@@ -200,7 +200,7 @@ def test_backward_validation():
     L = tpl.lib
     rowv, colv = view(K=256, N=128, mode=ROW, dtype=BF16), view(K=128, N=256, mode=COL, dtype=BF16)
     # row layer
-    assert L.tp_row_linear_backward(FAKE, 8, ctypes.byref(view(mode=ROW)), FAKE, FAKE, FAKE, None) == DTYPE
+    assert L.tp_row_linear_backward(FAKE + 2, 8, ctypes.byref(view(mode=ROW)), FAKE, FAKE, FAKE, None) == ALIGN  # fp32
     assert L.tp_row_linear_backward(FAKE, 8, ctypes.byref(colv), FAKE, FAKE, FAKE, None) == MODE
     assert L.tp_row_linear_backward(FAKE, -1, ctypes.byref(rowv), FAKE, FAKE, FAKE, None) == SHAPE
     assert L.tp_row_linear_backward(FAKE, 8, ctypes.byref(rowv), None, FAKE, FAKE, None) == NULL
@@ -214,8 +214,10 @@ def test_backward_validation():
     assert L.tp_column_linear_backward(FAKE, 0, ctypes.byref(colv), FAKE, None, FAKE, FAKE, None, 0, None) == OK
     # MLP block
     W1, W2 = view(K=128, N=256, mode=COL, dtype=BF16), view(K=256, N=128, mode=ROW, dtype=BF16)
-    need = L.tp_mlp_backward_workspace_bytes(8, 128, 256, 2, 4)
-    assert need > L.tp_mlp_backward_workspace_bytes(8, 128, 256, 2, 1) > 0
+    need = L.tp_mlp_backward_workspace_bytes(8, 128, 256, 2, 4, BF16)
+    assert need > L.tp_mlp_backward_workspace_bytes(8, 128, 256, 2, 1, BF16) > 0
+    assert L.tp_mlp_backward_workspace_bytes(8, 128, 256, 2, 4, F32) > 0
+    assert L.tp_mlp_backward_workspace_bytes(8, 128, 256, 2, 4, 7) == 0
     args = lambda act, Wu, U, ws_bytes, T=8: (FAKE, T, ctypes.byref(W1), Wu, ctypes.byref(W2), act, FAKE, U, FAKE,
                                               FAKE, None, FAKE, ws_bytes, FAKE, FAKE, None, FAKE, None)
     assert L.tp_mlp_backward(*args(9, None, None, need)) == MODE
@@ -224,6 +226,9 @@ def test_backward_validation():
     assert L.tp_mlp_backward(*args(4, ctypes.byref(W1), None, need)) == NULL  # and U
     assert L.tp_mlp_backward(*args(4, ctypes.byref(W1), FAKE, need - 1)) == WORKSPACE
     assert L.tp_mlp_backward(*args(4, ctypes.byref(W1), FAKE, need, T=0)) == OK
+    W2f = view(K=256, N=128, mode=ROW, dtype=F32)   # an fp32 row layer under a bf16 column layer
+    assert L.tp_mlp_backward(FAKE, 8, ctypes.byref(W1), None, ctypes.byref(W2f), 1, FAKE, None, FAKE, FAKE, None,
+                             FAKE, need, FAKE, FAKE, None, FAKE, None) == DTYPE
 
 
 def test_vocab_validation():

@@ -17,7 +17,7 @@ import torch
 
 import synth_inputs as S
 from oracle import tp_oracle as O
-from tests._util import TOL_BF16, assert_close, assert_close_stored, dev, f64, host
+from tests._util import TOL_BF16, TOL_F32, assert_close, assert_close_stored, assert_exact, dev, f64, host, i64
 
 
 def close_wgrad(gpu, ref, T, what):
@@ -160,14 +160,85 @@ def test_mlp_backward_partial_outputs_and_single_token():
 
 
 def test_backward_validation():
-    Sg = tpl.tp_shard_weights(torch.zeros((256, 512), dtype=torch.float32, device="cuda"), 2, "col")
-    with pytest.raises(tpl.TpError):  # fp32 is not served by the backward
-        tpl.tp_column_linear_backward(torch.zeros((8, 256), device="cuda"), Sg,
-                                      torch.zeros((2, 8, 256), device="cuda"))
     Sb = tpl.tp_shard_weights(torch.zeros((256, 512), dtype=B, device="cuda"), 2, "col")
     with pytest.raises(tpl.TpError):  # a column view where a row view is needed
         tpl.tp_row_linear_backward(torch.zeros((2, 8, 128), dtype=B, device="cuda"), Sb,
                                    torch.zeros((8, 512), dtype=B, device="cuda"))
+
+
+# --- fp32 views: the FFMA GEMM. Integer-valued inputs are exact, so the
+# dataflow of the backward (which shards are summed, which dY each shard
+# receives, the orientation of every weight gradient) is checked bit for bit
+# against the oracle's int64 arithmetic.
+F = torch.float32
+
+
+@pytest.mark.parametrize("tp,T,H,I", [(2, 16, 64, 256), (4, 37, 96, 160), (1, 5, 32, 48)])
+def test_int_relu_mlp_backward_bit_exact(tp, T, H, I):
+    """Saved values from the GPU's fp32 forward (exact on integers), then
+    the backward; the oracle recomputes everything in int64. Largest partial
+    sums: |dX| <= I * 3 * (H * 3 * 3) = 442368 < 2^24 at the integer MLP's
+    sizes (T = 16, H = 64, I = 256), less elsewhere."""
+    X = S.uniform_ints(451, (T, H))
+    W1, W2 = S.uniform_ints(452, (H, I)), S.uniform_ints(453, (I, H))
+    dY, dR = S.uniform_ints(454, (T, H)), S.uniform_ints(455, (T, H))
+    Xd = dev(X, F)
+    S1 = tpl.tp_shard_weights(dev(W1, F), tp, "col")
+    S2 = tpl.tp_shard_weights(dev(W2, F), tp, "row")
+    G = tpl.tp_column_linear(Xd, S1, act="none")
+    Hs = tpl.tp_column_linear(Xd, S1, act="relu")
+    g = tpl.tp_mlp_backward(Xd, S1, S2, G, Hs, dev(dY, F), dR=dev(dR, F), act="relu")
+    assert tpl.tp_get_error() == 0
+    ref = O.mlp_backward(i64(X), i64(W1), i64(W2), tp, i64(dY), "relu", dR=i64(dR))
+    assert_exact(g["dX"], ref["dX"], "dX")
+    assert_exact(g["dW1"], np.stack([w.T for w in ref["dW1"]]), "dW1 (storage layout)")
+    assert_exact(g["dW2"], np.stack([w.T for w in ref["dW2"]]), "dW2 (storage layout)")
+
+
+@pytest.mark.parametrize("tp,T,K,N", [(2, 16, 64, 256), (4, 37, 96, 160)])
+def test_int_single_linears_backward_bit_exact(tp, T, K, N):
+    """The two layers alone on integers: the row layer hands every shard the
+    same dY; the column layer sums its shards' input gradients (plus dR)."""
+    W, X, dY = S.uniform_ints(461, (K, N)), S.uniform_ints(462, (T, K)), S.uniform_ints(463, (T, N))
+    dR = S.uniform_ints(464, (T, K))
+    Sr = tpl.tp_shard_weights(dev(W, F), tp, "row")
+    Xs = torch.stack([t.contiguous() for t in dev(X, F).split(K // tp, dim=1)])
+    dXs, dW = tpl.tp_row_linear_backward(Xs, Sr, dev(dY, F))
+    assert tpl.tp_get_error() == 0
+    ref_dX, ref_dW = O.row_linear_backward(O.split_columns(i64(X), tp), i64(W), tp, i64(dY))
+    assert_exact(dXs, np.stack(ref_dX), "row dXs")
+    assert_exact(dW, np.stack([w.T for w in ref_dW]), "row dW")
+    Sc = tpl.tp_shard_weights(dev(W, F), tp, "col")
+    dYs = S.uniform_ints(465, (tp, T, N // tp))
+    dX, dWc = tpl.tp_column_linear_backward(dev(X, F), Sc, dev(dYs, F), dR=dev(dR, F))
+    assert tpl.tp_get_error() == 0
+    ref_dX, ref_dW = O.column_linear_backward(i64(X), i64(W), tp, [i64(dYs[s]) for s in range(tp)], i64(dR))
+    assert_exact(dX, ref_dX, "column dX")
+    assert_exact(dWc, np.stack([w.T for w in ref_dW]), "column dW")
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu", "silu", "swiglu"])
+def test_fp32_mlp_backward(act):
+    """Real values on the fp32 path, every activation, saved values given to
+    both sides: held to the fp32 bound, 1e-4 * RMS."""
+    tp, T, H, I = 4, 70, 96, 160
+    d = S.mlp_backward(T, H, I, seeds=(471, 472, 473, 474, 475), std=0.05)
+    G, U, Hs = saved_values(476, tp, T, I // tp, act)
+    dR = S.normal(479, (T, H))
+    Sg = tpl.tp_shard_weights(dev(d["Wg"], F), tp, "col")
+    Sd = tpl.tp_shard_weights(dev(d["Wd"], F), tp, "row")
+    Su = tpl.tp_shard_weights(dev(d["Wu"], F), tp, "col") if act == "swiglu" else None
+    g = tpl.tp_mlp_backward(dev(d["X"], F), Sg, Sd, dev(G, F), dev(Hs, F), dev(d["dY"], F), W_up=Su,
+                            U=None if U is None else dev(U, F), dR=dev(dR, F), act=act)
+    assert tpl.tp_get_error() == 0
+    ref = O.mlp_backward_saved(f64(d["X"]), f64(d["Wg"]), f64(d["Wd"]), tp, f64(d["dY"]), list(f64(G)),
+                               list(f64(Hs)), act, W_up=f64(d["Wu"]) if act == "swiglu" else None,
+                               U=None if U is None else list(f64(U)), dR=f64(dR))
+    assert_close(g["dX"], ref["dX"], TOL_F32, "dX")
+    assert_close(g["dW1"], np.stack([w.T for w in ref["dW1"]]), TOL_F32, "dW1")
+    assert_close(g["dW2"], np.stack([w.T for w in ref["dW2"]]), TOL_F32, "dW2")
+    if act == "swiglu":
+        assert_close(g["dW_up"], np.stack([w.T for w in ref["dW_up"]]), TOL_F32, "dW_up")
 
 
 def test_mlp_backward_full_size_sampled():
