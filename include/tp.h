@@ -608,7 +608,9 @@ tp_status tp_get_error(void* stream);
  *     (default 2e9 ns).
  *   tp_debug_inject(1): the next tensor-core GEMM launch's first block
  *     withholds one operand load, so its consumer's wait expires and the
- *     kernel takes its abort path. tp_debug_inject(0) disarms.
+ *     kernel takes its abort path; tp_debug_inject(2): the same in its
+ *     second block (in a launch of CTA pairs, the odd CTA of the first
+ *     pair). tp_debug_inject(0) disarms.
  */
 tp_status tp_debug_set_wait_limit_ns(uint64_t ns);
 tp_status tp_debug_inject(int kind);

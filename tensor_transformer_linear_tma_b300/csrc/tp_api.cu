@@ -1221,7 +1221,7 @@ tp_status tp_debug_set_wait_limit_ns(uint64_t ns) {
 }
 
 tp_status tp_debug_inject(int kind) {
-  if (kind < 0 || kind > 1) return TP_ERR_MODE;
+  if (kind < 0 || kind > 2) return TP_ERR_MODE;
   return cuda_ok(cudaMemcpyToSymbol(tpk::g_tp_inject, &kind, sizeof(int))) ? TP_OK : TP_ERR_CUDA;
 }
 

@@ -813,9 +813,13 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tfull = bars + 2 * Cfg::STAGES;     // [2]       MMA -> epilogue
   uint64_t* tempty = tfull + 2;                 // [2]       epilogue -> MMA
   uint64_t* drain = tempty + 2;                 // [1]       abort path only
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* xch = drain + 1;                    // [1]       abort path, CTA pairs: odd -> even (counts written)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xch + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;
+  // abort path, CTA pairs: the odd CTA's last issued use of each stage,
+  // written into the even CTA
+  volatile int* peer_issued = last_flag + 1;    // [STAGES]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -831,6 +835,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&tempty[i], PAIR ? 8 : 4);  // the epilogue warps of both CTAs of a pair
     }
     mbar_init(drain, 1);
+    mbar_init(xch, 1);
     *abort_flag = 0;
     *last_flag = 0;
     fence_mbar_init();
@@ -869,11 +874,15 @@ __global__ void __launch_bounds__(192, 1)
                                      : static_cast<uint32_t>((PAIR ? 2 : 1) * Cfg::STAGE_BYTES);
       int stage = 0;
       uint32_t phase = 0;
-      int issued[Cfg::STAGES];
+      int round = 0;            // passes over the ring so far: the use index of each stage this pass
+      int issued[Cfg::STAGES];  // per stage: the use index of the last load issued, or -1
 #pragma unroll
       for (int i = 0; i < Cfg::STAGES; ++i) issued[i] = -1;
       // test-only: withhold one load (the flag is consumed by the first launch that sees it)
-      bool skip_one = blockIdx.x == 0 && g_tp_inject == 1 && atomicExch(&g_tp_inject, 0) == 1;
+      // (kind 1: block 0, the even CTA of a pair; kind 2: block 1, the odd one)
+      const int inj = g_tp_inject;
+      bool skip_one = (inj == 1 || inj == 2) && static_cast<int>(blockIdx.x) == inj - 1 &&
+                      atomicExch(&g_tp_inject, 0) == inj;
       bool ok = true;
 
       SegIter it(args);
@@ -951,11 +960,12 @@ __global__ void __launch_bounds__(192, 1)
                 }
               }
             }
-            issued[stage] = static_cast<int>(phase);
+            issued[stage] = round;
           }
           if (++stage == Cfg::STAGES) {
             stage = 0;
             phase ^= 1u;
+            ++round;
           }
         }
       }
@@ -971,15 +981,38 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (!ok) {  // let every copy this block started land before it exits
-        if (!PAIR || rank == 0) {
+        if constexpr (!PAIR) {
           for (int i = 0; i < Cfg::STAGES; ++i)
-            if (issued[i] >= 0) mbar_wait_drain(&full[i], static_cast<uint32_t>(issued[i]));
+            if (issued[i] >= 0) mbar_wait_drain(&full[i], static_cast<uint32_t>(issued[i]) & 1u);
+        } else if (rank != 0) {
+          // The odd CTA's copies count on the even CTA's full barriers, which
+          // it cannot poll: it hands the even CTA its last issued use of each
+          // stage, then waits (bounded) until the even CTA reports that every
+          // such copy has landed.
+          for (int i = 0; i < Cfg::STAGES; ++i)
+            st_cluster_u32(mapa_shared(const_cast<int*>(peer_issued + i), 0), static_cast<uint32_t>(issued[i]));
+          mbar_arrive_cluster(mapa_shared(xch, 0));  // release: the words above are visible first
+          mbar_wait_drain(drain, 0);
         } else {
-          // the odd CTA's copies count on the even CTA's barrier, which it
-          // cannot poll: give them a fixed 50 us to land
-          const uint64_t t0 = globaltimer_ns();
-          while (globaltimer_ns() - t0 < 50000) {
+          // The even CTA: with the odd CTA's counts (if they come within the
+          // limit; else the odd CTA is taken to have issued what this one
+          // did), make the pending phase of each stage completable and wait
+          // for it. At most one phase per stage is pending (a CTA issues use
+          // k only once use k - 1 has been consumed): a use the odd CTA
+          // issued and this one did not is armed for the odd half alone; a
+          // use this one armed that the odd CTA never issued has the odd
+          // half counted as arrived. Then the odd CTA may leave.
+          const bool got = mbar_wait_drain(xch, 0);
+          const uint32_t half = static_cast<uint32_t>(Cfg::STAGE_BYTES);
+          for (int i = 0; i < Cfg::STAGES; ++i) {
+            const int e = issued[i], o = got ? peer_issued[i] : issued[i];
+            const int last = e > o ? e : o;
+            if (last < 0) continue;
+            if (o == last && e < last) mbar_arrive_expect_tx(&full[i], half);
+            else if (e == last && o < last) mbar_complete_tx(&full[i], half);
+            mbar_wait_drain(&full[i], static_cast<uint32_t>(last) & 1u);
           }
+          if (got) mbar_arrive_cluster(mapa_shared(drain, 1));
         }
       }
     }

@@ -38,12 +38,15 @@ def short_wait_limit():
     tpl.tp_get_error()
 
 
-@pytest.mark.parametrize("path", ["whole_tiles", "cluster_pairs", "weight_streaming"])
+@pytest.mark.parametrize("path", ["whole_tiles", "cluster_pairs", "cluster_pairs_odd", "weight_streaming"])
 def test_expired_wait_is_reported_and_context_survives(short_wait_limit, path):
     # 300 tokens: 3 token blocks, single CTAs; 512 tokens: 4 blocks, CTA pairs
     # on the 2-SM MMA, each CTA loading its own operand half (the withheld load
-    # starves the pair's MMA)
-    T = {"whole_tiles": 300, "cluster_pairs": 512, "weight_streaming": 8}[path]
+    # starves the pair's MMA). Withheld by the even CTA, the even CTA arms the
+    # odd CTA's half of that stage alone when it drains; withheld by the odd
+    # CTA, it counts the missing half as arrived. Either way the odd CTA
+    # leaves only once the even CTA has seen every copy it started land.
+    T = {"whole_tiles": 300, "cluster_pairs": 512, "cluster_pairs_odd": 512, "weight_streaming": 8}[path]
     K, N, tp = 256, 2 * 1024, 2
     X, W = S.normal(101, (T, K)), S.normal(102, (K, N), 0.05)
     Sc = tpl.tp_shard_weights(dev(W), tp, "col")
@@ -55,7 +58,7 @@ def test_expired_wait_is_reported_and_context_survives(short_wait_limit, path):
     Xd = dev(X)
     torch.cuda.synchronize()
 
-    tpl.tp_debug_inject(1)
+    tpl.tp_debug_inject(2 if path == "cluster_pairs_odd" else 1)
     tpl.tp_column_linear(Xd, Sc, workspace=ws)
     assert tpl.tp_get_error() == TP_ERR_TIMEOUT
 
