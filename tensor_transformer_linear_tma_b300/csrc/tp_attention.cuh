@@ -25,18 +25,23 @@
 //               O_t += P_t V with P_t in TMEM (over the first half of its
 //               scores) and V an MN-major operand straight from its TMA
 //               tile. Per key block the order is P_0 V, S_0(next),
-//               P_1 V, S_1(next);
+//               P_1 V, S_1(next), each P_t V in two halves of 64 keys:
+//               the first as soon as the softmax has stored P_t for them;
 //   warps 2..5  softmax of tile 0, warps 6..9 of tile 1, one thread per
 //               query row: the row's 128 scores from TMEM, the row maximum,
 //               exp2 with the log2(e)/sqrt(hd) scale folded into one paired
 //               FMA, the row sum, P packed to bf16 and stored over the
-//               scores; at the end of a unit O / l to the context.
+//               scores, handed over a half at a time (the first half's P V
+//               runs while the second half's exponentials are computed);
+//               at the end of a unit O / l to the context.
 // The exponent base m only moves when a row's maximum exceeds it by more
 // than 2^8 (P then stays below 256, exact enough in bf16), so O and l are
 // rescaled only on such jumps. S_t(j) is issued after P_t(j-1) V, and a
 // commit arrives once every earlier MMA of the issuer is complete, so the
 // scores of block j reaching the softmax mean that O_t holds blocks
-// 0..j-1 and no MMA writes it: the rescale needs no other wait.
+// 0..j-1 and no MMA writes it: a move in a block's first half needs no
+// other wait. A move in its second half waits until the first half's P V
+// is complete, then rescales O_t, which holds that half too.
 // The tensor core runs tcgen05 operations in issue order, so S_t(j+1) may be
 // issued into the buffer that holds P_t(j) right after P_t(j) V.
 // Every wait is bounded as in the GEMM kernel.
@@ -99,7 +104,7 @@ struct AttnCfg {
   static constexpr int TILE = PANELS * PANEL;       // 128 x HD bf16
   static constexpr int SLOTS = HD == 128 ? 5 : 8;   // K/V ring
   static constexpr int THREADS = 320;
-  static constexpr int AUX = 256;                   // barriers, TMEM address, abort flag
+  static constexpr int AUX = 512;                   // barriers, TMEM address, abort flag
   static constexpr int SMEM = (2 + SLOTS) * TILE + AUX + 1024;  // Q tiles, ring, aux; alignment
   static constexpr uint32_t TM_S = 0;               // scores / P of tile t at column 128 t
   static constexpr uint32_t TM_O = 256;             // O of tile t at 256 + HD t
@@ -153,32 +158,20 @@ __device__ __forceinline__ AtUnit at_decode(const AttnArgs& a, int u, int hd) {
   return w;
 }
 
-// A moved exponent base (rare): this warp's rows of O_t (blocks 0..jb-1; no
-// MMA writes O_t until P_t(jb) is handed over, see the top of this file)
-// and, when the base moved in the block's second half, the first half's P,
-// stored with the old base, are multiplied by alpha (1 for rows whose base
-// stayed). Kept out of line: its registers are paid for only when it runs.
+// A moved exponent base (rare): this warp's rows of O_t are multiplied by
+// alpha (1 for rows whose base stayed). The caller has made sure that no MMA
+// writes O_t meanwhile. Kept out of line: its registers are paid for only
+// when it runs.
 template <int HD>
-__device__ __noinline__ void at_rescale(uint32_t tO, uint32_t tS, float alpha, bool o_too, bool p_too) {
-  if (o_too) {
+__device__ __noinline__ void at_rescale(uint32_t tO, float alpha) {
 #pragma unroll 1
-    for (int c = 0; c < HD; c += 32) {
-      uint32_t rr[32];
-      tmem_ld32(tO + static_cast<uint32_t>(c), rr);
-      tmem_ld_wait_regs(rr);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-      tmem_st32(tO + static_cast<uint32_t>(c), rr);
-    }
-  }
-  if (p_too) {
+  for (int c = 0; c < HD; c += 32) {
     uint32_t rr[32];
-    tmem_st_wait();  // the first half's P has been written
-    tmem_ld32(tS, rr);
+    tmem_ld32(tO + static_cast<uint32_t>(c), rr);
     tmem_ld_wait_regs(rr);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) rr[i] = pack_bf16x2(bf16_lo(rr[i]) * alpha, bf16_hi(rr[i]) * alpha);
-    tmem_st32(tS, rr);
+    for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+    tmem_st32(tO + static_cast<uint32_t>(c), rr);
   }
 }
 
@@ -198,11 +191,13 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* r_full = bars + 4;            // [SLOTS] TMA -> MMA
   uint64_t* r_empty = r_full + SLOTS;     // [SLOTS] MMA -> TMA
   uint64_t* s_full = r_empty + SLOTS;     // [2] MMA -> softmax t (scores of tile t)
-  uint64_t* p_full = s_full + 2;          // [2] softmax t -> MMA (P_t stored, O_t rescaled)
+  uint64_t* p_full = s_full + 2;          // [2] softmax t -> MMA (all of P_t stored)
   uint64_t* o_done = p_full + 2;          // [2] MMA -> softmax t (the unit's last P_t V complete)
   uint64_t* o_free = o_done + 2;          // [2] softmax t -> MMA (O_t read out)
   uint64_t* drain = o_free + 2;           // abort path only
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* p_half = drain + 1;           // [2] softmax t -> MMA (P_t of keys 0..63 stored, O_t rescaled)
+  uint64_t* o_half = p_half + 2;          // [2] MMA -> softmax t (P_t V of keys 0..63 complete)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_half + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -223,6 +218,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&q_free[t], 1);
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], 4);
+      mbar_init(&p_half[t], 4);
+      mbar_init(&o_half[t], 1);
       mbar_init(&o_done[t], 1);
       mbar_init(&o_free[t], 4);
     }
@@ -324,17 +321,18 @@ __global__ void __launch_bounds__(320, 1)
       }
       issued_any = true;
     };
-    // O_t (+)= P_t V: M = 128 queries, N = HD, K = 128 keys in 8 steps; P_t
-    // sits in TMEM (key pairs at the first 64 columns of tile t's scores), V
-    // is MN-major (rows = keys, 64 hd values a row, the next 64 hd values one
-    // panel further). A unit's first block overwrites O_t. The caller has
-    // waited for the V tile and P_t.
-    auto issue_pv = [&](int t, int item, bool first) {
+    // O_t (+)= P_t V over keys 64 h .. 64 h + 63: M = 128 queries, N = HD,
+    // K = 64 keys in 4 steps; P_t sits in TMEM (key pairs at the first 64
+    // columns of tile t's scores), V is MN-major (rows = keys, 64 hd values a
+    // row, the next 64 hd values one panel further). A unit's first block
+    // overwrites O_t. The caller has waited for the V tile and that half of
+    // P_t.
+    auto issue_pv = [&](int t, int item, bool first, int h) {
       const uint32_t tP = tmem_base + Cfg::TM_S + static_cast<uint32_t>(t * 128);
       const uint32_t tO = tmem_base + Cfg::TM_O + static_cast<uint32_t>(t * HD);
       const uint64_t vd = ring_mn + static_cast<uint64_t>(((item % SLOTS) * TILE) >> 4);
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 4 * h; k < 4 * h + 4; ++k)
         tc_mma_bf16_ts_warp(tO, tP + static_cast<uint32_t>(k * 8), vd + static_cast<uint64_t>((k * 16 * 128) >> 4),
                             idesc_o, (!first || k > 0) ? 1u : 0u);
       issued_any = true;
@@ -370,12 +368,17 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (!ok || jb >= wu.nkb[t]) continue;
-          ok = wait_all(&p_full[t], static_cast<uint32_t>(pg[t]) & 1u) &&
+          ok = wait_all(&p_half[t], static_cast<uint32_t>(pg[t]) & 1u) &&
                (jb > 0 || ua[t] == 0 || wait_all(&o_free[t], static_cast<uint32_t>(ua[t] - 1) & 1u));
+          if (!ok) continue;
+          tc_fence_after();
+          issue_pv(t, iv, jb == 0, 0);
+          tc_commit_warp(&o_half[t]);
+          ok = wait_all(&p_full[t], static_cast<uint32_t>(pg[t]) & 1u);
           if (!ok) continue;
           ++pg[t];
           tc_fence_after();
-          issue_pv(t, iv, jb == 0);
+          issue_pv(t, iv, jb == 0, 1);
           if (jb + 1 < wu.nkb[t]) {
             issue_s(t, ik);
             tc_commit_warp(&s_full[t]);
@@ -432,9 +435,9 @@ __global__ void __launch_bounds__(320, 1)
         // softmax: its scores from TMEM, its maximum, a move of the base if
         // needed, its exponentials packed to bf16 over the score columns the
         // first half has already consumed (P keys 0..63 at columns 0..31,
-        // keys 64..127 at 32..63). A base that moves in the second half
-        // (rarely: only on a jump above 2^8) rescales the first half's P as
-        // well as O and l.
+        // keys 64..127 at 32..63), then the half handed to the MMA. A base
+        // that moves in the second half (rarely: only on a jump above 2^8)
+        // rescales O, once the first half's P V has been added to it, and l.
         const bool masked = (a.causal && jb == qb) || jb * 128 + 128 > a.T;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -479,8 +482,14 @@ __global__ void __launch_bounds__(320, 1)
             m = m_cand;
             l *= alpha;
           }
-          if (__any_sync(0xffffffffu, moved && (jb > 0 || h > 0)))
-            at_rescale<HD>(tO, tS, alpha, jb > 0, h > 0);
+          if (__any_sync(0xffffffffu, moved && (jb > 0 || h > 0))) {
+            const bool go = h == 0 || __all_sync(0xffffffffu, mbar_wait(&o_half[t], static_cast<uint32_t>(sg) & 1u,
+                                                                         abort_flag));
+            if (go) {
+              tc_fence_after();
+              at_rescale<HD>(tO, alpha);
+            }
+          }
           // P = 2^(s * scale - m), two at a time; the half's row sum in pairs
           const uint64_t negm = f2_make(-m, -m);
           uint64_t acc[2] = {f2_make(0.0f, 0.0f), f2_make(0.0f, 0.0f)};
@@ -498,11 +507,11 @@ __global__ void __launch_bounds__(320, 1)
           f2_split(acc[0], s0, s1);
           f2_split(acc[1], s2, s3);
           l += (s0 + s1) + (s2 + s3);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(h == 0 ? &p_half[t] : &p_full[t]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[t]);
       }
       if (!ok) break;
       const bool done = mbar_wait(&o_done[t], static_cast<uint32_t>(ua) & 1u, abort_flag);
