@@ -695,8 +695,12 @@ int attention_launch_hd(const void* qkv, int64_t T, int tp, int hq, int hkv, int
   using Cfg = tpk::AttnCfg<HD>;
   const int nq = hq / tp, nkv = hkv >= tp ? hkv / tp : 1;
   const int64_t nqkv = static_cast<int64_t>(nq + 2 * nkv) * HD;
-  CUtensorMap m;
+  CUtensorMap m, mc;
   if (!make_map_bf16(&m, qkv, nqkv, T, tp, 128)) return TP_ERR_CUDA;
+  const uint64_t nc = static_cast<uint64_t>(nq) * HD;  // context columns of a shard
+  if (!make_store_map(&mc, ctx, false, nc, static_cast<uint64_t>(T), static_cast<uint64_t>(tp), nc * 2,
+                      nc * 2 * static_cast<uint64_t>(T)))
+    return TP_ERR_CUDA;
   tpk::AttnArgs a{};
   a.ctx = static_cast<bf16*>(ctx);
   a.T = static_cast<int>(T);
@@ -732,7 +736,7 @@ int attention_launch_hd(const void* qkv, int64_t T, int tp, int hq, int hkv, int
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!cuda_ok(cudaLaunchKernelEx(&cfg, tpk::tp_attn_kernel<HD>, m, a))) return TP_ERR_CUDA;
+  if (!cuda_ok(cudaLaunchKernelEx(&cfg, tpk::tp_attn_kernel<HD>, m, mc, a))) return TP_ERR_CUDA;
   return launch_status();
 }
 

@@ -102,10 +102,11 @@ struct AttnCfg {
   static constexpr int PANEL = ROWS * 128;          // 128 rows x 128 bytes (64 bf16 columns)
   static constexpr int PANELS = HD / 64;
   static constexpr int TILE = PANELS * PANEL;       // 128 x HD bf16
-  static constexpr int SLOTS = HD == 128 ? 5 : 8;   // K/V ring
+  static constexpr int SLOTS = HD == 128 ? 4 : 8;   // K/V ring
+  static constexpr int STAGE = 8 * 4096;            // output staging: 4 KB per softmax warp
   static constexpr int THREADS = 320;
   static constexpr int AUX = 512;                   // barriers, TMEM address, abort flag
-  static constexpr int SMEM = (2 + SLOTS) * TILE + AUX + 1024;  // Q tiles, ring, aux; alignment
+  static constexpr int SMEM = (2 + SLOTS) * TILE + STAGE + AUX + 1024;  // Q tiles, ring, staging, aux; alignment
   static constexpr uint32_t TM_S = 0;               // scores / P of tile t at column 128 t
   static constexpr uint32_t TM_O = 256;             // O of tile t at 256 + HD t
 };
@@ -177,7 +178,8 @@ __device__ __noinline__ void at_rescale(uint32_t tO, float alpha) {
 
 template <int HD>
 __global__ void __launch_bounds__(320, 1)
-    tp_attn_kernel(const __grid_constant__ CUtensorMap mapQKV, const AttnArgs a) {
+    tp_attn_kernel(const __grid_constant__ CUtensorMap mapQKV, const __grid_constant__ CUtensorMap mapCtx,
+                   const AttnArgs a) {
   using Cfg = AttnCfg<HD>;
   constexpr int SLOTS = Cfg::SLOTS, TILE = Cfg::TILE, PANEL = Cfg::PANEL;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -185,7 +187,8 @@ __global__ void __launch_bounds__(320, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;                // [2] Q tiles
   uint8_t* ring = smem + 2 * TILE;   // [SLOTS]: K(j) is item 2j, V(j) item 2j+1
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (2 + SLOTS) * TILE);
+  uint8_t* stage = ring + SLOTS * TILE;  // [8] a softmax warp's output staging buffer
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + Cfg::STAGE);
   uint64_t* q_full = bars;                // [2] TMA -> MMA (a unit's Q tile t landed)
   uint64_t* q_free = bars + 2;            // [2] MMA -> TMA (the unit's last S_t is computed: Q_t tile free)
   uint64_t* r_full = bars + 4;            // [SLOTS] TMA -> MMA
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(320, 1)
   // the 1024-byte alignment of the tiles must leave room for the barriers (a
   // dynamic shared-memory base is 1024-aligned in practice; otherwise the
   // block reports an error instead of overrunning)
-  if ((smem - smem_raw) + (2 + SLOTS) * TILE + Cfg::AUX > Cfg::SMEM) {
+  if ((smem - smem_raw) + (2 + SLOTS) * TILE + Cfg::STAGE + Cfg::AUX > Cfg::SMEM) {
     if (threadIdx.x == 0) atomicCAS(&g_tp_error, TP_DEVERR_NONE, TP_DEVERR_LAYOUT);
     return;
   }
@@ -409,7 +412,6 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tS = tmem_base + Cfg::TM_S + static_cast<uint32_t>(t * 128) + lane_off;
     const uint32_t tO = tmem_base + Cfg::TM_O + static_cast<uint32_t>(t * HD) + lane_off;
     const uint64_t scale2 = f2_make(a.scale_log2, a.scale_log2);
-    const int nc = a.nq * HD;
     bool ok = true;
     int ua = 0, sg = 0;  // units with this tile, score blocks consumed
     for (int w = 0; ok; ++w) {
@@ -522,20 +524,33 @@ __global__ void __launch_bounds__(320, 1)
       ++ua;
       tc_fence_after();
       const float inv = 1.0f / l;
-      __nv_bfloat16* out = a.ctx + (static_cast<size_t>(wu.s) * a.T + tq) * nc + jq * HD;
+      // 64 columns at a time: the warp's 32 rows of O / l as bf16 into its
+      // staging buffer (128-byte-swizzled rows), then one bulk tensor store of
+      // the 32 x 64 box (rows past the sequence are clipped by the copy
+      // engine; a box wholly past it is not issued)
+      const int row0 = qb * 128 + q * 32;
+      uint8_t* sb = stage + (warp - 2) * 4096;
 #pragma unroll 1
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t rr[32];
-        tmem_ld32(tO + static_cast<uint32_t>(c), rr);
-        tmem_ld_wait_regs(rr);
-        if (tq < a.T) {
+      for (int c = 0; c < HD; c += 64) {
+        if (lane == 0) tma_store_wait_read<0>();  // the buffer's last store has read it
+        __syncwarp();
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t rr[32];
+          tmem_ld32(tO + static_cast<uint32_t>(c + 32 * hh), rr);
+          tmem_ld_wait_regs(rr);
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             float v[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(rr[i + e]) * inv;
-            store_bf16x8_f(out + c + i, v);
+            stage_put(sb, lane, 4 * hh + (i >> 3), pack_bf16x8(v));
           }
+        }
+        stage_ready();
+        if (lane == 0 && row0 < a.T) {
+          tma_store_3d(&mapCtx, sb, jq * HD + c, row0, wu.s);
+          tma_store_commit();
         }
       }
       // O_t is read out (each load waited for): the next unit's first P_t V
@@ -544,6 +559,8 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[t]);
     }
+    if (lane == 0) tma_store_wait_all();  // the context is written before the block exits
+    __syncwarp();
   }
 
   tc_fence_before();
