@@ -28,15 +28,19 @@
 //               P_1 V, S_1(next), each P_t V in two halves of 64 keys:
 //               the first as soon as the softmax has stored P_t for them;
 //   warps 2..5  softmax of tile 0, warps 6..9 of tile 1, one thread per
-//               query row: the row's 128 scores from TMEM, the row maximum,
-//               exp2 with the log2(e)/sqrt(hd) scale folded into one paired
+//               query row: the row's 128 scores from TMEM, exp2 with the
+//               log2(e)/sqrt(hd) scale and the base folded into one paired
 //               FMA, the row sum, P packed to bf16 and stored over the
 //               scores, handed over a half at a time (the first half's P V
 //               runs while the second half's exponentials are computed);
 //               at the end of a unit O / l to the context.
-// The exponent base m only moves when a row's maximum exceeds it by more
-// than 2^8 (P then stays below 256, exact enough in bf16), so O and l are
-// rescaled only on such jumps. S_t(j) is issued after P_t(j-1) V, and a
+// The exponent base m is any value that keeps P from overflowing: the
+// softmax is the same for every m, and P's bf16 rounding is relative at any
+// magnitude. It is set to the row maximum of a unit's first 64 keys; after
+// that no maximum is taken: each half-block's P is computed with the current
+// m, and only when the half's row sum exceeds 2^16 (some P above 2^16, or
+// an overflow) is its maximum taken, m moved there, the half's P computed
+// again and O and l rescaled. S_t(j) is issued after P_t(j-1) V, and a
 // commit arrives once every earlier MMA of the issuer is complete, so the
 // scores of block j reaching the softmax mean that O_t holds blocks
 // 0..j-1 and no MMA writes it: a move in a block's first half needs no
@@ -110,7 +114,7 @@ struct AttnCfg {
   static constexpr uint32_t TM_S = 0;               // scores / P of tile t at column 128 t
   static constexpr uint32_t TM_O = 256;             // O of tile t at 256 + HD t
 };
-constexpr float AT_RESCALE_LOG2 = 8.0f;  // move the exponent base only on a jump above 2^8
+constexpr float AT_SUM_LIMIT = 65536.0f;  // a half-block's row sum of P above this moves the base
 
 // The w-th unit of CTA c in a grid of g CTAs, or -1 past its last one.
 // Units are numbered longest first; wave w covers units w*g .. w*g + g - 1,
@@ -438,8 +442,9 @@ __global__ void __launch_bounds__(320, 1)
         // needed, its exponentials packed to bf16 over the score columns the
         // first half has already consumed (P keys 0..63 at columns 0..31,
         // keys 64..127 at 32..63), then the half handed to the MMA. A base
-        // that moves in the second half (rarely: only on a jump above 2^8)
-        // rescales O, once the first half's P V has been added to it, and l.
+        // that moves in the second half (rarely: only when the half's P sum
+        // exceeds 2^16) rescales O, once the first half's P V has been added
+        // to it, and l.
         const bool masked = (a.causal && jb == qb) || jb * 128 + 128 > a.T;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -463,52 +468,69 @@ __global__ void __launch_bounds__(320, 1)
             for (int i = 0; i < 64; ++i)
               if (kb + i > kmax) sv[i] = -INFINITY;
           }
-          float mx4[4];
+          // the half's maximum of the scaled scores (-inf if no key is visible)
+          auto half_max = [&]() -> float {
+            float mx4[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) mx4[i] = sv[i];
+            for (int i = 0; i < 4; ++i) mx4[i] = sv[i];
 #pragma unroll
-          for (int i = 4; i < 64; i += 8) {
-            mx4[0] = fmax3(mx4[0], sv[i], sv[i + 1]);
-            mx4[1] = fmax3(mx4[1], sv[i + 2], sv[i + 3]);
-            mx4[2] = fmax3(mx4[2], sv[i + 4], sv[i + 5]);
-            mx4[3] = fmax3(mx4[3], sv[i + 6], sv[i + 7]);
+            for (int i = 4; i < 64; i += 8) {
+              mx4[0] = fmax3(mx4[0], sv[i], sv[i + 1]);
+              mx4[1] = fmax3(mx4[1], sv[i + 2], sv[i + 3]);
+              mx4[2] = fmax3(mx4[2], sv[i + 4], sv[i + 5]);
+              mx4[3] = fmax3(mx4[3], sv[i + 6], sv[i + 7]);
+            }
+            return fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * a.scale_log2;  // (the scale is positive)
+          };
+          // P = 2^(s * scale - m), two at a time, packed; the half's row sum
+          uint32_t pk[32];
+          auto half_exp = [&]() -> float {
+            const uint64_t negm = f2_make(-m, -m);
+            uint64_t acc[2] = {f2_make(0.0f, 0.0f), f2_make(0.0f, 0.0f)};
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float x0, x1;
+              f2_split(f2_fma(f2_make(sv[2 * i], sv[2 * i + 1]), scale2, negm), x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              acc[i & 1] = f2_add(acc[i & 1], f2_make(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            float s0, s1, s2, s3;
+            f2_split(acc[0], s0, s1);
+            f2_split(acc[1], s2, s3);
+            return (s0 + s1) + (s2 + s3);
+          };
+          const bool unit_first = jb == 0 && h == 0;
+          if (unit_first) {  // key 0 is visible to every row, so the maximum is finite
+            const float mx = half_max();
+            m = mx > -INFINITY ? mx : 0.0f;
           }
-          const float m_cand = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * a.scale_log2;
-          // (the scale is positive: the same order; a half with no visible key
-          // gives -inf and moves nothing)
-          float alpha = 1.0f;
-          bool moved = false;
-          if (m_cand > m + AT_RESCALE_LOG2) {  // also the block's first half on a unit's first block
-            alpha = ex2_approx(m - m_cand);    // 0 while m = -inf
-            moved = true;
-            m = m_cand;
-            l *= alpha;
-          }
-          if (__any_sync(0xffffffffu, moved && (jb > 0 || h > 0))) {
-            const bool go = h == 0 || __all_sync(0xffffffffu, mbar_wait(&o_half[t], static_cast<uint32_t>(sg) & 1u,
-                                                                         abort_flag));
-            if (go) {
-              tc_fence_after();
-              at_rescale<HD>(tO, alpha);
+          float lh = half_exp();
+          if (!unit_first) {
+            const bool big = !(lh <= AT_SUM_LIMIT);  // (also an overflow to inf)
+            if (__any_sync(0xffffffffu, big)) {
+              // rare: move the base to the half's maximum (above m: some P
+              // exceeded 1), recompute the half, rescale O and l (rows whose
+              // base stayed use alpha = 1). O holds the blocks before this one
+              // (and, in the second half, the first half's P V once done).
+              float alpha = 1.0f;
+              if (big) {
+                const float mx = half_max();
+                alpha = ex2_approx(m - mx);
+                m = mx;
+                l *= alpha;
+                lh = half_exp();
+              }
+              const bool go = h == 0 || __all_sync(0xffffffffu, mbar_wait(&o_half[t], static_cast<uint32_t>(sg) & 1u,
+                                                                           abort_flag));
+              if (go) {
+                tc_fence_after();
+                at_rescale<HD>(tO, alpha);
+              }
             }
           }
-          // P = 2^(s * scale - m), two at a time; the half's row sum in pairs
-          const uint64_t negm = f2_make(-m, -m);
-          uint64_t acc[2] = {f2_make(0.0f, 0.0f), f2_make(0.0f, 0.0f)};
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float x0, x1;
-            f2_split(f2_fma(f2_make(sv[2 * i], sv[2 * i + 1]), scale2, negm), x0, x1);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            acc[i & 1] = f2_add(acc[i & 1], f2_make(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
-          }
           tmem_st32(tS + static_cast<uint32_t>(h * 32), pk);
-          float s0, s1, s2, s3;
-          f2_split(acc[0], s0, s1);
-          f2_split(acc[1], s2, s3);
-          l += (s0 + s1) + (s2 + s3);
+          l += lh;
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();

@@ -101,10 +101,10 @@ def test_attention_core(tp, T, hq, hkv, hd, causal):
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("hq,hkv,hd", [(2, 1, 128), (1, 1, 128), (2, 1, 64), (1, 1, 64)])
 def test_attention_growing_keys_move_the_exponent_base(causal, hq, hkv, hd):
-    """Key rows scaled by 1 + t/40, so that the scores of later key blocks
-    exceed the running base by more than 2^8 and O is rescaled in TMEM
-    (T = 700: six blocks, the last ragged), in units of two heads and in
-    units of two query blocks."""
+    """Key rows scaled by 1 + t/40, so that the exponentials of later key
+    blocks, taken with the running base, sum above 2^16 and the base moves,
+    with O rescaled in TMEM (T = 700: six blocks, the last ragged), in units
+    of two heads and in units of two query blocks."""
     tp, T = 1, 700
     qkv = qkv_input(341, tp, T, hq, hkv, hd)
     k0 = hq * hd
@@ -113,6 +113,24 @@ def test_attention_growing_keys_move_the_exponent_base(causal, hq, hkv, hd):
     ctx = tpl.tp_attention(dev(qkv), hq, hkv, hd, causal=causal)
     assert tpl.tp_get_error() == 0
     assert_within(ctx, *oracle_ctx_bound(qkv, hq, hkv, hd, causal), f"growing keys hq={hq} hd={hd} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("hq,hkv,hd", [(2, 1, 128), (1, 1, 128), (2, 1, 64)])
+def test_attention_outlier_keys_move_the_exponent_base(causal, hq, hkv, hd):
+    """Single keys scaled by 40 in the second half of the first block (key
+    100: the base moves while O holds only the first half's P V), in a first
+    half (key 300) and in a second half later on (key 500): every row that
+    sees one takes the slow path there, the others keep their base."""
+    tp, T = 1, 600
+    qkv = qkv_input(361, tp, T, hq, hkv, hd)
+    k0 = hq * hd
+    for key in (100, 300, 500):
+        qkv[:, key, k0:k0 + hd] *= 40.0
+    S.to_bf16_inplace(qkv)
+    ctx = tpl.tp_attention(dev(qkv), hq, hkv, hd, causal=causal)
+    assert tpl.tp_get_error() == 0
+    assert_within(ctx, *oracle_ctx_bound(qkv, hq, hkv, hd, causal), f"outlier keys hq={hq} hd={hd} causal={causal}")
 
 
 @pytest.mark.parametrize("hd", [64, 128])
