@@ -449,8 +449,9 @@ int col_bf16(const void* X, int64_t T, const tp_shards* W, const tp_shards* Wu, 
     ok = W->hd % 64 == 0 && make_store_map(&om.c, ctx, false, nc, T, tp, nc * es, T * nc * es);
   }
   a.tma_store = ok ? 1 : 0;
-  return swiglu ? gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mw, mu, om, a, sc, st)
-                : gemm_launch<tpk::GK_COL, false>(mx, mx, mw, mu, om, a, sc, st);
+  if (swiglu) return gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mw, mu, om, a, sc, st);
+  return ce_stats ? gemm_launch<tpk::GK_COL_CE, false>(mx, mx, mw, mu, om, a, sc, st)
+                  : gemm_launch<tpk::GK_COL, false>(mx, mx, mw, mu, om, a, sc, st);
 }
 
 // Row-parallel bf16 GEMM: fused shard sum (partials_out == nullptr) or

@@ -84,7 +84,10 @@
 
 namespace tpk {
 
-enum GemmKind : int { GK_COL = 0, GK_COL_SWIGLU = 1, GK_ROW_SUM = 2, GK_ROW_PARTIAL = 3 };
+// GK_COL_CE: GK_COL whose epilogue also reduces each token row to cross-
+// entropy statistics (GemmArgs::ce_stats); an instance of its own, so that
+// the plain column GEMM's epilogue carries none of that code.
+enum GemmKind : int { GK_COL = 0, GK_COL_SWIGLU = 1, GK_ROW_SUM = 2, GK_ROW_PARTIAL = 3, GK_COL_CE = 4 };
 
 
 template <int KIND_, bool SWAP_, bool PAIR_ = false>
@@ -93,7 +96,7 @@ struct GemmCfg {
   static constexpr bool SWAP = SWAP_;
   static constexpr bool PAIR = PAIR_;  // normal mode only: 2-SM MMA over a CTA pair
   static constexpr bool SWIGLU = KIND_ == GK_COL_SWIGLU;
-  static constexpr bool IS_COL = KIND_ == GK_COL || KIND_ == GK_COL_SWIGLU;
+  static constexpr bool IS_COL = KIND_ == GK_COL || KIND_ == GK_COL_SWIGLU || KIND_ == GK_COL_CE;
   static constexpr int NACC = (SWAP_ && SWIGLU) ? 2 : 1;  // A tiles per stage in swap mode
   static constexpr int BM = 128;
   static constexpr int BK = 64;
@@ -154,7 +157,7 @@ struct GemmArgs {
   // ROW_SUM: the K loop also runs over a second (A, B) pair (mapA1, mapB1),
   // so that out = sum_s A_s B_s^T + sum_s A'_s B'_s^T in one accumulator
   int two_src;
-  // COL without activation on a vocabulary-split LM head: the epilogue also
+  // GK_COL_CE (no activation, a vocabulary-split LM head): the epilogue also
   // reduces each token row of the tile to cross-entropy statistics of its
   // logits (taken from the fp32 accumulator), ce_stats[((s * M + t) * n_tiles
   // + n) * 3 + {0, 1, 2}] = {max, sum exp(z - max), the label's logit where
@@ -515,7 +518,7 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
         a.bias ? static_cast<const __nv_bfloat16*>(a.bias) + static_cast<size_t>(s) * a.Ns : nullptr;
     const __nv_bfloat16* bias_up = a.bias_up ? a.bias_up + static_cast<size_t>(s) * a.Ns : nullptr;
     const bool with_ctx = !Cfg::SWIGLU && a.ctx != nullptr;
-    const bool with_ce = !Cfg::SWIGLU && a.ce_stats != nullptr;
+    const bool with_ce = Cfg::KIND == GK_COL_CE && a.ce_stats != nullptr;
     CeAcc ce{-INFINITY, 0.0f, 0.0f};
     const int ce_loc = (with_ce && row_ok) ? __ldg(a.ce_labels + row) - s * a.Ns : -1;  // the label's shard column
 #pragma unroll 1
@@ -891,6 +894,8 @@ __global__ void __launch_bounds__(192, 1)
         int m, n = 0, s;
         if constexpr (SWAP) decode_tile_swap(args, sg.tile, m, s);
         else decode_tile_normal(args, sg.tile, rank, m, n, s);
+        // grouped experts: the tile's expert selects its shard set
+        const int wks = args.unit_expert ? __ldg(args.unit_expert + sg.tile % args.m_tiles) * args.tp : 0;
         for (int kb_i = sg.kb0; kb_i < sg.kb1; ++kb_i) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
@@ -918,8 +923,6 @@ __global__ void __launch_bounds__(192, 1)
               if (rank == 0) mbar_arrive_expect_tx(&full[stage], stage_tx);
               const uint32_t fb = mapa_shared(&full[stage], 0);
               const int a_s = Cfg::IS_COL ? (args.a_sharded ? s : 0) : ks;
-              // grouped experts: the tile's expert selects its shard set
-              const int wks = args.unit_expert ? __ldg(args.unit_expert + sg.tile % args.m_tiles) * args.tp : 0;
               const int b_s = (args.a_sharded ? 0 : ks) + wks;
               const CUtensorMap* ma = src1 ? &mapA1 : &mapA0;
               if constexpr (MN & 1) {  // [K][M]: M columns m*128 .. +127 as two panels
