@@ -166,11 +166,34 @@ struct GemmArgs {
   float* ce_stats;
   // Grouped experts (CTA pairs, whole tiles only): the token rows are the
   // experts' routed tokens, each expert's segment padded to 256-row units;
-  // unit_expert[u] is the expert of unit u (tile % m_tiles), or -1 for an
+  // unit_expert[u] is the expert of unit u (see tile_unit_pair), or -1 for an
   // unused unit, which every warp role skips. The weight maps hold the
   // experts' shard sets one after another: shard coordinate e * tp + s.
   const int* unit_expert;
+  // Grouped experts: the tile order takes the (column block, shard) pairs in
+  // groups of unit_group, every unit per group with the group's pairs
+  // fastest, so that a unit's permuted tokens serve unit_group tiles while
+  // they are in L2 and no more than that many tiles read them at once
+  // (0: units fastest over all pairs).
+  int unit_group;
 };
+
+// normal mode: the tile's unit (token-block unit, before the cluster rank)
+// and its (column block, shard) pair index, in the tile order above
+__device__ __forceinline__ void tile_unit_pair(const GemmArgs& a, int tile, int& mu, int& pr) {
+  if (a.unit_group > 0 && tile < a.r1_tiles) {
+    const int P = a.r1_tiles / a.m_tiles;               // pairs per unit
+    const int g = tile / (a.m_tiles * a.unit_group);
+    const int base = g * a.unit_group;
+    const int gl = min(a.unit_group, P - base);         // the last group may be partial
+    const int rem = tile - g * a.m_tiles * a.unit_group;
+    mu = rem / gl;
+    pr = base + rem % gl;
+  } else {
+    mu = tile % a.m_tiles;
+    pr = tile / a.m_tiles;
+  }
+}
 
 // ---------------------------------------------------------------------------
 // Schedule helpers (identical in every role, so all roles see one sequence)
@@ -201,7 +224,11 @@ struct SegIter {
     while (dp_next < a.dp_tiles) {
       const int t = dp_next;
       dp_next += gridDim.x / a.cluster;
-      if (a.unit_expert && __ldg(a.unit_expert + t % a.m_tiles) < 0) continue;  // an unused expert unit
+      if (a.unit_expert) {  // an unused expert unit
+        int mu, pr;
+        tile_unit_pair(a, t, mu, pr);
+        if (__ldg(a.unit_expert + mu) < 0) continue;
+      }
       s.tile = t;
       s.kb0 = 0;
       s.kb1 = a.kpt;
@@ -235,8 +262,8 @@ __device__ __forceinline__ void decode_tile_normal(const GemmArgs& a, int tile, 
                                                    int& s) {
   if (tile < a.r1_tiles) {
     const int nq = a.rep > 1 ? a.n_q_tiles : a.n_tiles;
-    m = tile % a.m_tiles;
-    const int r = tile / a.m_tiles;
+    int r;
+    tile_unit_pair(a, tile, m, r);
     n = r % nq;
     s = r / nq;
   } else {
@@ -895,7 +922,12 @@ __global__ void __launch_bounds__(192, 1)
         if constexpr (SWAP) decode_tile_swap(args, sg.tile, m, s);
         else decode_tile_normal(args, sg.tile, rank, m, n, s);
         // grouped experts: the tile's expert selects its shard set
-        const int wks = args.unit_expert ? __ldg(args.unit_expert + sg.tile % args.m_tiles) * args.tp : 0;
+        int wks = 0;
+        if (args.unit_expert) {
+          int mu, pr;
+          tile_unit_pair(args, sg.tile, mu, pr);
+          wks = __ldg(args.unit_expert + mu) * args.tp;
+        }
         for (int kb_i = sg.kb0; kb_i < sg.kb1; ++kb_i) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
