@@ -1776,7 +1776,7 @@ tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float
     a.num_tiles = a.m_tiles * a.n_tiles * tp;
     a.r1_tiles = a.num_tiles;
     a.unit_expert = unit_expert;
-    a.unit_group = 8;
+    a.unit_group = 16;
     OutMaps om{};
     a.tma_store = make_store_map(&om.y, Hs, false, Is, L.rows, tp, Is * 2, L.rows * Is * 2) ? 1 : 0;
     if ((r = gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mg, mu, om, a, nullptr, st))) return as_status(r);
@@ -1801,7 +1801,7 @@ tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.r1_tiles = a.num_tiles;
     a.unit_expert = unit_expert;
-    a.unit_group = 8;
+    a.unit_group = 16;
     OutMaps om{};
     a.tma_store = make_store_map(&om.y, Yp, true, H, L.rows, 1, H * 4, L.rows * H * 4) ? 1 : 0;
     if ((r = gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, om, a, nullptr, st))) return as_status(r);
