@@ -39,10 +39,14 @@ def oracle(X, ex, ids, w, tp, R=None):
 
 
 @pytest.mark.parametrize("tp,T,H,I,E,k", [(2, 300, 256, 512, 4, 2), (8, 129, 384, 1408, 8, 2),
-                                          (4, 64, 256, 1024, 3, 1), (1, 1, 256, 512, 2, 2), (2, 200, 256, 768, 6, 3)])
+                                          (4, 64, 256, 1024, 3, 1), (1, 1, 256, 512, 2, 2), (2, 200, 256, 768, 6, 3),
+                                          (2, 260, 4352, 5120, 4, 2)])
 def test_moe_block(tp, T, H, I, E, k):
     """Ragged tails: H = 384 (a 128-column last block of the down GEMM),
-    I/tp = 176; a single token; top-1 and top-3."""
+    I/tp = 176; a single token; top-1 and top-3. The last case has 40
+    (column block, shard) pairs per unit in the gate/up GEMM and 17 column
+    blocks in the down GEMM, so the grouped tile order runs full groups of
+    16 and a partial last group."""
     X = S.normal(601, (T, H))
     ex = S.moe_experts(E, H, I, seed=602, std=0.05)
     ids, w = S.moe_routing(603, T, E, k)
