@@ -1680,7 +1680,7 @@ namespace {
 
 struct MoeLayout {
   int64_t units, rows;  // 256-row units of the permuted buffers, and their rows
-  size_t xp, hs, yp, pos, inv, counts, off, unit_expert, total;
+  size_t xp, hs, yp, pos, inv, counts, off, unit_expert, unit_seg, total;
 };
 
 MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int k, int E) {
@@ -1701,6 +1701,7 @@ MoeLayout moe_layout(int64_t T, int64_t H, int64_t I, int k, int E) {
   L.counts = take(static_cast<size_t>(E) * 4);
   L.off = take(static_cast<size_t>(E) * 4);
   L.unit_expert = take(static_cast<size_t>(L.units) * 4);
+  L.unit_seg = take(static_cast<size_t>(L.units) * 8);
   L.total = o;
   return L;
 }
@@ -1742,12 +1743,13 @@ tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float
   int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
   int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
   int32_t* unit_expert = reinterpret_cast<int32_t*>(ws + L.unit_expert);
+  int2* unit_seg = reinterpret_cast<int2*>(ws + L.unit_seg);
   const int64_t n = T * k;
   const int64_t grid_cap = static_cast<int64_t>(std::max(1, num_sms())) * 16;
   // 1. dispatch
   tpk::moe_route_kernel<<<E, 1024, 0, st>>>(ids, n, E, pos, counts);
   if ((r = launch_status())) return as_status(r);
-  tpk::moe_units_kernel<<<1, 256, 0, st>>>(counts, E, static_cast<int>(L.units), off, unit_expert);
+  tpk::moe_units_kernel<<<1, 256, 0, st>>>(counts, E, static_cast<int>(L.units), off, unit_expert, unit_seg);
   if ((r = launch_status())) return as_status(r);
   tpk::moe_gather_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(n, 8), grid_cap)), 256, 0, st>>>(
       static_cast<const bf16*>(X), ids, pos, off, n, k, E, H, Xp, inv);
@@ -1777,6 +1779,7 @@ tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float
     a.r1_tiles = a.num_tiles;
     a.unit_expert = unit_expert;
     a.unit_group = 16;
+    a.unit_seg = unit_seg;
     OutMaps om{};
     a.tma_store = make_store_map(&om.y, Hs, false, Is, L.rows, tp, Is * 2, L.rows * Is * 2) ? 1 : 0;
     if ((r = gemm_launch<tpk::GK_COL_SWIGLU, false>(mx, mx, mg, mu, om, a, nullptr, st))) return as_status(r);
@@ -1802,6 +1805,7 @@ tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float
     a.r1_tiles = a.num_tiles;
     a.unit_expert = unit_expert;
     a.unit_group = 16;
+    a.unit_seg = unit_seg;
     OutMaps om{};
     a.tma_store = make_store_map(&om.y, Yp, true, H, L.rows, 1, H * 4, L.rows * H * 4) ? 1 : 0;
     if ((r = gemm_launch<tpk::GK_ROW_SUM, false>(mx, mx, mw, mw, om, a, nullptr, st))) return as_status(r);

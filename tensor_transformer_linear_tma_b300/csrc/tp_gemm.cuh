@@ -176,6 +176,12 @@ struct GemmArgs {
   // they are in L2 and no more than that many tiles read them at once
   // (0: units fastest over all pairs).
   int unit_group;
+  // Grouped experts: unit_seg[u] = {first unit, units} of the segment that
+  // holds unit u (an expert's units; an unused unit is a segment of its
+  // own). With it the grouped order runs segment by segment (every group of
+  // one expert before the next expert), so an expert's tokens stay in L2
+  // across its groups. Null: one segment of all units.
+  const int2* unit_seg;
 };
 
 // normal mode: the tile's unit (token-block unit, before the cluster rank)
@@ -183,12 +189,21 @@ struct GemmArgs {
 __device__ __forceinline__ void tile_unit_pair(const GemmArgs& a, int tile, int& mu, int& pr) {
   if (a.unit_group > 0 && tile < a.r1_tiles) {
     const int P = a.r1_tiles / a.m_tiles;               // pairs per unit
-    const int g = tile / (a.m_tiles * a.unit_group);
+    // a segment of units u0 .. u0 + nu - 1 owns tiles u0 * P .. (u0 + nu) * P - 1,
+    // so the unit tile / P lies in the tile's own segment
+    int u0 = 0, nu = a.m_tiles;
+    if (a.unit_seg) {
+      const int2 sg = __ldg(a.unit_seg + tile / P);
+      u0 = sg.x;
+      nu = sg.y;
+    }
+    const int rem = tile - u0 * P;
+    const int g = rem / (nu * a.unit_group);
     const int base = g * a.unit_group;
     const int gl = min(a.unit_group, P - base);         // the last group may be partial
-    const int rem = tile - g * a.m_tiles * a.unit_group;
-    mu = rem / gl;
-    pr = base + rem % gl;
+    const int r2 = rem - g * nu * a.unit_group;
+    mu = u0 + r2 / gl;
+    pr = base + r2 % gl;
   } else {
     mu = tile % a.m_tiles;
     pr = tile / a.m_tiles;

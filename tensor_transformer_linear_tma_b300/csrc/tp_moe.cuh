@@ -58,10 +58,12 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const int32_t* __restri
   if (threadIdx.x == 0) counts[e] = base;
 }
 
-// 1b. One CTA: segment offsets (each count padded to a multiple of 256) and
-// the unit -> expert table for n_units units. E <= 1024.
+// 1b. One CTA: segment offsets (each count padded to a multiple of 256), the
+// unit -> expert table for n_units units (-1 past the last segment) and each
+// unit's segment {first unit, units} (an unused unit: itself alone), which
+// orders the grouped GEMMs' tiles. E <= 1024.
 __global__ void moe_units_kernel(const int32_t* __restrict__ counts, int E, int n_units, int32_t* __restrict__ off,
-                                 int32_t* __restrict__ unit_expert) {
+                                 int32_t* __restrict__ unit_expert, int2* __restrict__ unit_seg) {
   __shared__ int s_off[1025];
   if (threadIdx.x == 0) {
     int acc = 0;
@@ -79,6 +81,7 @@ __global__ void moe_units_kernel(const int32_t* __restrict__ counts, int E, int 
     for (int e = 0; e < E; ++e)
       if (row >= s_off[e] && row < s_off[e + 1]) ex = e;
     unit_expert[u] = ex;
+    unit_seg[u] = ex >= 0 ? make_int2(s_off[ex] / MOE_UNIT, (s_off[ex + 1] - s_off[ex]) / MOE_UNIT) : make_int2(u, 1);
   }
 }
 
