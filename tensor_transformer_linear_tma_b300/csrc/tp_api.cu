@@ -1804,7 +1804,10 @@ tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float
     a.num_tiles = a.m_tiles * a.n_tiles;
     a.r1_tiles = a.num_tiles;
     a.unit_expert = unit_expert;
-    a.unit_group = 16;
+    // one column block at a time, the expert's units fastest: the few
+    // units that read a weight block do so side by side (the 16 blocks in one
+    // group spread them over two rounds, and the second read missed L2)
+    a.unit_group = 1;
     a.unit_seg = unit_seg;
     OutMaps om{};
     a.tma_store = make_store_map(&om.y, Yp, true, H, L.rows, 1, H * 4, L.rows * H * 4) ? 1 : 0;
