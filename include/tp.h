@@ -373,9 +373,14 @@ size_t tp_mlp_backward_workspace_bytes(int64_t T, int64_t H, int64_t I, int tp, 
  *   NULL. Any of dX, dW1, dW_up, dW2 may be NULL to skip it (dW_up must be
  *   NULL unless SwiGLU).
  *   workspace: >= tp_mlp_backward_workspace_bytes(T, H, I, tp, act, dtype) bytes,
- *   256-byte aligned: dHs, dG and dU (bf16 [tp][T][I/tp]) plus the
- *   split-tile scratch. Contents on return are unspecified.
- * Errors: as tp_column_linear_backward, plus TP_ERR_MODE for an unknown act.
+ *   256-byte aligned: dHs, dG and dU (T * I elements each) plus the
+ *   split-tile scratch. Contents on return are unspecified. (On the bf16
+ *   path dG and dU are kept token-major, [T][I] with the shards side by
+ *   side, so that dX is one contraction over I and dW1, dW_up one [I][H]
+ *   product each: the same sums, with no tile cut at a shard's end.)
+ * Errors: as tp_column_linear_backward, plus TP_ERR_MODE for an unknown act
+ *   and, on the bf16 path, TP_ERR_ALIGN if I/tp is not a multiple of 8 and
+ *   TP_ERR_UNSUPPORTED if T * I/tp >= 2^34.
  */
 tp_status tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const tp_shards* W_up,
                           const tp_shards* W2, int act, const void* G, const void* U, const void* Hs,

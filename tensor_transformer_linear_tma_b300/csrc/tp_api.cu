@@ -1350,8 +1350,11 @@ int col_bwd_bf16(const void* X, int64_t T, const tp_shards* W, const void* dYs, 
   return r;
 }
 
+// tok_rows > 0 (bf16 only): dG and dU token-major [tok_rows][tp * Is] (see
+// act_backward_kernel; Is % 8 == 0, tok_rows * Is / 8 < 2^31 and tp < 2^16,
+// checked by the caller).
 int act_bwd_launch(const void* dH, const void* G, const void* U, int64_t n, int act, void* dG, void* dU,
-                   cudaStream_t st, int dtype = TP_BF16) {
+                   cudaStream_t st, int dtype = TP_BF16, int64_t tok_rows = 0, int tp = 1, int64_t Is = 0) {
   if (dtype == TP_F32) {
     if (n == 0) return TP_OK;
     tpk::act_backward_f32_kernel<<<grid_for(n, 256), 256, 0, st>>>(
@@ -1361,6 +1364,19 @@ int act_bwd_launch(const void* dH, const void* G, const void* U, int64_t n, int 
   }
   const int64_t n8 = n / 8;
   if (n8 == 0) return TP_OK;
+  if (tok_rows > 0) {  // a grid row per shard; T * Is / 8 vectors each
+    const uint32_t d = static_cast<uint32_t>(Is / 8);
+    int shift = 0;
+    while ((1ull << shift) < d) ++shift;
+    const uint32_t magic = static_cast<uint32_t>((1ull << (32 + shift)) / d - (1ull << 32) + 1);
+    const int64_t per = tok_rows * d;
+    const dim3 grid(static_cast<unsigned>(std::max(1, std::min<int>(grid_for(per, 256), grid_for(n8, 256) / tp))),
+                    static_cast<unsigned>(tp));
+    tpk::act_backward_kernel<<<grid, 256, 0, st>>>(
+        static_cast<const bf16*>(dH), static_cast<const bf16*>(G), static_cast<const bf16*>(U), per, act,
+        static_cast<bf16*>(dG), static_cast<bf16*>(dU), d, magic, shift, tp);
+    return launch_status();
+  }
   tpk::act_backward_kernel<<<grid_for(n8, 256), 256, 0, st>>>(
       static_cast<const bf16*>(dH), static_cast<const bf16*>(G), static_cast<const bf16*>(U), n8, act,
       static_cast<bf16*>(dG), static_cast<bf16*>(dU));
@@ -1463,23 +1479,38 @@ tp_status tp_mlp_backward(const void* X, int64_t T, const tp_shards* W1, const t
   void* dHs = ws;
   void* dG = ws + inter;
   void* dU = gated ? ws + 2 * inter : nullptr;
-  const Scratch sc = carve_scratch(workspace, (gated ? 3 : 2) * inter, bwd_max_tiles(H, I, tp));
-  // row layer (every shard gets dY): dHs and dW2; then the local activation
-  if ((r = row_bwd_bf16(Hs, T, W2, dY, dHs, dW2, &sc, st))) return as_status(r);
-  if ((r = act_bwd_launch(dHs, G, U, static_cast<int64_t>(T) * I, act, dG, dU, st))) return as_status(r);
-  // column layer(s): the input gradient is the sum over shards, and over
-  // gate and up for SwiGLU (one accumulator), plus dR
-  if (!gated) return as_status(col_bwd_bf16(X, T, W1, dG, dR, dX, dW1, &sc, st));
   const int64_t Is = I / tp;
+  if (Is % 8 != 0) return TP_ERR_ALIGN;  // (16-byte rows, as every tensor map here needs)
+  if (static_cast<int64_t>(T) * (Is / 8) > INT32_MAX || tp > 65535) return TP_ERR_UNSUPPORTED;
+  const Scratch sc = carve_scratch(workspace, (gated ? 3 : 2) * inter, bwd_max_tiles(H, I, tp));
+  // row layer (every shard gets dY): dHs and dW2; then the local activation,
+  // which writes dG (and dU) token-major, [T][I] with the shards side by side
+  if ((r = row_bwd_bf16(Hs, T, W2, dY, dHs, dW2, &sc, st))) return as_status(r);
+  if ((r = act_bwd_launch(dHs, G, U, static_cast<int64_t>(T) * I, act, dG, dU, st, TP_BF16, T, tp, Is)))
+    return as_status(r);
+  // Column layer(s), each over all of I at once: the shards' contributions
+  // to dX are terms of one contraction over I, and their weight gradients
+  // are row blocks of one [I][H] product, so no tile is cut at a shard's
+  // ragged end (the column shards' storage [tp][Is][H] is [I][H]).
+  // dX: one accumulator over gate and up for SwiGLU, plus dR.
   if (dX) {
     CUtensorMap ma0, mb0, ma1, mb1;
-    if (!make_map_bf16(&ma0, dG, Is, T, tp, 128) || !make_map_bf16(&mb0, W1->data, H, Is, tp, 64) ||
-        !make_map_bf16(&ma1, dU, Is, T, tp, 128) || !make_map_bf16(&mb1, W_up->data, H, Is, tp, 64))
+    if (!make_map_bf16(&ma0, dG, I, T, 1, 128) || !make_map_bf16(&mb0, W1->data, H, I, 1, 64) ||
+        (gated && (!make_map_bf16(&ma1, dU, I, T, 1, 128) || !make_map_bf16(&mb1, W_up->data, H, I, 1, 64))))
       return TP_ERR_CUDA;
-    if ((r = gemm_bwd<tpk::GK_ROW_SUM, 2>(ma0, mb0, T, H, tp, Is, 0, dR, dX, &sc, st, &ma1, &mb1))) return as_status(r);
+    if ((r = gemm_bwd<tpk::GK_ROW_SUM, 2>(ma0, mb0, T, H, 1, I, 0, dR, dX, &sc, st, gated ? &ma1 : nullptr,
+                                          gated ? &mb1 : nullptr)))
+      return as_status(r);
   }
-  if ((r = col_bwd_bf16(X, T, W1, dG, nullptr, nullptr, dW1, &sc, st))) return as_status(r);
-  return as_status(col_bwd_bf16(X, T, W_up, dU, nullptr, nullptr, dW_up, &sc, st));
+  // dW = (X^T dG)^T: A = dG^T (M = I), B = X^T (N = H), both MN-major, K = T
+  auto dw = [&](const void* dA, void* dW) -> int {
+    if (!dW) return TP_OK;
+    CUtensorMap ma, mb;
+    if (!make_map_bf16(&ma, dA, I, T, 1, 64) || !make_map_bf16(&mb, X, H, T, 1, 64)) return TP_ERR_CUDA;
+    return gemm_bwd<tpk::GK_COL, 3>(ma, mb, I, H, 1, T, 1, nullptr, dW, &sc, st);
+  };
+  if ((r = dw(dG, dW1))) return as_status(r);
+  return as_status(gated ? dw(dU, dW_up) : TP_OK);
 }
 
 }  // extern "C"

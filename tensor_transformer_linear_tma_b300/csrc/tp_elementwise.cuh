@@ -229,33 +229,60 @@ __global__ void ctx_standin_kernel(const T* __restrict__ qkv, int tp, int64_t Tn
 // dU = dH * silu(G) (act_grad). bf16 in and out, fp32 arithmetic, eight
 // elements (16 bytes) per step; n8 = elements / 8. HBM-bound: per element 2
 // (SwiGLU 3) bf16 reads and 1 (2) bf16 writes.
+// With rows8 > 0, dG and dU are written token-major, [T][tp * I/tp] (the
+// shards side by side in each token row, so that the backward's GEMMs run
+// over all of I at once): vector t * rows8 + c of shard s (rows8 = I/tp / 8,
+// blockIdx.y = s, n8 = T * rows8 < 2^31 vectors a shard) goes to
+// (t * tp + s) * rows8 + c. t = i / rows8 is taken as
+// (umulhi(magic, i) + i) >> shift, the round-up method of Granlund and
+// Montgomery ("Division by invariant integers using multiplication", 1994),
+// with shift = ceil(log2 rows8) and magic = floor(2^(32 + shift) / rows8) -
+// 2^32 + 1, exact for every i < 2^31.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void act_backward_vec(const __nv_bfloat16* __restrict__ dH,
+                                                 const __nv_bfloat16* __restrict__ G,
+                                                 const __nv_bfloat16* __restrict__ U, int act, int64_t i, int64_t o,
+                                                 __nv_bfloat16* __restrict__ dG, __nv_bfloat16* __restrict__ dU) {
+  const uint4 h4 = reinterpret_cast<const uint4*>(dH)[i];
+  const uint4 g4 = reinterpret_cast<const uint4*>(G)[i];
+  const uint4 u4 = act == ACT_SWIGLU ? reinterpret_cast<const uint4*>(U)[i] : make_uint4(0, 0, 0, 0);
+  const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w},
+                 uw[4] = {u4.x, u4.y, u4.z, u4.w};
+  uint32_t og[4], ou[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float dg0, du0, dg1, du1;
+    // element 2w is the low half of a 32-bit word, 2w + 1 the high half
+    act_grad(act, __uint_as_float(hw[w] << 16), __uint_as_float(gw[w] << 16), __uint_as_float(uw[w] << 16), dg0,
+             du0);
+    act_grad(act, __uint_as_float(hw[w] & 0xFFFF0000u), __uint_as_float(gw[w] & 0xFFFF0000u),
+             __uint_as_float(uw[w] & 0xFFFF0000u), dg1, du1);
+    __nv_bfloat162 a = __floats2bfloat162_rn(dg0, dg1), b = __floats2bfloat162_rn(du0, du1);
+    og[w] = *reinterpret_cast<uint32_t*>(&a);
+    ou[w] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  reinterpret_cast<uint4*>(dG)[o] = make_uint4(og[0], og[1], og[2], og[3]);
+  if (act == ACT_SWIGLU) reinterpret_cast<uint4*>(dU)[o] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+}
+
 __global__ void act_backward_kernel(const __nv_bfloat16* __restrict__ dH, const __nv_bfloat16* __restrict__ G,
                                     const __nv_bfloat16* __restrict__ U, int64_t n8, int act,
-                                    __nv_bfloat16* __restrict__ dG, __nv_bfloat16* __restrict__ dU) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
-    const uint4 h4 = reinterpret_cast<const uint4*>(dH)[i];
-    const uint4 g4 = reinterpret_cast<const uint4*>(G)[i];
-    const uint4 u4 = act == ACT_SWIGLU ? reinterpret_cast<const uint4*>(U)[i] : make_uint4(0, 0, 0, 0);
-    const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w}, gw[4] = {g4.x, g4.y, g4.z, g4.w},
-                   uw[4] = {u4.x, u4.y, u4.z, u4.w};
-    uint32_t og[4], ou[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      float dg0, du0, dg1, du1;
-      // element 2w is the low half of a 32-bit word, 2w + 1 the high half
-      act_grad(act, __uint_as_float(hw[w] << 16), __uint_as_float(gw[w] << 16), __uint_as_float(uw[w] << 16),
-               dg0, du0);
-      act_grad(act, __uint_as_float(hw[w] & 0xFFFF0000u), __uint_as_float(gw[w] & 0xFFFF0000u),
-               __uint_as_float(uw[w] & 0xFFFF0000u), dg1, du1);
-      __nv_bfloat162 a = __floats2bfloat162_rn(dg0, dg1), b = __floats2bfloat162_rn(du0, du1);
-      og[w] = *reinterpret_cast<uint32_t*>(&a);
-      ou[w] = *reinterpret_cast<uint32_t*>(&b);
+                                    __nv_bfloat16* __restrict__ dG, __nv_bfloat16* __restrict__ dU,
+                                    uint32_t rows8 = 0, uint32_t magic = 0, int shift = 0, int tp = 1) {
+  if (rows8 > 0) {
+    const uint32_t per = static_cast<uint32_t>(n8);
+    const int64_t sh = blockIdx.y;
+    const uint32_t stride = gridDim.x * blockDim.x;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < per; i += stride) {
+      const uint32_t t = (__umulhi(magic, i) + i) >> shift;
+      const uint32_t c = i - t * rows8;
+      act_backward_vec(dH, G, U, act, sh * per + i, (static_cast<int64_t>(t) * tp + sh) * rows8 + c, dG, dU);
     }
-    reinterpret_cast<uint4*>(dG)[i] = make_uint4(og[0], og[1], og[2], og[3]);
-    if (act == ACT_SWIGLU) reinterpret_cast<uint4*>(dU)[i] = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+    return;
   }
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride)
+    act_backward_vec(dH, G, U, act, i, i, dG, dU);
 }
 
 // fp32 form of act_backward_kernel: one element per step, any count.
