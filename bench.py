@@ -63,7 +63,10 @@ def workload_spec(name: str, tp: int | None, tokens: int | None):
         T, H, I = tokens or 2048, 4096, 11008
         tp = tp or 8
         return dict(name="llama7b_swiglu_mlp_backward", T=T, H=H, I=I, tp=tp, flops=12.0 * T * H * I,
-                    dominant="weight-gradient GEMM of the gate shards (dW1, both operands MN-major)",
+                    dominant="weight-gradient GEMM of the gate shards (dW1, both operands MN-major), "
+                             "timed through tp_column_linear_backward, whose interface keeps each shard's "
+                             "gradient in its own tile rows (inside tp_mlp_backward the same product runs "
+                             "over all of I at once)",
                     dominant_flops=2.0 * T * H * I, bound="tensor",
                     sample_note="the first {r} of {T} tokens, a complete backward problem of its own "
                                 "(weight gradients sum over tokens)")
