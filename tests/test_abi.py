@@ -229,6 +229,15 @@ def test_backward_validation():
     W2f = view(K=256, N=128, mode=ROW, dtype=F32)   # an fp32 row layer under a bf16 column layer
     assert L.tp_mlp_backward(FAKE, 8, ctypes.byref(W1), None, ctypes.byref(W2f), 1, FAKE, None, FAKE, FAKE, None,
                              FAKE, need, FAKE, FAKE, None, FAKE, None) == DTYPE
+    # the bf16 path keeps dG and dU token-major in 16-byte vectors: I/tp a
+    # multiple of 8, and T * I/tp under 2^34
+    def mlp_bwd(T, I):
+        Wc, Wr = view(K=128, N=I, mode=COL, dtype=BF16), view(K=I, N=128, mode=ROW, dtype=BF16)
+        ws = L.tp_mlp_backward_workspace_bytes(T, 128, I, 2, 4, BF16)
+        return L.tp_mlp_backward(FAKE, T, ctypes.byref(Wc), ctypes.byref(Wc), ctypes.byref(Wr), 4, FAKE, FAKE,
+                                 FAKE, FAKE, None, FAKE, ws, FAKE, FAKE, FAKE, FAKE, None)
+    assert mlp_bwd(8, 260) == ALIGN              # I/tp = 130
+    assert mlp_bwd((1 << 34) // 1024, 2048) == UNSUP  # T * I/tp = 2^34
 
 
 def test_vocab_validation():
