@@ -1809,7 +1809,9 @@ tp_status tp_moe_block(const void* X, int64_t T, const int32_t* ids, const float
     a.num_tiles = a.m_tiles * a.n_tiles * tp;
     a.r1_tiles = a.num_tiles;
     a.unit_expert = unit_expert;
-    a.unit_group = 16;
+    // groups of 8 pairs within each expert: a weight tile's few readers
+    // (the expert's units) fall within 8 tiles of each other
+    a.unit_group = 8;
     a.unit_seg = unit_seg;
     OutMaps om{};
     a.tma_store = make_store_map(&om.y, Hs, false, Is, L.rows, tp, Is * 2, L.rows * Is * 2) ? 1 : 0;
