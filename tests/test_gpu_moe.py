@@ -40,13 +40,17 @@ def oracle(X, ex, ids, w, tp, R=None):
 
 @pytest.mark.parametrize("tp,T,H,I,E,k", [(2, 300, 256, 512, 4, 2), (8, 129, 384, 1408, 8, 2),
                                           (4, 64, 256, 1024, 3, 1), (1, 1, 256, 512, 2, 2), (2, 200, 256, 768, 6, 3),
-                                          (2, 260, 4352, 5120, 4, 2)])
+                                          (2, 260, 4352, 5120, 4, 2), (2, 600, 1024, 2560, 4, 2)])
 def test_moe_block(tp, T, H, I, E, k):
     """Ragged tails: H = 384 (a 128-column last block of the down GEMM),
-    I/tp = 176; a single token; top-1 and top-3. The last case has 40
-    (column block, shard) pairs per unit in the gate/up GEMM and 17 column
-    blocks in the down GEMM, so the grouped tile order runs full groups of
-    16 and a partial last group."""
+    I/tp = 176; a single token; top-1 and top-3. The gate/up GEMM takes its
+    (column block, shard) pairs in groups of 8 within each expert: 4 and 6
+    pairs make one partial group, 16 two full ones, 40 (with 17 down column
+    blocks) five, and 20 two full groups and a partial one, with each expert
+    on two units (about 300 rows). Y mixes two experts plus the residual and
+    is stored in bf16; its largest elements sit 6-7x above the RMS, so each
+    element's own storage rounding is added to the 2e-2 RMS bound, as in the
+    full-size check."""
     X = S.normal(601, (T, H))
     ex = S.moe_experts(E, H, I, seed=602, std=0.05)
     ids, w = S.moe_routing(603, T, E, k)
@@ -54,7 +58,7 @@ def test_moe_block(tp, T, H, I, E, k):
     Wg, Wu, Wd = gpu_experts(ex, tp)
     Y = tpl.tp_moe_block(dev(X), i32(ids), f32(w), Wg, Wu, Wd, E, residual=dev(R))
     assert tpl.tp_get_error() == 0
-    assert_close(Y, oracle(X, ex, ids, w, tp, R), TOL_BF16, "Y")
+    assert_close_stored(Y, oracle(X, ex, ids, w, tp, R), TOL_BF16, "Y")
 
 
 def test_moe_skewed_routing_and_unused_experts():
