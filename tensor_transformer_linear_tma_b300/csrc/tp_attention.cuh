@@ -56,13 +56,6 @@
 
 namespace tpk {
 
-// 2^x with the MUFU approximation (flushes subnormals; 2^-inf = 0).
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Two fp32 values in one 64-bit register pair (the first in the low half),
 // for the paired fp32 instructions: one instruction, two results.
 __device__ __forceinline__ uint64_t f2_make(float lo, float hi) {

@@ -532,18 +532,26 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
 struct CeAcc {
   float m, S, zy;
 };
-// Eight logits at once (all inside the shard or none: widths are multiples
-// of 8 on this path).
-__device__ __forceinline__ void ce_add8(CeAcc& c, const float* v) {
-  float mx = v[0];
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2 e)
+// 32 logits at once (columns past the shard hold -inf): one maximum and at
+// most one rescale per 32, each exponential one FMA and a MUFU 2^x.
+__device__ __forceinline__ void ce_add32(CeAcc& c, const float* z) {
+  float mx = z[0];
 #pragma unroll
-  for (int j = 1; j < 8; ++j) mx = fmaxf(mx, v[j]);
+  for (int j = 1; j < 32; ++j) mx = fmaxf(mx, z[j]);
   if (mx > c.m) {
-    c.S *= __expf(c.m - mx);  // exp(-inf) = 0 on the first group
+    c.S *= ex2_approx((c.m - mx) * kLog2e);  // 2^-inf = 0 on the first chunk
     c.m = mx;
   }
+  if (c.m == -INFINITY) return;  // no column of this row seen yet
+  const float mb = c.m * kLog2e;
+  float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) c.S += __expf(v[j] - c.m);
+  for (int j = 0; j < 32; j += 2) {
+    s0 += ex2_approx(fmaf(z[j], kLog2e, -mb));
+    s1 += ex2_approx(fmaf(z[j + 1], kLog2e, -mb));
+  }
+  c.S += s0 + s1;
 }
 
 // normal mode: this thread owns token row `row`; columns are output features.
@@ -599,9 +607,10 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = apply_act(a.act, v[j]);
-            if (with_ce && col_ok) {
-              ce_add8(ce, v);
-              if (ce_loc >= n && ce_loc < n + 8) {
+            if (with_ce) {  // the chunk's logits, kept for its statistics below
+#pragma unroll
+              for (int j = 0; j < 8; ++j) g[j8 + j] = col_ok ? v[j] : -INFINITY;
+              if (col_ok && ce_loc >= n && ce_loc < n + 8) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                   if (ce_loc == n + j) ce.zy = v[j];
@@ -625,6 +634,9 @@ __device__ __forceinline__ void epilogue_normal(const GemmArgs& a, const Src& sr
               }
             }
           }
+        }
+        if constexpr (!Cfg::SWIGLU) {
+          if (with_ce) ce_add32(ce, g);
         }
       }
       if (sb) {

@@ -441,6 +441,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
 // ---------------------------------------------------------------------------
 // Small numeric helpers shared by the epilogues
 // ---------------------------------------------------------------------------
+// 2^x with the MUFU approximation (flushes subnormals; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
